@@ -1,0 +1,616 @@
+/*
+ * CPU oracle for the topology-aware expert-routing plan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, single-threaded
+ * statement of what the GPU path must compute, used to check it bit for bit.
+ * Only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * load it.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (page title, section / equation / figure):
+ *   [TopoEP]  "TopoEP: Topology-Aware Load Balancing for Expert-Parallel MoE
+ *             Training" -- §4.1 (system model, Eqs. 3-4), §4.2 (constraints
+ *             C1-C5, Eqs. 5-8), §4.3 (two-stage solver, Eqs. 9-10, Fig. 9),
+ *             §2.3 (Fig. 3 byte accounting), §5 (receive counts on the GPU).
+ *   [Zyphra]  "Expert Coupling in MoE Pretraining" -- sections "Experts Are
+ *             Correlated Within a Layer" and "Routing Is Also Correlated
+ *             Across Layers".
+ *
+ * Where the pages leave a step open, the reading taken is stated at the step.
+ * Every function is a direct transcription of the step list, with no blocking,
+ * fusion or reordering.  Integers only; 64-bit where a product may overflow.
+ *
+ * Conventions shared with the inputs (not with any other code):
+ *   pair p = t*k + j; source rank src(t) = t / (T/R) (equal contiguous token
+ *   blocks, T % R == 0); domain dom(r) = r / ranks_per_node;
+ *   main(e) = e / (E/R) with local index e % (E/R) unless a main_rank map is
+ *   given, in which case the local index of e is the number of experts e' < e
+ *   with the same main rank; an instance (r, l) is packed as r*n_local + l,
+ *   n_local = E/R + n_slot, l < E/R a main, l >= E/R replica slot l - E/R.
+ *
+ * Return codes: 0 ok, -1 bad argument, -2 an id outside [0, E).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL -1
+#define ORC_ERANGE -2
+
+/* ------------------------------------------------------------------------ */
+/* Problem description                                                        */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int T, E, k, R, rpn, n_slot;
+    int64_t S_tok;   /* bytes of one routed activation [TopoEP §4.1] */
+    int64_t W;       /* ||W_e|| bytes, equal for all experts [TopoEP §4.1] */
+    int64_t c_intra; /* c_{s,r} for s != r in the same NVLink domain */
+    int64_t c_inter; /* c_{s,r} across domains */
+    int max_iters;   /* 0 = refine until no feasible candidate */
+    int M, E_R, n_local;
+    int *main_of;    /* [E] main(e) */
+    int *main_l;     /* [E] local index of e on main(e) */
+} Problem;
+
+static int dom(const Problem *P, int r) { return r / P->rpn; }
+
+/* Communication-time matrix C of [TopoEP §4.1]: c_{r,r} = 0, cheaper inside
+ * an NVLink domain than across domains (two-level integer reading). */
+static int64_t cost(const Problem *P, int s, int r) {
+    if (s == r) return 0;
+    if (dom(P, s) == dom(P, r)) return P->c_intra;
+    return P->c_inter;
+}
+
+static int problem_init(Problem *P, int T, int E, int k, int R, int rpn,
+                        int n_slot, int64_t S_tok, int64_t W, int64_t c_intra,
+                        int64_t c_inter, int max_iters, const int32_t *main_rank) {
+    memset(P, 0, sizeof *P);
+    if (T < 0 || E < 1 || k < 1 || R < 1 || rpn < 1 || n_slot < 0) return ORC_EINVAL;
+    if (R % rpn != 0 || E % R != 0 || T % R != 0) return ORC_EINVAL;
+    if (S_tok < 0 || W < 0 || c_intra < 1 || c_inter < c_intra || max_iters < 0) return ORC_EINVAL;
+    P->T = T; P->E = E; P->k = k; P->R = R; P->rpn = rpn; P->n_slot = n_slot;
+    P->S_tok = S_tok; P->W = W; P->c_intra = c_intra; P->c_inter = c_inter;
+    P->max_iters = max_iters;
+    P->M = R / rpn; P->E_R = E / R; P->n_local = P->E_R + n_slot;
+    P->main_of = (int *)malloc(sizeof(int) * E);
+    P->main_l = (int *)malloc(sizeof(int) * E);
+    int *owned = (int *)calloc(R, sizeof(int));
+    for (int e = 0; e < E; e++) {
+        int r = main_rank ? main_rank[e] : e / P->E_R;
+        if (r < 0 || r >= R) { free(owned); return ORC_EINVAL; }
+        P->main_of[e] = r;
+        P->main_l[e] = owned[r]++;   /* ascending e within the rank */
+    }
+    for (int r = 0; r < R; r++)
+        if (owned[r] != P->E_R) { free(owned); return ORC_EINVAL; }
+    free(owned);
+    return ORC_OK;
+}
+
+static void problem_free(Problem *P) {
+    free(P->main_of);
+    free(P->main_l);
+}
+
+/* ------------------------------------------------------------------------ */
+/* O1  Routing matrix Omega  [TopoEP §4.1, Eq. 3]                             */
+/* omega_{s,e} = number of token-expert assignments from source rank s that  */
+/* select expert e.                                                           */
+/* ------------------------------------------------------------------------ */
+
+int oracle_hist(int T, int E, int k, int R, int n_layers, const int32_t *ids,
+                int32_t *hist) {
+    if (T < 0 || E < 1 || k < 1 || R < 1 || n_layers < 0 || T % R != 0) return ORC_EINVAL;
+    int tpr = T / R;  /* tokens per source rank */
+    int rc = ORC_OK;
+    for (int l = 0; l < n_layers; l++) {
+        const int32_t *id = ids + (int64_t)l * T * k;
+        int32_t *h = hist + (int64_t)l * R * E;
+        memset(h, 0, sizeof(int32_t) * (size_t)R * E);
+        for (int t = 0; t < T; t++) {
+            int s = t / tpr;
+            for (int j = 0; j < k; j++) {
+                int e = id[(int64_t)t * k + j];
+                if (e < 0 || e >= E) { rc = ORC_ERANGE; continue; }
+                h[(int64_t)s * E + e] += 1;
+            }
+        }
+    }
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O2  Expert co-selection and cross-layer transition counts                  */
+/* [Zyphra, "Experts Are Correlated Within a Layer", "Routing Is Also         */
+/* Correlated Across Layers"].  With n_t^l the count vector of token t's      */
+/* choices at layer l:  co_l = sum_t n_t^l (n_t^l)^T,                         */
+/* tr_l = sum_t n_t^l (n_t^{l+1})^T.  The diagonal of co is kept (the page    */
+/* masks it only in a plot).  tr may be NULL.                                 */
+/* ------------------------------------------------------------------------ */
+
+int oracle_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co,
+                   int64_t *tr) {
+    if (L < 0 || T < 0 || E < 1 || k < 1) return ORC_EINVAL;
+    int rc = ORC_OK;
+    memset(co, 0, sizeof(int64_t) * (size_t)L * E * E);
+    if (tr && L > 1) memset(tr, 0, sizeof(int64_t) * (size_t)(L - 1) * E * E);
+    for (int l = 0; l < L; l++) {
+        const int32_t *a = ids + (int64_t)l * T * k;
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                int x = a[(int64_t)t * k + j];
+                if (x < 0 || x >= E) { rc = ORC_ERANGE; continue; }
+                for (int i = 0; i < k; i++) {
+                    int y = a[(int64_t)t * k + i];
+                    if (y < 0 || y >= E) continue;
+                    co[((int64_t)l * E + x) * E + y] += 1;
+                }
+            }
+        if (!tr || l == L - 1) continue;
+        const int32_t *b = ids + (int64_t)(l + 1) * T * k;
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                int x = a[(int64_t)t * k + j];
+                if (x < 0 || x >= E) continue;
+                for (int i = 0; i < k; i++) {
+                    int y = b[(int64_t)t * k + i];
+                    if (y < 0 || y >= E) { rc = ORC_ERANGE; continue; }
+                    tr[((int64_t)l * E + x) * E + y] += 1;
+                }
+            }
+    }
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plan state for one layer                                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const Problem *P;
+    const int32_t *hist;  /* [R][E] omega */
+    int32_t *slot_expert; /* [R][n_slot], -1 empty  (x for replicas) */
+    int32_t *q;           /* [R_src][R_dst][n_local] */
+    int32_t *U;           /* [R][n_local] instance loads */
+    int32_t *Lr;          /* [R] rank loads */
+    int *used;            /* [R] occupied replica slots */
+    int *host;            /* [R][E] local index of e on r, or -1  (x) */
+    int64_t stage1_replicas;
+    int64_t refine_iters;
+} Plan;
+
+static int32_t *Q(Plan *S, int s, int r, int l) {
+    const Problem *P = S->P;
+    return &S->q[((int64_t)s * P->R + r) * P->n_local + l];
+}
+
+static void place_replica(Plan *S, int r, int e) {
+    const Problem *P = S->P;
+    int slot = S->used[r]++;
+    S->slot_expert[(int64_t)r * P->n_slot + slot] = e;
+    S->host[(int64_t)r * P->E + e] = P->E_R + slot;
+}
+
+/* O3  Domain demand D_{d,e} = sum over sources s in domain d of omega_{s,e}
+ * [TopoEP §4.1, Eq. 4]. */
+static void demand(const Plan *S, int64_t *D) {
+    const Problem *P = S->P;
+    memset(D, 0, sizeof(int64_t) * (size_t)P->M * P->E);
+    for (int s = 0; s < P->R; s++)
+        for (int e = 0; e < P->E; e++)
+            D[(int64_t)dom(P, s) * P->E + e] += S->hist[(int64_t)s * P->E + e];
+}
+
+typedef struct { int64_t b; int e; } Cand;
+
+static int cand_cmp(const void *x, const void *y) {
+    const Cand *a = (const Cand *)x, *c = (const Cand *)y;
+    if (a->b != c->b) return a->b > c->b ? -1 : 1;   /* benefit descending */
+    return a->e < c->e ? -1 : (a->e > c->e);          /* then expert ascending */
+}
+
+/* O4  Stage 1, inter-node placement [TopoEP §4.3, Eq. 9; C4 of §4.2].
+ * For each domain d, every expert whose main lies outside d with benefit
+ * b_{d,e} = 2 D_{d,e} S_tok - ||W|| > 0 is a candidate; candidates are taken
+ * in descending benefit (ties: lower expert id first) and each is placed on
+ * the rank of d with a free slot that has the fewest occupied slots (ties:
+ * lower rank).  At most one stage-1 replica per (domain, expert).  A domain
+ * stops when none of its ranks has a free slot. */
+static void stage1_place(Plan *S, const int64_t *D) {
+    const Problem *P = S->P;
+    Cand *c = (Cand *)malloc(sizeof(Cand) * (size_t)(P->E ? P->E : 1));
+    for (int d = 0; d < P->M; d++) {
+        int n = 0;
+        for (int e = 0; e < P->E; e++) {
+            if (dom(P, P->main_of[e]) == d) continue;
+            int64_t b = 2 * D[(int64_t)d * P->E + e] * P->S_tok - P->W;
+            if (b > 0) { c[n].b = b; c[n].e = e; n++; }
+        }
+        qsort(c, (size_t)n, sizeof(Cand), cand_cmp);
+        for (int i = 0; i < n; i++) {
+            int best = -1;
+            for (int r = d * P->rpn; r < (d + 1) * P->rpn; r++) {
+                if (S->used[r] >= P->n_slot) continue;
+                if (best < 0 || S->used[r] < S->used[best]) best = r;
+            }
+            if (best < 0) break;
+            place_replica(S, best, c[i].e);
+            S->stage1_replicas++;
+        }
+    }
+    free(c);
+}
+
+/* Sort helper: ranks ordered by (c_{s,r}, r) ascending. */
+static const Problem *g_sortP;
+static int g_sort_s;
+static int rank_cost_cmp(const void *x, const void *y) {
+    int a = *(const int *)x, b = *(const int *)y;
+    int64_t ca = cost(g_sortP, g_sort_s, a), cb = cost(g_sortP, g_sort_s, b);
+    if (ca != cb) return ca < cb ? -1 : 1;
+    return a < b ? -1 : (a > b);
+}
+
+/* O5  Stage-1 routing [TopoEP §4.3, "Given the resulting placement ..."].
+ * For every (s, e) with omega_{s,e} > 0: the candidate instances are those
+ * of e inside dom(s) if any exist, else every instance of e.  omega_{s,e} is
+ * divided as evenly as integers allow: each of the n instances gets
+ * floor(omega / n) and the first (omega mod n) of them, in ascending
+ * (c_{s,r}, r) order, get one more.  Then U_{e,r} = sum_s q_{s,e,r} and
+ * L_r = sum of U over r's instances. */
+static void stage1_route(Plan *S) {
+    const Problem *P = S->P;
+    int *I = (int *)malloc(sizeof(int) * (size_t)P->R);
+    for (int s = 0; s < P->R; s++)
+        for (int e = 0; e < P->E; e++) {
+            int w = S->hist[(int64_t)s * P->E + e];
+            if (w == 0) continue;
+            int n = 0;
+            for (int r = 0; r < P->R; r++)
+                if (S->host[(int64_t)r * P->E + e] >= 0 && dom(P, r) == dom(P, s)) I[n++] = r;
+            if (n == 0)
+                for (int r = 0; r < P->R; r++)
+                    if (S->host[(int64_t)r * P->E + e] >= 0) I[n++] = r;
+            g_sortP = P; g_sort_s = s;
+            qsort(I, (size_t)n, sizeof(int), rank_cost_cmp);
+            int base = w / n, rem = w % n;
+            for (int i = 0; i < n; i++)
+                *Q(S, s, I[i], S->host[(int64_t)I[i] * P->E + e]) = base + (i < rem ? 1 : 0);
+        }
+    free(I);
+    memset(S->U, 0, sizeof(int32_t) * (size_t)P->R * P->n_local);
+    for (int s = 0; s < P->R; s++)
+        for (int r = 0; r < P->R; r++)
+            for (int l = 0; l < P->n_local; l++)
+                S->U[(int64_t)r * P->n_local + l] += *Q(S, s, r, l);
+    for (int r = 0; r < P->R; r++) {
+        int64_t sum = 0;
+        for (int l = 0; l < P->n_local; l++) sum += S->U[(int64_t)r * P->n_local + l];
+        S->Lr[r] = (int32_t)sum;
+    }
+}
+
+/* Source order for assignments that move from r_b to r_t: ascending
+ * (c_{s,r_t} - c_{s,r_b}, s), i.e. the moves that save the most token cost
+ * first.  (Reading: the pages do not say which assignments move.) */
+static int g_rt, g_rb;
+static int src_move_cmp(const void *x, const void *y) {
+    int a = *(const int *)x, b = *(const int *)y;
+    int64_t ka = cost(g_sortP, a, g_rt) - cost(g_sortP, a, g_rb);
+    int64_t kb = cost(g_sortP, b, g_rt) - cost(g_sortP, b, g_rb);
+    if (ka != kb) return ka < kb ? -1 : 1;
+    return a < b ? -1 : (a > b);
+}
+
+typedef struct {
+    int ok;
+    int64_t delta, Lt, cost;
+    int e, rt, lb, lt, is_new;
+} Move;
+
+/* Lexicographic candidate order of [TopoEP §4.3, after Eq. 10]: transfer
+ * amount (larger first), target load (smaller first), communication cost
+ * (smaller first); remaining ties by expert id, then target rank, ascending. */
+static int move_better(const Move *a, const Move *b) {
+    if (!b->ok) return 1;
+    if (a->delta != b->delta) return a->delta > b->delta;
+    if (a->Lt != b->Lt) return a->Lt < b->Lt;
+    if (a->cost != b->cost) return a->cost < b->cost;
+    if (a->e != b->e) return a->e < b->e;
+    return a->rt < b->rt;
+}
+
+/* O6  Stage 2, intra-node refinement [TopoEP §4.3, Eq. 10, Fig. 9].
+ * Each domain independently: take the busiest rank r_b (ties: lowest r);
+ * for every expert e with load on r_b and every other rank r_t of the domain
+ * that hosts e or has a free slot, the transfer amount is
+ *     delta = min(U_{e,r_b}, floor((L_{r_b} - L_{r_t}) / 2)),
+ * feasible when delta >= 1.  The assignments moved are taken from sources in
+ * the order of src_move_cmp, m_s = min(q_{s,e,r_b}, still to move).  The cost
+ * of a candidate is the change it makes to T_token + T_replica of Eq. 7:
+ *     2 S_tok sum_s m_s (c_{s,r_t} - c_{s,r_b}) + [r_t lacks e] c_{main(e),r_t} ||W||.
+ * The best candidate (move_better) is committed -- a new replica in r_t's
+ * next free slot if needed, the m_s moved in q, U and L updated -- and the
+ * loop repeats until the busiest rank has no feasible candidate (or the
+ * optional iteration cap).  Each commit lowers sum_r L_r^2 by
+ * 2 delta (gap - delta) >= 2, so the loop ends. */
+static void stage2_refine(Plan *S) {
+    const Problem *P = S->P;
+    int *order = (int *)malloc(sizeof(int) * (size_t)P->R);
+    int64_t *m = (int64_t *)malloc(sizeof(int64_t) * (size_t)P->R);
+    for (int d = 0; d < P->M; d++) {
+        int r0 = d * P->rpn, r1 = r0 + P->rpn;
+        int64_t iters = 0;
+        for (;;) {
+            if (P->max_iters > 0 && iters >= P->max_iters) break;
+            int rb = r0;
+            for (int r = r0; r < r1; r++)
+                if (S->Lr[r] > S->Lr[rb]) rb = r;
+            Move best; memset(&best, 0, sizeof best);
+            for (int lb = 0; lb < P->n_local; lb++) {
+                int64_t Ub = S->U[(int64_t)rb * P->n_local + lb];
+                if (Ub <= 0) continue;
+                int e = lb < P->E_R ? -1 : S->slot_expert[(int64_t)rb * P->n_slot + (lb - P->E_R)];
+                if (lb < P->E_R) {
+                    for (int x = 0; x < P->E; x++)
+                        if (P->main_of[x] == rb && P->main_l[x] == lb) e = x;
+                }
+                for (int rt = r0; rt < r1; rt++) {
+                    if (rt == rb) continue;
+                    int lt = S->host[(int64_t)rt * P->E + e];
+                    int is_new = lt < 0;
+                    if (is_new && S->used[rt] >= P->n_slot) continue;
+                    int64_t gap = (int64_t)S->Lr[rb] - S->Lr[rt];
+                    int64_t half = gap / 2;    /* gap >= 0: floor */
+                    int64_t delta = Ub < half ? Ub : half;
+                    if (delta < 1) continue;
+                    for (int s = 0; s < P->R; s++) order[s] = s;
+                    g_sortP = P; g_rt = rt; g_rb = rb;
+                    qsort(order, (size_t)P->R, sizeof(int), src_move_cmp);
+                    int64_t left = delta, tok = 0;
+                    for (int i = 0; i < P->R; i++) {
+                        int s = order[i];
+                        int64_t have = *Q(S, s, rb, lb);
+                        int64_t take = have < left ? have : left;
+                        left -= take;
+                        tok += take * (cost(P, s, rt) - cost(P, s, rb));
+                    }
+                    Move mv;
+                    mv.ok = 1; mv.delta = delta; mv.Lt = S->Lr[rt];
+                    mv.cost = 2 * P->S_tok * tok + (is_new ? cost(P, P->main_of[e], rt) * P->W : 0);
+                    mv.e = e; mv.rt = rt; mv.lb = lb; mv.lt = lt; mv.is_new = is_new;
+                    if (move_better(&mv, &best)) best = mv;
+                }
+            }
+            if (!best.ok) break;
+            /* commit */
+            int rt = best.rt, lb = best.lb, lt = best.lt;
+            if (best.is_new) {
+                place_replica(S, rt, best.e);
+                lt = S->host[(int64_t)rt * P->E + best.e];
+            }
+            for (int s = 0; s < P->R; s++) order[s] = s;
+            g_sortP = P; g_rt = rt; g_rb = rb;
+            qsort(order, (size_t)P->R, sizeof(int), src_move_cmp);
+            int64_t left = best.delta;
+            for (int i = 0; i < P->R; i++) {
+                int s = order[i];
+                int64_t have = *Q(S, s, rb, lb);
+                m[s] = have < left ? have : left;
+                left -= m[s];
+            }
+            for (int s = 0; s < P->R; s++) {
+                *Q(S, s, rb, lb) -= (int32_t)m[s];
+                *Q(S, s, rt, lt) += (int32_t)m[s];
+            }
+            S->U[(int64_t)rb * P->n_local + lb] -= (int32_t)best.delta;
+            S->U[(int64_t)rt * P->n_local + lt] += (int32_t)best.delta;
+            S->Lr[rb] -= (int32_t)best.delta;
+            S->Lr[rt] += (int32_t)best.delta;
+            iters++;
+        }
+        S->refine_iters += iters;
+    }
+    free(order);
+    free(m);
+}
+
+/* Plan statistics (per layer, int64[8]):
+ *   0 L_max            max_r L_r after refinement            [TopoEP §4.2, Eq. 5]
+ *   1 L_max_static     max_r of the load with mains only (no replicas)
+ *   2 n_replicas       occupied replica slots after refinement
+ *   3 n_stage1         replicas created by inter-node placement
+ *   4 refine_iters     refinement commits, all domains
+ *   5 T_token          2 S_tok sum_{s,e,r} c_{s,r} q_{s,e,r}   [Eq. 7]
+ *   6 T_replica        sum_{replicas} c_{main(e),r} ||W||      [Eq. 7]
+ *   7 sum_L            sum_r L_r (= T k)                                   */
+static void plan_stats(Plan *S, int64_t *st) {
+    const Problem *P = S->P;
+    int64_t lmax = 0, sum = 0;
+    for (int r = 0; r < P->R; r++) {
+        if (S->Lr[r] > lmax) lmax = S->Lr[r];
+        sum += S->Lr[r];
+    }
+    int64_t smax = 0;
+    for (int r = 0; r < P->R; r++) {
+        int64_t load = 0;
+        for (int e = 0; e < P->E; e++) {
+            if (P->main_of[e] != r) continue;
+            for (int s = 0; s < P->R; s++) load += S->hist[(int64_t)s * P->E + e];
+        }
+        if (load > smax) smax = load;
+    }
+    int64_t nrep = 0, trep = 0;
+    for (int r = 0; r < P->R; r++)
+        for (int j = 0; j < P->n_slot; j++) {
+            int e = S->slot_expert[(int64_t)r * P->n_slot + j];
+            if (e < 0) continue;
+            nrep++;
+            trep += cost(P, P->main_of[e], r) * P->W;
+        }
+    int64_t ttok = 0;
+    for (int s = 0; s < P->R; s++)
+        for (int r = 0; r < P->R; r++)
+            for (int l = 0; l < P->n_local; l++)
+                ttok += cost(P, s, r) * (int64_t)*Q(S, s, r, l);
+    ttok *= 2 * P->S_tok;
+    st[0] = lmax; st[1] = smax; st[2] = nrep; st[3] = S->stage1_replicas;
+    st[4] = S->refine_iters; st[5] = ttok; st[6] = trep; st[7] = sum;
+}
+
+int oracle_plan(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok,
+                int64_t W, int64_t c_intra, int64_t c_inter, int max_iters,
+                const int32_t *main_rank, int n_layers, const int32_t *hist,
+                int32_t *slot_expert, int32_t *route_cnt, int32_t *inst_load,
+                int32_t *rank_load, int64_t *stats) {
+    Problem P;
+    int rc = problem_init(&P, T, E, k, R, rpn, n_slot, S_tok, W, c_intra, c_inter,
+                          max_iters, main_rank);
+    if (rc != ORC_OK || n_layers < 0) { problem_free(&P); return ORC_EINVAL; }
+    int64_t *D = (int64_t *)malloc(sizeof(int64_t) * (size_t)P.M * E);
+    int *used = (int *)malloc(sizeof(int) * (size_t)R);
+    int *host = (int *)malloc(sizeof(int) * (size_t)R * E);
+    for (int l = 0; l < n_layers; l++) {
+        Plan S;
+        S.P = &P;
+        S.hist = hist + (int64_t)l * R * E;
+        S.slot_expert = slot_expert + (int64_t)l * R * n_slot;
+        S.q = route_cnt + (int64_t)l * R * R * P.n_local;
+        S.U = inst_load + (int64_t)l * R * P.n_local;
+        S.Lr = rank_load + (int64_t)l * R;
+        S.used = used; S.host = host;
+        S.stage1_replicas = 0; S.refine_iters = 0;
+        for (int64_t i = 0; i < (int64_t)R * n_slot; i++) S.slot_expert[i] = -1;
+        memset(S.q, 0, sizeof(int32_t) * (size_t)R * R * P.n_local);
+        memset(used, 0, sizeof(int) * (size_t)R);
+        for (int64_t i = 0; i < (int64_t)R * E; i++) host[i] = -1;
+        for (int e = 0; e < E; e++) host[(int64_t)P.main_of[e] * E + e] = P.main_l[e];  /* C5 */
+        demand(&S, D);
+        stage1_place(&S, D);
+        stage1_route(&S);
+        stage2_refine(&S);
+        plan_stats(&S, stats + (int64_t)l * 8);
+    }
+    free(D); free(used); free(host);
+    problem_free(&P);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O7  Rerouting of each (token, slot) pair to an expert instance             */
+/* [TopoEP §1 and Fig. 5, "token rerouting"; the rule is not given].          */
+/* Reading: within source s the pairs that select e are taken in ascending  */
+/* pair order; the instances of e are listed in ascending (r, l); the o-th    */
+/* such pair goes to the instance whose running range of q_{s,e,.} holds o.  */
+/* ------------------------------------------------------------------------ */
+
+int oracle_reroute(int T, int E, int k, int R, int rpn, int n_slot,
+                   const int32_t *main_rank, int n_layers, const int32_t *ids,
+                   const int32_t *slot_expert, const int32_t *route_cnt,
+                   int32_t *dst_inst) {
+    Problem P;
+    int rc = problem_init(&P, T, E, k, R, rpn, n_slot, 0, 0, 1, 1, 0, main_rank);
+    if (rc != ORC_OK || n_layers < 0) { problem_free(&P); return ORC_EINVAL; }
+    int tpr = T / R;
+    int64_t npairs = (int64_t)T * k;
+    int32_t *occ = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int *host = (int *)malloc(sizeof(int) * (size_t)R * E);
+    rc = ORC_OK;
+    for (int l = 0; l < n_layers; l++) {
+        const int32_t *id = ids + l * npairs;
+        const int32_t *se = slot_expert + (int64_t)l * R * n_slot;
+        const int32_t *q = route_cnt + (int64_t)l * R * R * P.n_local;
+        int32_t *dst = dst_inst + l * npairs;
+        for (int64_t i = 0; i < (int64_t)R * E; i++) host[i] = -1;
+        for (int e = 0; e < E; e++) host[(int64_t)P.main_of[e] * E + e] = P.main_l[e];
+        for (int r = 0; r < R; r++)
+            for (int j = 0; j < n_slot; j++) {
+                int e = se[(int64_t)r * n_slot + j];
+                if (e >= 0 && e < E) host[(int64_t)r * E + e] = P.E_R + j;
+            }
+        for (int s = 0; s < R; s++) {
+            memset(occ, 0, sizeof(int32_t) * (size_t)E);
+            for (int64_t p = (int64_t)s * tpr * k; p < (int64_t)(s + 1) * tpr * k; p++) {
+                int e = id[p];
+                dst[p] = -1;
+                if (e < 0 || e >= E) { rc = ORC_ERANGE; continue; }
+                int64_t o = occ[e]++;
+                int64_t pre = 0;
+                for (int r = 0; r < R; r++) {
+                    int li = host[(int64_t)r * E + e];
+                    if (li < 0) continue;
+                    int64_t c = q[((int64_t)s * R + r) * P.n_local + li];
+                    if (o < pre + c) { dst[p] = r * P.n_local + li; break; }
+                    pre += c;
+                }
+            }
+        }
+    }
+    free(occ); free(host);
+    problem_free(&P);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O8  Dispatch layout [TopoEP §5: receive counts derived on the GPU;        */
+/* §2.3 Fig. 3 and §6 Fig. 16 for the byte / locality accounting].            */
+/*   sorted_pairs: stable ascending sort of the pair indices by dst_inst     */
+/*                 (gather form: sorted_pairs[pos] = p);                      */
+/*   seg_off:      exclusive prefix of the per-instance pair counts, [R*n_local+1]; */
+/*   send_counts:  [R][R] pairs from source s to destination rank r;         */
+/*   layout_stats: int64[8] = pairs local (s = r), intra-domain, inter-domain;  */
+/*                 their dispatch bytes (count * S_tok); pairs served by a    */
+/*                 replica (l >= E/R); 0.                                     */
+/* A dst_inst outside [0, R*n_local) is an argument error.                    */
+/* ------------------------------------------------------------------------ */
+
+int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok,
+                  int n_layers, const int32_t *dst_inst, int32_t *sorted_pairs,
+                  int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats) {
+    if (T < 0 || E < 1 || k < 1 || R < 1 || rpn < 1 || n_slot < 0) return ORC_EINVAL;
+    if (R % rpn != 0 || E % R != 0 || T % R != 0 || n_layers < 0) return ORC_EINVAL;
+    int E_R = E / R, n_local = E_R + n_slot, nkeys = R * n_local;
+    int tpr = T / R;
+    int64_t npairs = (int64_t)T * k;
+    int64_t *count = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nkeys + 1));
+    for (int l = 0; l < n_layers; l++) {
+        const int32_t *key = dst_inst + l * npairs;
+        int32_t *out = sorted_pairs + l * npairs;
+        int32_t *off = seg_off + (int64_t)l * (nkeys + 1);
+        int64_t *sc = send_counts + (int64_t)l * R * R;
+        int64_t *st = layout_stats + (int64_t)l * 8;
+        for (int64_t p = 0; p < npairs; p++)
+            if (key[p] < 0 || key[p] >= nkeys) { free(count); return ORC_EINVAL; }
+        /* counting sort: count, exclusive prefix, stable placement */
+        memset(count, 0, sizeof(int64_t) * (size_t)(nkeys + 1));
+        for (int64_t p = 0; p < npairs; p++) count[key[p]]++;
+        int64_t run = 0;
+        for (int i = 0; i < nkeys; i++) {
+            off[i] = (int32_t)run;
+            run += count[i];
+        }
+        off[nkeys] = (int32_t)run;
+        for (int i = 0; i < nkeys; i++) count[i] = off[i];
+        for (int64_t p = 0; p < npairs; p++) out[count[key[p]]++] = (int32_t)p;
+        /* send counts and locality */
+        memset(sc, 0, sizeof(int64_t) * (size_t)R * R);
+        memset(st, 0, sizeof(int64_t) * 8);
+        for (int64_t p = 0; p < npairs; p++) {
+            int s = (int)((p / k) / tpr);
+            int r = key[p] / n_local, li = key[p] % n_local;
+            sc[(int64_t)s * R + r]++;
+            if (s == r) st[0]++;
+            else if (s / rpn == r / rpn) st[1]++;
+            else st[2]++;
+            if (li >= E_R) st[6]++;
+        }
+        st[3] = st[0] * S_tok;
+        st[4] = st[1] * S_tok;
+        st[5] = st[2] * S_tok;
+        st[7] = 0;
+    }
+    free(count);
+    return ORC_OK;
+}
