@@ -1,0 +1,199 @@
+/*
+ * topo.h -- C ABI of the GB300 topology-aware expert-routing plan library
+ * (libtopoep.so, sm_103a).
+ *
+ * The library turns one MoE layer's Top-k routing result (T tokens x k int32
+ * expert ids) into a deterministic, topology-aware expert-parallel plan, as
+ * defined in "TopoEP: Topology-Aware Load Balancing for Expert-Parallel MoE
+ * Training" (§4.1 system model, §4.2 constraints C1-C5, §4.3 two-stage solver)
+ * and, for the correlation statistics, "Expert Coupling in MoE Pretraining".
+ *
+ * Model.  R expert-parallel ranks form M = R / ranks_per_node NVLink domains
+ * (dom(r) = r / ranks_per_node).  Token t of a layer belongs to source rank
+ * src(t) = t / (T / R) (equal contiguous blocks).  Pair p = t*k + j is the
+ * j-th expert choice of token t.  Expert e has its main instance on rank
+ * main(e) (= e / (E/R) by default, or main_rank[e]) with local index l < E/R
+ * (ascending e among the rank's mains); each rank also has n_slot replica
+ * slots, local indices E/R .. E/R+n_slot-1.  n_local = E/R + n_slot.  An
+ * instance is packed as r*n_local + l.  The per-byte communication cost is
+ * c(s,r) = 0 if s == r, c_intra inside a domain, c_inter across domains.
+ *
+ * Conventions for every call.
+ *   - Pointers named "device" are device memory; the caller allocates every
+ *     buffer, including the workspace ws.  The library never allocates,
+ *     frees or synchronises; each call only enqueues kernels on `stream`.
+ *   - n_layers independent problems (layers or microbatches) are handled per
+ *     call; array arguments are stacked with layer as the slowest dimension.
+ *   - Outputs are fully overwritten.
+ *   - Host-detectable problems return a negative code before anything is
+ *     enqueued.  Problems only the device can see (an id outside [0, E), a
+ *     workspace that does not hold what the call needs) set a sticky error
+ *     word in ws; outputs are then unspecified.  Read it with
+ *     topo_read_error after synchronising.  No kernel traps or asserts.
+ *   - All results are integers and are bit-for-bit deterministic.
+ *   - Thread safety: calls on distinct workspaces are independent.
+ */
+#ifndef TOPO_H
+#define TOPO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return / error-word codes. */
+#define TOPO_OK 0
+#define TOPO_EINVAL (-1)   /* bad argument: dimension, divisibility, NULL, range */
+#define TOPO_ENOSPC (-2)   /* ws_bytes smaller than topo_workspace_bytes() */
+#define TOPO_ECUDA (-3)    /* a CUDA runtime call or launch failed */
+#define TOPO_ERANGE (-4)   /* device: an expert id outside [0, E) */
+#define TOPO_ESTATE (-5)   /* device: ws does not hold the index this call needs */
+#define TOPO_EMAP (-6)     /* device: main_rank is not a balanced map onto [0, R) */
+
+/* Workspace needs per call (argument `which_call` of topo_workspace_bytes). */
+#define TOPO_CALL_HIST 0
+#define TOPO_CALL_PLAN 1
+#define TOPO_CALL_REROUTE 2
+#define TOPO_CALL_LAYOUT 3
+#define TOPO_CALL_COOCCUR 4
+#define TOPO_CALL_CHAIN 5   /* hist -> plan -> reroute -> dispatch_layout on one ws */
+
+#define TOPO_STATS 8        /* int64 plan statistics per layer */
+#define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
+
+/* Problem configuration (TopoEP §4.1: N_slot, C, S_tok, ||W_e||, main(e)). */
+typedef struct {
+    int32_t T;                /* tokens per layer; T % R == 0; T*k <= 2^31-1 */
+    int32_t E;                /* logical experts; E % R == 0 */
+    int32_t k;                /* expert choices per token (Top-k) */
+    int32_t R;                /* expert-parallel ranks; R % ranks_per_node == 0 */
+    int32_t ranks_per_node;   /* ranks per NVLink domain */
+    int32_t n_slot;           /* replica slots per rank (C3) */
+    int64_t tok_bytes;        /* S_tok: bytes of one routed activation (>= 0) */
+    int64_t expert_bytes;     /* ||W_e||: parameter bytes of one expert (>= 0) */
+    int32_t c_intra;          /* integer per-byte cost inside a domain, >= 1 */
+    int32_t c_inter;          /* integer per-byte cost across domains, >= c_intra */
+    int32_t max_refine_iters; /* cap on refinement commits per domain; 0 = none */
+    int32_t reserved;         /* must be 0 */
+    const int32_t *main_rank; /* device [E] main rank of each expert, or NULL for
+                                 e / (E/R); each rank must own exactly E/R mains */
+} topo_cfg;
+
+/* Plan outputs (TopoEP §4.2 decision variables x and q, loads U and L).
+ * All device pointers, caller-allocated, layer-major. */
+typedef struct {
+    int32_t *slot_expert;  /* [L][R][n_slot] expert in each replica slot, -1 empty
+                              (x_{e,r} for replicas; mains are implicit, C5) */
+    int32_t *route_cnt;    /* [L][R][R][n_local] q: assignments from source s
+                              executed on instance (r, l) */
+    int32_t *inst_load;    /* [L][R][n_local] U: load of each instance */
+    int32_t *rank_load;    /* [L][R] L_r: load of each rank */
+    int64_t *stats;        /* [L][TOPO_STATS]: 0 L_max, 1 L_max of the static
+                              placement, 2 replicas, 3 replicas from inter-node
+                              placement, 4 refinement commits, 5 T_token,
+                              6 T_replica (Eq. 7 in the integer cost units),
+                              7 sum_r L_r */
+} topo_plan_t;
+
+/* Bytes of workspace a call needs.  One workspace of
+ * topo_workspace_bytes(cfg, n_layers, TOPO_CALL_CHAIN) serves the whole chain
+ * hist -> plan -> reroute -> dispatch_layout; TOPO_CALL_COOCCUR needs only the
+ * header (cfg may then be NULL).  Returns 0 for an invalid cfg. */
+size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call);
+
+/* Clear the workspace header (error word, indices' fingerprints and
+ * counters).  Call once on a fresh workspace and after reading an error.
+ * ws: device, at least TOPO_CALL_COOCCUR bytes. */
+int topo_ws_reset(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Routing matrix Omega [TopoEP §4.1, Eq. 3]:
+ *   hist[l][s][e] = #pairs of layer l whose token belongs to source rank s
+ *                   and whose expert is e.
+ * ids:  device int32 [n_layers][T][k].
+ * hist: device int32 [n_layers][R][E].
+ * ws:   device; also receives the per-tile expert-count index that
+ *       topo_reroute and topo_dispatch_layout read for these ids.
+ * Device errors: TOPO_ERANGE (the id is skipped). */
+int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t *hist,
+              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Expert co-selection and cross-layer transition counts ["Expert Coupling in
+ * MoE Pretraining": within-layer correlation, cross-layer correlation]:
+ *   co[l][a][b] = sum_t n_t^l[a] * n_t^l[b]
+ *   tr[l][a][b] = sum_t n_t^l[a] * n_t^{l+1}[b]      (l < L-1)
+ * where n_t^l is the count vector of token t's ids at layer l (the diagonal
+ * of co is each expert's load).
+ * ids: device int32 [L][T][k]; co: device int64 [L][E][E];
+ * tr: device int64 [L-1][E][E] or NULL.  ws: >= TOPO_CALL_COOCCUR bytes.
+ * Device errors: TOPO_ERANGE. */
+int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids, int64_t *co,
+                 int64_t *tr, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Two-stage topology-aware replication plan [TopoEP §4.3, Eqs. 9-10], one per
+ * layer of hist (device int32 [n_layers][R][E]), following these rules:
+ *  1. Demand D_{d,e} = sum of hist rows of domain d (Eq. 4).
+ *  2. Inter-node placement (Eq. 9): per domain, experts whose main is outside
+ *     the domain with b = 2 D S_tok - ||W|| > 0, in descending b (ties: lower
+ *     e), each placed on the domain's rank with the fewest used slots (ties:
+ *     lower rank); the domain stops when its slots are full.
+ *  3. Routing: each (s, e) is split over e's instances in dom(s), or over all
+ *     of e's instances if dom(s) has none: floor share each, the remainder one
+ *     apiece to the first instances in ascending (c(s,r), r).
+ *  4. Intra-node refinement (Eq. 10): per domain, repeatedly take the busiest
+ *     rank r_b (ties: lower rank) and, over its experts e and the other ranks
+ *     r_t of the domain that host e or have a free slot, the move of
+ *     delta = min(U, floor((L_b - L_t)/2)) >= 1 assignments that is best by
+ *     (delta desc, L_t asc, cost asc, e asc, r_t asc), where the moved
+ *     assignments come from sources in ascending (c(s,r_t) - c(s,r_b), s) and
+ *     cost is the resulting change of T_token + T_replica (Eq. 7); stop when
+ *     r_b has no such move or after max_refine_iters commits.
+ * Outputs: *plan (all fields required).  ws: TOPO_CALL_PLAN bytes.
+ * Device errors: TOPO_EMAP. */
+int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const topo_plan_t *plan,
+              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Rerouting of every (token, slot) pair to an expert instance [TopoEP §1,
+ * Fig. 5 "token rerouting"; the rule is this library's reading]: within
+ * source s, the pairs selecting e are taken in ascending pair order and fill
+ * e's instances in ascending rank order, q[s][r][l] pairs each.
+ *   dst_inst[l][p] = r*n_local + l_inst.
+ * ids: device int32 [n_layers][T][k], the same ids (same pointer) that
+ * topo_hist indexed into this ws.  plan: from topo_plan (or any plan whose
+ * route_cnt rows sum to hist).  dst_inst: device int32 [n_layers][T*k].
+ * ws: TOPO_CALL_REROUTE bytes; receives the routing index that
+ * topo_dispatch_layout reads.  Device errors: TOPO_ESTATE (no index for these
+ * ids in ws), TOPO_ERANGE. */
+int topo_reroute(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, const topo_plan_t *plan,
+                 int32_t *dst_inst, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Dispatch layout [TopoEP §5: receive counts derived on the GPU; §2.3 Fig. 3
+ * byte accounting]:
+ *   sorted_pairs[l][pos]: pair indices stably sorted by dst_inst (gather form);
+ *   seg_off[l][i]: start of instance i's segment, [n_layers][R*n_local + 1];
+ *   send_counts[l][s][r]: pairs from source s to rank r, int64 [n_layers][R][R];
+ *   layout_stats[l][8]: pairs with s == r, same domain, other domain; their
+ *     dispatch bytes (pairs * tok_bytes); pairs served by a replica; 0.
+ * dst_inst must be topo_reroute's output for this plan on this ws (checked:
+ * TOPO_ESTATE otherwise).  All output pointers required. */
+int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst,
+                         const topo_plan_t *plan, int32_t *sorted_pairs, int32_t *seg_off,
+                         int64_t *send_counts, int64_t *layout_stats, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* Synchronous: copies the error word out of ws (device) and returns it
+ * (TOPO_OK or a negative code; TOPO_ECUDA if the copy fails).  Call after
+ * the stream that used ws has been synchronised. */
+int topo_read_error(const void *ws);
+
+/* Static description of a code. */
+const char *topo_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPO_H */

@@ -1,0 +1,94 @@
+// Internal definitions shared by the library's kernels and its C-ABI layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "topo.h"
+
+namespace topo {
+
+// Pairs per tile of the pair-scan kernels (hist, reroute, layout).  Tiles
+// never straddle a source rank's block of pairs.
+constexpr int kTile = 16384;
+constexpr int kScanThreads = 512;                  // threads of a tile CTA
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kWarpSeg = kTile / kScanWarps;       // pairs per warp in a tile
+constexpr int kMaxRanksPerNode = 32;               // one warp lane per rank of a domain
+
+// Workspace header, 256 bytes at offset 0 of every workspace.
+struct WsHeader {
+    int32_t error;       // first device error code, 0 if none
+    int32_t pad0;
+    uint64_t hist_fp;    // fingerprint of the tile index written by topo_hist
+    uint64_t route_fp;   // fingerprint of the routing index written by topo_reroute
+    uint64_t pad[29];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+// Geometry of one call, derived on the host and passed by value to kernels.
+struct Geo {
+    int32_t T, E, k, R, rpn, n_slot, M, E_R, n_local, L;
+    int32_t tps;            // tiles per source rank
+    int32_t n_inst_cap;     // E + R * n_slot: most instances a layer can hold
+    int32_t n_keys;         // R * n_local
+    int32_t c_intra, c_inter, max_iters;
+    int64_t pps;            // pairs per source rank
+    int64_t npairs;         // pairs per layer = T * k
+    int64_t S_tok, W;
+    // workspace regions (byte offsets)
+    size_t off_tile;        // int32 [L][R][tps][E]   tile counts -> exclusive prefix
+    size_t off_done;        // int32 [L][R]           tiles finished per source
+    size_t off_main;        // int32 [2E + R*E_R]     main(e), local index, mains[r][j]
+    size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
+    size_t off_iexp;        // int32 [L][n_keys]      expert held by each instance
+    size_t off_ioff;        // int32 [L][E+1]         instance list offsets by expert
+    size_t off_ilist;       // int32 [L][n_inst_cap]  instances, ascending rank per expert
+    size_t off_roff;        // int32 [L][R][E+1]      per-(s,e) entry offsets in row s
+    size_t off_rent;        // int4  [L][R][n_inst_cap] (inst, cum_start, cum_end, out_base)
+    size_t off_soff;        // int32 [L][R][n_keys]   column prefix of q over sources
+    size_t off_ccnt;        // int32 [L][n_keys]      column totals of q
+    size_t total;
+};
+
+__host__ __device__ inline int dom_of(int r, int rpn) { return r / rpn; }
+
+__host__ __device__ inline int64_t cost_sr(const Geo &g, int s, int r) {
+    if (s == r) return 0;
+    return (s / g.rpn == r / g.rpn) ? g.c_intra : g.c_inter;
+}
+
+// Record the first device error in the header (sticky).
+__device__ inline void set_error(WsHeader *h, int code) { atomicCAS(&h->error, 0, code); }
+
+// 64-bit fingerprint mixing (splitmix64 finaliser).
+__host__ __device__ inline uint64_t fp_mix(uint64_t h, uint64_t v) {
+    uint64_t z = h + 0x9e3779b97f4a7c15ull + v;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+template <typename T>
+__host__ __device__ inline T *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (defined in the kernel translation units).  Each returns
+// the cudaError_t of its launches.
+// ---------------------------------------------------------------------------
+cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *ws, uint64_t fp,
+                        cudaStream_t st);
+cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
+                        const topo_plan_t &p, void *ws, cudaStream_t st);
+cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
+                           const topo_plan_t &p, int32_t *dst, void *ws, uint64_t hist_fp,
+                           uint64_t route_part, cudaStream_t st);
+cudaError_t launch_layout(const Geo &g, const int32_t *dst, const topo_plan_t &p, int32_t *sorted,
+                          int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
+                          uint64_t route_part, cudaStream_t st);
+cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
+                           void *ws, cudaStream_t st);
+
+}  // namespace topo

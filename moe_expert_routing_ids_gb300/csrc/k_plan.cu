@@ -1,0 +1,455 @@
+// Two-stage topology-aware replication plan (TopoEP §4.3, Eqs. 9-10).
+//
+//   k_main_tables   main(e), its local index, and the experts of each rank
+//   k_plan_place    one CTA per (domain, layer): demand D (Eq. 4), benefit
+//                   b = 2 D S_tok - ||W|| (Eq. 9) and the inter-node placement
+//   k_plan_route    one CTA per (source, layer): the even split of omega_{s,e}
+//                   over the chosen instances; U and L by integer atomics
+//   k_plan_refine   one warp per (domain, layer): intra-node refinement (Eq. 10)
+//
+// Inter-node placement in closed form: every rank of a domain starts with no
+// used slot, so placing candidates one by one on the rank with the fewest used
+// slots (ties: lower rank) is a round robin -- the i-th candidate in
+// descending-benefit order lands on rank d*rpn + i % rpn, slot i / rpn, while
+// i < rpn * n_slot.  The kernel ranks candidates and applies that directly.
+//
+// Refinement cost in closed form: with a two-level cost matrix only three
+// sources change cost when assignments move from r_b to r_t in one domain --
+// r_t's own tokens (-c_intra), r_b's own tokens (+c_intra), everyone else 0 --
+// so a candidate's cost needs only q[r_t][r_b][l], q[r_b][r_b][l] and U, which
+// the warp keeps in shared memory for the domain's own sources.
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace topo {
+namespace {
+
+__device__ __forceinline__ int64_t block_sum64(int64_t v, int64_t *red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    int64_t t = 0;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// main(e), local index of e on main(e), and mains[r][j] (ascending e).
+__global__ void k_main_tables(const int32_t *__restrict__ main_rank, int32_t *tab, int64_t *stats,
+                              int n_stats, WsHeader *hdr, Geo g) {
+    extern __shared__ int own[];
+    __shared__ int bad;
+    const int E = g.E, R = g.R, ER = g.E_R;
+    int32_t *main_of = tab, *main_l = tab + E, *mains = tab + 2 * E;
+    for (int i = threadIdx.x; i < n_stats; i += blockDim.x) stats[i] = 0;
+    if (threadIdx.x == 0) {
+        bad = 0;
+        if (stats) hdr->route_fp = 0;   // a new plan makes any routing index stale
+    }
+    for (int r = threadIdx.x; r < R; r += blockDim.x) own[r] = 0;
+    __syncthreads();
+    if (main_rank) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            int r = main_rank[e];
+            if (r < 0 || r >= R) bad = 1;
+            else atomicAdd(&own[r], 1);
+        }
+        __syncthreads();
+        for (int r = threadIdx.x; r < R; r += blockDim.x)
+            if (own[r] != ER) bad = 1;
+        __syncthreads();
+        if (!bad) {
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
+                const int r = main_rank[e];
+                int li = 0;
+                for (int x = 0; x < e; ++x) li += (main_rank[x] == r);
+                main_of[e] = r;
+                main_l[e] = li;
+                mains[r * ER + li] = e;
+            }
+            return;
+        }
+        if (threadIdx.x == 0) set_error(hdr, TOPO_EMAP);
+    }
+    // contiguous map (also the in-bounds fallback after TOPO_EMAP)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        main_of[e] = e / ER;
+        main_l[e] = e % ER;
+        mains[e] = e;
+    }
+}
+
+__global__ void __launch_bounds__(512)
+k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, int32_t *slot_expert,
+             int32_t *rep, int32_t *inst_load, int32_t *rank_load, int64_t *stats, Geo g) {
+    extern __shared__ long long keyv[];          // [E] benefit, LLONG_MIN if not a candidate
+    __shared__ int ncand;
+    __shared__ int64_t red[32];
+    __shared__ int stat_load[kMaxRanksPerNode];
+    const int d = blockIdx.x, l = blockIdx.y;
+    const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local;
+    const int32_t *main_of = tab, *mains = tab + 2 * E;
+    const int32_t *H = hist + (int64_t)l * R * E;
+    if (threadIdx.x == 0) ncand = 0;
+    if (threadIdx.x < rpn) stat_load[threadIdx.x] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int64_t D = 0;
+        for (int j = 0; j < rpn; ++j) D += H[(int64_t)(d * rpn + j) * E + e];
+        const int64_t b = 2 * D * g.S_tok - g.W;
+        const bool cand = (main_of[e] / rpn != d) && b > 0;
+        keyv[e] = cand ? (long long)b : LLONG_MIN;
+        if (cand) atomicAdd(&ncand, 1);
+    }
+    int32_t *SE = slot_expert + (int64_t)l * R * ns;
+    for (int i = threadIdx.x; i < rpn * ns; i += blockDim.x) SE[(int64_t)d * rpn * ns + i] = -1;
+    __syncthreads();
+    const int cap = rpn * ns;
+    int64_t repcost = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t code = -1;
+        const long long b = keyv[e];
+        if (b != LLONG_MIN) {
+            int rank = 0;
+            for (int x = 0; x < E; ++x) {
+                const long long bx = keyv[x];
+                rank += (bx > b) || (bx == b && x < e);
+            }
+            if (rank < cap) {
+                const int r = d * rpn + rank % rpn, slot = rank / rpn;
+                SE[(int64_t)r * ns + slot] = e;
+                code = r * nl + g.E_R + slot;
+                repcost += cost_sr(g, main_of[e], r) * g.W;
+            }
+        }
+        rep[((int64_t)l * E + e) * g.M + d] = code;
+    }
+    // static loads of the domain's ranks (mains only) and zeroed U, L
+    for (int i = threadIdx.x; i < rpn * g.E_R; i += blockDim.x) {
+        const int j = i / g.E_R, r = d * rpn + j;
+        const int e = mains[r * g.E_R + i % g.E_R];
+        int load = 0;
+        for (int s = 0; s < R; ++s) load += H[(int64_t)s * E + e];
+        atomicAdd(&stat_load[j], load);
+    }
+    for (int i = threadIdx.x; i < rpn * nl; i += blockDim.x)
+        inst_load[((int64_t)l * R + d * rpn) * nl + i] = 0;
+    for (int j = threadIdx.x; j < rpn; j += blockDim.x) rank_load[(int64_t)l * R + d * rpn + j] = 0;
+    const int64_t tot = block_sum64(repcost, red);
+    if (threadIdx.x < rpn)
+        atomicMax(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 1]),
+                  (unsigned long long)stat_load[threadIdx.x]);
+    if (threadIdx.x == 0) {
+        const int placed = ncand < cap ? ncand : cap;
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 3]),
+                  (unsigned long long)placed);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 6]),
+                  (unsigned long long)tot);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
+             const int32_t *__restrict__ rep, int32_t *q, int32_t *inst_load, int32_t *rank_load,
+             int64_t *stats, Geo g) {
+    __shared__ int64_t red[32];
+    const int s = blockIdx.x, l = blockIdx.y;
+    const int E = g.E, R = g.R, rpn = g.rpn, nl = g.n_local, M = g.M;
+    const int32_t *main_of = tab, *main_l = tab + E;
+    int32_t *row = q + ((int64_t)l * R + s) * R * nl;
+    int32_t *U = inst_load + (int64_t)l * R * nl;
+    int32_t *Lr = rank_load + (int64_t)l * R;
+    for (int i = threadIdx.x; i < R * nl; i += blockDim.x) row[i] = 0;
+    __syncthreads();
+    const int ds = s / rpn;
+    int64_t tok = 0, wsum = 0;
+    const int32_t *H = hist + ((int64_t)l * R + s) * E;
+    const int32_t *REP = rep + (int64_t)l * E * M;
+    auto emit = [&](int r, int li, int amt) {
+        if (amt <= 0) return;
+        row[r * nl + li] = amt;
+        atomicAdd(&U[r * nl + li], amt);
+        atomicAdd(&Lr[r], amt);
+        tok += cost_sr(g, s, r) * amt;
+    };
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int w = H[e];
+        if (w == 0) continue;
+        wsum += w;
+        const int me = main_of[e], dm = me / rpn;
+        if (dm == ds) { emit(me, main_l[e], w); continue; }
+        const int32_t *re = REP + (int64_t)e * M;
+        const int code = re[ds];
+        if (code >= 0) { emit(code / nl, code % nl, w); continue; }
+        // no instance in dom(s): every instance of e, in rank (= domain) order;
+        // all are cross-domain, so (c, r) order is rank order
+        int n = 1;
+        for (int d = 0; d < M; ++d) n += (d != dm && re[d] >= 0);
+        const int base = w / n, rem = w % n;
+        int i = 0;
+        for (int d = 0; d < M; ++d) {
+            int r, li;
+            if (d == dm) { r = me; li = main_l[e]; }
+            else if (re[d] >= 0) { r = re[d] / nl; li = re[d] % nl; }
+            else continue;
+            emit(r, li, base + (i < rem ? 1 : 0));
+            ++i;
+        }
+    }
+    const int64_t t = block_sum64(tok, red);
+    const int64_t ws = block_sum64(wsum, red);
+    if (threadIdx.x == 0) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 5]),
+                  (unsigned long long)(2 * g.S_tok * t));
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 7]),
+                  (unsigned long long)ws);
+    }
+}
+
+struct Key {
+    unsigned long long a, b, c;   // lexicographic, larger is better; a == 0: none
+};
+
+__device__ __forceinline__ bool key_gt(const Key &x, const Key &y) {
+    if (x.a != y.a) return x.a > y.a;
+    if (x.b != y.b) return x.b > y.b;
+    return x.c > y.c;
+}
+
+__device__ __forceinline__ Key warp_max_key(Key k) {
+    for (int o = 16; o > 0; o >>= 1) {
+        Key y;
+        y.a = __shfl_xor_sync(0xffffffffu, k.a, o);
+        y.b = __shfl_xor_sync(0xffffffffu, k.b, o);
+        y.c = __shfl_xor_sync(0xffffffffu, k.c, o);
+        if (key_gt(y, k)) k = y;
+    }
+    return k;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
+// One warp refines one domain of one layer.
+__global__ void __launch_bounds__(32)
+k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
+              int32_t *rank_load, int64_t *stats, Geo g) {
+    extern __shared__ int sm[];
+    const int d = blockIdx.x, l = blockIdx.y, lane = threadIdx.x;
+    const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
+    const int32_t *main_of = tab, *mains = tab + 2 * E;
+    int *Lr = sm;                               // [rpn]
+    int *used = Lr + rpn;                       // [rpn]
+    int *U = used + rpn;                        // [rpn][nl]
+    int *xe = U + rpn * nl;                     // [rpn][nl] expert of each instance
+    int *qloc = xe + rpn * nl;                  // [rpn src][rpn dst][nl]
+    short *hl = reinterpret_cast<short *>(qloc + rpn * rpn * nl);   // [rpn][E] local index or -1
+    const int r0 = d * rpn;
+    int32_t *Q = q + (int64_t)l * R * R * nl;
+    int32_t *SE = slot_expert + (int64_t)l * R * ns;
+
+    for (int j = lane; j < rpn; j += 32) Lr[j] = rank_load[(int64_t)l * R + r0 + j];
+    for (int i = lane; i < rpn * E; i += 32) hl[i] = -1;
+    __syncwarp();
+    for (int i = lane; i < rpn * nl; i += 32) {
+        const int j = i / nl, li = i % nl, r = r0 + j;
+        U[i] = inst_load[((int64_t)l * R + r) * nl + li];
+        const int e = li < ER ? mains[r * ER + li] : SE[(int64_t)r * ns + (li - ER)];
+        xe[i] = e;
+        if (e >= 0) hl[j * E + e] = (short)li;
+    }
+    for (int j = lane; j < rpn; j += 32) {
+        int u = 0;
+        while (u < ns && SE[(int64_t)(r0 + j) * ns + u] >= 0) ++u;
+        used[j] = u;
+    }
+    for (int i = lane; i < rpn * rpn * nl; i += 32) {
+        const int js = i / (rpn * nl), jd = (i / nl) % rpn, li = i % nl;
+        qloc[i] = Q[((int64_t)(r0 + js) * R + (r0 + jd)) * nl + li];
+    }
+    __syncwarp();
+
+    int iters = 0;
+    int64_t tokd = 0, repd = 0;
+    const int ncand = nl * rpn;
+    // Each commit lowers sum L^2 by at least 2, so the loop ends; the hard cap
+    // only guards against a corrupted input state.
+    constexpr int kHardCap = 1 << 24;
+    while ((g.max_iters == 0 || iters < g.max_iters) && iters < kHardCap) {
+        // busiest rank, lowest index on ties
+        int bv = lane < rpn ? Lr[lane] : -1, bj = lane;
+        for (int o = 16; o > 0; o >>= 1) {
+            const int ov = __shfl_xor_sync(0xffffffffu, bv, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
+            if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        const int jb = bj, Lb = bv;
+        Key best{0ull, 0ull, 0ull};
+        for (int c = lane; c < ncand; c += 32) {
+            const int lb = c / rpn, jt = c % rpn;
+            if (jt == jb) continue;
+            const int Ub = U[jb * nl + lb];
+            if (Ub <= 0) continue;
+            const int e = xe[jb * nl + lb];
+            if (e < 0) continue;
+            const int lt = hl[jt * E + e];
+            const bool is_new = lt < 0;
+            if (is_new && used[jt] >= ns) continue;
+            const int Lt = Lr[jt];
+            const int half = (Lb - Lt) >> 1;
+            const int delta = Ub < half ? Ub : half;
+            if (delta < 1) continue;
+            const int q_rt = qloc[(jt * rpn + jb) * nl + lb];
+            const int q_rb = qloc[(jb * rpn + jb) * nl + lb];
+            const int m_rt = q_rt < delta ? q_rt : delta;
+            const int rest = delta - m_rt;
+            const int others = Ub - q_rt - q_rb;
+            const int m_o = others < rest ? others : rest;
+            const int m_rb = rest - m_o;
+            const int64_t cst = 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt) +
+                                (is_new ? cost_sr(g, main_of[e], r0 + jt) * g.W : 0);
+            Key k;
+            k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)Lt);
+            k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
+            k.c = ~(((unsigned long long)e << 32) | (unsigned)jt);
+            if (key_gt(k, best)) best = k;
+        }
+        best = warp_max_key(best);
+        if (best.a == 0) break;
+        // commit
+        const int delta = (int)(best.a >> 32);
+        const int e = (int)((~best.c) >> 32);
+        const int jt = (int)(unsigned)(~best.c);
+        const int lb = hl[jb * E + e];
+        const int rb = r0 + jb, rt = r0 + jt;
+        int lt = hl[jt * E + e];
+        const bool is_new = lt < 0;
+        if (is_new) lt = ER + used[jt];
+        const int m_rt = min(qloc[(jt * rpn + jb) * nl + lb], delta);
+        int remaining = delta - m_rt;
+        __syncwarp();
+        if (is_new) {
+            repd += cost_sr(g, main_of[e], rt) * g.W;
+            if (lane == 0) {
+                used[jt] += 1;
+                hl[jt * E + e] = (short)lt;
+                xe[jt * nl + lt] = e;
+                SE[(int64_t)rt * ns + (lt - ER)] = e;
+            }
+        }
+        // other sources, ascending, skipping r_t and r_b
+        for (int base = 0; base < R && remaining > 0; base += 32) {
+            const int s = base + lane;
+            int32_t *pb = Q + ((int64_t)s * R + rb) * nl + lb;
+            int32_t *pt = Q + ((int64_t)s * R + rt) * nl + lt;
+            const int v = (s < R && s != rt && s != rb) ? *pb : 0;
+            const int incl = warp_incl_scan(v);
+            const int excl = incl - v;
+            int take = remaining - excl;
+            take = take < 0 ? 0 : (take > v ? v : take);
+            if (take > 0) {
+                *pb -= take;
+                *pt += take;
+                if (s >= r0 && s < r0 + rpn) {
+                    const int js = s - r0;
+                    qloc[(js * rpn + jb) * nl + lb] -= take;
+                    qloc[(js * rpn + jt) * nl + lt] += take;
+                }
+            }
+            const int tot = __shfl_sync(0xffffffffu, incl, 31);
+            remaining -= tot < remaining ? tot : remaining;
+        }
+        const int m_rb = remaining;
+        __syncwarp();
+        if (lane == 0) {
+            if (m_rt > 0) {
+                Q[((int64_t)rt * R + rb) * nl + lb] -= m_rt;
+                Q[((int64_t)rt * R + rt) * nl + lt] += m_rt;
+                qloc[(jt * rpn + jb) * nl + lb] -= m_rt;
+                qloc[(jt * rpn + jt) * nl + lt] += m_rt;
+            }
+            if (m_rb > 0) {
+                Q[((int64_t)rb * R + rb) * nl + lb] -= m_rb;
+                Q[((int64_t)rb * R + rt) * nl + lt] += m_rb;
+                qloc[(jb * rpn + jb) * nl + lb] -= m_rb;
+                qloc[(jb * rpn + jt) * nl + lt] += m_rb;
+            }
+            U[jb * nl + lb] -= delta;
+            U[jt * nl + lt] += delta;
+            Lr[jb] -= delta;
+            Lr[jt] += delta;
+        }
+        tokd += 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt);
+        ++iters;
+        __syncwarp();
+    }
+    // write back the domain's loads and statistics
+    for (int j = lane; j < rpn; j += 32) rank_load[(int64_t)l * R + r0 + j] = Lr[j];
+    for (int i = lane; i < rpn * nl; i += 32) inst_load[((int64_t)l * R + r0) * nl + i] = U[i];
+    int lmax = lane < rpn ? Lr[lane] : 0, nused = lane < rpn ? used[lane] : 0;
+    for (int o = 16; o > 0; o >>= 1) {
+        lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+        nused += __shfl_xor_sync(0xffffffffu, nused, o);
+    }
+    if (lane == 0) {
+        int64_t *st = stats + l * TOPO_STATS;
+        atomicMax(reinterpret_cast<unsigned long long *>(&st[0]), (unsigned long long)lmax);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&st[2]), (unsigned long long)nused);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&st[4]), (unsigned long long)iters);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&st[5]), (unsigned long long)tokd);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&st[6]), (unsigned long long)repd);
+    }
+}
+
+}  // namespace
+
+size_t refine_smem_bytes(const Geo &g) {
+    return (size_t)(2 * g.rpn + 2 * g.rpn * g.n_local + g.rpn * g.rpn * g.n_local) * 4 +
+           (size_t)g.rpn * g.E * 2;
+}
+
+cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
+                               int n_stats, cudaStream_t st) {
+    k_main_tables<<<1, 1024, (size_t)g.R * 4, st>>>(main_rank, ws_at<int32_t>(ws, g.off_main), stats,
+                                                   n_stats, ws_at<WsHeader>(ws, 0), g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
+                        const topo_plan_t &p, void *ws, cudaStream_t st) {
+    cudaError_t e;
+    const int32_t *tab = ws_at<int32_t>(ws, g.off_main);
+    int32_t *rep = ws_at<int32_t>(ws, g.off_rep);
+    if ((e = launch_main_tables(g, main_rank, ws, p.stats, g.L * TOPO_STATS, st)) != cudaSuccess)
+        return e;
+    const size_t smem_place = (size_t)g.E * 8;
+    if (smem_place > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(k_plan_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem_place)) != cudaSuccess)
+        return e;
+    k_plan_place<<<dim3(g.M, g.L), 512, smem_place, st>>>(hist, tab, p.slot_expert, rep, p.inst_load,
+                                                          p.rank_load, p.stats, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_plan_route<<<dim3(g.R, g.L), 256, 0, st>>>(hist, tab, rep, p.route_cnt, p.inst_load, p.rank_load,
+                                                p.stats, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t smem_ref = refine_smem_bytes(g);
+    if (smem_ref > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(k_plan_refine, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem_ref)) != cudaSuccess)
+        return e;
+    k_plan_refine<<<dim3(g.M, g.L), 32, smem_ref, st>>>(tab, p.slot_expert, p.route_cnt, p.inst_load,
+                                                        p.rank_load, p.stats, g);
+    return cudaGetLastError();
+}
+
+}  // namespace topo

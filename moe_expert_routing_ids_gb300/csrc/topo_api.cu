@@ -1,0 +1,192 @@
+// C-ABI entry points: argument validation, workspace layout, launches.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstring>
+
+#include "common.cuh"
+
+using namespace topo;
+
+namespace {
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Validates cfg and fills the geometry (including the workspace layout).
+int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
+    if (!c || n_layers < 0) return TOPO_EINVAL;
+    if (c->T < 0 || c->E < 1 || c->k < 1 || c->R < 1 || c->ranks_per_node < 1 || c->n_slot < 0)
+        return TOPO_EINVAL;
+    if (c->ranks_per_node > kMaxRanksPerNode) return TOPO_EINVAL;
+    if (c->R % c->ranks_per_node || c->E % c->R || c->T % c->R) return TOPO_EINVAL;
+    if ((int64_t)c->T * c->k > INT32_MAX) return TOPO_EINVAL;
+    if (c->tok_bytes < 0 || c->expert_bytes < 0 || c->c_intra < 1 || c->c_inter < c->c_intra)
+        return TOPO_EINVAL;
+    if (c->max_refine_iters < 0 || c->reserved != 0) return TOPO_EINVAL;
+    // keep every int64 cost product exact: S_tok*c < 2^31, ||W||*c < 2^40
+    if (c->tok_bytes * (int64_t)c->c_inter >= (int64_t(1) << 31)) return TOPO_EINVAL;
+    if (c->expert_bytes * (int64_t)c->c_inter >= (int64_t(1) << 40)) return TOPO_EINVAL;
+    if ((int64_t)c->R * c->n_slot > (1 << 20)) return TOPO_EINVAL;
+    // shared-memory capacity of the kernels (227 KB per CTA on sm_103a)
+    const int64_t kSmem = 227 * 1024, E = c->E, R = c->R, rpn = c->ranks_per_node;
+    const int64_t nl = E / R + c->n_slot;
+    if (nl > 32767) return TOPO_EINVAL;
+    if ((int64_t)kTile * 4 + (int64_t)kScanWarps * E * 4 > kSmem) return TOPO_EINVAL;
+    if (E * ((R + 31) / 32 + 1) * 4 > kSmem) return TOPO_EINVAL;
+    if ((2 * rpn + 2 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmem) return TOPO_EINVAL;
+    std::memset(g, 0, sizeof *g);
+    g->T = c->T; g->E = c->E; g->k = c->k; g->R = c->R; g->rpn = c->ranks_per_node;
+    g->n_slot = c->n_slot; g->M = c->R / c->ranks_per_node; g->E_R = c->E / c->R;
+    g->n_local = g->E_R + c->n_slot; g->L = n_layers;
+    g->c_intra = c->c_intra; g->c_inter = c->c_inter; g->max_iters = c->max_refine_iters;
+    g->S_tok = c->tok_bytes; g->W = c->expert_bytes;
+    g->pps = (int64_t)(c->T / c->R) * c->k;
+    g->npairs = (int64_t)c->T * c->k;
+    g->tps = g->pps == 0 ? 1 : (int32_t)((g->pps + kTile - 1) / kTile);
+    g->n_inst_cap = c->E + c->R * c->n_slot;
+    g->n_keys = c->R * g->n_local;
+    const size_t L = (size_t)n_layers;
+    size_t off = sizeof(WsHeader);
+    g->off_tile = off;  off = align_up(off + L * R * g->tps * E * 4);
+    g->off_done = off;  off = align_up(off + L * R * 4);
+    g->off_main = off;  off = align_up(off + 3 * E * 4);
+    g->off_rep = off;   off = align_up(off + L * E * g->M * 4);
+    g->off_iexp = off;  off = align_up(off + L * g->n_keys * 4);
+    g->off_ioff = off;  off = align_up(off + L * (E + 1) * 4);
+    g->off_ilist = off; off = align_up(off + L * g->n_inst_cap * 4);
+    g->off_roff = off;  off = align_up(off + L * R * (E + 1) * 4);
+    g->off_rent = off;  off = align_up(off + L * R * g->n_inst_cap * 16);
+    g->off_soff = off;  off = align_up(off + L * R * g->n_keys * 4);
+    g->off_ccnt = off;  off = align_up(off + L * g->n_keys * 4);
+    g->total = off;
+    return TOPO_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? TOPO_OK : TOPO_ECUDA; }
+
+uint64_t hist_fingerprint(const Geo &g, const int32_t *ids) {
+    uint64_t h = fp_mix(0x48495354ull, (uint64_t)g.T);
+    h = fp_mix(h, (uint64_t)g.E);
+    h = fp_mix(h, (uint64_t)g.k);
+    h = fp_mix(h, (uint64_t)g.R);
+    h = fp_mix(h, (uint64_t)g.L);
+    h = fp_mix(h, (uint64_t)g.tps);
+    return fp_mix(h, (uint64_t)(uintptr_t)ids);
+}
+
+// Part of the routing-index fingerprint that does not depend on ws contents;
+// the device mixes it with the stored hist fingerprint.
+uint64_t route_fingerprint(const Geo &g, const topo_plan_t &p, const int32_t *dst,
+                           const int32_t *main_rank) {
+    uint64_t h = fp_mix(0x524f5554ull, (uint64_t)g.n_slot);
+    h = fp_mix(h, (uint64_t)g.rpn);
+    h = fp_mix(h, (uint64_t)(uintptr_t)p.slot_expert);
+    h = fp_mix(h, (uint64_t)(uintptr_t)p.route_cnt);
+    h = fp_mix(h, (uint64_t)(uintptr_t)p.inst_load);
+    h = fp_mix(h, (uint64_t)(uintptr_t)main_rank);
+    return fp_mix(h, (uint64_t)(uintptr_t)dst);
+}
+
+bool plan_ok(const topo_plan_t *p) {
+    return p && p->slot_expert && p->route_cnt && p->inst_load && p->rank_load && p->stats;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call) {
+    if (which_call == TOPO_CALL_COOCCUR) return sizeof(WsHeader);
+    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_CHAIN) return 0;
+    Geo g;
+    if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
+    return g.total;
+}
+
+int topo_ws_reset(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!ws || ws_bytes < sizeof(WsHeader)) return TOPO_EINVAL;
+    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(WsHeader), stream));
+}
+
+int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t *hist, void *ws,
+              size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!hist || !ws || (!ids && g.npairs > 0 && n_layers > 0)) return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream));
+}
+
+int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const topo_plan_t *plan,
+              void *ws, size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!hist || !ws || !plan_ok(plan)) return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_plan(g, cfg->main_rank, hist, *plan, ws, stream));
+}
+
+int topo_reroute(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, const topo_plan_t *plan,
+                 int32_t *dst_inst, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!ws || !plan_ok(plan) || ((!ids || !dst_inst) && g.npairs > 0 && n_layers > 0))
+        return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_reroute(g, cfg->main_rank, ids, *plan, dst_inst, ws, hist_fingerprint(g, ids),
+                                  route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
+}
+
+int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst,
+                         const topo_plan_t *plan, int32_t *sorted_pairs, int32_t *seg_off,
+                         int64_t *send_counts, int64_t *layout_stats, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!ws || !plan_ok(plan) || !seg_off || !send_counts || !layout_stats) return TOPO_EINVAL;
+    if ((!dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_layout(g, dst_inst, *plan, sorted_pairs, seg_off, send_counts, layout_stats,
+                                 ws, route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
+}
+
+int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids, int64_t *co,
+                 int64_t *tr, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (L < 0 || T < 0 || E < 1 || k < 1 || !ws) return TOPO_EINVAL;
+    if ((int64_t)T * k > INT32_MAX || (int64_t)E * E > INT32_MAX) return TOPO_EINVAL;
+    if (L > 0 && !co) return TOPO_EINVAL;
+    if (L > 0 && T > 0 && !ids) return TOPO_EINVAL;
+    if (ws_bytes < sizeof(WsHeader)) return TOPO_ENOSPC;
+    if (L == 0) return TOPO_OK;
+    return cuda_rc(launch_cooccur(L, T, E, k, ids, co, L > 1 ? tr : nullptr, ws, stream));
+}
+
+int topo_read_error(const void *ws) {
+    if (!ws) return TOPO_EINVAL;
+    int32_t e = 0;
+    if (cudaMemcpy(&e, ws, sizeof e, cudaMemcpyDeviceToHost) != cudaSuccess) return TOPO_ECUDA;
+    return e;
+}
+
+const char *topo_strerror(int code) {
+    switch (code) {
+        case TOPO_OK: return "ok";
+        case TOPO_EINVAL: return "invalid argument";
+        case TOPO_ENOSPC: return "workspace too small";
+        case TOPO_ECUDA: return "CUDA runtime error";
+        case TOPO_ERANGE: return "expert id outside [0, E)";
+        case TOPO_ESTATE: return "workspace does not hold the index this call needs";
+        case TOPO_EMAP: return "main_rank is not a balanced map onto the ranks";
+        default: return "unknown error";
+    }
+}
+
+}  // extern "C"

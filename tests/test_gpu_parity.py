@@ -1,0 +1,240 @@
+"""GPU parity: every output of the CUDA path equals the CPU oracle bit for bit.
+
+All calls go through the C ABI (ctypes binding).  Integer work, so the bar is
+exact equality.  Covers the five named workloads at full size and edge cases:
+empty input, ragged and unaligned tiles, several tiles per source, one expert
+per rank, no replica slots, one domain, all ids equal, free and prohibitive
+replicas, a main-rank map, an iteration cap, the widest domain, k = 1.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from moe_expert_routing_ids_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def gpu_chain(cfg, ids):
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    L = ids.shape[0]
+    mr = cfg.get("main_rank")
+    gcfg = dict(cfg, main_rank=None if mr is None else torch.as_tensor(mr, dtype=torch.int32, device=dev))
+    P = Planner(gcfg, L, dev)
+    d_ids = torch.as_tensor(ids, device=dev).contiguous()
+    P.run(d_ids)
+    err = P.error()
+    out = P.numpy()
+    return out, err
+
+
+def oracle_chain(cfg, ids):
+    L = ids.shape[0]
+    h = oracle.hist(ids, cfg["R"], cfg["E"])
+    p = oracle.plan(cfg, h)
+    d = oracle.reroute(cfg, ids, p)
+    sp, so, sc, st = oracle.layout(cfg, d)
+    return dict(hist=h, slot_expert=p["slot_expert"], route_cnt=p["route_cnt"],
+                inst_load=p["inst_load"], rank_load=p["rank_load"], stats=p["stats"],
+                dst_inst=d, sorted_pairs=sp, seg_off=so, send_counts=sc, layout_stats=st)
+
+
+def assert_same(gpu, orc, keys=None):
+    for key in keys or orc:
+        a, b = np.asarray(gpu[key]), np.asarray(orc[key])
+        assert a.shape == b.shape, (key, a.shape, b.shape)
+        if not np.array_equal(a, b):
+            idx = np.argwhere(a != b)
+            first = tuple(idx[0])
+            raise AssertionError(f"{key}: {len(idx)} mismatches, first at {first}: gpu {a[first]} "
+                                 f"oracle {b[first]}")
+
+
+def check(cfg, ids):
+    gpu, err = gpu_chain(cfg, ids)
+    assert err == 0, f"device error {err}"
+    assert_same(gpu, oracle_chain(cfg, ids))
+    return gpu
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 5])
+def test_named_workloads_full_size(index):
+    w = W.CONFIGS[index]
+    check(w.plan_cfg, w.ids())
+
+
+def _cfg(T, E, k, R, rpn, ns, S=2048, Wb=4_718_592, **kw):
+    return dict(T=T, E=E, k=k, R=R, ranks_per_node=rpn, n_slot=ns, tok_bytes=S, expert_bytes=Wb,
+                c_intra=1, c_inter=4, max_refine_iters=0, main_rank=None, **kw)
+
+
+EDGE = {
+    # name: (cfg, ids-maker)
+    "unaligned_tiles": (_cfg(8 * 1001, 16, 3, 8, 4, 2, S=64, Wb=10_000),
+                        lambda c: W.random_small(1, c["T"], c["E"], c["k"], 2, s=1.3)),
+    "multi_tile_ragged": (_cfg(2 * 10001, 8, 4, 2, 2, 3, S=64, Wb=1000),
+                          lambda c: W.random_small(2, c["T"], c["E"], c["k"], 1, s=1.5)),
+    "many_tiles_per_source": (_cfg(8 * 20000, 32, 5, 8, 2, 4, S=128, Wb=50_000),
+                              lambda c: W.random_small(3, c["T"], c["E"], c["k"], 2, s=1.2)),
+    "empty": (_cfg(0, 8, 2, 4, 2, 1), lambda c: np.zeros((1, 0, 2), np.int32)),
+    "one_expert_per_rank_k1": (_cfg(4000, 8, 1, 8, 4, 2, S=256, Wb=1000),
+                               lambda c: W.random_small(4, c["T"], c["E"], c["k"], 1, s=1.1)),
+    "no_slots": (_cfg(4000, 16, 3, 8, 4, 0, S=256, Wb=1000),
+                 lambda c: W.random_small(5, c["T"], c["E"], c["k"], 1, s=1.3)),
+    "single_domain": (_cfg(6000, 32, 4, 8, 8, 3, S=256, Wb=0),
+                      lambda c: W.random_small(6, c["T"], c["E"], c["k"], 1, s=1.6)),
+    "all_ids_equal": (_cfg(4096, 8, 1, 8, 2, 2, S=64, Wb=100),
+                      lambda c: np.full((1, c["T"], 1), 5, np.int32)),
+    "free_replicas": (_cfg(8000, 32, 4, 8, 2, 4, S=256, Wb=0),
+                      lambda c: W.random_small(7, c["T"], c["E"], c["k"], 1, s=1.0)),
+    "prohibitive_replicas": (_cfg(8000, 32, 4, 8, 2, 4, S=1, Wb=1 << 36),
+                             lambda c: W.random_small(8, c["T"], c["E"], c["k"], 1, s=1.4)),
+    "iteration_cap": (_cfg(8000, 32, 4, 16, 4, 4, S=256, Wb=10_000, ),
+                      lambda c: W.random_small(9, c["T"], c["E"], c["k"], 1, s=1.4)),
+    "widest_domain": (_cfg(64 * 300, 128, 6, 64, 32, 6, S=512, Wb=200_000),
+                      lambda c: W.random_small(10, c["T"], c["E"], c["k"], 1, s=1.2)),
+    "tiny": (_cfg(2, 2, 1, 2, 1, 1, S=1, Wb=1), lambda c: np.array([[[1], [1]]], np.int32)),
+    "three_layers": (_cfg(16 * 700, 64, 6, 16, 8, 8, S=8192, Wb=34_603_008),
+                     lambda c: W.random_small(11, c["T"], c["E"], c["k"], 3, s=1.2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(name):
+    cfg, mk = EDGE[name]
+    cfg = dict(cfg)
+    if name == "iteration_cap":
+        cfg["max_refine_iters"] = 1
+    check(cfg, mk(cfg))
+
+
+def test_main_rank_map():
+    cfg = _cfg(8 * 900, 32, 4, 8, 4, 3, S=256, Wb=20_000)
+    cfg["main_rank"] = (W.rng_for(21, 0).permutation(32) % 8).astype(np.int32)
+    check(cfg, W.random_small(12, cfg["T"], cfg["E"], cfg["k"], 2, s=1.3))
+
+
+def test_repeat_runs_are_byte_identical():
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    w = W.CONFIGS[2]
+    ids = torch.as_tensor(w.ids(), device=dev)
+    P = Planner(w.plan_cfg, w.n_layers, dev)
+    P.run(ids)
+    ref = P.numpy()
+    for _ in range(9):
+        P.run(ids)
+        again = P.numpy()
+        for key in ref:
+            assert np.array_equal(ref[key], again[key]), key
+    assert P.error() == 0
+
+
+# ---------------------------------------------------------------- co-occurrence
+
+def gpu_cooccur(ids, E, transitions=True):
+    from moe_expert_routing_ids_gb300.planner import Cooccur
+    dev = _dev()
+    L, T, k = ids.shape
+    C = Cooccur(L, T, E, k, dev, transitions)
+    C.run(torch.as_tensor(ids, device=dev).contiguous())
+    err = C.error()
+    co = C.co.cpu().numpy()
+    tr = C.tr.cpu().numpy() if C.tr is not None else None
+    return co, tr, err
+
+
+def test_cooccur_full_size():
+    w = W.CONFIGS[4]
+    ids = w.ids()
+    co, tr, err = gpu_cooccur(ids, w.E)
+    assert err == 0
+    oco, otr = oracle.cooccur(ids, w.E)
+    assert np.array_equal(co, oco)
+    assert np.array_equal(tr, otr)
+
+
+@pytest.mark.parametrize("L,T,E,k", [(3, 5000, 16, 4), (1, 3000, 32, 8), (2, 1, 8, 2),
+                                     (2, 777, 40, 20), (2, 900, 300, 6), (4, 2048, 128, 16)])
+def test_cooccur_shapes(L, T, E, k):
+    ids = W.random_small(T + E + k, T, E, k, L, s=1.1)
+    co, tr, err = gpu_cooccur(ids, E)
+    assert err == 0
+    oco, otr = oracle.cooccur(ids, E)
+    assert np.array_equal(co, oco)
+    if L > 1:
+        assert np.array_equal(tr, otr)
+
+
+def test_cooccur_repeated_ids():
+    ids = np.array([[[1, 1, 2], [0, 0, 0]], [[0, 2, 2], [1, 2, 1]]], np.int32)
+    co, tr, err = gpu_cooccur(ids, 3)
+    oco, otr = oracle.cooccur(ids, 3)
+    assert err == 0 and np.array_equal(co, oco) and np.array_equal(tr, otr)
+
+
+def test_cooccur_without_transitions():
+    ids = W.random_small(5, 1000, 16, 4, 3)
+    co, tr, err = gpu_cooccur(ids, 16, transitions=False)
+    assert err == 0 and tr is None
+    assert np.array_equal(co, oracle.cooccur(ids, 16, transitions=False))
+
+
+# ---------------------------------------------------------------- device errors
+
+def test_out_of_range_id_sets_error_word():
+    from moe_expert_routing_ids_gb300 import TOPO_ERANGE
+    cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)
+    ids = W.random_small(1, 400, 8, 2, 1)
+    ids[0, 17, 1] = 8
+    _, err = gpu_chain(cfg, ids)
+    assert err == TOPO_ERANGE
+
+
+def test_reroute_without_hist_index_is_rejected():
+    from moe_expert_routing_ids_gb300 import TOPO_ESTATE
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)
+    ids = torch.as_tensor(W.random_small(2, 400, 8, 2, 1), device=dev)
+    other = ids.clone()
+    P = Planner(cfg, 1, dev)
+    P.hist(ids)
+    P.make_plan()
+    P.reroute(other)             # index was built for `ids`, not `other`
+    assert P.error() == TOPO_ESTATE
+    P.reset_error()
+    P.reroute(ids)
+    P.layout()
+    assert P.error() == 0
+
+
+def test_layout_with_foreign_dst_is_rejected():
+    from moe_expert_routing_ids_gb300 import TOPO_ESTATE
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)
+    ids = torch.as_tensor(W.random_small(3, 400, 8, 2, 1), device=dev)
+    P = Planner(cfg, 1, dev)
+    P.run(ids)
+    assert P.error() == 0
+    P.buf.dst_inst = P.buf.dst_inst.clone()   # not the buffer topo_reroute wrote
+    P.layout()
+    assert P.error() == TOPO_ESTATE
+
+
+def test_unbalanced_main_rank_sets_error_word():
+    from moe_expert_routing_ids_gb300 import TOPO_EMAP
+    cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)
+    cfg["main_rank"] = np.array([0, 0, 0, 1, 2, 2, 3, 3], np.int32)
+    _, err = gpu_chain(cfg, W.random_small(4, 400, 8, 2, 1))
+    assert err == TOPO_EMAP
