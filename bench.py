@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the topology-aware expert-routing plan on GB300.
+
+One step = the whole hot path on one batch of synthetic routing ids already
+resident in HBM: topo_hist -> topo_plan -> topo_reroute ->
+topo_dispatch_layout.  The workload is the stress configuration (T = 1,048,576
+tokens x k = 10 over E = 512 experts, R = 128 ranks in 16 nodes of 8, 64
+replica slots per rank, 4 microbatches planned per call): 41.9 M
+(token, slot) pairs per step, 168 MB of ids -- larger than the 129 MB L2, so
+no flush is needed between steps.
+
+Printed (one JSON line, rank 0): pairs/s for the device-resident step
+(`value`), the same through host buffers with the copies inside the timed
+region (`e2e`), the dominant call's roofline against the measured HBM
+bandwidth, the oracle timed on a bounded sample of the same workload on the
+host cores (`cpu_baseline`), plus the planner latency on the T = 16384,
+E = 64, R = 32 workload and the co-occurrence kernel's HBM fraction on the
+L = 8, T = 262144, E = 128 workload as secondary figures.
+
+--impl reference times the CPU oracle (the only reference this method has)
+on bounded samples of the same workload.
+Multi-GPU (torchrun): each rank plans its own independent replica of the
+workload (weak scaling, no data-path collective); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = 5                 # the stress configuration
+PLAN_LATENCY_WORKLOAD = 2    # T=16384, E=64, k=6, R=32 (4 x 8), 8 slots
+COOCCUR_WORKLOAD = 4
+BYTES_PER_PAIR = {"hist": 4, "reroute": 8, "layout": 8}   # algorithmic HBM bytes
+KERNELS_PER_CALL = {"hist": 1, "plan": 4, "reroute": 4, "layout": 4, "cooccur": 1}
+CALLS = ("hist", "plan", "reroute", "layout")
+CALL_SOURCE = {"hist": "k_hist.cu", "plan": "k_plan.cu", "reroute": "k_route.cu",
+               "layout": "k_route.cu", "cooccur": "k_cooccur.cu"}
+CALL_KERNEL = {"hist": "k_hist_tiles", "reroute": "k_reroute_tiles", "layout": "k_layout_tiles",
+               "cooccur": "k_cooccur"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
+    ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
+    ap.add_argument("--skip-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------- utils
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_sha(call: str) -> str:
+    path = os.path.join(ROOT, "moe_expert_routing_ids_gb300", "csrc", CALL_SOURCE[call])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(call: str, units: int):
+    """DRAM bytes per launch of the call's main kernel from the committed ncu
+    summary, scaled to `units` pairs (or ids), or None if absent or stale."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f).get(call)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_sha(call):
+        return None
+    return rec["dram_bytes"] * units / rec["units"]
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [int(r[1]) for r in rows]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": int(statistics.median(sm)), "sm_max_mhz": int(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_sample_chain(w, ids_layer):
+    """Oracle chain on one microbatch: (seconds, pairs)."""
+    import oracle
+    cfg = w.plan_cfg
+    t0 = time.perf_counter()
+    h = oracle.hist(ids_layer, w.R, w.E)
+    p = oracle.plan(cfg, h)
+    d = oracle.reroute(cfg, ids_layer, p)
+    oracle.layout(cfg, d)
+    return time.perf_counter() - t0, int(ids_layer.size)
+
+
+# ------------------------------------------------------------------ reference
+
+def run_reference(args, rank):
+    """CPU oracle arm: each step is the oracle chain on one microbatch of the
+    stress workload (a bounded sample); metric and unit as ours."""
+    if rank != 0:
+        return
+    import oracle
+    from moe_expert_routing_ids_gb300 import workloads as W
+    oracle.build()
+    w = W.CONFIGS[WORKLOAD]
+    ids = w.ids(n_layers=1)
+    steps = max(1, min(args.steps, 3))
+    warm = max(0, min(args.warmup, 1))
+    for _ in range(warm):
+        cpu_sample_chain(w, ids)
+    secs, pairs = 0.0, 0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        s, n = cpu_sample_chain(w, ids)
+        secs += s
+        pairs += n
+    wall = time.perf_counter() - t0
+    value = pairs / secs
+    sample = f"1 of 4 microbatches ({pairs // steps} pairs) per step, oracle hist+plan+reroute+layout"
+    line = {"impl": "reference", "metric": "routed (token,slot) pairs/sec", "value": value,
+            "unit": "pairs/s", "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+            "ms_per_step": 1e3 * wall / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "R": w.R,
+                       "ranks_per_node": w.ranks_per_node, "n_slot": w.n_slot,
+                       "microbatches": w.n_layers, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ ours
+
+def time_chain(P, d_ids, steps, stream):
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(CALLS) + 1)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for k in range(steps):
+            e = ev[k]
+            e[0].record(stream)
+            P.hist(d_ids)
+            e[1].record(stream)
+            P.make_plan()
+            e[2].record(stream)
+            P.reroute(d_ids)
+            e[3].record(stream)
+            P.layout()
+            e[4].record(stream)
+        t1.record(stream)
+    return t0, t1, ev
+
+
+def secondary_plan_latency(dev, stream):
+    """topo_plan latency per layer on the T=16384, E=64, R=32 workload, mean of
+    200 calls after 20 warm-ups (TopoEP §6.3 protocol)."""
+    import torch
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    w = W.CONFIGS[PLAN_LATENCY_WORKLOAD]
+    P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
+    ids = torch.as_tensor(w.ids(), device=dev)
+    with torch.cuda.stream(stream):
+        P.hist(ids)
+        for _ in range(20):
+            P.make_plan()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(200):
+            P.make_plan()
+        b.record(stream)
+    b.synchronize()
+    us = a.elapsed_time(b) * 1e3 / 200 / w.n_layers
+    return {"workload": w.name, "us_per_layer": round(us, 2), "reps": 200, "warmup": 20,
+            "target_us": 50}
+
+
+def secondary_cooccur(dev, stream, hbm_peak):
+    import torch
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Cooccur
+    w = W.CONFIGS[COOCCUR_WORKLOAD]
+    C = Cooccur(w.n_layers, w.T, w.E, w.k, dev)
+    ids = torch.as_tensor(w.ids(), device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(13):
+            flush.fill_(i)                      # evict the ids from L2 (64 MiB < L2)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            C.run(ids, stream)
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[3:])
+    nbytes = w.n_layers * w.T * w.k * 4 + (2 * w.n_layers - 1) * w.E * w.E * 8
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "ms": round(ms, 4), "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "l2": "flushed (256 MB write) before each call", "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    w = W.CONFIGS[WORKLOAD]
+    ids = w.ids(replica=rank)
+    pairs = int(ids.size)
+    d_ids = torch.as_tensor(ids, device=dev)
+    P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            P.run(d_ids)
+    torch.cuda.synchronize(dev)
+    err = P.error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err}")
+
+    clocks = Clocks(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0, t1, ev = time_chain(P, d_ids, args.steps, stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_call = {c: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i, c in enumerate(CALLS)}
+    if P.error() != 0:
+        raise RuntimeError("device error after the timed region")
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if rank != 0:
+        return
+    ms_step = total_ms / args.steps
+    value = pairs * world / (ms_step * 1e-3)
+    hbm, peak_kind = peaks()
+    # dominant HBM call
+    scan = {c: per_call[c] for c in BYTES_PER_PAIR}
+    dom = max(scan, key=scan.get)
+    achieved = BYTES_PER_PAIR[dom] * pairs / (per_call[dom] * 1e-3) / 1e9
+    traffic = profiled_traffic(dom, pairs)
+    calls = {c: {"ms": round(per_call[c], 4),
+                 **({"achieved_gbs": round(BYTES_PER_PAIR[c] * pairs / (per_call[c] * 1e-3) / 1e9, 1)}
+                    if c in BYTES_PER_PAIR else {})} for c in CALLS}
+    calls["plan"]["us_per_microbatch"] = round(per_call["plan"] * 1e3 / w.n_layers, 2)
+    line = {"metric": "routed (token,slot) pairs/sec", "value": value, "unit": "pairs/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "R": w.R,
+                       "ranks_per_node": w.ranks_per_node, "n_slot": w.n_slot,
+                       "microbatches": w.n_layers, "pairs_per_step": pairs,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "ids 168 MB > 129 MB L2 per step, no flush"},
+            "gpu_launches": args.steps * sum(KERNELS_PER_CALL[c] for c in CALLS),
+            "calls": calls,
+            "roofline": {"bound": "hbm", "kernel": f"{dom} call ({CALL_KERNEL[dom]} + index kernels)",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_pair": BYTES_PER_PAIR[dom],
+                         "traffic": traffic}}
+    if clk:
+        line["clocks"] = clk
+    if not args.skip_e2e:
+        line["e2e"] = e2e(P, ids, dev, stream, max(3, min(args.steps, 20)))
+    if not args.skip_secondary:
+        line["plan_latency"] = secondary_plan_latency(dev, stream)
+        line["cooccur"] = secondary_cooccur(dev, stream, hbm)
+    if not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, ids)
+    print(json.dumps(line), flush=True)
+
+
+def e2e(P, ids, dev, stream, steps):
+    """Same metric through host buffers: per step, H2D copy of the ids from
+    pinned memory, the four calls, D2H of the plan and layout outputs."""
+    import torch
+    h_ids = torch.from_numpy(ids).pin_memory()
+    b = P.buf
+    outs = [b.dst_inst, b.sorted_pairs, b.seg_off, b.send_counts, b.layout_stats, b.slot_expert,
+            b.rank_load, b.stats]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    d_ids = torch.empty_like(P.buf.dst_inst).view(ids.shape)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one():
+        d_ids.copy_(h_ids, non_blocking=True)
+        P.run(d_ids)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+        stream.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        z.record(stream)
+    z.synchronize()
+    ms = a.elapsed_time(z) / steps
+    return {"value": ids.size / (ms * 1e-3), "unit": "pairs/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(ids.nbytes),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs)),
+            "steps": steps}
+
+
+def cpu_baseline(w, ids):
+    import oracle
+    oracle.build()
+    secs, pairs, n = 0.0, 0, 0
+    while secs < 10.0 and n < w.n_layers * 3:
+        s, p = cpu_sample_chain(w, ids[n % w.n_layers][None])
+        secs += s
+        pairs += p
+        n += 1
+    return {"value": pairs / secs, "unit": "pairs/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} microbatch(es) of the workload, {pairs} pairs, oracle chain "
+                      f"hist+plan+reroute+layout single-threaded, {secs:.1f} s"}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank)
+        else:
+            import __graft_entry__
+            __graft_entry__.build()
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -87,7 +87,8 @@ typedef struct {
  * All device pointers, caller-allocated, layer-major. */
 typedef struct {
     int32_t *slot_expert;  /* [L][R][n_slot] expert in each replica slot, -1 empty
-                              (x_{e,r} for replicas; mains are implicit, C5) */
+                              (x_{e,r} for replicas; mains are implicit, C5);
+                              may be NULL when n_slot == 0 */
     int32_t *route_cnt;    /* [L][R][R][n_local] q: assignments from source s
                               executed on instance (r, l) */
     int32_t *inst_load;    /* [L][R][n_local] U: load of each instance */

@@ -87,8 +87,10 @@ uint64_t route_fingerprint(const Geo &g, const topo_plan_t &p, const int32_t *ds
     return fp_mix(h, (uint64_t)(uintptr_t)dst);
 }
 
-bool plan_ok(const topo_plan_t *p) {
-    return p && p->slot_expert && p->route_cnt && p->inst_load && p->rank_load && p->stats;
+// slot_expert may be NULL only when there are no slots (a zero-size array).
+bool plan_ok(const topo_plan_t *p, const Geo &g) {
+    return p && (p->slot_expert || g.n_slot == 0 || g.L == 0) && p->route_cnt && p->inst_load &&
+           p->rank_load && p->stats;
 }
 
 }  // namespace
@@ -124,7 +126,7 @@ int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const 
     Geo g;
     int rc = make_geo(cfg, n_layers, &g);
     if (rc) return rc;
-    if (!hist || !ws || !plan_ok(plan)) return TOPO_EINVAL;
+    if (!hist || !ws || !plan_ok(plan, g)) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
     return cuda_rc(launch_plan(g, cfg->main_rank, hist, *plan, ws, stream));
@@ -135,7 +137,7 @@ int topo_reroute(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, cons
     Geo g;
     int rc = make_geo(cfg, n_layers, &g);
     if (rc) return rc;
-    if (!ws || !plan_ok(plan) || ((!ids || !dst_inst) && g.npairs > 0 && n_layers > 0))
+    if (!ws || !plan_ok(plan, g) || ((!ids || !dst_inst) && g.npairs > 0 && n_layers > 0))
         return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
@@ -150,7 +152,7 @@ int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *d
     Geo g;
     int rc = make_geo(cfg, n_layers, &g);
     if (rc) return rc;
-    if (!ws || !plan_ok(plan) || !seg_off || !send_counts || !layout_stats) return TOPO_EINVAL;
+    if (!ws || !plan_ok(plan, g) || !seg_off || !send_counts || !layout_stats) return TOPO_EINVAL;
     if ((!dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;

@@ -169,25 +169,30 @@ class Workload:
     def pairs(self) -> int:
         return self.T * self.k * self.n_layers
 
-    def ids(self) -> np.ndarray:
-        """int32 [n_layers, T, k]."""
-        return GENERATORS[self.index](self)
+    def ids(self, replica: int = 0, n_layers: int | None = None) -> np.ndarray:
+        """int32 [n_layers, T, k].  ``replica`` > 0 draws an independent copy
+        (another data-parallel replica); ``n_layers`` truncates the stack."""
+        return GENERATORS[self.index](self, replica, self.n_layers if n_layers is None else n_layers)
 
 
-def _gen_zipf_single(w: Workload, s: float) -> np.ndarray:
-    out = np.empty((w.n_layers, w.T, w.k), np.int32)
-    for l in range(w.n_layers):
-        rng = rng_for(w.index, l)
+def _seed(w: Workload, replica: int, l: int):
+    return rng_for(w.index, l) if replica == 0 else rng_for(w.index, l, replica)
+
+
+def _gen_zipf_single(w: Workload, s: float, replica: int, n_layers: int) -> np.ndarray:
+    out = np.empty((n_layers, w.T, w.k), np.int32)
+    for l in range(n_layers):
+        rng = _seed(w, replica, l)
         order = rng.permutation(w.E)
         out[l] = topk_without_replacement(rng, zipf_probs(w.E, s, order), w.T, w.k)
     return out
 
 
-def _gen_cfg3(w: Workload) -> np.ndarray:
+def _gen_cfg3(w: Workload, replica: int, n_layers: int) -> np.ndarray:
     s_per_layer = (0.8, 1.2, 1.6, 1.2)
-    out = np.empty((w.n_layers, w.T, w.k), np.int32)
-    for l in range(w.n_layers):
-        rng = rng_for(w.index, l)
+    out = np.empty((n_layers, w.T, w.k), np.int32)
+    for l in range(n_layers):
+        rng = _seed(w, replica, l)
         order = rng.permutation(w.E)
         p = zipf_probs(w.E, s_per_layer[l % len(s_per_layer)], order)
         if l == 0:
@@ -198,10 +203,10 @@ def _gen_cfg3(w: Workload) -> np.ndarray:
     return out
 
 
-def _gen_cfg4(w: Workload) -> np.ndarray:
-    out = np.empty((w.n_layers, w.T, w.k), np.int32)
-    for l in range(w.n_layers):
-        rng = rng_for(w.index, l)
+def _gen_cfg4(w: Workload, replica: int, n_layers: int) -> np.ndarray:
+    out = np.empty((n_layers, w.T, w.k), np.int32)
+    for l in range(n_layers):
+        rng = _seed(w, replica, l)
         groups = rng.permutation(w.E).reshape(16, w.E // 16)
         out[l] = grouped_topk(rng, w.E, w.T, w.k, groups, stay=0.7)
     return out
@@ -220,11 +225,11 @@ CONFIGS = {
 }
 
 GENERATORS = {
-    1: lambda w: _gen_zipf_single(w, 1.0),
-    2: lambda w: _gen_zipf_single(w, 1.2),
+    1: lambda w, r, n: _gen_zipf_single(w, 1.0, r, n),
+    2: lambda w, r, n: _gen_zipf_single(w, 1.2, r, n),
     3: _gen_cfg3,
     4: _gen_cfg4,
-    5: lambda w: _gen_zipf_single(w, 1.4),
+    5: lambda w, r, n: _gen_zipf_single(w, 1.4, r, n),
 }
 
 

@@ -212,9 +212,11 @@ def test_reroute_without_hist_index_is_rejected():
     P.make_plan()
     P.reroute(other)             # index was built for `ids`, not `other`
     assert P.error() == TOPO_ESTATE
-    P.reset_error()
+    P.reset_error()              # clears the error word and the indices' fingerprints
     P.reroute(ids)
-    P.layout()
+    assert P.error() == TOPO_ESTATE
+    P.reset_error()
+    P.run(ids)                   # the chain restarts from topo_hist
     assert P.error() == 0
 
 
