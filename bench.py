@@ -2,8 +2,8 @@
 """Benchmark of the topology-aware expert-routing plan on GB300.
 
 One step = the whole hot path on one batch of synthetic routing ids already
-resident in HBM: topo_hist -> topo_plan -> topo_reroute ->
-topo_dispatch_layout.  The workload is the stress configuration (T = 1,048,576
+resident in HBM: topo_hist -> topo_plan -> topo_reroute_layout (rerouting and
+dispatch layout in one pass over the pairs).  The workload is the stress configuration (T = 1,048,576
 tokens x k = 10 over E = 512 experts, R = 128 ranks in 16 nodes of 8, 64
 replica slots per rank, 4 microbatches planned per call): 41.9 M
 (token, slot) pairs per step, 168 MB of ids -- larger than the 129 MB L2, so
@@ -43,13 +43,14 @@ import numpy as np  # noqa: E402
 WORKLOAD = 5                 # the stress configuration
 PLAN_LATENCY_WORKLOAD = 2    # T=16384, E=64, k=6, R=32 (4 x 8), 8 slots
 COOCCUR_WORKLOAD = 4
-BYTES_PER_PAIR = {"hist": 4, "reroute": 8, "layout": 8}   # algorithmic HBM bytes
-KERNELS_PER_CALL = {"hist": 1, "plan": 4, "reroute": 4, "layout": 4, "cooccur": 1}
-CALLS = ("hist", "plan", "reroute", "layout")
-CALL_SOURCE = {"hist": "k_hist.cu", "plan": "k_plan.cu", "reroute": "k_route.cu",
-               "layout": "k_route.cu", "cooccur": "k_cooccur.cu"}
-CALL_KERNEL = {"hist": "k_hist_tiles", "reroute": "k_reroute_tiles", "layout": "k_layout_tiles",
-               "cooccur": "k_cooccur"}
+# algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
+# reroute+layout reads the id and writes dst_inst and sorted_pairs
+BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
+KERNELS_PER_CALL = {"hist": 1, "plan": 4, "reroute_layout": 8, "cooccur": 1}
+CALLS = ("hist", "plan", "reroute_layout")
+CALL_SOURCE = {"hist": "k_hist.cu", "plan": "k_plan.cu", "reroute_layout": "k_route.cu",
+               "cooccur": "k_cooccur.cu"}
+CALL_KERNEL = {"hist": "k_hist_tiles", "reroute_layout": "k_route_tiles", "cooccur": "k_cooccur"}
 
 
 def parse():
@@ -207,10 +208,8 @@ def time_chain(P, d_ids, steps, stream):
             e[1].record(stream)
             P.make_plan()
             e[2].record(stream)
-            P.reroute(d_ids)
+            P.reroute_layout(d_ids)
             e[3].record(stream)
-            P.layout()
-            e[4].record(stream)
         t1.record(stream)
     return t0, t1, ev
 
@@ -329,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "ids 168 MB > 129 MB L2 per step, no flush"},
             "gpu_launches": args.steps * sum(KERNELS_PER_CALL[c] for c in CALLS),
             "calls": calls,
-            "roofline": {"bound": "hbm", "kernel": f"{dom} call ({CALL_KERNEL[dom]} + index kernels)",
+            "roofline": {"bound": "hbm", "kernel": f"{dom} call ({CALL_KERNEL[dom]} + its index kernels)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_pair": BYTES_PER_PAIR[dom],

@@ -25,6 +25,7 @@
  *   - n_layers independent problems (layers or microbatches) are handled per
  *     call; array arguments are stacked with layer as the slowest dimension.
  *   - Outputs are fully overwritten.
+ *   - k <= 64; the shared-memory budget bounds E (about 2000 for R = 128).
  *   - Host-detectable problems return a negative code before anything is
  *     enqueued.  Problems only the device can see (an id outside [0, E), a
  *     workspace that does not hold what the call needs) set a sticky error
@@ -61,6 +62,7 @@ extern "C" {
 #define TOPO_CALL_LAYOUT 3
 #define TOPO_CALL_COOCCUR 4
 #define TOPO_CALL_CHAIN 5   /* hist -> plan -> reroute -> dispatch_layout on one ws */
+#define TOPO_CALL_REROUTE_LAYOUT 6
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -178,12 +180,23 @@ int topo_reroute(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, cons
  *   send_counts[l][s][r]: pairs from source s to rank r, int64 [n_layers][R][R];
  *   layout_stats[l][8]: pairs with s == r, same domain, other domain; their
  *     dispatch bytes (pairs * tok_bytes); pairs served by a replica; 0.
- * dst_inst must be topo_reroute's output for this plan on this ws (checked:
- * TOPO_ESTATE otherwise).  All output pointers required. */
+ * dst_inst must be topo_reroute's output for this plan on this ws: topo_reroute
+ * already ranked every pair and left its position in ws, so this call only
+ * scatters (checked: TOPO_ESTATE otherwise).  All output pointers required. */
 int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst,
                          const topo_plan_t *plan, int32_t *sorted_pairs, int32_t *seg_off,
                          int64_t *send_counts, int64_t *layout_stats, void *ws, size_t ws_bytes,
                          cudaStream_t stream);
+
+/* topo_reroute followed by topo_dispatch_layout in one pass over the pairs:
+ * the same dst_inst, sorted_pairs, seg_off, send_counts and layout_stats, with
+ * each pair read once and no per-pair positions kept in ws.  Same arguments
+ * and requirements as the two calls (ids indexed by topo_hist on this ws).
+ * Device errors: TOPO_ESTATE, TOPO_ERANGE. */
+int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids,
+                        const topo_plan_t *plan, int32_t *dst_inst, int32_t *sorted_pairs,
+                        int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
+                        size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronous: copies the error word out of ws (device) and returns it
  * (TOPO_OK or a negative code; TOPO_ECUDA if the copy fails).  Call after

@@ -23,11 +23,12 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtopoep.so")
 TOPO_OK, TOPO_EINVAL, TOPO_ENOSPC, TOPO_ECUDA = 0, -1, -2, -3
 TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP = -4, -5, -6
 TOPO_CALL_HIST, TOPO_CALL_PLAN, TOPO_CALL_REROUTE, TOPO_CALL_LAYOUT = 0, 1, 2, 3
-TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN = 4, 5
+TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN, TOPO_CALL_REROUTE_LAYOUT = 4, 5, 6
 TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
 EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan",
-           "topo_reroute", "topo_dispatch_layout", "topo_read_error", "topo_strerror")
+           "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
+           "topo_strerror")
 
 
 class TopoError(RuntimeError):
@@ -75,11 +76,12 @@ def lib():
             L.topo_plan.argtypes = [cfgp, i32, vp, planp, vp, sz, vp]
             L.topo_reroute.argtypes = [cfgp, i32, vp, planp, vp, vp, sz, vp]
             L.topo_dispatch_layout.argtypes = [cfgp, i32, vp, planp, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_reroute_layout.argtypes = [cfgp, i32, vp, planp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
-                      "topo_dispatch_layout", "topo_read_error"):
+                      "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -165,6 +167,15 @@ def topo_dispatch_layout(cfg: TopoCfg, n_layers: int, dst_inst, plan: TopoPlan, 
                                            ctypes.byref(plan), _p(sorted_pairs), _p(seg_off),
                                            _p(send_counts), _p(layout_stats), _p(ws), ws_bytes,
                                            _s(stream)))
+
+
+def topo_reroute_layout(cfg: TopoCfg, n_layers: int, ids, plan: TopoPlan, dst_inst, sorted_pairs,
+                        seg_off, send_counts, layout_stats, ws, ws_bytes: int, stream=None) -> int:
+    return _chk("topo_reroute_layout",
+                lib().topo_reroute_layout(ctypes.byref(cfg), n_layers, _p(ids), ctypes.byref(plan),
+                                          _p(dst_inst), _p(sorted_pairs), _p(seg_off),
+                                          _p(send_counts), _p(layout_stats), _p(ws), ws_bytes,
+                                          _s(stream)))
 
 
 def topo_read_error(ws) -> int:

@@ -8,12 +8,16 @@
 
 namespace topo {
 
-// Pairs per tile of the pair-scan kernels (hist, reroute, layout).  Tiles
-// never straddle a source rank's block of pairs.
-constexpr int kTile = 16384;
-constexpr int kScanThreads = 512;                  // threads of a tile CTA
-constexpr int kScanWarps = kScanThreads / 32;
-constexpr int kWarpSeg = kTile / kScanWarps;       // pairs per warp in a tile
+// Pair-scan tiling.  A tile is TT consecutive tokens of one source rank
+// (TT = 32 * kRankWarps * RW, RW rounds of 32 tokens per warp), so tiles never
+// straddle a source and every token's k pairs sit in one tile.  hist, reroute
+// and layout share the tiling: the tile index topo_hist leaves is per tile.
+constexpr int kRankWarps = 8;
+constexpr int kRankThreads = kRankWarps * 32;
+constexpr int kTilePairsTarget = 16384;            // pairs per tile aimed for
+constexpr int kRankSmemTarget = 110 * 1024;        // two rank CTAs per SM
+constexpr int kSmemMax = 227 * 1024;               // per CTA on sm_103a
+constexpr int kMaxK = 64;
 constexpr int kMaxRanksPerNode = 32;               // one warp lane per rank of a domain
 
 // Workspace header, 256 bytes at offset 0 of every workspace.
@@ -30,6 +34,10 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 struct Geo {
     int32_t T, E, k, R, rpn, n_slot, M, E_R, n_local, L;
     int32_t tps;            // tiles per source rank
+    int32_t tpr;            // tokens per source rank
+    int32_t TT, RW;         // tokens per tile, rounds of 32 tokens per warp
+    int32_t kp;             // shared-memory stride of a token's ids (k, made odd)
+    uint32_t kmagic;        // ceil(2^32 / k) for k >= 2: i / k == umulhi(i, kmagic), i < 2^26
     int32_t n_inst_cap;     // E + R * n_slot: most instances a layer can hold
     int32_t n_keys;         // R * n_local
     int32_t c_intra, c_inter, max_iters;
@@ -38,6 +46,8 @@ struct Geo {
     int64_t S_tok, W;
     // workspace regions (byte offsets)
     size_t off_tile;        // int32 [L][R][tps][E]   tile counts -> exclusive prefix
+    size_t off_pos;         // int32 [L][R][tps][TT*k] layout position of each pair,
+                            //        in (warp, round, slot, lane) order within a tile
     size_t off_done;        // int32 [L][R]           tiles finished per source
     size_t off_main;        // int32 [2E + R*E_R]     main(e), local index, mains[r][j]
     size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
@@ -48,6 +58,9 @@ struct Geo {
     size_t off_rent;        // int4  [L][R][n_inst_cap] (inst, cum_start, cum_end, out_base)
     size_t off_soff;        // int32 [L][R][n_keys]   column prefix of q over sources
     size_t off_ccnt;        // int32 [L][n_keys]      column totals of q
+    size_t off_lseg;        // int32 [L][n_keys+1]    segment offsets
+    size_t off_lsend;       // int64 [L][R][R]        send counts
+    size_t off_lstat;       // int64 [L][8]           layout statistics
     size_t total;
 };
 
@@ -69,6 +82,12 @@ __host__ __device__ inline uint64_t fp_mix(uint64_t h, uint64_t v) {
     return z ^ (z >> 31);
 }
 
+// i / k for 0 <= i < 2^26 without a hardware divide (k = 1 is the identity;
+// its reciprocal does not fit in 32 bits).
+__device__ __forceinline__ int div_k(const Geo &g, int i) {
+    return g.k == 1 ? i : (int)__umulhi((unsigned)i, g.kmagic);
+}
+
 template <typename T>
 __host__ __device__ inline T *ws_at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
@@ -85,9 +104,14 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
                            const topo_plan_t &p, int32_t *dst, void *ws, uint64_t hist_fp,
                            uint64_t route_part, cudaStream_t st);
-cudaError_t launch_layout(const Geo &g, const int32_t *dst, const topo_plan_t &p, int32_t *sorted,
-                          int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
-                          uint64_t route_part, cudaStream_t st);
+cudaError_t launch_layout(const Geo &g, int32_t *sorted, int32_t *seg_off, int64_t *send_counts,
+                          int64_t *layout_stats, void *ws, uint64_t route_part, cudaStream_t st);
+cudaError_t launch_reroute_layout(const Geo &g, const int32_t *main_rank, const int32_t *ids,
+                                  const topo_plan_t &p, int32_t *dst, int32_t *sorted,
+                                  int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
+                                  void *ws, uint64_t hist_fp, cudaStream_t st);
+// Shared-memory bytes of the rank kernel for this geometry.
+size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
 

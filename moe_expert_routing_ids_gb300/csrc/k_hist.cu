@@ -1,11 +1,11 @@
 // Routing matrix Omega (TopoEP §4.1, Eq. 3) and the per-tile expert index.
 //
-// One CTA per tile of kTile pairs inside one source rank's block.  The tile's
+// One CTA per tile of TT tokens inside one source rank's block.  The tile's
 // ids are streamed once with 16-byte loads and counted into a shared-memory
 // histogram (integer shared atomics, no float).  Each CTA stores its counts;
-// the last CTA of a source (threadfence + counter, no waiting) turns the
-// source's tile counts into exclusive prefixes -- the index that lets the
-// rerouting and layout kernels rank pairs in one pass -- and writes the
+// the last CTA of a source (one release fence + counter by thread 0, no
+// waiting) turns the source's tile counts into exclusive prefixes -- the index
+// that lets the rerouting kernel rank pairs in one pass -- and writes the
 // source's row of Omega.
 #include <cuda_runtime.h>
 
@@ -14,6 +14,8 @@
 namespace topo {
 namespace {
 
+constexpr int kHistThreads = 512;
+
 __device__ __forceinline__ void count_id(int e, int E, int *cnt, bool &bad) {
     if ((unsigned)e < (unsigned)E)
         atomicAdd(&cnt[e], 1);
@@ -21,7 +23,7 @@ __device__ __forceinline__ void count_id(int e, int E, int *cnt, bool &bad) {
         bad = true;
 }
 
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kHistThreads)
 k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ hist, int32_t *tile_cnt,
              int32_t *done, WsHeader *hdr, Geo g, uint64_t fp) {
     extern __shared__ int cnt[];
@@ -34,17 +36,15 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ hist, int32_
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
 
-    const int64_t p0 = (int64_t)s * g.pps + (int64_t)t * kTile;
-    int64_t p1 = p0 + kTile;
-    const int64_t pend = (int64_t)(s + 1) * g.pps;
-    if (p1 > pend) p1 = pend;
+    const int tok0 = t * g.TT;
+    const int ntok = max(0, min(g.TT, g.tpr - tok0));
     bool bad = false;
-    if (p1 > p0) {
-        const int32_t *a = ids + (int64_t)l * g.npairs + p0;
-        const int n = (int)(p1 - p0);
+    if (ntok > 0) {
+        const int32_t *a = ids + (int64_t)l * g.npairs + ((int64_t)s * g.tpr + tok0) * g.k;
+        const int n = ntok * g.k;
         int head = (int)(((16 - ((uintptr_t)a & 15)) & 15) >> 2);
         if (head > n) head = n;
-        for (int i = threadIdx.x; i < head; i += blockDim.x) count_id(a[i], E, cnt, bad);
+        for (int i = threadIdx.x; i < head; i += blockDim.x) count_id(__ldg(a + i), E, cnt, bad);
         const int4 *v = reinterpret_cast<const int4 *>(a + head);
         const int nv = (n - head) >> 2;
         int i = threadIdx.x;
@@ -65,22 +65,23 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ hist, int32_
             count_id(x.x, E, cnt, bad); count_id(x.y, E, cnt, bad);
             count_id(x.z, E, cnt, bad); count_id(x.w, E, cnt, bad);
         }
-        for (int j = head + nv * 4 + threadIdx.x; j < n; j += blockDim.x) count_id(a[j], E, cnt, bad);
+        for (int j = head + nv * 4 + threadIdx.x; j < n; j += blockDim.x)
+            count_id(__ldg(a + j), E, cnt, bad);
     }
     if (bad) set_error(hdr, TOPO_ERANGE);
     __syncthreads();
 
     int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) mine[e] = cnt[e];
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        int old = atomicAdd(&done[l * g.R + s], 1);
+        __threadfence();                        // release this CTA's counts (cumulative)
+        const int old = atomicAdd(&done[l * g.R + s], 1);
         is_last = (old == g.tps - 1);
+        if (is_last) __threadfence();           // acquire the other CTAs' counts
     }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
     // Last tile of source s: exclusive prefix over the source's tiles, and the
     // source's row of Omega.
     int32_t *first = tile_cnt + ((int64_t)l * g.R + s) * g.tps * E;
@@ -88,14 +89,13 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ hist, int32_
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
         for (int u = 0; u < g.tps; ++u) {
-            int c = __ldcg(first + (int64_t)u * E + e);
+            const int c = __ldcg(first + (int64_t)u * E + e);
             first[(int64_t)u * E + e] = run;
             run += c;
         }
         hrow[e] = run;
     }
     if (threadIdx.x == 0) {
-        done[l * g.R + s] = 0;                  // ready for the next call
         hdr->hist_fp = fp;
         hdr->route_fp = 0;                      // any routing index is now stale
     }
@@ -116,7 +116,7 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    k_hist_tiles<<<(unsigned)tiles, kScanThreads, smem, st>>>(
+    k_hist_tiles<<<(unsigned)tiles, kHistThreads, smem, st>>>(
         ids, hist, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_done),
         ws_at<WsHeader>(ws, 0), g, fp);
     return cudaGetLastError();

@@ -2,20 +2,26 @@
 // dispatch layout (TopoEP §1 / Fig. 5 token rerouting; §5 receive counts
 // derived on the GPU).
 //
-// Both pair scans need, for pair p of source s selecting expert e, its
-// occurrence index o = number of earlier pairs of s that select e.  The tile
-// index left by topo_hist gives o up to the start of p's tile; inside the
-// tile a CTA ranks pairs with warp match_any: each warp owns a contiguous
-// slice, counts per expert (pass 1), the slices are prefixed per expert
-// (pass 2), and pass 3 walks the slice again in pair order adding
-// popc(peers below the lane).  Everything is an integer count, so the result
-// is exact and the same on every run.
+// Reading used for the pair -> instance rule: within source s, the pairs that
+// select e are taken in pair order; the o-th of them (its occurrence index)
+// goes to the instance of e whose running range of q[s][.] over e's instances
+// in ascending rank order holds o.  The layout is the stable sort of pairs by
+// instance, so a pair's position is  seg_off[i] + sum_{s'<s} q[s'][i] +
+// (o - start of i's range)  =  out_base(s, i) + o.
 //
-// The instance a pair goes to follows from o: within (s, e) the instances of
-// e are filled in ascending rank order, q[s][r][l] pairs each.  The routing
-// index stores, per (s, e), the nonzero instances with their running ranges
-// [cum_start, cum_end) and -- for the layout -- the output position of the
-// range's first pair, out_base, so that a pair's position is out_base + o.
+// Everything therefore follows from one number per pair, o, computed once by
+// k_route_tiles:
+//   * topo_hist's tile index gives the occurrences before the tile;
+//   * inside a tile (TT tokens, 8 warps, lane = token) each warp counts its
+//     rounds per expert (shared atomics), the warps' counts are prefixed, and
+//     each round of 32 tokens is ranked with a per-expert token bitmask:
+//     every lane ORs its bit into mask[e] for each of its k ids, then a pair's
+//     rank in the round is popc(mask[e] & lanes below) -- the earlier tokens
+//     of the round holding e.  Top-k ids of one token are distinct, so no
+//     token meets the same expert twice in a round; a tile where one does is
+//     redone by the warp match_any path below, which is exact in any case.
+// The routing index (per (s, e) entries {instance, cum_start, cum_end,
+// out_base}) is built by the prep kernels from the plan alone.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -31,7 +37,7 @@ struct Entry {
     int32_t code;       // instance r * n_local + l
     int32_t cum_start;  // first occurrence index routed here
     int32_t cum_end;    // one past the last
-    int32_t out_base;   // layout position of occurrence 0 of this (s, e) range
+    int32_t out_base;   // layout position minus occurrence index
 };
 static_assert(sizeof(Entry) == 16, "entry size");
 
@@ -65,6 +71,10 @@ __device__ int block_excl_scan(int *a, int n, int *warp_tot) {
     return carry;
 }
 
+// ---------------------------------------------------------------------------
+// Prep: instance index, routing index, layout offsets (from the plan only)
+// ---------------------------------------------------------------------------
+
 // Instances of each expert in ascending rank order, and the expert of each
 // instance.  One CTA per layer.
 __global__ void __launch_bounds__(512)
@@ -86,8 +96,7 @@ k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict_
     for (int i = threadIdx.x; i < g.n_keys; i += blockDim.x) {
         const int r = i / nl, li = i % nl;
         int e = li < ER ? mains[r * ER + li] : SE[(int64_t)r * ns + (li - ER)];
-        if (e >= E) { bad = true; e = -1; }
-        if (e < -1) { bad = true; e = -1; }
+        if (e >= E || e < -1) { bad = true; e = -1; }
         iexp[(int64_t)l * g.n_keys + i] = e;
         if (e >= 0) {
             const unsigned bit = 1u << (r & 31);
@@ -112,7 +121,6 @@ k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict_
         if (e < 0) continue;
         const int r = i / nl;
         const unsigned bit = 1u << (r & 31);
-        if (!(mask[e * RW + (r >> 5)] & bit)) continue;
         int below = 0;
         for (int w = 0; w < (r >> 5); ++w) below += __popc(mask[e * RW + w]);
         below += __popc(mask[e * RW + (r >> 5)] & (bit - 1));
@@ -120,8 +128,8 @@ k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict_
     }
 }
 
-// Routing index of one source row: per expert, its nonzero instances in
-// rank order with running occurrence ranges.  One CTA per (source, layer).
+// Routing index of one source row: per expert, its nonzero instances in rank
+// order with running occurrence ranges.  One CTA per (source, layer).
 __global__ void __launch_bounds__(256)
 k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff,
             const int32_t *__restrict__ ilist, int32_t *roff, Entry *rent, Geo g) {
@@ -154,150 +162,9 @@ k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff,
     if (threadIdx.x == 0) ro[E] = total;
 }
 
-// ---------------------------------------------------------------------------
-// Tile scan shared by rerouting and layout.
-// ---------------------------------------------------------------------------
-
-struct TileGeo {
-    int l, s, t;
-    int64_t p0;   // first pair of the tile within its layer
-    int n;        // pairs in the tile
-};
-
-__device__ __forceinline__ TileGeo tile_geo(const Geo &g) {
-    TileGeo tg;
-    const int tile = blockIdx.x;
-    tg.t = tile % g.tps;
-    tg.s = (tile / g.tps) % g.R;
-    tg.l = tile / (g.tps * g.R);
-    tg.p0 = (int64_t)tg.s * g.pps + (int64_t)tg.t * kTile;
-    int64_t p1 = tg.p0 + kTile;
-    const int64_t pend = (int64_t)(tg.s + 1) * g.pps;
-    if (p1 > pend) p1 = pend;
-    tg.n = p1 > tg.p0 ? (int)(p1 - tg.p0) : 0;
-    return tg;
-}
-
-// Copy n int32 from global to shared with 16-byte loads where aligned.
-__device__ __forceinline__ void stage_tile(const int32_t *a, int n, int32_t *dst) {
-    int head = (int)(((16 - ((uintptr_t)a & 15)) & 15) >> 2);
-    if (head > n) head = n;
-    for (int i = threadIdx.x; i < head; i += blockDim.x) dst[i] = __ldg(a + i);
-    const int4 *v = reinterpret_cast<const int4 *>(a + head);
-    const int nv = (n - head) >> 2;
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        const int4 x = __ldg(v + i);
-        int32_t *o = dst + head + 4 * i;
-        o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-    }
-    for (int i = head + nv * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(a + i);
-}
-
-// Occurrence ranking inside a staged tile.  key_of(idx) gives the expert of
-// the tile's idx-th pair, or -1 for a pair that is skipped.  cntw: [warps][E].
-// On return cntw[w][e] holds, for warp w, the occurrence index of the first
-// pair of e in w's slice (tile base included); emit(idx, e, occ) is then
-// called for every pair in pair order within each warp.
-template <typename KeyOf, typename Emit>
-__device__ __forceinline__ void rank_tile(int n, int E, const int32_t *tile_base, int *cntw,
-                                          KeyOf key_of, Emit emit) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int i = threadIdx.x; i < kScanWarps * E; i += blockDim.x) cntw[i] = 0;
-    __syncthreads();
-    int *mine = cntw + w * E;
-    const int beg = w * kWarpSeg;
-    for (int r = 0; r < kWarpSeg / 32 && beg + r * 32 < n; ++r) {
-        const int idx = beg + r * 32 + lane;
-        const int e = idx < n ? key_of(idx) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = tile_base[e];
-        for (int x = 0; x < kScanWarps; ++x) {
-            const int c = cntw[x * E + e];
-            cntw[x * E + e] = run;
-            run += c;
-        }
-    }
-    __syncthreads();
-    for (int r = 0; r < kWarpSeg / 32 && beg + r * 32 < n; ++r) {
-        const int idx = beg + r * 32 + lane;
-        const int e = idx < n ? key_of(idx) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int occ = e >= 0 ? mine[e] + __popc(peers & lt_mask) : 0;
-        __syncwarp();
-        if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
-        if (idx < n) emit(idx, e, occ);
-        __syncwarp();
-    }
-}
-
-__device__ __forceinline__ bool check_fp(const WsHeader *hdr, uint64_t want, bool mix_hist,
-                                         uint64_t part, int *flag) {
-    if (threadIdx.x == 0) {
-        const uint64_t have = mix_hist ? hdr->route_fp : hdr->hist_fp;
-        const uint64_t exp = mix_hist ? fp_mix(hdr->hist_fp, part) : want;
-        *flag = (have == exp && have != 0);
-    }
-    __syncthreads();
-    return *flag != 0;
-}
-
-__global__ void __launch_bounds__(kScanThreads)
-k_reroute_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_idx,
-                const int32_t *__restrict__ roff, const Entry *__restrict__ rent, int32_t *dst,
-                WsHeader *hdr, Geo g, uint64_t hist_fp, uint64_t route_part) {
-    extern __shared__ int smem_i[];
-    __shared__ int ok;
-    int32_t *tile = smem_i;                    // [kTile]
-    int *cntw = smem_i + kTile;                // [warps][E]
-    if (!check_fp(hdr, hist_fp, false, 0, &ok)) {
-        if (threadIdx.x == 0) set_error(hdr, TOPO_ESTATE);
-        return;
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->route_fp = fp_mix(hist_fp, route_part);
-    const TileGeo tg = tile_geo(g);
-    const int E = g.E;
-    stage_tile(ids + (int64_t)tg.l * g.npairs + tg.p0, tg.n, tile);
-    __syncthreads();
-    const int32_t *base = tile_idx + (((int64_t)tg.l * g.R + tg.s) * g.tps + tg.t) * E;
-    const int32_t *ro = roff + ((int64_t)tg.l * g.R + tg.s) * (E + 1);
-    const Entry *re = rent + ((int64_t)tg.l * g.R + tg.s) * g.n_inst_cap;
-    int32_t *out = dst + (int64_t)tg.l * g.npairs + tg.p0;
-    bool bad_id = false, bad_state = false;
-    rank_tile(
-        tg.n, E, base, cntw,
-        [&](int idx) {
-            const int e = tile[idx];
-            return (unsigned)e < (unsigned)E ? e : -1;
-        },
-        [&](int idx, int e, int occ) {
-            int code = -1;
-            if (e < 0) {
-                bad_id = true;
-            } else {
-                const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
-                for (int j = b; j < en; ++j) {
-                    const int ce = __ldg(&re[j].cum_end);
-                    if (occ < ce) { code = __ldg(&re[j].code); break; }
-                }
-                if (code < 0) bad_state = true;
-            }
-            out[idx] = code;
-        });
-    if (bad_id) set_error(hdr, TOPO_ERANGE);
-    if (bad_state) set_error(hdr, TOPO_ESTATE);
-}
-
-// Column prefix of q over sources (only where q != 0) and column totals.
+// Column prefix of q over sources (stored only where q != 0) and column totals.
 __global__ void __launch_bounds__(256)
-k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, const WsHeader *hdr, Geo g,
-           uint64_t route_part) {
-    __shared__ int ok;
-    if (!check_fp(hdr, 0, true, route_part, &ok)) return;
+k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
     const int l = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= g.n_keys) return;
@@ -325,18 +192,16 @@ k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, const Ws
     ccnt[(int64_t)l * g.n_keys + i] = run;
 }
 
-// Segment offsets (exclusive prefix of column totals); zeroes layout stats.
+// Segment offsets (exclusive prefix of the column totals); zeroes the layout
+// statistics.  One CTA per layer.
 __global__ void __launch_bounds__(1024)
-k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *seg_off, int64_t *layout_stats,
-          const WsHeader *hdr, Geo g, uint64_t route_part) {
-    __shared__ int ok;
+k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g) {
     __shared__ int warp_tot[32];
     __shared__ int carry;
-    if (!check_fp(hdr, 0, true, route_part, &ok)) return;
     const int l = blockIdx.x;
-    if (threadIdx.x < TOPO_LAYOUT_STATS) layout_stats[l * TOPO_LAYOUT_STATS + threadIdx.x] = 0;
+    if (threadIdx.x < TOPO_LAYOUT_STATS) lstat[l * TOPO_LAYOUT_STATS + threadIdx.x] = 0;
     const int32_t *c = ccnt + (int64_t)l * g.n_keys;
-    int32_t *o = seg_off + (int64_t)l * (g.n_keys + 1);
+    int32_t *o = lseg + (int64_t)l * (g.n_keys + 1);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
@@ -368,19 +233,16 @@ k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *seg_off, int64_t *layout_st
 // routing index.  One CTA per (source, layer).
 __global__ void __launch_bounds__(256)
 k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__restrict__ soff,
-              const int32_t *__restrict__ seg_off, int64_t *send_counts, int64_t *layout_stats,
-              const WsHeader *hdr, Geo g, uint64_t route_part) {
+              const int32_t *__restrict__ lseg, int64_t *lsend, int64_t *lstat, Geo g) {
     extern __shared__ long long sc[];            // [R]
-    __shared__ int ok;
     __shared__ long long red[4][32];
-    if (!check_fp(hdr, 0, true, route_part, &ok)) return;
     const int s = blockIdx.x, l = blockIdx.y, R = g.R, nl = g.n_local;
     for (int r = threadIdx.x; r < R; r += blockDim.x) sc[r] = 0;
     __syncthreads();
     const int32_t *ro = roff + ((int64_t)l * R + s) * (g.E + 1);
     Entry *re = rent + ((int64_t)l * R + s) * g.n_inst_cap;
     const int32_t *so = soff + ((int64_t)l * R + s) * g.n_keys;
-    const int32_t *seg = seg_off + (int64_t)l * (g.n_keys + 1);
+    const int32_t *seg = lseg + (int64_t)l * (g.n_keys + 1);
     const int n = ro[g.E];
     long long loc = 0, intra = 0, inter = 0, repl = 0;
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -403,12 +265,12 @@ k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__re
         if (lane == 0) red[k][w] = v;
     }
     __syncthreads();
-    int64_t *sc_out = send_counts + ((int64_t)l * R + s) * R;
+    int64_t *sc_out = lsend + ((int64_t)l * R + s) * R;
     for (int r = threadIdx.x; r < R; r += blockDim.x) sc_out[r] = sc[r];
     if (threadIdx.x < 4) {
         long long t = 0;
         for (int x = 0; x < (int)(blockDim.x >> 5); ++x) t += red[threadIdx.x][x];
-        int64_t *st = layout_stats + l * TOPO_LAYOUT_STATS;
+        int64_t *st = lstat + l * TOPO_LAYOUT_STATS;
         const int slot = threadIdx.x == 3 ? 6 : threadIdx.x;
         atomicAdd(reinterpret_cast<unsigned long long *>(&st[slot]), (unsigned long long)t);
         if (threadIdx.x < 3)
@@ -417,73 +279,362 @@ k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__re
     }
 }
 
-__global__ void __launch_bounds__(kScanThreads)
-k_layout_tiles(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_idx,
-               const int32_t *__restrict__ iexp, const int32_t *__restrict__ roff,
-               const Entry *__restrict__ rent, int32_t *sorted, WsHeader *hdr, Geo g,
-               uint64_t route_part) {
-    extern __shared__ int smem_i[];
+// ---------------------------------------------------------------------------
+// Tile kernels
+// ---------------------------------------------------------------------------
+
+struct TileGeo {
+    int l, s, t;
+    int ntok;        // tokens in this tile
+    int64_t p0;      // first pair of the tile within its layer
+    int64_t slot0;   // base of the tile in the position array (TT * k entries)
+};
+
+__device__ __forceinline__ TileGeo tile_geo(const Geo &g) {
+    TileGeo tg;
+    const int tile = blockIdx.x;
+    tg.t = tile % g.tps;
+    tg.s = (tile / g.tps) % g.R;
+    tg.l = tile / (g.tps * g.R);
+    const int tok0 = tg.t * g.TT;
+    tg.ntok = max(0, min(g.TT, g.tpr - tok0));
+    tg.p0 = ((int64_t)tg.s * g.tpr + tok0) * g.k;
+    tg.slot0 = (int64_t)tile * g.TT * g.k;
+    return tg;
+}
+
+__device__ __forceinline__ bool check_fp(const WsHeader *hdr, uint64_t want, bool routed,
+                                         uint64_t part, int *flag) {
+    if (threadIdx.x == 0) {
+        const uint64_t have = routed ? hdr->route_fp : hdr->hist_fp;
+        const uint64_t exp = routed ? fp_mix(hdr->hist_fp, part) : want;
+        *flag = (have == exp && have != 0);
+    }
+    __syncthreads();
+    return *flag != 0;
+}
+
+// Instance and layout base for occurrence occ of an expert in this source
+// row.  f: the expert's first entry {code, cum_end, out_base, index};
+// ro_next: offset one past its last entry (read only when f does not hold occ).
+__device__ __forceinline__ int route_lookup(int4 f, int occ, const int32_t *ro_next, const Entry *re,
+                                            int *out_base) {
+    if (occ < f.y) { *out_base = f.z; return f.x; }
+    const int en = __ldg(ro_next);
+    for (int j = f.w + 1; j < en; ++j) {
+        const int ce = __ldg(&re[j].cum_end);
+        if (occ < ce) {
+            *out_base = __ldg(&re[j].out_base);
+            return __ldg(&re[j].code);
+        }
+    }
+    return -1;
+}
+
+// Position-array index of pair (token t of the tile, slot j).
+__device__ __forceinline__ int64_t pos_index(const Geo &g, const TileGeo &tg, int t, int j) {
+    return tg.slot0 + ((int64_t)(t >> 5) * g.k + j) * 32 + (t & 31);
+}
+
+// Exact ranking of one tile with warp match_any, pair-major, ids read from
+// global memory.  Used for k > KMAX and for tiles where a token repeats an
+// expert.  cntw: [kRankWarps][E] shared.
+template <bool kFused>
+__device__ void rank_tile_exact(const Geo &g, const TileGeo &tg, const int32_t *ids_layer,
+                                const int32_t *tile_base, const int32_t *ro, const Entry *re,
+                                int *cntw, int32_t *dst_layer, int32_t *pos_ws,
+                                int32_t *sorted_layer, bool &bad_id, bool &bad_state) {
+    const int E = g.E, k = g.k;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int n = tg.ntok * k;
+    const int seg = ((n + kRankWarps - 1) / kRankWarps + 31) & ~31;
+    const int beg = w * seg, end = min(n, beg + seg);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cntw[i] = 0;
+    __syncthreads();
+    int *mine = cntw + w * E;
+    for (int b = beg; b < end; b += 32) {
+        const int idx = b + lane;
+        int e = idx < end ? __ldg(ids_layer + tg.p0 + idx) : -1;
+        if ((unsigned)e >= (unsigned)E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = __ldg(tile_base + e);
+        for (int x = 0; x < kRankWarps; ++x) {
+            const int c = cntw[x * E + e];
+            cntw[x * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int b = beg; b < end; b += 32) {
+        const int idx = b + lane;
+        const bool valid = idx < end;
+        int e = valid ? __ldg(ids_layer + tg.p0 + idx) : -1;
+        if (valid && (unsigned)e >= (unsigned)E) { bad_id = true; e = -1; }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int occ = e >= 0 ? mine[e] + __popc(peers & lt_mask) : 0;
+        __syncwarp();
+        if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
+        if (valid) {
+            int code = -1, ob = 0;
+            if (e >= 0) {
+                const int f = __ldg(ro + e), en = __ldg(ro + e + 1);
+                for (int j = f; j < en; ++j) {
+                    if (occ < __ldg(&re[j].cum_end)) {
+                        code = __ldg(&re[j].code);
+                        ob = __ldg(&re[j].out_base);
+                        break;
+                    }
+                }
+                if (code < 0) bad_state = true;
+            }
+            const int t = idx / k, j = idx - t * k;
+            dst_layer[tg.p0 + idx] = code;
+            const int64_t pos = code >= 0 ? (int64_t)ob + occ : -1;
+            if (kFused) {
+                if (pos >= 0 && pos < g.npairs) sorted_layer[pos] = (int32_t)(tg.p0 + idx);
+                else if (code >= 0) bad_state = true;
+            } else {
+                pos_ws[pos_index(g, tg, t, j)] = (int32_t)pos;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Shared-memory layout of k_route_tiles.
+struct RankSmem {
+    int4 *first;     // [E] first routing entry of each expert in this row
+    int *basew;      // [kRankWarps][E] per-warp running occurrence base
+    unsigned *mskw;  // [kRankWarps][E] per-warp token bitmask of the round
+    int32_t *keys;   // [TT][kp] ids, then the instance codes, in place
+};
+
+__device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
+    RankSmem r;
+    r.first = reinterpret_cast<int4 *>(sm);
+    r.basew = sm + 4 * g.E;
+    r.mskw = reinterpret_cast<unsigned *>(r.basew + kRankWarps * g.E);
+    r.keys = reinterpret_cast<int32_t *>(r.mskw + kRankWarps * g.E);
+    return r;
+}
+
+// One CTA per tile.  kFused: write the layout (sorted pairs) directly;
+// otherwise store each pair's layout position in the workspace for
+// topo_dispatch_layout.  KMAX: compile-time bound on k for the fast path.
+template <int KMAX, bool kFused>
+__global__ void __launch_bounds__(kRankThreads, 2)
+k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_idx,
+              const int32_t *__restrict__ roff, const Entry *__restrict__ rent, int32_t *dst,
+              int32_t *pos_ws, int32_t *sorted, WsHeader *hdr, Geo g, uint64_t hist_fp,
+              uint64_t route_part) {
+    extern __shared__ int sm[];
     __shared__ int ok;
-    int32_t *tile = smem_i;
-    int *cntw = smem_i + kTile;
+    if (!check_fp(hdr, hist_fp, false, 0, &ok)) {
+        if (threadIdx.x == 0) set_error(hdr, TOPO_ESTATE);
+        return;
+    }
+    if (!kFused && blockIdx.x == 0 && threadIdx.x == 0) hdr->route_fp = fp_mix(hist_fp, route_part);
+    const TileGeo tg = tile_geo(g);
+    const int E = g.E, k = g.k, kp = g.kp;
+    const RankSmem S = rank_smem(g, sm);
+    const int32_t *ids_layer = ids + (int64_t)tg.l * g.npairs;
+    int32_t *dst_layer = dst + (int64_t)tg.l * g.npairs;
+    int32_t *sorted_layer = kFused ? sorted + (int64_t)tg.l * g.npairs : nullptr;
+    const int32_t *tbase = tile_idx + (((int64_t)tg.l * g.R + tg.s) * g.tps + tg.t) * E;
+    const int32_t *ro = roff + ((int64_t)tg.l * g.R + tg.s) * (E + 1);
+    const Entry *re = rent + ((int64_t)tg.l * g.R + tg.s) * g.n_inst_cap;
+    bool bad_id = false, bad_state = false;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned bit = 1u << lane, lt_mask = bit - 1u;
+
+    // stage: ids token-major with an odd stride (conflict-free per lane),
+    // first routing entry per expert, zeroed per-warp tables
+    const bool fast = k <= KMAX;
+    if (fast) {
+        const int32_t *src = ids_layer + tg.p0;
+        for (int t = threadIdx.x; t < tg.ntok; t += blockDim.x)
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < k) S.keys[t * kp + j] = __ldg(src + (int64_t)t * k + j);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
+        int4 f = make_int4(-1, 0, 0, b);
+        if (b < en) {
+            const Entry x = re[b];
+            f = make_int4(x.code, x.cum_end, x.out_base, b);
+        }
+        S.first[e] = f;
+    }
+    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) {
+        S.basew[i] = 0;
+        S.mskw[i] = 0;
+    }
+    __syncthreads();
+
+    bool dup = !fast;
+    if (fast) {
+        int *mybase = S.basew + w * E;
+        unsigned *mymsk = S.mskw + w * E;
+        // pass 1: per-warp counts over its rounds
+        for (int r = 0; r < g.RW; ++r) {
+            const int t = (w * g.RW + r) * 32 + lane;
+            if (t < tg.ntok) {
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= k) break;
+                    const int e = S.keys[t * kp + j];
+                    if ((unsigned)e < (unsigned)E) atomicAdd(&mybase[e], 1);
+                }
+            }
+        }
+        __syncthreads();
+        // pass 2: warp bases = tile base + counts of the warps before
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            int run = __ldg(tbase + e);
+#pragma unroll
+            for (int x = 0; x < kRankWarps; ++x) {
+                const int c = S.basew[x * E + e];
+                S.basew[x * E + e] = run;
+                run += c;
+            }
+        }
+        __syncthreads();
+        // pass 3: rank each round of 32 tokens with per-expert token bitmasks
+        for (int r = 0; r < g.RW; ++r) {
+            const int t = (w * g.RW + r) * 32 + lane;
+            const bool vt = t < tg.ntok;
+            int ek[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                ek[j] = -1;
+                if (j < k && vt) {
+                    const int e = S.keys[t * kp + j];
+                    if ((unsigned)e < (unsigned)E) ek[j] = e;
+                    else bad_id = true;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (ek[j] >= 0) dup |= (atomicOr(&mymsk[ek[j]], bit) & bit) != 0;
+            __syncwarp();
+            int nb[KMAX];
+            unsigned lead = 0;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                nb[j] = 0;
+                if (j >= k) continue;
+                int code = -1, ob = 0, occ = 0;
+                if (ek[j] >= 0) {
+                    const unsigned m = mymsk[ek[j]];
+                    const int b = mybase[ek[j]];
+                    const int rk = __popc(m & lt_mask);
+                    occ = b + rk;
+                    if (rk == 0) {
+                        lead |= 1u << j;
+                        nb[j] = b + __popc(m);
+                    }
+                    code = route_lookup(S.first[ek[j]], occ, ro + ek[j] + 1, re, &ob);
+                    if (code < 0) bad_state = true;
+                }
+                if (vt) {
+                    S.keys[t * kp + j] = code;
+                    if (kFused) {
+                        const int64_t pos = (int64_t)ob + occ;
+                        if (code >= 0 && pos >= 0 && pos < g.npairs)
+                            sorted_layer[pos] = (int32_t)(tg.p0 + (int64_t)t * k + j);
+                        else if (code >= 0)
+                            bad_state = true;
+                    }
+                }
+                if (!kFused)
+                    pos_ws[pos_index(g, tg, t, j)] = (vt && code >= 0) ? ob + occ : -1;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if ((lead >> j) & 1u) {
+                    mybase[ek[j]] = nb[j];
+                    mymsk[ek[j]] = 0;
+                }
+            __syncwarp();
+        }
+    }
+    if (__syncthreads_or(dup)) {
+        // a token repeats an expert (or k > KMAX): redo the tile exactly
+        rank_tile_exact<kFused>(g, tg, ids_layer, tbase, ro, re, S.basew, dst_layer, pos_ws,
+                                sorted_layer, bad_id, bad_state);
+    } else {
+        // instance codes out, pair order, coalesced
+        const int n = tg.ntok * k;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int t = div_k(g, i);
+            dst_layer[tg.p0 + i] = S.keys[t * kp + (i - t * k)];
+        }
+    }
+    if (bad_id) set_error(hdr, TOPO_ERANGE);
+    if (bad_state) set_error(hdr, TOPO_ESTATE);
+}
+
+// Layout from the positions topo_reroute stored: sorted[pos] = pair.
+__global__ void __launch_bounds__(256)
+k_layout_scatter(const int32_t *__restrict__ pos_ws, int32_t *sorted, WsHeader *hdr, Geo g,
+                 uint64_t route_part) {
+    __shared__ int ok;
     if (!check_fp(hdr, 0, true, route_part, &ok)) {
         if (threadIdx.x == 0) set_error(hdr, TOPO_ESTATE);
         return;
     }
     const TileGeo tg = tile_geo(g);
-    const int E = g.E;
-    stage_tile(dst + (int64_t)tg.l * g.npairs + tg.p0, tg.n, tile);
-    __syncthreads();
-    const int32_t *base = tile_idx + (((int64_t)tg.l * g.R + tg.s) * g.tps + tg.t) * E;
-    const int32_t *ro = roff + ((int64_t)tg.l * g.R + tg.s) * (E + 1);
-    const Entry *re = rent + ((int64_t)tg.l * g.R + tg.s) * g.n_inst_cap;
-    const int32_t *ie = iexp + (int64_t)tg.l * g.n_keys;
+    const int k = g.k;
+    const int n = g.TT * k;
     int32_t *out = sorted + (int64_t)tg.l * g.npairs;
-    const int n_keys = g.n_keys;
-    const int64_t npairs = g.npairs;
     bool bad = false;
-    rank_tile(
-        tg.n, E, base, cntw,
-        [&](int idx) {
-            const int code = tile[idx];
-            return (unsigned)code < (unsigned)n_keys ? __ldg(ie + code) : -1;
-        },
-        [&](int idx, int e, int occ) {
-            const int code = tile[idx];
-            if (e < 0) { bad = true; return; }
-            const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
-            for (int j = b; j < en; ++j) {
-                if (__ldg(&re[j].code) != code) continue;
-                const int cs = __ldg(&re[j].cum_start), ce = __ldg(&re[j].cum_end);
-                if (occ < cs || occ >= ce) break;
-                const int64_t pos = (int64_t)__ldg(&re[j].out_base) + occ;
-                if (pos < 0 || pos >= npairs) break;          // plan inconsistent with the pairs
-                out[pos] = (int32_t)(tg.p0 + idx);
-                return;
-            }
-            bad = true;
-        });
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int wr = div_k(g, i >> 5);   // (i / 32) / k
+        const int t = wr * 32 + (i & 31);
+        if (t >= tg.ntok) continue;
+        const int v = __ldcs(pos_ws + tg.slot0 + i);
+        const int j = (i >> 5) - wr * k;
+        if (v < 0 || v >= g.npairs) { bad = true; continue; }
+        out[v] = (int32_t)(tg.p0 + (int64_t)t * k + j);
+    }
     if (bad) set_error(hdr, TOPO_ESTATE);
 }
 
-size_t tile_smem_bytes(const Geo &g) { return (size_t)kTile * 4 + (size_t)kScanWarps * g.E * 4; }
+// Copy the small layout outputs computed by the prep kernels.
+__global__ void __launch_bounds__(256)
+k_lay_copy(const int32_t *__restrict__ lseg, const int64_t *__restrict__ lsend,
+           const int64_t *__restrict__ lstat, int32_t *seg_off, int64_t *send_counts,
+           int64_t *layout_stats, const WsHeader *hdr, Geo g, uint64_t route_part, int check) {
+    __shared__ int ok;
+    if (check && !check_fp(hdr, 0, true, route_part, &ok)) return;
+    const int64_t nseg = (int64_t)g.L * (g.n_keys + 1);
+    const int64_t nsend = (int64_t)g.L * g.R * g.R;
+    const int64_t nst = (int64_t)g.L * TOPO_LAYOUT_STATS;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nseg + nsend + nst;
+         i += stride) {
+        if (i < nseg) seg_off[i] = lseg[i];
+        else if (i < nseg + nsend) send_counts[i - nseg] = lsend[i - nseg];
+        else layout_stats[i - nseg - nsend] = lstat[i - nseg - nsend];
+    }
+}
 
 cudaError_t set_smem(const void *fn, size_t bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-}  // namespace
-
-size_t route_smem_bytes(const Geo &g) {
-    const size_t a = tile_smem_bytes(g);
-    const size_t b = (size_t)g.E * ((g.R + 31) / 32) * 4 + (size_t)g.E * 4;
-    return a > b ? a : b;
-}
-
-cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
-                           const topo_plan_t &p, int32_t *dst, void *ws, uint64_t hist_fp,
-                           uint64_t route_part, cudaStream_t st) {
+// Prep shared by topo_reroute and topo_reroute_layout.
+cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_t &p, void *ws,
+                        cudaStream_t st) {
     cudaError_t e;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     if ((e = launch_main_tables(g, main_rank, ws, nullptr, 0, st)) != cudaSuccess) return e;
@@ -500,39 +651,80 @@ cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t
         p.route_cnt, ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem_t = tile_smem_bytes(g);
-    if ((e = set_smem((const void *)k_reroute_tiles, smem_t)) != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
-    k_reroute_tiles<<<(unsigned)tiles, kScanThreads, smem_t, st>>>(
-        ids, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_roff),
-        ws_at<Entry>(ws, g.off_rent), dst, hdr, g, hist_fp, route_part);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_layout(const Geo &g, const int32_t *dst, const topo_plan_t &p, int32_t *sorted,
-                          int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
-                          uint64_t route_part, cudaStream_t st) {
-    cudaError_t e;
-    WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     k_lay_cols<<<dim3((g.n_keys + 255) / 256, g.L), 256, 0, st>>>(
-        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), hdr, g, route_part);
+        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_lay_seg<<<g.L, 1024, 0, st>>>(ws_at<int32_t>(ws, g.off_ccnt), seg_off, layout_stats, hdr, g,
-                                    route_part);
+    k_lay_seg<<<g.L, 1024, 0, st>>>(ws_at<int32_t>(ws, g.off_ccnt), ws_at<int32_t>(ws, g.off_lseg),
+                                    ws_at<int64_t>(ws, g.off_lstat), g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem_e = (size_t)g.R * 8;
     if ((e = set_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
     k_lay_entries<<<dim3(g.R, g.L), 256, smem_e, st>>>(
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), ws_at<int32_t>(ws, g.off_soff),
-        seg_off, send_counts, layout_stats, hdr, g, route_part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem_t = tile_smem_bytes(g);
-    if ((e = set_smem((const void *)k_layout_tiles, smem_t)) != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
-    k_layout_tiles<<<(unsigned)tiles, kScanThreads, smem_t, st>>>(
-        dst, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_iexp),
-        ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), sorted, hdr, g, route_part);
+        ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
+        ws_at<int64_t>(ws, g.off_lstat), g);
     return cudaGetLastError();
+}
+
+template <bool kFused>
+cudaError_t launch_tiles(const Geo &g, const int32_t *ids, int32_t *dst, int32_t *sorted, void *ws,
+                         uint64_t hist_fp, uint64_t route_part, cudaStream_t st) {
+    auto kern = g.k <= 4 ? k_route_tiles<4, kFused>
+                         : (g.k <= 8 ? k_route_tiles<8, kFused> : k_route_tiles<16, kFused>);
+    const size_t smem = rank_smem_bytes(g);
+    cudaError_t e;
+    if ((e = set_smem((const void *)kern, smem)) != cudaSuccess) return e;
+    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    kern<<<(unsigned)tiles, kRankThreads, smem, st>>>(
+        ids, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_roff),
+        ws_at<Entry>(ws, g.off_rent), dst, ws_at<int32_t>(ws, g.off_pos), sorted,
+        ws_at<WsHeader>(ws, 0), g, hist_fp, route_part);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
+                        void *ws, uint64_t route_part, int check, cudaStream_t st) {
+    const int64_t n = (int64_t)g.L * (g.n_keys + 1 + (int64_t)g.R * g.R + TOPO_LAYOUT_STATS);
+    const int64_t want = (n + 255) / 256;
+    const int blocks = (int)(want < 1024 ? want : 1024);
+    k_lay_copy<<<blocks, 256, 0, st>>>(ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
+                                       ws_at<int64_t>(ws, g.off_lstat), seg_off, send_counts,
+                                       layout_stats, ws_at<WsHeader>(ws, 0), g, route_part, check);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t rank_smem_bytes(const Geo &g) {
+    return (size_t)g.E * 16 + (size_t)kRankWarps * g.E * 8 + (size_t)g.TT * g.kp * 4;
+}
+
+cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
+                           const topo_plan_t &p, int32_t *dst, void *ws, uint64_t hist_fp,
+                           uint64_t route_part, cudaStream_t st) {
+    cudaError_t e;
+    if ((e = launch_prep(g, main_rank, p, ws, st)) != cudaSuccess) return e;
+    return launch_tiles<false>(g, ids, dst, nullptr, ws, hist_fp, route_part, st);
+}
+
+cudaError_t launch_layout(const Geo &g, int32_t *sorted, int32_t *seg_off, int64_t *send_counts,
+                          int64_t *layout_stats, void *ws, uint64_t route_part, cudaStream_t st) {
+    cudaError_t e;
+    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    k_layout_scatter<<<(unsigned)tiles, 256, 0, st>>>(ws_at<int32_t>(ws, g.off_pos), sorted,
+                                                      ws_at<WsHeader>(ws, 0), g, route_part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_copy(g, seg_off, send_counts, layout_stats, ws, route_part, 1, st);
+}
+
+cudaError_t launch_reroute_layout(const Geo &g, const int32_t *main_rank, const int32_t *ids,
+                                  const topo_plan_t &p, int32_t *dst, int32_t *sorted,
+                                  int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
+                                  void *ws, uint64_t hist_fp, cudaStream_t st) {
+    cudaError_t e;
+    if ((e = launch_prep(g, main_rank, p, ws, st)) != cudaSuccess) return e;
+    if ((e = launch_tiles<true>(g, ids, dst, sorted, ws, hist_fp, 0, st)) != cudaSuccess) return e;
+    return launch_copy(g, seg_off, send_counts, layout_stats, ws, 0, 0, st);
 }
 
 }  // namespace topo

@@ -27,27 +27,56 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     if (c->tok_bytes * (int64_t)c->c_inter >= (int64_t(1) << 31)) return TOPO_EINVAL;
     if (c->expert_bytes * (int64_t)c->c_inter >= (int64_t(1) << 40)) return TOPO_EINVAL;
     if ((int64_t)c->R * c->n_slot > (1 << 20)) return TOPO_EINVAL;
+    if (c->k > kMaxK) return TOPO_EINVAL;
     // shared-memory capacity of the kernels (227 KB per CTA on sm_103a)
-    const int64_t kSmem = 227 * 1024, E = c->E, R = c->R, rpn = c->ranks_per_node;
+    const int64_t E = c->E, R = c->R, rpn = c->ranks_per_node;
     const int64_t nl = E / R + c->n_slot;
     if (nl > 32767) return TOPO_EINVAL;
-    if ((int64_t)kTile * 4 + (int64_t)kScanWarps * E * 4 > kSmem) return TOPO_EINVAL;
-    if (E * ((R + 31) / 32 + 1) * 4 > kSmem) return TOPO_EINVAL;
-    if ((2 * rpn + 2 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmem) return TOPO_EINVAL;
+    if (E * ((R + 31) / 32 + 1) * 4 > kSmemMax) return TOPO_EINVAL;
+    if ((2 * rpn + 2 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmemMax) return TOPO_EINVAL;
     std::memset(g, 0, sizeof *g);
     g->T = c->T; g->E = c->E; g->k = c->k; g->R = c->R; g->rpn = c->ranks_per_node;
     g->n_slot = c->n_slot; g->M = c->R / c->ranks_per_node; g->E_R = c->E / c->R;
-    g->n_local = g->E_R + c->n_slot; g->L = n_layers;
+    g->n_local = (int32_t)nl; g->L = n_layers;
     g->c_intra = c->c_intra; g->c_inter = c->c_inter; g->max_iters = c->max_refine_iters;
     g->S_tok = c->tok_bytes; g->W = c->expert_bytes;
-    g->pps = (int64_t)(c->T / c->R) * c->k;
+    g->tpr = c->T / c->R;
+    g->pps = (int64_t)g->tpr * c->k;
     g->npairs = (int64_t)c->T * c->k;
-    g->tps = g->pps == 0 ? 1 : (int32_t)((g->pps + kTile - 1) / kTile);
+    g->kp = (c->k & 1) ? c->k : c->k + 1;
+    g->kmagic = c->k == 1 ? 0u : (uint32_t)(((uint64_t(1) << 32) + c->k - 1) / c->k);
+    // Tile geometry: RW rounds of 32 tokens per warp, within the shared-memory
+    // budget of two rank CTAs per SM and about kTilePairsTarget pairs; among
+    // the admissible RW take the one with the least work per source counting
+    // a fixed per-tile cost of 1.5 rounds.
+    const int64_t tables = E * (16 + 8 * kRankWarps);
+    const int64_t round_bytes = (int64_t)kRankThreads * g->kp * 4;
+    int64_t rw_max = kTilePairsTarget / ((int64_t)kRankThreads * c->k);
+    const int64_t rw_smem = (kRankSmemTarget - tables) / round_bytes;
+    if (rw_smem < rw_max) rw_max = rw_smem;
+    if (rw_max < 1) {
+        rw_max = 1;
+        if (tables + round_bytes > kSmemMax - 1024) return TOPO_EINVAL;
+    }
+    const int64_t rw_need = (g->tpr + kRankThreads - 1) / kRankThreads;
+    if (rw_max > rw_need && rw_need > 0) rw_max = rw_need;
+    int64_t best_rw = 1;
+    double best_cost = -1.0;
+    for (int64_t rw = 1; rw <= rw_max; ++rw) {
+        const int64_t tps = g->tpr == 0 ? 1 : (g->tpr + kRankThreads * rw - 1) / (kRankThreads * rw);
+        const double cost = (double)tps * ((double)rw + 1.5);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_rw = rw; }
+    }
+    g->RW = (int32_t)best_rw;
+    g->TT = kRankThreads * g->RW;
+    g->tps = g->tpr == 0 ? 1 : (g->tpr + g->TT - 1) / g->TT;
     g->n_inst_cap = c->E + c->R * c->n_slot;
     g->n_keys = c->R * g->n_local;
     const size_t L = (size_t)n_layers;
+    const size_t tiles = L * (size_t)R * g->tps;
     size_t off = sizeof(WsHeader);
-    g->off_tile = off;  off = align_up(off + L * R * g->tps * E * 4);
+    g->off_tile = off;  off = align_up(off + tiles * E * 4);
+    g->off_pos = off;   off = align_up(off + tiles * g->TT * c->k * 4);
     g->off_done = off;  off = align_up(off + L * R * 4);
     g->off_main = off;  off = align_up(off + 3 * E * 4);
     g->off_rep = off;   off = align_up(off + L * E * g->M * 4);
@@ -58,6 +87,9 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     g->off_rent = off;  off = align_up(off + L * R * g->n_inst_cap * 16);
     g->off_soff = off;  off = align_up(off + L * R * g->n_keys * 4);
     g->off_ccnt = off;  off = align_up(off + L * g->n_keys * 4);
+    g->off_lseg = off;  off = align_up(off + L * (g->n_keys + 1) * 4);
+    g->off_lsend = off; off = align_up(off + L * R * R * 8);
+    g->off_lstat = off; off = align_up(off + L * TOPO_LAYOUT_STATS * 8);
     g->total = off;
     return TOPO_OK;
 }
@@ -99,7 +131,7 @@ extern "C" {
 
 size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call) {
     if (which_call == TOPO_CALL_COOCCUR) return sizeof(WsHeader);
-    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_CHAIN) return 0;
+    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_REROUTE_LAYOUT) return 0;
     Geo g;
     if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
     return g.total;
@@ -156,8 +188,24 @@ int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *d
     if ((!dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
-    return cuda_rc(launch_layout(g, dst_inst, *plan, sorted_pairs, seg_off, send_counts, layout_stats,
-                                 ws, route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
+    return cuda_rc(launch_layout(g, sorted_pairs, seg_off, send_counts, layout_stats, ws,
+                                 route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
+}
+
+int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids,
+                        const topo_plan_t *plan, int32_t *dst_inst, int32_t *sorted_pairs,
+                        int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!ws || !plan_ok(plan, g) || !seg_off || !send_counts || !layout_stats) return TOPO_EINVAL;
+    if ((!ids || !dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_reroute_layout(g, cfg->main_rank, ids, *plan, dst_inst, sorted_pairs, seg_off,
+                                         send_counts, layout_stats, ws, hist_fingerprint(g, ids),
+                                         stream));
 }
 
 int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids, int64_t *co,

@@ -11,7 +11,7 @@ import torch
 
 from . import (TOPO_CALL_CHAIN, TOPO_CALL_COOCCUR, TOPO_LAYOUT_STATS, TOPO_STATS, make_cfg,
                make_plan, topo_cooccur, topo_dispatch_layout, topo_hist, topo_plan, topo_read_error,
-               topo_reroute, topo_workspace_bytes, topo_ws_reset)
+               topo_reroute, topo_reroute_layout, topo_workspace_bytes, topo_ws_reset)
 
 
 @dataclasses.dataclass
@@ -89,12 +89,22 @@ class Planner:
         topo_dispatch_layout(self.cfg, self.L, b.dst_inst, self.plan, b.sorted_pairs, b.seg_off,
                              b.send_counts, b.layout_stats, self.ws, self.ws_bytes, self._stream())
 
-    def run(self, ids: torch.Tensor):
-        """The whole hot path on one batch of ids (device int32 [L, T, k])."""
+    def reroute_layout(self, ids: torch.Tensor):
+        b = self.buf
+        topo_reroute_layout(self.cfg, self.L, ids, self.plan, b.dst_inst, b.sorted_pairs, b.seg_off,
+                            b.send_counts, b.layout_stats, self.ws, self.ws_bytes, self._stream())
+
+    def run(self, ids: torch.Tensor, fused: bool = True):
+        """The whole hot path on one batch of ids (device int32 [L, T, k]):
+        histogram, plan, rerouting and dispatch layout (fused into one pass
+        over the pairs unless fused=False)."""
         self.hist(ids)
         self.make_plan()
-        self.reroute(ids)
-        self.layout()
+        if fused:
+            self.reroute_layout(ids)
+        else:
+            self.reroute(ids)
+            self.layout()
 
     def error(self) -> int:
         """Device error word (synchronises the device)."""

@@ -23,7 +23,7 @@ def _dev():
     return torch.device("cuda:0")
 
 
-def gpu_chain(cfg, ids):
+def gpu_chain(cfg, ids, fused=True):
     from moe_expert_routing_ids_gb300.planner import Planner
     dev = _dev()
     L = ids.shape[0]
@@ -31,7 +31,7 @@ def gpu_chain(cfg, ids):
     gcfg = dict(cfg, main_rank=None if mr is None else torch.as_tensor(mr, dtype=torch.int32, device=dev))
     P = Planner(gcfg, L, dev)
     d_ids = torch.as_tensor(ids, device=dev).contiguous()
-    P.run(d_ids)
+    P.run(d_ids, fused=fused)
     err = P.error()
     out = P.numpy()
     return out, err
@@ -59,11 +59,13 @@ def assert_same(gpu, orc, keys=None):
                                  f"oracle {b[first]}")
 
 
-def check(cfg, ids):
-    gpu, err = gpu_chain(cfg, ids)
-    assert err == 0, f"device error {err}"
-    assert_same(gpu, oracle_chain(cfg, ids))
-    return gpu
+def check(cfg, ids, both=True):
+    """Both the fused reroute+layout call and the separate calls."""
+    want = oracle_chain(cfg, ids)
+    for fused in ((True, False) if both else (True,)):
+        gpu, err = gpu_chain(cfg, ids, fused)
+        assert err == 0, f"device error {err} (fused={fused})"
+        assert_same(gpu, want)
 
 
 @pytest.mark.parametrize("index", [1, 2, 3, 5])
@@ -105,7 +107,25 @@ EDGE = {
     "tiny": (_cfg(2, 2, 1, 2, 1, 1, S=1, Wb=1), lambda c: np.array([[[1], [1]]], np.int32)),
     "three_layers": (_cfg(16 * 700, 64, 6, 16, 8, 8, S=8192, Wb=34_603_008),
                      lambda c: W.random_small(11, c["T"], c["E"], c["k"], 3, s=1.2)),
+    "k_above_fast_path": (_cfg(8 * 600, 64, 20, 8, 4, 4, S=256, Wb=20_000),
+                          lambda c: W.random_small(13, c["T"], c["E"], c["k"], 1, s=1.1)),
+    "k16_two_rounds": (_cfg(4 * 1100, 64, 16, 4, 2, 4, S=256, Wb=20_000),
+                       lambda c: W.random_small(14, c["T"], c["E"], c["k"], 1, s=1.1)),
+    "k3_odd": (_cfg(8 * 777, 24, 3, 8, 4, 3, S=256, Wb=5_000),
+               lambda c: W.random_small(15, c["T"], c["E"], c["k"], 1, s=1.3)),
+    "repeated_ids_in_a_token": (_cfg(8 * 700, 16, 4, 8, 4, 2, S=256, Wb=5_000),
+                                lambda c: _with_repeats(W.random_small(16, c["T"], c["E"], c["k"], 1, s=1.2))),
 }
+
+
+def _with_repeats(ids):
+    """Plant a repeated expert inside some tokens (not Top-k, but the
+    definitions use count vectors and the kernels must stay exact)."""
+    ids = ids.copy()
+    ids[0, 5, 1] = ids[0, 5, 0]
+    ids[0, 1300, 3] = ids[0, 1300, 2]
+    ids[0, -1, 2] = ids[0, -1, 0]
+    return ids
 
 
 @pytest.mark.parametrize("name", sorted(EDGE))
@@ -227,7 +247,7 @@ def test_layout_with_foreign_dst_is_rejected():
     cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)
     ids = torch.as_tensor(W.random_small(3, 400, 8, 2, 1), device=dev)
     P = Planner(cfg, 1, dev)
-    P.run(ids)
+    P.run(ids, fused=False)
     assert P.error() == 0
     P.buf.dst_inst = P.buf.dst_inst.clone()   # not the buffer topo_reroute wrote
     P.layout()
