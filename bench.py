@@ -142,6 +142,46 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class GraphEvents:
+    """CUDA events recorded as graph nodes (cudaEventRecordExternal), so a
+    captured step keeps per-call timestamps on every replay."""
+
+    def __init__(self, n):
+        import ctypes
+        import ctypes.util
+        names = ["libcudart.so.13", "libcudart.so", ctypes.util.find_library("cudart") or ""]
+        for n_ in names:
+            try:
+                self.rt = ctypes.CDLL(n_)
+                break
+            except OSError:
+                continue
+        else:
+            raise RuntimeError("libcudart not found")
+        self.ct = ctypes
+        self.ev = []
+        for _ in range(n):
+            h = ctypes.c_void_p()
+            if self.rt.cudaEventCreate(ctypes.byref(h)) != 0:
+                raise RuntimeError("cudaEventCreate failed")
+            self.ev.append(h)
+
+    def record(self, i, stream):
+        rc = self.rt.cudaEventRecordWithFlags(self.ev[i], self.ct.c_void_p(stream.cuda_stream), 1)
+        if rc != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed: {rc}")
+
+    def elapsed(self, i, j):
+        ms = self.ct.c_float()
+        if self.rt.cudaEventElapsedTime(self.ct.byref(ms), self.ev[i], self.ev[j]) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return ms.value
+
+    def close(self):
+        for h in self.ev:
+            self.rt.cudaEventDestroy(h)
+
+
 def cpu_sample_chain(w, ids_layer):
     """Oracle chain on one microbatch: (seconds, pairs)."""
     import oracle
@@ -195,28 +235,59 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------------ ours
 
-def time_chain(P, d_ids, steps, stream):
+STEPS_PER_GRAPH = 20
+
+
+def capture_steps(P, d_ids, n_steps, stream, gev):
+    """One CUDA graph of n_steps whole steps, with an event node before every
+    call and after the last one (len(CALLS) * n_steps + 1 events)."""
     import torch
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(CALLS) + 1)] for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for k in range(steps):
-            e = ev[k]
-            e[0].record(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(n_steps):
+            base = k * len(CALLS)
+            gev.record(base, stream)
             P.hist(d_ids)
-            e[1].record(stream)
+            gev.record(base + 1, stream)
             P.make_plan()
-            e[2].record(stream)
+            gev.record(base + 2, stream)
             P.reroute_layout(d_ids)
-            e[3].record(stream)
-        t1.record(stream)
-    return t0, t1, ev
+        gev.record(n_steps * len(CALLS), stream)
+    return graph
+
+
+def time_chain(P, d_ids, steps, stream):
+    """Replays a captured 20-step graph until `steps` steps ran; returns total
+    ms (events around all replays) and mean ms per call."""
+    import torch
+    n_in = min(STEPS_PER_GRAPH, steps)
+    reps = -(-steps // n_in)
+    gev = GraphEvents(n_in * len(CALLS) + 1)
+    graph = capture_steps(P, d_ids, n_in, stream, gev)
+    graph.replay()                                  # settle
+    torch.cuda.synchronize()
+    per_call = {c: [] for c in CALLS}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            graph.replay()
+            t1.record(stream)
+        t1.synchronize()
+        total += t0.elapsed_time(t1)
+        for k in range(n_in):
+            for i, c in enumerate(CALLS):
+                per_call[c].append(gev.elapsed(k * len(CALLS) + i, k * len(CALLS) + i + 1))
+    gev.close()
+    del graph
+    return total, reps * n_in, {c: statistics.mean(v) for c, v in per_call.items()}
 
 
 def secondary_plan_latency(dev, stream):
-    """topo_plan latency per layer on the T=16384, E=64, R=32 workload, mean of
-    200 calls after 20 warm-ups (TopoEP §6.3 protocol)."""
+    """topo_plan latency per layer on the T=16384, E=64, R=32 workload: 200
+    calls captured in one CUDA graph, after 20 warm-up calls (TopoEP §6.3
+    protocol), mean per call."""
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
     from moe_expert_routing_ids_gb300.planner import Planner
@@ -227,15 +298,22 @@ def secondary_plan_latency(dev, stream):
         P.hist(ids)
         for _ in range(20):
             P.make_plan()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
         for _ in range(200):
             P.make_plan()
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        graph.replay()
         b.record(stream)
     b.synchronize()
     us = a.elapsed_time(b) * 1e3 / 200 / w.n_layers
     return {"workload": w.name, "us_per_layer": round(us, 2), "reps": 200, "warmup": 20,
-            "target_us": 50}
+            "target_us": 50, "timing": "200 calls in one CUDA graph"}
 
 
 def secondary_cooccur(dev, stream, hbm_peak):
@@ -246,22 +324,29 @@ def secondary_cooccur(dev, stream, hbm_peak):
     C = Cooccur(w.n_layers, w.T, w.E, w.k, dev)
     ids = torch.as_tensor(w.ids(), device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    times = []
+    gev = GraphEvents(2)
     with torch.cuda.stream(stream):
-        for i in range(13):
-            flush.fill_(i)                      # evict the ids from L2 (64 MiB < L2)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            C.run(ids, stream)
-            b.record(stream)
-            times.append((a, b))
-    torch.cuda.synchronize(dev)
-    ms = statistics.median(a.elapsed_time(b) for a, b in times[3:])
+        C.run(ids, stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        flush.fill_(1)                          # evict the ids from L2 (64 MiB < L2)
+        gev.record(0, stream)
+        C.run(ids, stream)
+        gev.record(1, stream)
+    times = []
+    for _ in range(13):
+        graph.replay()
+        torch.cuda.synchronize()
+        times.append(gev.elapsed(0, 1))
+    gev.close()
+    ms = statistics.median(times[3:])
     nbytes = w.n_layers * w.T * w.k * 4 + (2 * w.n_layers - 1) * w.E * w.E * 8
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": w.name, "ms": round(ms, 4), "algorithmic_bytes": nbytes,
             "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
-            "l2": "flushed (256 MB write) before each call", "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
+            "l2": "flushed (256 MB write) before each call",
+            "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -290,13 +375,11 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    t0, t1, ev = time_chain(P, d_ids, args.steps, stream)
+    total_ms, steps_run, per_call = time_chain(P, d_ids, args.steps, stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    per_call = {c: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i, c in enumerate(CALLS)}
     if P.error() != 0:
         raise RuntimeError("device error after the timed region")
     if world > 1:
@@ -305,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
         total_ms = float(t.item())
     if rank != 0:
         return
-    ms_step = total_ms / args.steps
+    ms_step = total_ms / steps_run
     value = pairs * world / (ms_step * 1e-3)
     hbm, peak_kind = peaks()
     # dominant HBM call
@@ -318,7 +401,7 @@ def run_ours(args, rank, world, local_rank):
                     if c in BYTES_PER_PAIR else {})} for c in CALLS}
     calls["plan"]["us_per_microbatch"] = round(per_call["plan"] * 1e3 / w.n_layers, 2)
     line = {"metric": "routed (token,slot) pairs/sec", "value": value, "unit": "pairs/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": world, "steps": steps_run, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "R": w.R,
@@ -326,7 +409,9 @@ def run_ours(args, rank, world, local_rank):
                        "microbatches": w.n_layers, "pairs_per_step": pairs,
                        "parallelism": f"replicas x{world}",
                        "l2": "ids 168 MB > 129 MB L2 per step, no flush"},
-            "gpu_launches": args.steps * sum(KERNELS_PER_CALL[c] for c in CALLS),
+            "gpu_launches": steps_run * sum(KERNELS_PER_CALL[c] for c in CALLS),
+            "timing": f"CUDA graph of {min(STEPS_PER_GRAPH, args.steps)} steps replayed; "
+                      "per-call times from event nodes inside the graph",
             "calls": calls,
             "roofline": {"bound": "hbm", "kernel": f"{dom} call ({CALL_KERNEL[dom]} + its index kernels)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",

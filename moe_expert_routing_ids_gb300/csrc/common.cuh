@@ -93,6 +93,11 @@ __host__ __device__ inline T *ws_at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device, once per (kernel, device): later calls, including calls
+// made while a stream is being captured into a CUDA graph, launch only.
+cudaError_t ensure_smem(const void *fn, size_t bytes);
+
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the kernel translation units).  Each returns
 // the cudaError_t of its launches.

@@ -222,19 +222,13 @@ cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64
     cfg.numAttrs = 1;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     if (k <= 8) {
-        if ((e = cudaFuncSetAttribute(k_cooccur<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem)) != cudaSuccess)
-            return e;
+        if ((e = ensure_smem((const void *)k_cooccur<8>, smem)) != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, k_cooccur<8>, ids, co, tr, hdr, L, T, E, k, rows, tok_per_cta);
     } else if (k <= 16) {
-        if ((e = cudaFuncSetAttribute(k_cooccur<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem)) != cudaSuccess)
-            return e;
+        if ((e = ensure_smem((const void *)k_cooccur<16>, smem)) != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, k_cooccur<16>, ids, co, tr, hdr, L, T, E, k, rows, tok_per_cta);
     } else {
-        if ((e = cudaFuncSetAttribute(k_cooccur_any, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem)) != cudaSuccess)
-            return e;
+        if ((e = ensure_smem((const void *)k_cooccur_any, smem)) != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, k_cooccur_any, ids, co, tr, hdr, L, T, E, k, rows, tok_per_cta);
     }
     if (e != cudaSuccess) return e;

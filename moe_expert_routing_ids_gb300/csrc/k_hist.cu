@@ -111,11 +111,8 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
     cudaError_t e0 = cudaMemsetAsync(ws_at<int32_t>(ws, g.off_done), 0, (size_t)g.L * g.R * 4, st);
     if (e0 != cudaSuccess) return e0;
     const size_t smem = (size_t)g.E * sizeof(int);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_hist_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e1 = ensure_smem((const void *)k_hist_tiles, smem);
+    if (e1 != cudaSuccess) return e1;
     k_hist_tiles<<<(unsigned)tiles, kHistThreads, smem, st>>>(
         ids, hist, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_done),
         ws_at<WsHeader>(ws, 0), g, fp);

@@ -432,10 +432,7 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
     if ((e = launch_main_tables(g, main_rank, ws, p.stats, g.L * TOPO_STATS, st)) != cudaSuccess)
         return e;
     const size_t smem_place = (size_t)g.E * 8;
-    if (smem_place > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(k_plan_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_place)) != cudaSuccess)
-        return e;
+    if ((e = ensure_smem((const void *)k_plan_place, smem_place)) != cudaSuccess) return e;
     k_plan_place<<<dim3(g.M, g.L), 512, smem_place, st>>>(hist, tab, p.slot_expert, rep, p.inst_load,
                                                           p.rank_load, p.stats, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -443,10 +440,7 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
                                                 p.stats, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem_ref = refine_smem_bytes(g);
-    if (smem_ref > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(k_plan_refine, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_ref)) != cudaSuccess)
-        return e;
+    if ((e = ensure_smem((const void *)k_plan_refine, smem_ref)) != cudaSuccess) return e;
     k_plan_refine<<<dim3(g.M, g.L), 32, smem_ref, st>>>(tab, p.slot_expert, p.route_cnt, p.inst_load,
                                                         p.rank_load, p.stats, g);
     return cudaGetLastError();

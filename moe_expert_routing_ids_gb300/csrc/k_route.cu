@@ -410,29 +410,32 @@ __device__ void rank_tile_exact(const Geo &g, const TileGeo &tg, const int32_t *
 // Shared-memory layout of k_route_tiles.
 struct RankSmem {
     int4 *first;     // [E] first routing entry of each expert in this row
-    int *basew;      // [kRankWarps][E] per-warp running occurrence base
-    unsigned *mskw;  // [kRankWarps][E] per-warp token bitmask of the round
+    int2 *mb;        // [kRankWarps][E] per-warp {token bitmask of the round, running base}
     int32_t *keys;   // [TT][kp] ids, then the instance codes, in place
 };
 
 __device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
     RankSmem r;
     r.first = reinterpret_cast<int4 *>(sm);
-    r.basew = sm + 4 * g.E;
-    r.mskw = reinterpret_cast<unsigned *>(r.basew + kRankWarps * g.E);
-    r.keys = reinterpret_cast<int32_t *>(r.mskw + kRankWarps * g.E);
+    r.mb = reinterpret_cast<int2 *>(sm + 4 * g.E);
+    r.keys = reinterpret_cast<int32_t *>(sm + 4 * g.E + 2 * kRankWarps * g.E);
     return r;
 }
 
 // One CTA per tile.  kFused: write the layout (sorted pairs) directly;
 // otherwise store each pair's layout position in the workspace for
-// topo_dispatch_layout.  KMAX: compile-time bound on k for the fast path.
-template <int KMAX, bool kFused>
+// topo_dispatch_layout.  K > 0: k known at compile time; K == 0: any k up to
+// KMAX.  Each lane visits its token's slots starting at lane % k, so a hot
+// expert that Top-k puts in the same slot of many tokens does not serialise
+// one shared atomic across the warp (the order inside a round is free: a
+// round is ranked only after all its slots are in the bitmasks).
+template <int K, int KMAX, bool kFused>
 __global__ void __launch_bounds__(kRankThreads, 2)
 k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_idx,
               const int32_t *__restrict__ roff, const Entry *__restrict__ rent, int32_t *dst,
               int32_t *pos_ws, int32_t *sorted, WsHeader *hdr, Geo g, uint64_t hist_fp,
               uint64_t route_part) {
+    constexpr int KB = K > 0 ? K : KMAX;
     extern __shared__ int sm[];
     __shared__ int ok;
     if (!check_fp(hdr, hist_fp, false, 0, &ok)) {
@@ -441,7 +444,9 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     }
     if (!kFused && blockIdx.x == 0 && threadIdx.x == 0) hdr->route_fp = fp_mix(hist_fp, route_part);
     const TileGeo tg = tile_geo(g);
-    const int E = g.E, k = g.k, kp = g.kp;
+    const int E = g.E;
+    const int k = K > 0 ? K : g.k;
+    const int kp = K > 0 ? ((K & 1) ? K : K + 1) : g.kp;
     const RankSmem S = rank_smem(g, sm);
     const int32_t *ids_layer = ids + (int64_t)tg.l * g.npairs;
     int32_t *dst_layer = dst + (int64_t)tg.l * g.npairs;
@@ -452,18 +457,34 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     bool bad_id = false, bad_state = false;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const unsigned bit = 1u << lane, lt_mask = bit - 1u;
+    const int rot = lane % k;                        // first slot this lane visits
+    const int n = tg.ntok * k;
+    auto div = [&](int i) { return K > 0 ? i / K : div_k(g, i); };
 
     // stage: ids token-major with an odd stride (conflict-free per lane),
     // first routing entry per expert, zeroed per-warp tables
-    const bool fast = k <= KMAX;
+    const bool fast = k <= KB;
     if (fast) {
         const int32_t *src = ids_layer + tg.p0;
-        for (int t = threadIdx.x; t < tg.ntok; t += blockDim.x)
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < k) S.keys[t * kp + j] = __ldg(src + (int64_t)t * k + j);
+        int i = threadIdx.x;
+        for (; i + 3 * kRankThreads < n; i += 4 * kRankThreads) {
+            const int v0 = __ldg(src + i), v1 = __ldg(src + i + kRankThreads);
+            const int v2 = __ldg(src + i + 2 * kRankThreads), v3 = __ldg(src + i + 3 * kRankThreads);
+            int t = div(i);
+            S.keys[t * kp + (i - t * k)] = v0;
+            t = div(i + kRankThreads);
+            S.keys[t * kp + (i + kRankThreads - t * k)] = v1;
+            t = div(i + 2 * kRankThreads);
+            S.keys[t * kp + (i + 2 * kRankThreads - t * k)] = v2;
+            t = div(i + 3 * kRankThreads);
+            S.keys[t * kp + (i + 3 * kRankThreads - t * k)] = v3;
+        }
+        for (; i < n; i += kRankThreads) {
+            const int t = div(i);
+            S.keys[t * kp + (i - t * k)] = __ldg(src + i);
+        }
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    for (int e = threadIdx.x; e < E; e += kRankThreads) {
         const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
         int4 f = make_int4(-1, 0, 0, b);
         if (b < en) {
@@ -472,36 +493,35 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
         }
         S.first[e] = f;
     }
-    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) {
-        S.basew[i] = 0;
-        S.mskw[i] = 0;
-    }
+    for (int i = threadIdx.x; i < kRankWarps * E; i += kRankThreads) S.mb[i] = make_int2(0, 0);
     __syncthreads();
 
     bool dup = !fast;
     if (fast) {
-        int *mybase = S.basew + w * E;
-        unsigned *mymsk = S.mskw + w * E;
+        int2 *my = S.mb + w * E;
         // pass 1: per-warp counts over its rounds
         for (int r = 0; r < g.RW; ++r) {
             const int t = (w * g.RW + r) * 32 + lane;
             if (t < tg.ntok) {
+                int j = rot;
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (j >= k) break;
-                    const int e = S.keys[t * kp + j];
-                    if ((unsigned)e < (unsigned)E) atomicAdd(&mybase[e], 1);
+                for (int jj = 0; jj < KB; ++jj) {
+                    if (jj < k) {
+                        const int e = S.keys[t * kp + j];
+                        if ((unsigned)e < (unsigned)E) atomicAdd(&my[e].y, 1);
+                        j = (j + 1 == k) ? 0 : j + 1;
+                    }
                 }
             }
         }
         __syncthreads();
         // pass 2: warp bases = tile base + counts of the warps before
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        for (int e = threadIdx.x; e < E; e += kRankThreads) {
             int run = __ldg(tbase + e);
 #pragma unroll
             for (int x = 0; x < kRankWarps; ++x) {
-                const int c = S.basew[x * E + e];
-                S.basew[x * E + e] = run;
+                const int c = S.mb[x * E + e].y;
+                S.mb[x * E + e].y = run;
                 run += c;
             }
         }
@@ -510,71 +530,78 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
         for (int r = 0; r < g.RW; ++r) {
             const int t = (w * g.RW + r) * 32 + lane;
             const bool vt = t < tg.ntok;
-            int ek[KMAX];
+            int ek[KB];
+            {
+                int j = rot;
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                ek[j] = -1;
-                if (j < k && vt) {
-                    const int e = S.keys[t * kp + j];
-                    if ((unsigned)e < (unsigned)E) ek[j] = e;
-                    else bad_id = true;
+                for (int jj = 0; jj < KB; ++jj) {
+                    ek[jj] = -1;
+                    if (jj < k) {
+                        if (vt) {
+                            const int e = S.keys[t * kp + j];
+                            if ((unsigned)e < (unsigned)E) ek[jj] = e;
+                            else bad_id = true;
+                        }
+                        j = (j + 1 == k) ? 0 : j + 1;
+                    }
                 }
             }
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (ek[j] >= 0) dup |= (atomicOr(&mymsk[ek[j]], bit) & bit) != 0;
+            for (int jj = 0; jj < KB; ++jj)
+                if (ek[jj] >= 0)
+                    dup |= (atomicOr(reinterpret_cast<unsigned *>(&my[ek[jj]].x), bit) & bit) != 0;
             __syncwarp();
-            int nb[KMAX];
+            int nb[KB];
             unsigned lead = 0;
+            {
+                int j = rot;
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                nb[j] = 0;
-                if (j >= k) continue;
-                int code = -1, ob = 0, occ = 0;
-                if (ek[j] >= 0) {
-                    const unsigned m = mymsk[ek[j]];
-                    const int b = mybase[ek[j]];
-                    const int rk = __popc(m & lt_mask);
-                    occ = b + rk;
-                    if (rk == 0) {
-                        lead |= 1u << j;
-                        nb[j] = b + __popc(m);
+                for (int jj = 0; jj < KB; ++jj) {
+                    nb[jj] = 0;
+                    if (jj >= k) continue;
+                    int code = -1, ob = 0, occ = 0;
+                    if (ek[jj] >= 0) {
+                        const int2 v = my[ek[jj]];
+                        const int rk = __popc((unsigned)v.x & lt_mask);
+                        occ = v.y + rk;
+                        if (rk == 0) {
+                            lead |= 1u << jj;
+                            nb[jj] = v.y + __popc((unsigned)v.x);
+                        }
+                        code = route_lookup(S.first[ek[jj]], occ, ro + ek[jj] + 1, re, &ob);
+                        if (code < 0) bad_state = true;
                     }
-                    code = route_lookup(S.first[ek[j]], occ, ro + ek[j] + 1, re, &ob);
-                    if (code < 0) bad_state = true;
-                }
-                if (vt) {
-                    S.keys[t * kp + j] = code;
-                    if (kFused) {
-                        const int64_t pos = (int64_t)ob + occ;
-                        if (code >= 0 && pos >= 0 && pos < g.npairs)
-                            sorted_layer[pos] = (int32_t)(tg.p0 + (int64_t)t * k + j);
-                        else if (code >= 0)
-                            bad_state = true;
+                    if (vt) {
+                        S.keys[t * kp + j] = code;
+                        if (kFused) {
+                            const int pos = ob + occ;
+                            if (code >= 0 && pos >= 0 && pos < g.npairs)
+                                sorted_layer[pos] = (int32_t)(tg.p0 + t * k + j);
+                            else if (code >= 0)
+                                bad_state = true;
+                        }
                     }
+                    if (!kFused)
+                        pos_ws[tg.slot0 + ((t >> 5) * k + j) * 32 + lane] =
+                            (vt && code >= 0) ? ob + occ : -1;
+                    j = (j + 1 == k) ? 0 : j + 1;
                 }
-                if (!kFused)
-                    pos_ws[pos_index(g, tg, t, j)] = (vt && code >= 0) ? ob + occ : -1;
             }
             __syncwarp();
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if ((lead >> j) & 1u) {
-                    mybase[ek[j]] = nb[j];
-                    mymsk[ek[j]] = 0;
-                }
+            for (int jj = 0; jj < KB; ++jj)
+                if ((lead >> jj) & 1u) my[ek[jj]] = make_int2(0, nb[jj]);
             __syncwarp();
         }
     }
     if (__syncthreads_or(dup)) {
-        // a token repeats an expert (or k > KMAX): redo the tile exactly
-        rank_tile_exact<kFused>(g, tg, ids_layer, tbase, ro, re, S.basew, dst_layer, pos_ws,
-                                sorted_layer, bad_id, bad_state);
+        // a token repeats an expert (or k > KB): redo the tile exactly
+        rank_tile_exact<kFused>(g, tg, ids_layer, tbase, ro, re, reinterpret_cast<int *>(S.mb),
+                                dst_layer, pos_ws, sorted_layer, bad_id, bad_state);
     } else {
         // instance codes out, pair order, coalesced
-        const int n = tg.ntok * k;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const int t = div_k(g, i);
+        for (int i = threadIdx.x; i < n; i += kRankThreads) {
+            const int t = div(i);
             dst_layer[tg.p0 + i] = S.keys[t * kp + (i - t * k)];
         }
     }
@@ -627,11 +654,6 @@ k_lay_copy(const int32_t *__restrict__ lseg, const int64_t *__restrict__ lsend,
     }
 }
 
-cudaError_t set_smem(const void *fn, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 // Prep shared by topo_reroute and topo_reroute_layout.
 cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_t &p, void *ws,
                         cudaStream_t st) {
@@ -639,14 +661,14 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     if ((e = launch_main_tables(g, main_rank, ws, nullptr, 0, st)) != cudaSuccess) return e;
     const size_t smem_inst = (size_t)g.E * ((g.R + 31) / 32) * 4 + (size_t)g.E * 4;
-    if ((e = set_smem((const void *)k_inst_index, smem_inst)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void *)k_inst_index, smem_inst)) != cudaSuccess) return e;
     k_inst_index<<<g.L, 512, smem_inst, st>>>(p.slot_expert, ws_at<int32_t>(ws, g.off_main),
                                               ws_at<int32_t>(ws, g.off_iexp),
                                               ws_at<int32_t>(ws, g.off_ioff),
                                               ws_at<int32_t>(ws, g.off_ilist), hdr, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem_row = (size_t)g.E * 4;
-    if ((e = set_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;
     k_row_index<<<dim3(g.R, g.L), 256, smem_row, st>>>(
         p.route_cnt, ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), g);
@@ -658,7 +680,7 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
                                     ws_at<int64_t>(ws, g.off_lstat), g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t smem_e = (size_t)g.R * 8;
-    if ((e = set_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
     k_lay_entries<<<dim3(g.R, g.L), 256, smem_e, st>>>(
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), ws_at<int32_t>(ws, g.off_soff),
         ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
@@ -667,13 +689,30 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
 }
 
 template <bool kFused>
+using RouteKernel = void (*)(const int32_t *, const int32_t *, const int32_t *, const Entry *,
+                             int32_t *, int32_t *, int32_t *, WsHeader *, Geo, uint64_t, uint64_t);
+
+template <bool kFused>
+RouteKernel<kFused> pick_route_kernel(int k) {
+    switch (k) {
+        case 1: return k_route_tiles<1, 1, kFused>;
+        case 2: return k_route_tiles<2, 2, kFused>;
+        case 4: return k_route_tiles<4, 4, kFused>;
+        case 6: return k_route_tiles<6, 6, kFused>;
+        case 8: return k_route_tiles<8, 8, kFused>;
+        case 10: return k_route_tiles<10, 10, kFused>;
+        case 16: return k_route_tiles<16, 16, kFused>;
+        default: return k_route_tiles<0, 16, kFused>;
+    }
+}
+
+template <bool kFused>
 cudaError_t launch_tiles(const Geo &g, const int32_t *ids, int32_t *dst, int32_t *sorted, void *ws,
                          uint64_t hist_fp, uint64_t route_part, cudaStream_t st) {
-    auto kern = g.k <= 4 ? k_route_tiles<4, kFused>
-                         : (g.k <= 8 ? k_route_tiles<8, kFused> : k_route_tiles<16, kFused>);
+    RouteKernel<kFused> kern = pick_route_kernel<kFused>(g.k);
     const size_t smem = rank_smem_bytes(g);
     cudaError_t e;
-    if ((e = set_smem((const void *)kern, smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void *)kern, smem)) != cudaSuccess) return e;
     const int64_t tiles = (int64_t)g.L * g.R * g.tps;
     kern<<<(unsigned)tiles, kRankThreads, smem, st>>>(
         ids, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_roff),

@@ -3,10 +3,32 @@
 
 #include <climits>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
 using namespace topo;
+
+namespace topo {
+
+cudaError_t ensure_smem(const void *fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &have = done[{fn, dev}];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
+
+}  // namespace topo
 
 namespace {
 
