@@ -210,27 +210,6 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
     }
 }
 
-struct Key {
-    unsigned long long a, b, c;   // lexicographic, larger is better; a == 0: none
-};
-
-__device__ __forceinline__ bool key_gt(const Key &x, const Key &y) {
-    if (x.a != y.a) return x.a > y.a;
-    if (x.b != y.b) return x.b > y.b;
-    return x.c > y.c;
-}
-
-__device__ __forceinline__ Key warp_max_key(Key k) {
-    for (int o = 16; o > 0; o >>= 1) {
-        Key y;
-        y.a = __shfl_xor_sync(0xffffffffu, k.a, o);
-        y.b = __shfl_xor_sync(0xffffffffu, k.b, o);
-        y.c = __shfl_xor_sync(0xffffffffu, k.c, o);
-        if (key_gt(y, k)) k = y;
-    }
-    return k;
-}
-
 __device__ __forceinline__ int warp_incl_scan(int v) {
     const int lane = threadIdx.x & 31;
     for (int o = 1; o < 32; o <<= 1) {
@@ -240,182 +219,300 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
     return v;
 }
 
-// One warp refines one domain of one layer.
-__global__ void __launch_bounds__(32)
+// Candidate key, lexicographic, larger is better; a == 0: no candidate.
+//   a = delta << 32 | ~L_t          (more moved first, then the lighter target)
+//   b = order-preserving map of -cost (cheaper first)
+//   c = ~(e << 5 | j_t)              (lower expert, then lower target rank)
+struct Key {
+    unsigned long long a, b;
+    unsigned c;
+};
+
+__device__ __forceinline__ bool key_gt(const Key &x, const Key &y) {
+    if (x.a != y.a) return x.a > y.a;
+    if (x.b != y.b) return x.b > y.b;
+    return x.c > y.c;
+}
+
+// Lanes holding the warp's largest key: five 32-bit redux steps, each
+// keeping only the lanes that tie on every word so far.
+__device__ __forceinline__ unsigned warp_argmax_lanes(const Key &k) {
+    unsigned live = 0xffffffffu;
+    const unsigned words[5] = {(unsigned)(k.a >> 32), (unsigned)k.a, (unsigned)(k.b >> 32),
+                               (unsigned)k.b, k.c};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const bool in = (live >> (threadIdx.x & 31)) & 1u;
+        const unsigned m = __reduce_max_sync(0xffffffffu, in ? words[i] : 0u);
+        live = __ballot_sync(0xffffffffu, in && words[i] == m);
+    }
+    return live;
+}
+
+constexpr int kRefineMaxWarps = 8;
+
+// One CTA per (domain, layer) refines the domain (TopoEP §4.3, Eq. 10).
+// Candidates (instance at the busiest rank x other rank of the domain) are
+// spread over the CTA's warps; each warp reduces with redux/ballot steps, the
+// warps' winners meet in shared memory (skipped with one warp, which then
+// runs barrier-free), and warp 0 commits.  The domain's columns of q (every
+// source, the domain's ranks) live in shared memory when they fit
+// (colcache), else in global memory with the domain's own sources mirrored in
+// shared memory for the candidate costs.
+__global__ void __launch_bounds__(kRefineMaxWarps * 32)
 k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
-              int32_t *rank_load, int64_t *stats, Geo g) {
+              int32_t *rank_load, int64_t *stats, Geo g, int colcache) {
     extern __shared__ int sm[];
-    const int d = blockIdx.x, l = blockIdx.y, lane = threadIdx.x;
+    __shared__ Key kbuf[kRefineMaxWarps];
+    __shared__ int cbuf[kRefineMaxWarps];
+    const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nthr = blockDim.x, nwarp = nthr >> 5;
     const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
     const int32_t *main_of = tab, *mains = tab + 2 * E;
     int *Lr = sm;                               // [rpn]
     int *used = Lr + rpn;                       // [rpn]
     int *U = used + rpn;                        // [rpn][nl]
     int *xe = U + rpn * nl;                     // [rpn][nl] expert of each instance
-    int *qloc = xe + rpn * nl;                  // [rpn src][rpn dst][nl]
-    short *hl = reinterpret_cast<short *>(qloc + rpn * rpn * nl);   // [rpn][E] local index or -1
+    int *xc = xe + rpn * nl;                    // [rpn][nl] main rank of that expert, or
+                                                //   -1 - main rank when it is in another domain
+    // colcache: qc[s][j][l] for every source s; else qc[js][j][l] for the
+    // domain's own sources only
+    int *qc = xc + rpn * nl;
+    const int nsrc = colcache ? R : rpn;
+    short *hl = reinterpret_cast<short *>(qc + nsrc * rpn * nl);   // [rpn][E] local index or -1
     const int r0 = d * rpn;
+    const int src0 = colcache ? 0 : r0;         // source index of qc's first row
     int32_t *Q = q + (int64_t)l * R * R * nl;
     int32_t *SE = slot_expert + (int64_t)l * R * ns;
 
-    for (int j = lane; j < rpn; j += 32) Lr[j] = rank_load[(int64_t)l * R + r0 + j];
-    for (int i = lane; i < rpn * E; i += 32) hl[i] = -1;
-    __syncwarp();
-    for (int i = lane; i < rpn * nl; i += 32) {
-        const int j = i / nl, li = i % nl, r = r0 + j;
-        U[i] = inst_load[((int64_t)l * R + r) * nl + li];
-        const int e = li < ER ? mains[r * ER + li] : SE[(int64_t)r * ns + (li - ER)];
-        xe[i] = e;
-        if (e >= 0) hl[j * E + e] = (short)li;
-    }
-    for (int j = lane; j < rpn; j += 32) {
+    for (int j = tid; j < rpn; j += nthr) {
+        Lr[j] = rank_load[(int64_t)l * R + r0 + j];
         int u = 0;
         while (u < ns && SE[(int64_t)(r0 + j) * ns + u] >= 0) ++u;
         used[j] = u;
     }
-    for (int i = lane; i < rpn * rpn * nl; i += 32) {
-        const int js = i / (rpn * nl), jd = (i / nl) % rpn, li = i % nl;
-        qloc[i] = Q[((int64_t)(r0 + js) * R + (r0 + jd)) * nl + li];
+    for (int i = tid; i < rpn * E; i += nthr) hl[i] = -1;
+    __syncthreads();
+    for (int i = tid; i < rpn * nl; i += nthr) {
+        const int j = i / nl, li = i % nl, r = r0 + j;
+        U[i] = inst_load[((int64_t)l * R + r) * nl + li];
+        const int e = li < ER ? mains[r * ER + li] : SE[(int64_t)r * ns + (li - ER)];
+        xe[i] = e;
+        if (e >= 0) {
+            hl[j * E + e] = (short)li;
+            const int m = main_of[e];
+            xc[i] = (m / rpn == d) ? m : -1 - m;
+        } else {
+            xc[i] = 0;
+        }
     }
-    __syncwarp();
+    for (int i = tid; i < nsrc * rpn * nl; i += nthr) {
+        const int sr = i / (rpn * nl), rest = i % (rpn * nl);
+        qc[i] = Q[(int64_t)(src0 + sr) * R * nl + (int64_t)r0 * nl + rest];
+    }
+    __syncthreads();
+
+    auto qcell = [&](int s, int j, int li) -> int * { return &qc[((s - src0) * rpn + j) * nl + li]; };
+    // per-byte cost of a replica on rank r0 + jt of the expert whose main class is xcv
+    auto repl_cost = [&](int xcv, int jt) -> int64_t {
+        if (xcv < 0) return g.c_inter;
+        return xcv == r0 + jt ? 0 : g.c_intra;
+    };
 
     int iters = 0;
     int64_t tokd = 0, repd = 0;
     const int ncand = nl * rpn;
-    // Each commit lowers sum L^2 by at least 2, so the loop ends; the hard cap
-    // only guards against a corrupted input state.
-    constexpr int kHardCap = 1 << 24;
+    // this thread's first candidate (lb, jt) and the stride in (lb, jt) form
+    const int c_lb0 = tid / rpn, c_jt0 = tid % rpn;
+    const int s_lb = nthr / rpn, s_jt = nthr % rpn;
+    constexpr int kHardCap = 1 << 24;   // commits provably end; guards a corrupted state only
     while ((g.max_iters == 0 || iters < g.max_iters) && iters < kHardCap) {
-        // busiest rank, lowest index on ties
-        int bv = lane < rpn ? Lr[lane] : -1, bj = lane;
-        for (int o = 16; o > 0; o >>= 1) {
-            const int ov = __shfl_xor_sync(0xffffffffu, bv, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
-            if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
-        }
-        const int jb = bj, Lb = bv;
-        Key best{0ull, 0ull, 0ull};
-        for (int c = lane; c < ncand; c += 32) {
-            const int lb = c / rpn, jt = c % rpn;
-            if (jt == jb) continue;
-            const int Ub = U[jb * nl + lb];
-            if (Ub <= 0) continue;
-            const int e = xe[jb * nl + lb];
-            if (e < 0) continue;
-            const int lt = hl[jt * E + e];
-            const bool is_new = lt < 0;
-            if (is_new && used[jt] >= ns) continue;
-            const int Lt = Lr[jt];
-            const int half = (Lb - Lt) >> 1;
-            const int delta = Ub < half ? Ub : half;
-            if (delta < 1) continue;
-            const int q_rt = qloc[(jt * rpn + jb) * nl + lb];
-            const int q_rb = qloc[(jb * rpn + jb) * nl + lb];
-            const int m_rt = q_rt < delta ? q_rt : delta;
-            const int rest = delta - m_rt;
-            const int others = Ub - q_rt - q_rb;
-            const int m_o = others < rest ? others : rest;
-            const int m_rb = rest - m_o;
-            const int64_t cst = 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt) +
-                                (is_new ? cost_sr(g, main_of[e], r0 + jt) * g.W : 0);
-            Key k;
-            k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)Lt);
-            k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
-            k.c = ~(((unsigned long long)e << 32) | (unsigned)jt);
-            if (key_gt(k, best)) best = k;
-        }
-        best = warp_max_key(best);
-        if (best.a == 0) break;
-        // commit
-        const int delta = (int)(best.a >> 32);
-        const int e = (int)((~best.c) >> 32);
-        const int jt = (int)(unsigned)(~best.c);
-        const int lb = hl[jb * E + e];
-        const int rb = r0 + jb, rt = r0 + jt;
-        int lt = hl[jt * E + e];
-        const bool is_new = lt < 0;
-        if (is_new) lt = ER + used[jt];
-        const int m_rt = min(qloc[(jt * rpn + jb) * nl + lb], delta);
-        int remaining = delta - m_rt;
-        __syncwarp();
-        if (is_new) {
-            repd += cost_sr(g, main_of[e], rt) * g.W;
-            if (lane == 0) {
-                used[jt] += 1;
-                hl[jt * E + e] = (short)lt;
-                xe[jt * nl + lt] = e;
-                SE[(int64_t)rt * ns + (lt - ER)] = e;
-            }
-        }
-        // other sources, ascending, skipping r_t and r_b
-        for (int base = 0; base < R && remaining > 0; base += 32) {
-            const int s = base + lane;
-            int32_t *pb = Q + ((int64_t)s * R + rb) * nl + lb;
-            int32_t *pt = Q + ((int64_t)s * R + rt) * nl + lt;
-            const int v = (s < R && s != rt && s != rb) ? *pb : 0;
-            const int incl = warp_incl_scan(v);
-            const int excl = incl - v;
-            int take = remaining - excl;
-            take = take < 0 ? 0 : (take > v ? v : take);
-            if (take > 0) {
-                *pb -= take;
-                *pt += take;
-                if (s >= r0 && s < r0 + rpn) {
-                    const int js = s - r0;
-                    qloc[(js * rpn + jb) * nl + lb] -= take;
-                    qloc[(js * rpn + jt) * nl + lt] += take;
+        // busiest rank, lowest index on ties (every warp computes it)
+        const int myL = lane < rpn ? Lr[lane] : -1;
+        const int Lb = __reduce_max_sync(0xffffffffu, myL);
+        const int jb = __ffs(__ballot_sync(0xffffffffu, myL == Lb)) - 1;
+        Key best{0ull, 0ull, 0u};
+        int bc = 0;                              // packed (lb << 5 | jt) of best
+        int lb = c_lb0, jt = c_jt0;
+        for (int c = tid; c < ncand; c += nthr) {
+            if (jt != jb) {
+                const int Ub = U[jb * nl + lb];
+                const int e = xe[jb * nl + lb];
+                const int xcv = xc[jb * nl + lb];
+                const int Lt = Lr[jt];
+                const int usedt = used[jt];
+                const int q_rt = *qcell(r0 + jt, jb, lb);
+                const int q_rb = *qcell(r0 + jb, jb, lb);
+                if (Ub > 0 && e >= 0) {
+                    const int lt = hl[jt * E + e];
+                    const bool is_new = lt < 0;
+                    const int half = (Lb - Lt) >> 1;
+                    const int delta = Ub < half ? Ub : half;
+                    if (delta >= 1 && (!is_new || usedt < ns)) {
+                        const int m_rt = q_rt < delta ? q_rt : delta;
+                        const int rest = delta - m_rt;
+                        const int others = Ub - q_rt - q_rb;
+                        const int m_o = others < rest ? others : rest;
+                        const int m_rb = rest - m_o;
+                        const int64_t cst = 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt) +
+                                            (is_new ? repl_cost(xcv, jt) * g.W : 0);
+                        Key k;
+                        k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)Lt);
+                        k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
+                        k.c = ~(((unsigned)e << 5) | (unsigned)jt);
+                        if (key_gt(k, best)) {
+                            best = k;
+                            bc = (lb << 5) | jt;
+                        }
+                    }
                 }
             }
-            const int tot = __shfl_sync(0xffffffffu, incl, 31);
-            remaining -= tot < remaining ? tot : remaining;
+            lb += s_lb;
+            jt += s_jt;
+            if (jt >= rpn) { jt -= rpn; ++lb; }
         }
-        const int m_rb = remaining;
-        __syncwarp();
-        if (lane == 0) {
-            if (m_rt > 0) {
-                Q[((int64_t)rt * R + rb) * nl + lb] -= m_rt;
-                Q[((int64_t)rt * R + rt) * nl + lt] += m_rt;
-                qloc[(jt * rpn + jb) * nl + lb] -= m_rt;
-                qloc[(jt * rpn + jt) * nl + lt] += m_rt;
+        const unsigned win = warp_argmax_lanes(best);
+        const int wl = __ffs(win) - 1;
+        Key wk;
+        wk.a = __shfl_sync(0xffffffffu, best.a, wl);
+        wk.b = __shfl_sync(0xffffffffu, best.b, wl);
+        wk.c = __shfl_sync(0xffffffffu, best.c, wl);
+        int wc = __shfl_sync(0xffffffffu, bc, wl);
+        if (nwarp > 1) {
+            if (lane == 0) {
+                kbuf[w] = wk;
+                cbuf[w] = wc;
             }
-            if (m_rb > 0) {
-                Q[((int64_t)rb * R + rb) * nl + lb] -= m_rb;
-                Q[((int64_t)rb * R + rt) * nl + lt] += m_rb;
-                qloc[(jb * rpn + jb) * nl + lb] -= m_rb;
-                qloc[(jb * rpn + jt) * nl + lt] += m_rb;
-            }
-            U[jb * nl + lb] -= delta;
-            U[jt * nl + lt] += delta;
-            Lr[jb] -= delta;
-            Lr[jt] += delta;
+            __syncthreads();
+            wk = kbuf[0];
+            wc = cbuf[0];
+            for (int x = 1; x < nwarp; ++x)
+                if (key_gt(kbuf[x], wk)) {
+                    wk = kbuf[x];
+                    wc = cbuf[x];
+                }
         }
-        tokd += 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt);
+        if (wk.a == 0) break;                   // uniform: every thread saw the same keys
+        if (w == 0) {
+            const int delta = (int)(wk.a >> 32);
+            const int blb = wc >> 5, bjt = wc & 31;
+            const int e = xe[jb * nl + blb];
+            const int xcv = xc[jb * nl + blb];
+            const int rb = r0 + jb, rt = r0 + bjt;
+            int lt = hl[bjt * E + e];
+            const bool is_new = lt < 0;
+            if (is_new) lt = ER + used[bjt];
+            const int m_rt = min(*qcell(rt, jb, blb), delta);
+            int remaining = delta - m_rt;
+            __syncwarp();
+            if (is_new) {
+                repd += repl_cost(xcv, bjt) * g.W;
+                if (lane == 0) {
+                    used[bjt] += 1;
+                    hl[bjt * E + e] = (short)lt;
+                    xe[bjt * nl + lt] = e;
+                    xc[bjt * nl + lt] = xcv;
+                    SE[(int64_t)rt * ns + (lt - ER)] = e;
+                }
+            }
+            // other sources, ascending, skipping r_t and r_b
+            for (int base = 0; base < R && remaining > 0; base += 32) {
+                const int s = base + lane;
+                const bool in = s < R && s != rt && s != rb;
+                const bool cached = colcache || (s >= r0 && s < r0 + rpn);
+                int32_t *pb = Q + ((int64_t)s * R + rb) * nl + blb;
+                int32_t *pt = Q + ((int64_t)s * R + rt) * nl + lt;
+                const int v = in ? (cached ? *qcell(s, jb, blb) : *pb) : 0;
+                const int incl = warp_incl_scan(v);
+                const int excl = incl - v;
+                int take = remaining - excl;
+                take = take < 0 ? 0 : (take > v ? v : take);
+                if (take > 0) {
+                    if (cached) {
+                        *qcell(s, jb, blb) -= take;
+                        *qcell(s, bjt, lt) += take;
+                    }
+                    if (!colcache) {
+                        *pb -= take;
+                        *pt += take;
+                    }
+                }
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                remaining -= tot < remaining ? tot : remaining;
+            }
+            const int m_rb = remaining;
+            __syncwarp();
+            if (lane == 0) {
+                if (m_rt > 0) {
+                    *qcell(rt, jb, blb) -= m_rt;
+                    *qcell(rt, bjt, lt) += m_rt;
+                    if (!colcache) {
+                        Q[((int64_t)rt * R + rb) * nl + blb] -= m_rt;
+                        Q[((int64_t)rt * R + rt) * nl + lt] += m_rt;
+                    }
+                }
+                if (m_rb > 0) {
+                    *qcell(rb, jb, blb) -= m_rb;
+                    *qcell(rb, bjt, lt) += m_rb;
+                    if (!colcache) {
+                        Q[((int64_t)rb * R + rb) * nl + blb] -= m_rb;
+                        Q[((int64_t)rb * R + rt) * nl + lt] += m_rb;
+                    }
+                }
+                U[jb * nl + blb] -= delta;
+                U[bjt * nl + lt] += delta;
+                Lr[jb] -= delta;
+                Lr[bjt] += delta;
+            }
+            tokd += 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt);
+            __syncwarp();
+        }
         ++iters;
-        __syncwarp();
+        if (nwarp > 1) __syncthreads();
     }
-    // write back the domain's loads and statistics
-    for (int j = lane; j < rpn; j += 32) rank_load[(int64_t)l * R + r0 + j] = Lr[j];
-    for (int i = lane; i < rpn * nl; i += 32) inst_load[((int64_t)l * R + r0) * nl + i] = U[i];
-    int lmax = lane < rpn ? Lr[lane] : 0, nused = lane < rpn ? used[lane] : 0;
-    for (int o = 16; o > 0; o >>= 1) {
-        lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-        nused += __shfl_xor_sync(0xffffffffu, nused, o);
-    }
-    if (lane == 0) {
-        int64_t *st = stats + l * TOPO_STATS;
-        atomicMax(reinterpret_cast<unsigned long long *>(&st[0]), (unsigned long long)lmax);
-        atomicAdd(reinterpret_cast<unsigned long long *>(&st[2]), (unsigned long long)nused);
-        atomicAdd(reinterpret_cast<unsigned long long *>(&st[4]), (unsigned long long)iters);
-        atomicAdd(reinterpret_cast<unsigned long long *>(&st[5]), (unsigned long long)tokd);
-        atomicAdd(reinterpret_cast<unsigned long long *>(&st[6]), (unsigned long long)repd);
+    // write back the domain's state and statistics
+    if (nwarp > 1) __syncthreads();
+    if (colcache)
+        for (int i = tid; i < R * rpn * nl; i += nthr) {
+            const int sr = i / (rpn * nl), rest = i % (rpn * nl);
+            Q[(int64_t)sr * R * nl + (int64_t)r0 * nl + rest] = qc[i];
+        }
+    for (int j = tid; j < rpn; j += nthr) rank_load[(int64_t)l * R + r0 + j] = Lr[j];
+    for (int i = tid; i < rpn * nl; i += nthr) inst_load[((int64_t)l * R + r0) * nl + i] = U[i];
+    if (w == 0) {
+        int lmax = lane < rpn ? Lr[lane] : 0, nused = lane < rpn ? used[lane] : 0;
+        for (int o = 16; o > 0; o >>= 1) {
+            lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            nused += __shfl_xor_sync(0xffffffffu, nused, o);
+        }
+        if (lane == 0) {
+            int64_t *st = stats + l * TOPO_STATS;
+            atomicMax(reinterpret_cast<unsigned long long *>(&st[0]), (unsigned long long)lmax);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&st[2]), (unsigned long long)nused);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&st[4]), (unsigned long long)iters);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&st[5]), (unsigned long long)tokd);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&st[6]), (unsigned long long)repd);
+        }
     }
 }
 
 }  // namespace
 
-size_t refine_smem_bytes(const Geo &g) {
-    return (size_t)(2 * g.rpn + 2 * g.rpn * g.n_local + g.rpn * g.rpn * g.n_local) * 4 +
+// Shared memory of the refinement kernel; colcache: all sources' columns.
+size_t refine_smem_bytes(const Geo &g, bool colcache) {
+    const size_t nsrc = colcache ? (size_t)g.R : (size_t)g.rpn;
+    return (2 * (size_t)g.rpn + 3 * (size_t)g.rpn * g.n_local + nsrc * g.rpn * g.n_local) * 4 +
            (size_t)g.rpn * g.E * 2;
 }
+
+// Warps of the refinement CTA: about two candidates per lane, at most 8.
+int refine_warps(const Geo &g) {
+    const int ncand = g.n_local * g.rpn;
+    int w = (ncand + 63) / 64;
+    return w < 1 ? 1 : (w > kRefineMaxWarps ? kRefineMaxWarps : w);
+}
+
+bool refine_colcache(const Geo &g) { return refine_smem_bytes(g, true) <= 160 * 1024; }
 
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st) {
@@ -439,10 +536,11 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
     k_plan_route<<<dim3(g.R, g.L), 256, 0, st>>>(hist, tab, rep, p.route_cnt, p.inst_load, p.rank_load,
                                                 p.stats, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem_ref = refine_smem_bytes(g);
+    const bool cc = refine_colcache(g);
+    const size_t smem_ref = refine_smem_bytes(g, cc);
     if ((e = ensure_smem((const void *)k_plan_refine, smem_ref)) != cudaSuccess) return e;
-    k_plan_refine<<<dim3(g.M, g.L), 32, smem_ref, st>>>(tab, p.slot_expert, p.route_cnt, p.inst_load,
-                                                        p.rank_load, p.stats, g);
+    k_plan_refine<<<dim3(g.M, g.L), refine_warps(g) * 32, smem_ref, st>>>(
+        tab, p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, cc ? 1 : 0);
     return cudaGetLastError();
 }
 

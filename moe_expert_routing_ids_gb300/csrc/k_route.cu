@@ -314,23 +314,6 @@ __device__ __forceinline__ bool check_fp(const WsHeader *hdr, uint64_t want, boo
     return *flag != 0;
 }
 
-// Instance and layout base for occurrence occ of an expert in this source
-// row.  f: the expert's first entry {code, cum_end, out_base, index};
-// ro_next: offset one past its last entry (read only when f does not hold occ).
-__device__ __forceinline__ int route_lookup(int4 f, int occ, const int32_t *ro_next, const Entry *re,
-                                            int *out_base) {
-    if (occ < f.y) { *out_base = f.z; return f.x; }
-    const int en = __ldg(ro_next);
-    for (int j = f.w + 1; j < en; ++j) {
-        const int ce = __ldg(&re[j].cum_end);
-        if (occ < ce) {
-            *out_base = __ldg(&re[j].out_base);
-            return __ldg(&re[j].code);
-        }
-    }
-    return -1;
-}
-
 // Position-array index of pair (token t of the tile, slot j).
 __device__ __forceinline__ int64_t pos_index(const Geo &g, const TileGeo &tg, int t, int j) {
     return tg.slot0 + ((int64_t)(t >> 5) * g.k + j) * 32 + (t & 31);
@@ -409,17 +392,43 @@ __device__ void rank_tile_exact(const Geo &g, const TileGeo &tg, const int32_t *
 
 // Shared-memory layout of k_route_tiles.
 struct RankSmem {
-    int4 *first;     // [E] first routing entry of each expert in this row
-    int2 *mb;        // [kRankWarps][E] per-warp {token bitmask of the round, running base}
+    int *ec;         // [E] code of the expert's only routing entry in this row;
+                     //     -1: several entries; -2: none
+    int *base;       // [kRankWarps][E] per-warp running base: the layout position
+                     //     of the next pair (single entry) or its occurrence index
+    unsigned *msk;   // [kRankWarps][E] per-warp token bitmask of the round
     int32_t *keys;   // [TT][kp] ids, then the instance codes, in place
 };
 
 __device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
     RankSmem r;
-    r.first = reinterpret_cast<int4 *>(sm);
-    r.mb = reinterpret_cast<int2 *>(sm + 4 * g.E);
-    r.keys = reinterpret_cast<int32_t *>(sm + 4 * g.E + 2 * kRankWarps * g.E);
+    r.ec = sm;
+    r.base = sm + g.E;
+    r.msk = reinterpret_cast<unsigned *>(sm + g.E + kRankWarps * g.E);
+    r.keys = reinterpret_cast<int32_t *>(sm + g.E + 2 * kRankWarps * g.E);
     return r;
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Instance code and layout position for occurrence occ of an expert with
+// several entries in this row (entries in rank order, running ranges).
+__device__ __forceinline__ int route_walk(int occ, const int32_t *ro_e, const Entry *re, int *pos) {
+    const int b = __ldg(ro_e), en = __ldg(ro_e + 1);
+    for (int j = b; j < en; ++j) {
+        if (occ < __ldg(&re[j].cum_end)) {
+            *pos = __ldg(&re[j].out_base) + occ;
+            return __ldg(&re[j].code);
+        }
+    }
+    return -1;
 }
 
 // One CTA per tile.  kFused: write the layout (sorted pairs) directly;
@@ -461,68 +470,65 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     const int n = tg.ntok * k;
     auto div = [&](int i) { return K > 0 ? i / K : div_k(g, i); };
 
-    // stage: ids token-major with an odd stride (conflict-free per lane),
-    // first routing entry per expert, zeroed per-warp tables
+    // stage: ids token-major with an odd stride (conflict-free per lane) by
+    // asynchronous 4-byte copies, all in flight at once; the per-expert
+    // routing table; zeroed per-warp tables
     const bool fast = k <= KB;
     if (fast) {
         const int32_t *src = ids_layer + tg.p0;
-        int i = threadIdx.x;
-        for (; i + 3 * kRankThreads < n; i += 4 * kRankThreads) {
-            const int v0 = __ldg(src + i), v1 = __ldg(src + i + kRankThreads);
-            const int v2 = __ldg(src + i + 2 * kRankThreads), v3 = __ldg(src + i + 3 * kRankThreads);
-            int t = div(i);
-            S.keys[t * kp + (i - t * k)] = v0;
-            t = div(i + kRankThreads);
-            S.keys[t * kp + (i + kRankThreads - t * k)] = v1;
-            t = div(i + 2 * kRankThreads);
-            S.keys[t * kp + (i + 2 * kRankThreads - t * k)] = v2;
-            t = div(i + 3 * kRankThreads);
-            S.keys[t * kp + (i + 3 * kRankThreads - t * k)] = v3;
-        }
-        for (; i < n; i += kRankThreads) {
+        for (int i = threadIdx.x; i < n; i += kRankThreads) {
             const int t = div(i);
-            S.keys[t * kp + (i - t * k)] = __ldg(src + i);
+            cp_async4(&S.keys[t * kp + (i - t * k)], src + i);
         }
     }
     for (int e = threadIdx.x; e < E; e += kRankThreads) {
         const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
-        int4 f = make_int4(-1, 0, 0, b);
-        if (b < en) {
-            const Entry x = re[b];
-            f = make_int4(x.code, x.cum_end, x.out_base, b);
+        const int ne = en - b;
+        const int code = ne == 1 ? __ldg(&re[b].code) : (ne == 0 ? -2 : -1);
+        S.ec[e] = code;
+        // per-warp base: tile base (+ out_base when the expert has one entry);
+        // pass 1 then adds each warp's count into the following warps' bases
+        const int b0 = __ldg(tbase + e) + (ne == 1 ? __ldg(&re[b].out_base) : 0);
+#pragma unroll
+        for (int x = 0; x < kRankWarps; ++x) {
+            S.base[x * E + e] = x == 0 ? b0 : 0;
+            S.msk[x * E + e] = 0;
         }
-        S.first[e] = f;
     }
-    for (int i = threadIdx.x; i < kRankWarps * E; i += kRankThreads) S.mb[i] = make_int2(0, 0);
+    if (fast) cp_async_wait_all();
     __syncthreads();
 
     bool dup = !fast;
     if (fast) {
-        int2 *my = S.mb + w * E;
-        // pass 1: per-warp counts over its rounds
-        for (int r = 0; r < g.RW; ++r) {
-            const int t = (w * g.RW + r) * 32 + lane;
-            if (t < tg.ntok) {
-                int j = rot;
+        int *mybase = S.base + w * E;
+        unsigned *mymsk = S.msk + w * E;
+        // pass 1: per-warp counts over its rounds, added into the next warp's
+        // base (shifted by one so pass 2 is a plain prefix)
+        if (w + 1 < kRankWarps) {
+            int *nextbase = S.base + (w + 1) * E;
+            for (int r = 0; r < g.RW; ++r) {
+                const int t = (w * g.RW + r) * 32 + lane;
+                if (t < tg.ntok) {
+                    int j = rot;
 #pragma unroll
-                for (int jj = 0; jj < KB; ++jj) {
-                    if (jj < k) {
-                        const int e = S.keys[t * kp + j];
-                        if ((unsigned)e < (unsigned)E) atomicAdd(&my[e].y, 1);
-                        j = (j + 1 == k) ? 0 : j + 1;
+                    for (int jj = 0; jj < KB; ++jj) {
+                        if (jj < k) {
+                            const int e = S.keys[t * kp + j];
+                            if ((unsigned)e < (unsigned)E) atomicAdd(&nextbase[e], 1);
+                            j = (j + 1 == k) ? 0 : j + 1;
+                        }
                     }
                 }
             }
         }
         __syncthreads();
-        // pass 2: warp bases = tile base + counts of the warps before
+        // pass 2: inclusive prefix over warps
         for (int e = threadIdx.x; e < E; e += kRankThreads) {
-            int run = __ldg(tbase + e);
+            int run = 0;
 #pragma unroll
             for (int x = 0; x < kRankWarps; ++x) {
-                const int c = S.mb[x * E + e].y;
-                S.mb[x * E + e].y = run;
-                run += c;
+                run += S.base[x * E + e];
+                S.base[x * E + e] = run;
             }
         }
         __syncthreads();
@@ -548,8 +554,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
             }
 #pragma unroll
             for (int jj = 0; jj < KB; ++jj)
-                if (ek[jj] >= 0)
-                    dup |= (atomicOr(reinterpret_cast<unsigned *>(&my[ek[jj]].x), bit) & bit) != 0;
+                if (ek[jj] >= 0) dup |= (atomicOr(&mymsk[ek[jj]], bit) & bit) != 0;
             __syncwarp();
             int nb[KB];
             unsigned lead = 0;
@@ -559,22 +564,23 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                 for (int jj = 0; jj < KB; ++jj) {
                     nb[jj] = 0;
                     if (jj >= k) continue;
-                    int code = -1, ob = 0, occ = 0;
+                    int code = -1, pos = -1;
                     if (ek[jj] >= 0) {
-                        const int2 v = my[ek[jj]];
-                        const int rk = __popc((unsigned)v.x & lt_mask);
-                        occ = v.y + rk;
+                        const unsigned m = mymsk[ek[jj]];
+                        const int b = mybase[ek[jj]];
+                        const int rk = __popc(m & lt_mask);
                         if (rk == 0) {
                             lead |= 1u << jj;
-                            nb[jj] = v.y + __popc((unsigned)v.x);
+                            nb[jj] = b + __popc(m);
                         }
-                        code = route_lookup(S.first[ek[jj]], occ, ro + ek[jj] + 1, re, &ob);
+                        code = S.ec[ek[jj]];
+                        if (code >= 0) pos = b + rk;
+                        else if (code == -1) code = route_walk(b + rk, ro + ek[jj], re, &pos);
                         if (code < 0) bad_state = true;
                     }
                     if (vt) {
                         S.keys[t * kp + j] = code;
                         if (kFused) {
-                            const int pos = ob + occ;
                             if (code >= 0 && pos >= 0 && pos < g.npairs)
                                 sorted_layer[pos] = (int32_t)(tg.p0 + t * k + j);
                             else if (code >= 0)
@@ -583,21 +589,24 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                     }
                     if (!kFused)
                         pos_ws[tg.slot0 + ((t >> 5) * k + j) * 32 + lane] =
-                            (vt && code >= 0) ? ob + occ : -1;
+                            (vt && code >= 0) ? pos : -1;
                     j = (j + 1 == k) ? 0 : j + 1;
                 }
             }
             __syncwarp();
 #pragma unroll
             for (int jj = 0; jj < KB; ++jj)
-                if ((lead >> jj) & 1u) my[ek[jj]] = make_int2(0, nb[jj]);
+                if ((lead >> jj) & 1u) {
+                    mybase[ek[jj]] = nb[jj];
+                    mymsk[ek[jj]] = 0;
+                }
             __syncwarp();
         }
     }
     if (__syncthreads_or(dup)) {
         // a token repeats an expert (or k > KB): redo the tile exactly
-        rank_tile_exact<kFused>(g, tg, ids_layer, tbase, ro, re, reinterpret_cast<int *>(S.mb),
-                                dst_layer, pos_ws, sorted_layer, bad_id, bad_state);
+        rank_tile_exact<kFused>(g, tg, ids_layer, tbase, ro, re, S.base, dst_layer, pos_ws,
+                                sorted_layer, bad_id, bad_state);
     } else {
         // instance codes out, pair order, coalesced
         for (int i = threadIdx.x; i < n; i += kRankThreads) {
@@ -735,7 +744,7 @@ cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, in
 }  // namespace
 
 size_t rank_smem_bytes(const Geo &g) {
-    return (size_t)g.E * 16 + (size_t)kRankWarps * g.E * 8 + (size_t)g.TT * g.kp * 4;
+    return (size_t)g.E * 4 + (size_t)kRankWarps * g.E * 8 + (size_t)g.TT * g.kp * 4;
 }
 
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,

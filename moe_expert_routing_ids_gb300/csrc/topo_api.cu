@@ -55,7 +55,8 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     const int64_t nl = E / R + c->n_slot;
     if (nl > 32767) return TOPO_EINVAL;
     if (E * ((R + 31) / 32 + 1) * 4 > kSmemMax) return TOPO_EINVAL;
-    if ((2 * rpn + 2 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmemMax) return TOPO_EINVAL;
+    if ((2 * rpn + 3 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmemMax) return TOPO_EINVAL;  // refinement
+    if (E >= (1 << 26)) return TOPO_EINVAL;
     std::memset(g, 0, sizeof *g);
     g->T = c->T; g->E = c->E; g->k = c->k; g->R = c->R; g->rpn = c->ranks_per_node;
     g->n_slot = c->n_slot; g->M = c->R / c->ranks_per_node; g->E_R = c->E / c->R;
@@ -71,7 +72,7 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     // budget of two rank CTAs per SM and about kTilePairsTarget pairs; among
     // the admissible RW take the one with the least work per source counting
     // a fixed per-tile cost of 1.5 rounds.
-    const int64_t tables = E * (16 + 8 * kRankWarps);
+    const int64_t tables = E * (4 + 8 * kRankWarps);
     const int64_t round_bytes = (int64_t)kRankThreads * g->kp * 4;
     int64_t rw_max = kTilePairsTarget / ((int64_t)kRankThreads * c->k);
     const int64_t rw_smem = (kRankSmemTarget - tables) / round_bytes;
