@@ -394,6 +394,10 @@ __device__ void rank_tile_exact(const Geo &g, const TileGeo &tg, const int32_t *
 struct RankSmem {
     int *ec;         // [E] code of the expert's only routing entry in this row;
                      //     -1: several entries; -2: none
+    int *ro;         // [E+1] entry offsets of the row
+    int *ent_ce;     // [kRankEntCap] entries' cum_end, code, out_base (when the
+    int *ent_code;   //     row has at most kRankEntCap entries)
+    int *ent_ob;
     int *base;       // [kRankWarps][E] per-warp running base: the layout position
                      //     of the next pair (single entry) or its occurrence index
     unsigned *msk;   // [kRankWarps][E] per-warp token bitmask of the round
@@ -402,10 +406,15 @@ struct RankSmem {
 
 __device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
     RankSmem r;
-    r.ec = sm;
-    r.base = sm + g.E;
-    r.msk = reinterpret_cast<unsigned *>(sm + g.E + kRankWarps * g.E);
-    r.keys = reinterpret_cast<int32_t *>(sm + g.E + 2 * kRankWarps * g.E);
+    int *p = sm;
+    r.ec = p; p += g.E;
+    r.ro = p; p += g.E + 1;
+    r.ent_ce = p; p += kRankEntCap;
+    r.ent_code = p; p += kRankEntCap;
+    r.ent_ob = p; p += kRankEntCap;
+    r.base = p; p += kRankWarps * g.E;
+    r.msk = reinterpret_cast<unsigned *>(p); p += kRankWarps * g.E;
+    r.keys = reinterpret_cast<int32_t *>(p);
     return r;
 }
 
@@ -418,10 +427,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Instance code and layout position for occurrence occ of an expert with
-// several entries in this row (entries in rank order, running ranges).
-__device__ __forceinline__ int route_walk(int occ, const int32_t *ro_e, const Entry *re, int *pos) {
-    const int b = __ldg(ro_e), en = __ldg(ro_e + 1);
+// Instance code and layout position for occurrence occ of expert e with
+// several entries in this row (entries in rank order, running ranges), from
+// shared memory when the row's entries fit there.
+__device__ __forceinline__ int route_walk(int occ, int e, const RankSmem &S, bool row_in_smem,
+                                          const Entry *re, int *pos) {
+    const int b = S.ro[e], en = S.ro[e + 1];
+    if (row_in_smem) {
+        for (int j = b; j < en; ++j)
+            if (occ < S.ent_ce[j]) {
+                *pos = S.ent_ob[j] + occ;
+                return S.ent_code[j];
+            }
+        return -1;
+    }
     for (int j = b; j < en; ++j) {
         if (occ < __ldg(&re[j].cum_end)) {
             *pos = __ldg(&re[j].out_base) + occ;
@@ -481,11 +500,21 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
             cp_async4(&S.keys[t * kp + (i - t * k)], src + i);
         }
     }
+    const int n_ent = __ldg(ro + E);
+    const bool row_in_smem = n_ent <= kRankEntCap;
+    if (row_in_smem)
+        for (int j = threadIdx.x; j < n_ent; j += kRankThreads) {
+            S.ent_ce[j] = __ldg(&re[j].cum_end);
+            S.ent_code[j] = __ldg(&re[j].code);
+            S.ent_ob[j] = __ldg(&re[j].out_base);
+        }
+    if (threadIdx.x == 0) S.ro[E] = n_ent;
     for (int e = threadIdx.x; e < E; e += kRankThreads) {
         const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
         const int ne = en - b;
         const int code = ne == 1 ? __ldg(&re[b].code) : (ne == 0 ? -2 : -1);
         S.ec[e] = code;
+        S.ro[e] = b;
         // per-warp base: tile base (+ out_base when the expert has one entry);
         // pass 1 then adds each warp's count into the following warps' bases
         const int b0 = __ldg(tbase + e) + (ne == 1 ? __ldg(&re[b].out_base) : 0);
@@ -575,7 +604,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                         }
                         code = S.ec[ek[jj]];
                         if (code >= 0) pos = b + rk;
-                        else if (code == -1) code = route_walk(b + rk, ro + ek[jj], re, &pos);
+                        else if (code == -1) code = route_walk(b + rk, ek[jj], S, row_in_smem, re, &pos);
                         if (code < 0) bad_state = true;
                     }
                     if (vt) {
@@ -744,7 +773,8 @@ cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, in
 }  // namespace
 
 size_t rank_smem_bytes(const Geo &g) {
-    return (size_t)g.E * 4 + (size_t)kRankWarps * g.E * 8 + (size_t)g.TT * g.kp * 4;
+    return ((size_t)2 * g.E + 1 + 3 * (size_t)kRankEntCap) * 4 + (size_t)kRankWarps * g.E * 8 +
+           (size_t)g.TT * g.kp * 4;
 }
 
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
