@@ -53,8 +53,7 @@ struct Geo {
     size_t off_main;        // int32 [2E + R*E_R]     main(e), local index, mains[r][j]
     size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
     size_t off_iexp;        // int32 [L][n_keys]      expert held by each instance
-    size_t off_ioff;        // int32 [L][E+1]         instance list offsets by expert
-    size_t off_ilist;       // int32 [L][n_inst_cap]  instances, ascending rank per expert
+    size_t off_imask;       // u32   [L][E][ceil(R/32)] ranks holding an instance of each expert
     size_t off_roff;        // int32 [L][R][E+1]      per-(s,e) entry offsets in row s
     size_t off_rent;        // int4  [L][R][n_inst_cap] (inst, cum_start, cum_end, out_base)
     size_t off_soff;        // int32 [L][R][n_keys]   column prefix of q over sources
@@ -117,6 +116,7 @@ cudaError_t launch_reroute_layout(const Geo &g, const int32_t *main_rank, const 
                                   int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
                                   void *ws, uint64_t hist_fp, cudaStream_t st);
 // Shared-memory bytes of the rank kernel for this geometry.
+size_t row_index_smem(const Geo &g);
 size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
