@@ -54,6 +54,8 @@ struct Geo {
     size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
     size_t off_iexp;        // int32 [L][n_keys]      expert held by each instance
     size_t off_imask;       // u32   [L][E][ceil(R/32)] ranks holding an instance of each expert
+    size_t off_ioff;        // int32 [L][E+1]         start of each expert's instances in ilist
+    size_t off_ilist;       // int32 [L][n_keys]      instances grouped by expert, ascending rank
     size_t off_roff;        // int32 [L][R][E+1]      per-(s,e) entry offsets in row s
     size_t off_rent;        // int4  [L][R][n_inst_cap] (inst, cum_start, cum_end, out_base)
     size_t off_soff;        // int32 [L][R][n_keys]   column prefix of q over sources
@@ -97,6 +99,39 @@ __host__ __device__ inline T *ws_at(void *ws, size_t off) {
 // current device, once per (kernel, device): later calls, including calls
 // made while a stream is being captured into a CUDA graph, launch only.
 cudaError_t ensure_smem(const void *fn, size_t bytes);
+
+// Routing-index entry of one (source, instance) pair with a nonzero count:
+// the instance code r * n_local + l, the source's occurrences of the expert
+// routed there [cum_start, cum_end), and the layout position of occurrence
+// cum_start minus cum_start.
+struct Entry {
+    int32_t code;
+    int32_t cum_start;
+    int32_t cum_end;
+    int32_t out_base;
+};
+static_assert(sizeof(Entry) == 16, "entry size");
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Prep of the rerouting calls (instance index, routing index, layout
+// offsets), from the plan alone; defined in k_prep.cu.
+cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_t &p, void *ws,
+                        cudaStream_t st);
+cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
+                               int n_stats, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the kernel translation units).  Each returns

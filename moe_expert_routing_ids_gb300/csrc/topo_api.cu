@@ -54,7 +54,8 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     const int64_t E = c->E, R = c->R, rpn = c->ranks_per_node;
     const int64_t nl = E / R + c->n_slot;
     if (nl > 32767) return TOPO_EINVAL;
-    if ((2 * R * nl + 4 + E * ((R + 31) / 32) + 3 * E + 1) * 4 + 2560 > kSmemMax) return TOPO_EINVAL;  // row index
+    if ((2 * (R * nl + 3) + E + 4 + 2 * E) * 4 + 2560 > kSmemMax) return TOPO_EINVAL;       // row index
+    if ((E * ((R + 31) / 32) + E + 1) * 4 + 256 > kSmemMax) return TOPO_EINVAL;             // instance list
     if ((2 * rpn + 3 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmemMax) return TOPO_EINVAL;  // refinement
     if (E >= (1 << 26)) return TOPO_EINVAL;
     std::memset(g, 0, sizeof *g);
@@ -105,6 +106,8 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     g->off_rep = off;   off = align_up(off + L * E * g->M * 4);
     g->off_iexp = off;  off = align_up(off + L * g->n_keys * 4);
     g->off_imask = off; off = align_up(off + L * E * ((R + 31) / 32) * 4);
+    g->off_ioff = off;  off = align_up(off + L * (E + 1) * 4);
+    g->off_ilist = off; off = align_up(off + L * g->n_keys * 4);
     g->off_roff = off;  off = align_up(off + L * R * (E + 1) * 4);
     g->off_rent = off;  off = align_up(off + L * R * g->n_inst_cap * 16);
     g->off_soff = off;  off = align_up(off + L * R * g->n_keys * 4);
