@@ -48,8 +48,10 @@ COOCCUR_WORKLOAD = 4
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
 KERNELS_PER_CALL = {"hist": 1, "plan": 4, "reroute_layout": 8, "cooccur": 1}
 CALLS = ("hist", "plan", "reroute_layout")
-CALL_SOURCE = {"hist": "k_hist.cu", "plan": "k_plan.cu", "reroute_layout": "k_route.cu",
-               "cooccur": "k_cooccur.cu"}
+# kernel sources of each call (with the shared header): recorded DRAM traffic
+# counts only while these are unchanged
+CALL_SOURCE = {"hist": ("k_hist.cu",), "plan": ("k_plan.cu",),
+               "reroute_layout": ("k_prep.cu", "k_route.cu"), "cooccur": ("k_cooccur.cu",)}
 CALL_KERNEL = {"hist": "k_hist_tiles", "reroute_layout": "k_route_tiles", "cooccur": "k_cooccur"}
 
 
@@ -77,9 +79,11 @@ def peaks():
 
 
 def source_sha(call: str) -> str:
-    path = os.path.join(ROOT, "moe_expert_routing_ids_gb300", "csrc", CALL_SOURCE[call])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in CALL_SOURCE[call] + ("common.cuh",):
+        with open(os.path.join(ROOT, "moe_expert_routing_ids_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(call: str, units: int):
