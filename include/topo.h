@@ -198,6 +198,38 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
                         int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
                         size_t ws_bytes, cudaStream_t stream);
 
+/* topo_hist without a caller-supplied workspace.  No passage of the pages
+ * has a counterpart: it computes exactly what topo_hist computes (Omega), for
+ * callers that cannot hand the library device memory on the step path -- C
+ * or C++ hosts with no device allocator of their own, and processes that
+ * reserve the device's memory up front, where a cudaMalloc during a step
+ * would fail or would make a caching allocator release memory and
+ * synchronise the device.
+ *
+ * Scratch: one fixed array of TOPO_HIST_NOALLOC_SCRATCH_BYTES per device,
+ * compiled into the library; the call allocates nothing.  It holds a 256-byte
+ * error header, n_layers * R int32 tile counters and the per-tile expert
+ * counts, n_layers * R * tiles_per_source * E int32 (each region 256-byte
+ * aligned).  Shapes that need more return TOPO_ENOSPC before anything runs.
+ * Each call clears the header and the counters on `stream` before its kernel.
+ *
+ * The first call on a device looks the array's address up (with that device
+ * current) and caches it; make that first call before any stream capture.
+ * All calls on one device share the array: calls that overlap in time (on
+ * different streams, or from several host threads without ordering) race on
+ * it and give undefined results.  The tile index left in the array is not
+ * usable by topo_reroute or topo_dispatch_layout.
+ *
+ * ids:  device int32 [n_layers][T][k].   hist: device int32 [n_layers][R][E].
+ * err:  device int32, or NULL; receives the call's device error word
+ *       (TOPO_OK, or TOPO_ERANGE when an id lies outside [0, E), which is
+ *       skipped), in stream order.
+ * Returns TOPO_EINVAL / TOPO_ENOSPC on the host, TOPO_ECUDA if the lookup or a
+ * launch fails. */
+#define TOPO_HIST_NOALLOC_SCRATCH_BYTES (16u << 20)
+int topo_hist_noalloc(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t *hist,
+                      int32_t *err, cudaStream_t stream);
+
 /* Synchronous: copies the error word out of ws (device) and returns it
  * (TOPO_OK or a negative code; TOPO_ECUDA if the copy fails).  Call after
  * the stream that used ws has been synchronised. */

@@ -28,7 +28,8 @@ TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
 EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-           "topo_strerror")
+           "topo_strerror", "topo_hist_noalloc")
+TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class TopoError(RuntimeError):
@@ -77,11 +78,13 @@ def lib():
             L.topo_reroute.argtypes = [cfgp, i32, vp, planp, vp, vp, sz, vp]
             L.topo_dispatch_layout.argtypes = [cfgp, i32, vp, planp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_reroute_layout.argtypes = [cfgp, i32, vp, planp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_hist_noalloc.argtypes = [cfgp, i32, vp, vp, vp, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
-                      "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error"):
+                      "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
+                      "topo_hist_noalloc"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -176,6 +179,13 @@ def topo_reroute_layout(cfg: TopoCfg, n_layers: int, ids, plan: TopoPlan, dst_in
                                           _p(dst_inst), _p(sorted_pairs), _p(seg_off),
                                           _p(send_counts), _p(layout_stats), _p(ws), ws_bytes,
                                           _s(stream)))
+
+
+def topo_hist_noalloc(cfg: TopoCfg, n_layers: int, ids, hist, err=None, stream=None) -> int:
+    """topo_hist with the library's fixed scratch array instead of a workspace;
+    err: optional device int32 that receives the device error word."""
+    return _chk("topo_hist_noalloc", lib().topo_hist_noalloc(ctypes.byref(cfg), n_layers, _p(ids),
+                                                             _p(hist), _p(err), _s(stream)))
 
 
 def topo_read_error(ws) -> int:

@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstddef>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -265,3 +266,60 @@ const char *topo_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// topo_hist_noalloc: topo_hist with its scratch in a fixed per-device array,
+// for callers that cannot give the library device memory during a step.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TOPO_HIST_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+
+// Address of the scratch array on the current device, looked up once per
+// device (the lookup may load the module, so it belongs before any capture).
+cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int topo_hist_noalloc(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids,
+                                 int32_t *hist, int32_t *err, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (!hist || (!ids && g.npairs > 0 && n_layers > 0)) return TOPO_EINVAL;
+    // Compact layout: header, tile counters, tile counts (the histogram
+    // kernel reads no other region).
+    const size_t tiles = (size_t)n_layers * g.R * g.tps;
+    g.off_done = sizeof(WsHeader);
+    g.off_tile = align_up(g.off_done + (size_t)n_layers * g.R * sizeof(int32_t));
+    g.total = align_up(g.off_tile + tiles * g.E * sizeof(int32_t));
+    if (g.total > TOPO_HIST_NOALLOC_SCRATCH_BYTES) return TOPO_ENOSPC;
+    void *ws = nullptr;
+    cudaError_t e = noalloc_scratch(&ws);
+    if (e != cudaSuccess) return TOPO_ECUDA;
+    e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), stream);     // error word starts at 0
+    if (e == cudaSuccess && n_layers > 0)
+        e = launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream);   // clears the counters
+    if (e == cudaSuccess && err)
+        e = cudaMemcpyAsync(err, static_cast<char *>(ws) + offsetof(WsHeader, error), sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, stream);
+    return cuda_rc(e);
+}
