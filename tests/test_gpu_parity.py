@@ -202,6 +202,41 @@ def test_cooccur_repeated_ids():
     assert err == 0 and np.array_equal(co, oco) and np.array_equal(tr, otr)
 
 
+@pytest.mark.parametrize("L,T,E,k", [(2, 3001, 159, 10), (2, 1500, 160, 8), (3, 2000, 64, 6),
+                                     (2, 500, 100, 2)])
+def test_cooccur_shapes_around_the_shared_memory_limit(L, T, E, k):
+    # E <= 159 keeps both (E+1)^2 matrices of a CTA in shared memory; 160 does not
+    ids = W.random_small(T + 3 * E + k, T, E, k, L, s=1.2)
+    co, tr, err = gpu_cooccur(ids, E)
+    assert err == 0
+    oco, otr = oracle.cooccur(ids, E)
+    assert np.array_equal(co, oco) and np.array_equal(tr, otr)
+
+
+def test_cooccur_repeated_ids_exact_k():
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, 5, size=(3, 700, 4)).astype(np.int32)   # many repeats per token
+    co, tr, err = gpu_cooccur(ids, 5)
+    oco, otr = oracle.cooccur(ids, 5)
+    assert err == 0 and np.array_equal(co, oco) and np.array_equal(tr, otr)
+
+
+@pytest.mark.parametrize("k", [8, 3])
+def test_cooccur_out_of_range_id_is_dropped_and_flagged(k):
+    from moe_expert_routing_ids_gb300 import TOPO_ERANGE
+    E = 32
+    ids = W.random_small(9, 600, E, k, 2)
+    ids[0, 17, 1] = E + 5
+    ids[1, 40, k - 1] = -1
+    co, tr, err = gpu_cooccur(ids, E)
+    assert err == TOPO_ERANGE
+    # the same counts as with the bad ids moved to a spare expert E and dropped
+    spare = ids.copy()
+    spare[(spare < 0) | (spare >= E)] = E
+    oco, otr = oracle.cooccur(spare, E + 1)
+    assert np.array_equal(co, oco[:, :E, :E]) and np.array_equal(tr, otr[:, :E, :E])
+
+
 def test_cooccur_without_transitions():
     ids = W.random_small(5, 1000, 16, 4, 3)
     co, tr, err = gpu_cooccur(ids, 16, transitions=False)
