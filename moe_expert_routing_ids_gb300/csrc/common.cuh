@@ -74,7 +74,11 @@ __host__ __device__ inline int64_t cost_sr(const Geo &g, int s, int r) {
 }
 
 // Record the first device error in the header (sticky).
-__device__ inline void set_error(WsHeader *h, int code) { atomicCAS(&h->error, 0, code); }
+// First error wins; once the word is set, later reporters only read it (no
+// atomic traffic on one address when every thread of a launch reports).
+__device__ inline void set_error(WsHeader *h, int code) {
+    if (*reinterpret_cast<volatile int32_t *>(&h->error) == 0) atomicCAS(&h->error, 0, code);
+}
 
 // 64-bit fingerprint mixing (splitmix64 finaliser).
 __host__ __device__ inline uint64_t fp_mix(uint64_t h, uint64_t v) {
