@@ -46,7 +46,7 @@ COOCCUR_WORKLOAD = 4
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 1, "plan": 4, "reroute_layout": 8, "cooccur": 1}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged

@@ -108,8 +108,8 @@ typedef struct {
  * header (cfg may then be NULL).  Returns 0 for an invalid cfg. */
 size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call);
 
-/* Clear the workspace header (error word, indices' fingerprints and
- * counters).  Call once on a fresh workspace and after reading an error.
+ /* Clear the workspace header (error word and the indices' fingerprints;
+ * nothing else).  Call once on a fresh workspace and after reading an error.
  * ws: device, at least TOPO_CALL_COOCCUR bytes. */
 int topo_ws_reset(void *ws, size_t ws_bytes, cudaStream_t stream);
 
@@ -208,10 +208,10 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
  *
  * Scratch: one fixed array of TOPO_HIST_NOALLOC_SCRATCH_BYTES per device,
  * compiled into the library; the call allocates nothing.  It holds a 256-byte
- * error header, n_layers * R int32 tile counters and the per-tile expert
- * counts, n_layers * R * tiles_per_source * E int32 (each region 256-byte
- * aligned).  Shapes that need more return TOPO_ENOSPC before anything runs.
- * Each call clears the header and the counters on `stream` before its kernel.
+ * error header and the per-tile expert counts, n_layers * R *
+ * tiles_per_source * E int32.  Shapes that need more return TOPO_ENOSPC
+ * before anything runs.  Each call clears the header on `stream` before its
+ * kernels (every tile count is rewritten).
  *
  * The first call on a device looks the array's address up (with that device
  * current) and caches it; make that first call before any stream capture.

@@ -49,7 +49,6 @@ struct Geo {
     size_t off_tile;        // int32 [L][R][tps][E]   tile counts -> exclusive prefix
     size_t off_pos;         // int32 [L][R][tps][TT*k] layout position of each pair,
                             //        in (warp, round, slot, lane) order within a tile
-    size_t off_done;        // int32 [L][R]           tiles finished per source
     size_t off_main;        // int32 [2E + R*E_R]     main(e), local index, mains[r][j]
     size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
     size_t off_iexp;        // int32 [L][n_keys]      expert held by each instance

@@ -102,7 +102,6 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     size_t off = sizeof(WsHeader);
     g->off_tile = off;  off = align_up(off + tiles * E * 4);
     g->off_pos = off;   off = align_up(off + tiles * g->TT * c->k * 4);
-    g->off_done = off;  off = align_up(off + L * R * 4);
     g->off_main = off;  off = align_up(off + 3 * E * 4);
     g->off_rep = off;   off = align_up(off + L * E * g->M * 4);
     g->off_iexp = off;  off = align_up(off + L * g->n_keys * 4);
@@ -305,11 +304,10 @@ extern "C" int topo_hist_noalloc(const topo_cfg *cfg, int32_t n_layers, const in
     int rc = make_geo(cfg, n_layers, &g);
     if (rc) return rc;
     if (!hist || (!ids && g.npairs > 0 && n_layers > 0)) return TOPO_EINVAL;
-    // Compact layout: header, tile counters, tile counts (the histogram
-    // kernel reads no other region).
+    // Compact layout: header, tile counts (the histogram kernels touch no
+    // other region).
     const size_t tiles = (size_t)n_layers * g.R * g.tps;
-    g.off_done = sizeof(WsHeader);
-    g.off_tile = align_up(g.off_done + (size_t)n_layers * g.R * sizeof(int32_t));
+    g.off_tile = sizeof(WsHeader);
     g.total = align_up(g.off_tile + tiles * g.E * sizeof(int32_t));
     if (g.total > TOPO_HIST_NOALLOC_SCRATCH_BYTES) return TOPO_ENOSPC;
     void *ws = nullptr;
@@ -317,7 +315,7 @@ extern "C" int topo_hist_noalloc(const topo_cfg *cfg, int32_t n_layers, const in
     if (e != cudaSuccess) return TOPO_ECUDA;
     e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), stream);     // error word starts at 0
     if (e == cudaSuccess && n_layers > 0)
-        e = launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream);   // clears the counters
+        e = launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream);
     if (e == cudaSuccess && err)
         e = cudaMemcpyAsync(err, static_cast<char *>(ws) + offsetof(WsHeader, error), sizeof(int32_t),
                             cudaMemcpyDeviceToDevice, stream);

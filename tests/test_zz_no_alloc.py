@@ -52,7 +52,7 @@ def test_hist_noalloc_matches_topo_hist_twice_in_a_row():
     cases = []
     # the full-size 4-microbatch workloads (T = 1048576 with 8 tiles per
     # source, then T = 65536), then a small ragged one: no call may see the
-    # previous call's counters
+    # previous call's counts or error word
     for n in (5, 3):
         w = W.CONFIGS[n]
         cases.append((_cfg(w.T, w.E, w.k, w.R, w.ranks_per_node, w.n_slot), w.n_layers,
