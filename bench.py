@@ -40,9 +40,6 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-WORKLOAD = 5                 # the stress configuration
-PLAN_LATENCY_WORKLOAD = 2    # T=16384, E=64, k=6, R=32 (4 x 8), 8 slots
-COOCCUR_WORKLOAD = 4
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
@@ -64,6 +61,8 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="--impl reference: seconds the oracle steps should take in total")
     return ap.parse_args()
 
 
@@ -97,6 +96,18 @@ def profiled_traffic(call: str, units: int):
     if not rec or rec.get("source_sha") != source_sha(call):
         return None
     return rec["dram_bytes"] * units / rec["units"]
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest x over the ranks of the default process group (x itself
+    without one): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 class Clocks:
@@ -187,9 +198,10 @@ class GraphEvents:
 
 
 def cpu_sample_chain(w, ids_layer):
-    """Oracle chain on one microbatch: (seconds, pairs)."""
+    """Oracle chain on one microbatch of ids [1, T', k] (T' may be a slice of
+    the workload's T, a multiple of R): (seconds, pairs)."""
     import oracle
-    cfg = w.plan_cfg
+    cfg = dict(w.plan_cfg, T=int(ids_layer.shape[1]))
     t0 = time.perf_counter()
     h = oracle.hist(ids_layer, w.R, w.E)
     p = oracle.plan(cfg, h)
@@ -198,38 +210,59 @@ def cpu_sample_chain(w, ids_layer):
     return time.perf_counter() - t0, int(ids_layer.size)
 
 
+def reference_slice_tokens(w, rate: float, steps: int, warmup: int, budget_s: float) -> int:
+    """Tokens per oracle step so that warm-up + steps take about budget_s at
+    `rate` pairs/s: a multiple of R, between R and T."""
+    per_step = budget_s / max(1, steps + warmup)
+    t = int(per_step * rate / w.k) // w.R * w.R
+    return max(w.R, min(w.T, t))
+
+
 # ------------------------------------------------------------------ reference
 
 def run_reference(args, rank):
-    """CPU oracle arm: each step is the oracle chain on one microbatch of the
-    stress workload (a bounded sample); metric and unit as ours."""
+    """CPU oracle arm, rank 0 only: exactly `steps` timed steps, each the
+    oracle chain (hist, plan, reroute, layout) on one token slice of a stress
+    microbatch; the slice is sized from a calibration run so the whole arm
+    takes about --ref-budget-s seconds, and consecutive steps take
+    consecutive slices.  Metric and unit as ours."""
     if rank != 0:
         return
     import oracle
     from moe_expert_routing_ids_gb300 import workloads as W
     oracle.build()
-    w = W.CONFIGS[WORKLOAD]
+    w = W.STRESS
     ids = w.ids(n_layers=1)
-    steps = max(1, min(args.steps, 3))
-    warm = max(0, min(args.warmup, 1))
-    for _ in range(warm):
-        cpu_sample_chain(w, ids)
+    cal_t = max(w.R, (w.T // 64) // w.R * w.R)
+    cal_s, cal_n = cpu_sample_chain(w, ids[:, :cal_t])
+    t_s = reference_slice_tokens(w, cal_n / max(cal_s, 1e-9), args.steps, args.warmup,
+                                 args.ref_budget_s)
+    n_slices = max(1, w.T // t_s)
+
+    def step(i):
+        o = (i % n_slices) * t_s
+        return cpu_sample_chain(w, ids[:, o:o + t_s])
+
+    for i in range(args.warmup):
+        step(i)
     secs, pairs = 0.0, 0
     t0 = time.perf_counter()
-    for _ in range(steps):
-        s, n = cpu_sample_chain(w, ids)
+    for i in range(args.steps):
+        s, n = step(args.warmup + i)
         secs += s
         pairs += n
     wall = time.perf_counter() - t0
     value = pairs / secs
-    sample = f"1 of 4 microbatches ({pairs // steps} pairs) per step, oracle hist+plan+reroute+layout"
+    sample = (f"per step {t_s} of the {w.T} tokens of one stress microbatch ({t_s * w.k} pairs), "
+              f"oracle hist+plan+reroute+layout single-threaded; {args.steps} steps, {secs:.1f} s")
     line = {"impl": "reference", "metric": "routed (token,slot) pairs/sec", "value": value,
-            "unit": "pairs/s", "n_gpus": args.gpus, "steps": steps, "warmup": warm,
-            "ms_per_step": 1e3 * wall / steps, "higher_is_better": True, "scaling": "weak",
+            "unit": "pairs/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "R": w.R,
                        "ranks_per_node": w.ranks_per_node, "n_slot": w.n_slot,
-                       "microbatches": w.n_layers, "parallelism": "replicas"},
+                       "microbatches": w.n_layers, "tokens_per_step": t_s,
+                       "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
@@ -295,7 +328,7 @@ def secondary_plan_latency(dev, stream):
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
     from moe_expert_routing_ids_gb300.planner import Planner
-    w = W.CONFIGS[PLAN_LATENCY_WORKLOAD]
+    w = W.PLAN_LATENCY
     P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
     ids = torch.as_tensor(w.ids(), device=dev)
     with torch.cuda.stream(stream):
@@ -324,7 +357,7 @@ def secondary_cooccur(dev, stream, hbm_peak):
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
     from moe_expert_routing_ids_gb300.planner import Cooccur
-    w = W.CONFIGS[COOCCUR_WORKLOAD]
+    w = W.COOCCUR
     C = Cooccur(w.n_layers, w.T, w.E, w.k, dev)
     ids = torch.as_tensor(w.ids(), device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -361,7 +394,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
-    w = W.CONFIGS[WORKLOAD]
+    w = W.STRESS
     ids = w.ids(replica=rank)
     pairs = int(ids.size)
     d_ids = torch.as_tensor(ids, device=dev)
@@ -386,10 +419,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     if P.error() != 0:
         raise RuntimeError("device error after the timed region")
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     if rank != 0:
         return
     ms_step = total_ms / steps_run

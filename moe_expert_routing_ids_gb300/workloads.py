@@ -17,10 +17,11 @@ structure of the pages' workloads:
   fall in seeded groups; later slots stay in the first slot's group with a
   fixed probability.
 
-Every array is produced by numpy ``Generator(PCG64(SeedSequence([config,
-layer])))`` so a config is reproducible on any machine.
+Every array is produced by numpy ``Generator(PCG64(SeedSequence([seed,
+layer])))`` so a workload is reproducible on any machine.
 
-The five named workloads (``CONFIGS``) carry the planner parameters the pages
+The five named workloads (``WORKLOADS``, by name; ``SMALL``, ``PLAN_LATENCY``,
+``FOUR_LAYER``, ``COOCCUR``, ``STRESS``) carry the planner parameters the pages
 fix or imply: S_tok = 2 * hidden (BF16 activations, TopoEP §2.3 / §4.1) and
 ||W|| = 3 * hidden * intermediate * 2 bytes (gate, up and down projections in
 BF16; TopoEP §2.3 Fig. 3 and Table 1), with integer per-byte costs
@@ -141,9 +142,10 @@ def grouped_topk(rng, E: int, T: int, k: int, groups: np.ndarray, stay: float) -
 @dataclasses.dataclass(frozen=True)
 class Workload:
     """One named workload.  ``plan_cfg`` is the planner's parameter set."""
-    index: int
+    seed: int                 # first key of every layer's random stream
     name: str
     kind: str                 # "plan" (hist, plan, reroute, layout) or "cooccur"
+    structure: str            # "zipf", "neighbourhood" or "grouped"
     T: int
     E: int
     k: int
@@ -155,6 +157,7 @@ class Workload:
     intermediate: int = 0
     c_intra: int = 1
     c_inter: int = 4
+    zipf_s: float = 1.0
 
     @property
     def plan_cfg(self) -> dict:
@@ -172,14 +175,19 @@ class Workload:
     def ids(self, replica: int = 0, n_layers: int | None = None) -> np.ndarray:
         """int32 [n_layers, T, k].  ``replica`` > 0 draws an independent copy
         (another data-parallel replica); ``n_layers`` truncates the stack."""
-        return GENERATORS[self.index](self, replica, self.n_layers if n_layers is None else n_layers)
+        n = self.n_layers if n_layers is None else n_layers
+        if self.structure == "zipf":
+            return _gen_zipf(self, self.zipf_s, replica, n)
+        if self.structure == "neighbourhood":
+            return _gen_neighbourhood(self, replica, n)
+        return _gen_grouped(self, replica, n)
 
 
 def _seed(w: Workload, replica: int, l: int):
-    return rng_for(w.index, l) if replica == 0 else rng_for(w.index, l, replica)
+    return rng_for(w.seed, l) if replica == 0 else rng_for(w.seed, l, replica)
 
 
-def _gen_zipf_single(w: Workload, s: float, replica: int, n_layers: int) -> np.ndarray:
+def _gen_zipf(w: Workload, s: float, replica: int, n_layers: int) -> np.ndarray:
     out = np.empty((n_layers, w.T, w.k), np.int32)
     for l in range(n_layers):
         rng = _seed(w, replica, l)
@@ -188,7 +196,7 @@ def _gen_zipf_single(w: Workload, s: float, replica: int, n_layers: int) -> np.n
     return out
 
 
-def _gen_cfg3(w: Workload, replica: int, n_layers: int) -> np.ndarray:
+def _gen_neighbourhood(w: Workload, replica: int, n_layers: int) -> np.ndarray:
     s_per_layer = (0.8, 1.2, 1.6, 1.2)
     out = np.empty((n_layers, w.T, w.k), np.int32)
     for l in range(n_layers):
@@ -203,7 +211,7 @@ def _gen_cfg3(w: Workload, replica: int, n_layers: int) -> np.ndarray:
     return out
 
 
-def _gen_cfg4(w: Workload, replica: int, n_layers: int) -> np.ndarray:
+def _gen_grouped(w: Workload, replica: int, n_layers: int) -> np.ndarray:
     out = np.empty((n_layers, w.T, w.k), np.int32)
     for l in range(n_layers):
         rng = _seed(w, replica, l)
@@ -212,25 +220,22 @@ def _gen_cfg4(w: Workload, replica: int, n_layers: int) -> np.ndarray:
     return out
 
 
-CONFIGS = {
-    1: Workload(1, "t4096_e8_k2_r8", "plan", T=4096, E=8, k=2, n_layers=1, R=8,
-                ranks_per_node=4, n_slot=2, hidden=1024, intermediate=768),
-    2: Workload(2, "t16384_e64_k6_r32", "plan", T=16384, E=64, k=6, n_layers=1, R=32,
-                ranks_per_node=8, n_slot=8, hidden=4096, intermediate=1408),
-    3: Workload(3, "t65536_e256_k8_r64_4layers", "plan", T=65536, E=256, k=8, n_layers=4,
-                R=64, ranks_per_node=8, n_slot=32, hidden=7168, intermediate=1536),
-    4: Workload(4, "cooccur_l8_t262144_e128_k8", "cooccur", T=262144, E=128, k=8, n_layers=8),
-    5: Workload(5, "t1048576_e512_k10_r128_4mb", "plan", T=1048576, E=512, k=10, n_layers=4,
-                R=128, ranks_per_node=8, n_slot=64, hidden=7168, intermediate=1536),
-}
+SMALL = Workload(1, "t4096_e8_k2_r8", "plan", "zipf", T=4096, E=8, k=2, n_layers=1, R=8,
+                 ranks_per_node=4, n_slot=2, hidden=1024, intermediate=768, zipf_s=1.0)
+PLAN_LATENCY = Workload(2, "t16384_e64_k6_r32", "plan", "zipf", T=16384, E=64, k=6, n_layers=1,
+                        R=32, ranks_per_node=8, n_slot=8, hidden=4096, intermediate=1408,
+                        zipf_s=1.2)
+FOUR_LAYER = Workload(3, "t65536_e256_k8_r64_4layers", "plan", "neighbourhood", T=65536, E=256,
+                      k=8, n_layers=4, R=64, ranks_per_node=8, n_slot=32, hidden=7168,
+                      intermediate=1536)
+COOCCUR = Workload(4, "cooccur_l8_t262144_e128_k8", "cooccur", "grouped", T=262144, E=128, k=8,
+                   n_layers=8)
+STRESS = Workload(5, "t1048576_e512_k10_r128_4mb", "plan", "zipf", T=1048576, E=512, k=10,
+                  n_layers=4, R=128, ranks_per_node=8, n_slot=64, hidden=7168, intermediate=1536,
+                  zipf_s=1.4)
 
-GENERATORS = {
-    1: lambda w, r, n: _gen_zipf_single(w, 1.0, r, n),
-    2: lambda w, r, n: _gen_zipf_single(w, 1.2, r, n),
-    3: _gen_cfg3,
-    4: _gen_cfg4,
-    5: lambda w, r, n: _gen_zipf_single(w, 1.4, r, n),
-}
+WORKLOADS = {w.name: w for w in (SMALL, PLAN_LATENCY, FOUR_LAYER, COOCCUR, STRESS)}
+PLAN_WORKLOADS = (SMALL, PLAN_LATENCY, FOUR_LAYER, STRESS)
 
 
 def random_small(seed: int, T: int, E: int, k: int, n_layers: int = 1, s: float = 1.0) -> np.ndarray:

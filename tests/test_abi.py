@@ -115,8 +115,7 @@ def test_null_and_short_workspace(lib):
 
 def test_workspace_sizes(lib):
     from moe_expert_routing_ids_gb300 import workloads as W
-    for i in (1, 2, 3, 5):
-        w = W.CONFIGS[i]
+    for w in W.PLAN_WORKLOADS:
         n = topo.topo_workspace_bytes(topo.make_cfg(**w.plan_cfg), w.n_layers, topo.TOPO_CALL_CHAIN)
         assert 256 < n < (1 << 30)
     assert topo.topo_workspace_bytes(None, 0, topo.TOPO_CALL_COOCCUR) == 256

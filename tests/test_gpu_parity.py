@@ -68,9 +68,8 @@ def check(cfg, ids, both=True):
         assert_same(gpu, want)
 
 
-@pytest.mark.parametrize("index", [1, 2, 3, 5])
-def test_named_workloads_full_size(index):
-    w = W.CONFIGS[index]
+@pytest.mark.parametrize("w", W.PLAN_WORKLOADS, ids=lambda w: w.name)
+def test_named_workloads_full_size(w):
     check(w.plan_cfg, w.ids())
 
 
@@ -146,7 +145,7 @@ def test_main_rank_map():
 def test_repeat_runs_are_byte_identical():
     from moe_expert_routing_ids_gb300.planner import Planner
     dev = _dev()
-    w = W.CONFIGS[2]
+    w = W.PLAN_LATENCY
     ids = torch.as_tensor(w.ids(), device=dev)
     P = Planner(w.plan_cfg, w.n_layers, dev)
     P.run(ids)
@@ -174,7 +173,7 @@ def gpu_cooccur(ids, E, transitions=True):
 
 
 def test_cooccur_full_size():
-    w = W.CONFIGS[4]
+    w = W.COOCCUR
     ids = w.ids()
     co, tr, err = gpu_cooccur(ids, w.E)
     assert err == 0

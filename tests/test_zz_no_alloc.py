@@ -53,8 +53,7 @@ def test_hist_noalloc_matches_topo_hist_twice_in_a_row():
     # the full-size 4-microbatch workloads (T = 1048576 with 8 tiles per
     # source, then T = 65536), then a small ragged one: no call may see the
     # previous call's counts or error word
-    for n in (5, 3):
-        w = W.CONFIGS[n]
+    for w in (W.STRESS, W.FOUR_LAYER):
         cases.append((_cfg(w.T, w.E, w.k, w.R, w.ranks_per_node, w.n_slot), w.n_layers,
                       w.ids()))
     ids_small = W.random_small(seed=11, T=8 * 300, E=24, k=3, n_layers=2)
