@@ -44,7 +44,7 @@ def test_plan_hand_cases(golden, name):
 def test_fig3_bytes_and_eq9_threshold(golden):
     g = golden("fig3_bytes.json")
     ex = g["expected"]
-    w = W.Workload(0, "fig3", "plan", T=4, E=4, k=1, n_layers=1, R=4, ranks_per_node=2,
+    w = W.Workload(0, "fig3", "plan", "zipf", T=4, E=4, k=1, n_layers=1, R=4, ranks_per_node=2,
                    n_slot=1, hidden=g["hidden"], intermediate=g["intermediate"])
     cfg = w.plan_cfg
     assert cfg["tok_bytes"] == ex["tok_bytes"]
@@ -145,7 +145,7 @@ def check_constraints(cfg, hist, p):
 
 
 def _random_case(seed, R, rpn, E, ns, T, k, s=1.2, Wmul=1.0):
-    w = W.Workload(0, "t", "plan", T=T, E=E, k=k, n_layers=1, R=R, ranks_per_node=rpn,
+    w = W.Workload(0, "t", "plan", "zipf", T=T, E=E, k=k, n_layers=1, R=R, ranks_per_node=rpn,
                    n_slot=ns, hidden=64, intermediate=64)
     cfg = dict(w.plan_cfg)
     cfg["expert_bytes"] = int(cfg["expert_bytes"] * Wmul)
