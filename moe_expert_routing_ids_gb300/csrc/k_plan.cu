@@ -415,30 +415,38 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                     SE[(int64_t)rt * ns + (lt - ER)] = e;
                 }
             }
-            // other sources, ascending, skipping r_t and r_b
-            for (int base = 0; base < R && remaining > 0; base += 32) {
-                const int s = base + lane;
-                const bool in = s < R && s != rt && s != rb;
-                const bool cached = colcache || (s >= r0 && s < r0 + rpn);
-                int32_t *pb = Q + ((int64_t)s * R + rb) * nl + blb;
-                int32_t *pt = Q + ((int64_t)s * R + rt) * nl + lt;
-                const int v = in ? (cached ? *qcell(s, jb, blb) : *pb) : 0;
-                const int incl = warp_incl_scan(v);
-                const int excl = incl - v;
-                int take = remaining - excl;
-                take = take < 0 ? 0 : (take > v ? v : take);
-                if (take > 0) {
-                    if (cached) {
-                        *qcell(s, jb, blb) -= take;
-                        *qcell(s, bjt, lt) += take;
-                    }
-                    if (!colcache) {
-                        *pb -= take;
-                        *pt += take;
-                    }
+            // other sources, ascending, skipping r_t and r_b: a block of 256
+            // sources' q values is requested at once, then scanned 32 at a time
+            for (int base = 0; base < R && remaining > 0; base += 256) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int s = base + 32 * u + lane;
+                    const bool in = s < R && s != rt && s != rb;
+                    const bool cached = colcache || (s >= r0 && s < r0 + rpn);
+                    v[u] = in ? (cached ? *qcell(s, jb, blb) : Q[((int64_t)s * R + rb) * nl + blb]) : 0;
                 }
-                const int tot = __shfl_sync(0xffffffffu, incl, 31);
-                remaining -= tot < remaining ? tot : remaining;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (remaining <= 0) break;
+                    const int s = base + 32 * u + lane;
+                    const int incl = warp_incl_scan(v[u]);
+                    const int excl = incl - v[u];
+                    int take = remaining - excl;
+                    take = take < 0 ? 0 : (take > v[u] ? v[u] : take);
+                    if (take > 0) {
+                        if (colcache || (s >= r0 && s < r0 + rpn)) {
+                            *qcell(s, jb, blb) -= take;
+                            *qcell(s, bjt, lt) += take;
+                        }
+                        if (!colcache) {
+                            Q[((int64_t)s * R + rb) * nl + blb] -= take;
+                            Q[((int64_t)s * R + rt) * nl + lt] += take;
+                        }
+                    }
+                    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                    remaining -= tot < remaining ? tot : remaining;
+                }
             }
             const int m_rb = remaining;
             __syncwarp();
