@@ -99,6 +99,7 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int64_t D = 0;
+#pragma unroll 8
         for (int j = 0; j < rpn; ++j) D += H[(int64_t)(d * rpn + j) * E + e];
         const int64_t b = 2 * D * g.S_tok - g.W;
         const bool cand = (main_of[e] / rpn != d) && b > 0;
@@ -128,14 +129,20 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
         }
         rep[((int64_t)l * E + e) * g.M + d] = code;
     }
-    // static loads of the domain's ranks (mains only) and zeroed U, L
-    for (int i = threadIdx.x; i < rpn * g.E_R; i += blockDim.x) {
-        const int j = i / g.E_R, r = d * rpn + j;
-        const int e = mains[r * g.E_R + i % g.E_R];
+    // static loads of the domain's ranks (mains only): each thread sums one
+    // main over a strided group of sources, the groups meet in shared atomics
+    const int nm = rpn * g.E_R;
+    const int groups = nm < (int)blockDim.x ? (int)blockDim.x / nm : 1;
+    for (int i = threadIdx.x; i < nm * groups; i += blockDim.x) {
+        const int jm = i % nm, grp = i / nm;
+        const int j = jm / g.E_R, r = d * rpn + j;
+        const int e = mains[r * g.E_R + jm % g.E_R];
         int load = 0;
-        for (int s = 0; s < R; ++s) load += H[(int64_t)s * E + e];
+#pragma unroll 8
+        for (int s = grp; s < R; s += groups) load += H[(int64_t)s * E + e];
         atomicAdd(&stat_load[j], load);
     }
+    // zeroed U, L
     for (int i = threadIdx.x; i < rpn * nl; i += blockDim.x)
         inst_load[((int64_t)l * R + d * rpn) * nl + i] = 0;
     for (int j = threadIdx.x; j < rpn; j += blockDim.x) rank_load[(int64_t)l * R + d * rpn + j] = 0;
@@ -160,6 +167,7 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
     const int s = blockIdx.x, l = blockIdx.y;
     const int E = g.E, R = g.R, rpn = g.rpn, nl = g.n_local, M = g.M;
     const int32_t *main_of = tab, *main_l = tab + E;
+    const int32_t *REP = rep + (int64_t)l * E * M;
     int32_t *row = q + ((int64_t)l * R + s) * R * nl;
     int32_t *U = inst_load + (int64_t)l * R * nl;
     int32_t *Lr = rank_load + (int64_t)l * R;
@@ -168,7 +176,6 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
     const int ds = s / rpn;
     int64_t tok = 0, wsum = 0;
     const int32_t *H = hist + ((int64_t)l * R + s) * E;
-    const int32_t *REP = rep + (int64_t)l * E * M;
     auto emit = [&](int r, int li, int amt) {
         if (amt <= 0) return;
         row[r * nl + li] = amt;
@@ -257,7 +264,8 @@ constexpr int kRefineMaxWarps = 8;
 // warps' winners meet in shared memory (skipped with one warp, which then
 // runs barrier-free), and warp 0 commits.  The domain's columns of q (every
 // source, the domain's ranks) live in shared memory when they fit
-// (colcache), else in global memory with the domain's own sources mirrored in
+// (colcache), else in global memory -- updated there by atomic adds that do
+// not wait, and re-read past L1 -- with the domain's own sources mirrored in
 // shared memory for the candidate costs.
 __global__ void __launch_bounds__(kRefineMaxWarps * 32)
 k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
@@ -424,7 +432,8 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                     const int s = base + 32 * u + lane;
                     const bool in = s < R && s != rt && s != rb;
                     const bool cached = colcache || (s >= r0 && s < r0 + rpn);
-                    v[u] = in ? (cached ? *qcell(s, jb, blb) : Q[((int64_t)s * R + rb) * nl + blb]) : 0;
+                    v[u] = in ? (cached ? *qcell(s, jb, blb) : __ldcg(&Q[((int64_t)s * R + rb) * nl + blb]))
+                              : 0;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -439,9 +448,9 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                             *qcell(s, jb, blb) -= take;
                             *qcell(s, bjt, lt) += take;
                         }
-                        if (!colcache) {
-                            Q[((int64_t)s * R + rb) * nl + blb] -= take;
-                            Q[((int64_t)s * R + rt) * nl + lt] += take;
+                        if (!colcache) {   // no return value: the lane does not wait
+                            atomicAdd(&Q[((int64_t)s * R + rb) * nl + blb], -take);
+                            atomicAdd(&Q[((int64_t)s * R + rt) * nl + lt], take);
                         }
                     }
                     const int tot = __shfl_sync(0xffffffffu, incl, 31);
@@ -455,16 +464,16 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                     *qcell(rt, jb, blb) -= m_rt;
                     *qcell(rt, bjt, lt) += m_rt;
                     if (!colcache) {
-                        Q[((int64_t)rt * R + rb) * nl + blb] -= m_rt;
-                        Q[((int64_t)rt * R + rt) * nl + lt] += m_rt;
+                        atomicAdd(&Q[((int64_t)rt * R + rb) * nl + blb], -m_rt);
+                        atomicAdd(&Q[((int64_t)rt * R + rt) * nl + lt], m_rt);
                     }
                 }
                 if (m_rb > 0) {
                     *qcell(rb, jb, blb) -= m_rb;
                     *qcell(rb, bjt, lt) += m_rb;
                     if (!colcache) {
-                        Q[((int64_t)rb * R + rb) * nl + blb] -= m_rb;
-                        Q[((int64_t)rb * R + rt) * nl + lt] += m_rb;
+                        atomicAdd(&Q[((int64_t)rb * R + rb) * nl + blb], -m_rb);
+                        atomicAdd(&Q[((int64_t)rb * R + rt) * nl + lt], m_rb);
                     }
                 }
                 U[jb * nl + blb] -= delta;
