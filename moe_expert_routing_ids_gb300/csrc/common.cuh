@@ -136,6 +136,31 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st);
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the previous kernel of the stream is still finishing: it must
+// call pdl_wait() before reading anything earlier kernels wrote (or writing
+// anything they read); pdl_wait() returns once those kernels have completed
+// and their writes are visible.  pdl_trigger() lets the next kernel start
+// launching; both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the kernel translation units).  Each returns
 // the cudaError_t of its launches.

@@ -43,6 +43,8 @@ __global__ void k_main_tables(const int32_t *__restrict__ main_rank, int32_t *ta
                               int n_stats, WsHeader *hdr, Geo g) {
     extern __shared__ int own[];
     __shared__ int bad;
+    pdl_wait();
+    pdl_trigger();
     const int E = g.E, R = g.R, ER = g.E_R;
     int32_t *main_of = tab, *main_l = tab + E, *mains = tab + 2 * E;
     for (int i = threadIdx.x; i < n_stats; i += blockDim.x) stats[i] = 0;
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(512)
 k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, int32_t *slot_expert,
              int32_t *rep, int32_t *inst_load, int32_t *rank_load, int64_t *stats, Geo g) {
     extern __shared__ long long keyv[];          // [E] benefit, LLONG_MIN if not a candidate
+    pdl_wait();
+    pdl_trigger();
     __shared__ int ncand;
     __shared__ int64_t red[32];
     __shared__ int stat_load[kMaxRanksPerNode];
@@ -164,6 +168,8 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
              const int32_t *__restrict__ rep, int32_t *q, int32_t *inst_load, int32_t *rank_load,
              int64_t *stats, Geo g) {
     __shared__ int64_t red[32];
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x, l = blockIdx.y;
     const int E = g.E, R = g.R, rpn = g.rpn, nl = g.n_local, M = g.M;
     const int32_t *main_of = tab, *main_l = tab + E;
@@ -271,6 +277,8 @@ __global__ void __launch_bounds__(kRefineMaxWarps * 32)
 k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
               int32_t *rank_load, int64_t *stats, Geo g, int colcache) {
     extern __shared__ int sm[];
+    pdl_wait();
+    pdl_trigger();
     __shared__ Key kbuf[kRefineMaxWarps];
     __shared__ int cbuf[kRefineMaxWarps];
     const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -525,7 +533,7 @@ size_t refine_smem_bytes(const Geo &g, bool colcache) {
 // Warps of the refinement CTA: about two candidates per lane, at most 8.
 int refine_warps(const Geo &g) {
     const int ncand = g.n_local * g.rpn;
-    int w = (ncand + 63) / 64;
+    int w = (ncand + 31) / 32;                      // one warp per 32 candidates (measured best)
     return w < 1 ? 1 : (w > kRefineMaxWarps ? kRefineMaxWarps : w);
 }
 
@@ -533,9 +541,8 @@ bool refine_colcache(const Geo &g) { return refine_smem_bytes(g, true) <= 160 * 
 
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st) {
-    k_main_tables<<<1, 1024, (size_t)g.R * 4, st>>>(main_rank, ws_at<int32_t>(ws, g.off_main), stats,
-                                                   n_stats, ws_at<WsHeader>(ws, 0), g);
-    return cudaGetLastError();
+    return launch_pdl(k_main_tables, dim3(1), dim3(1024), (size_t)g.R * 4, st, main_rank,
+                      ws_at<int32_t>(ws, g.off_main), stats, n_stats, ws_at<WsHeader>(ws, 0), g);
 }
 
 cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
@@ -547,18 +554,17 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
         return e;
     const size_t smem_place = (size_t)g.E * 8;
     if ((e = ensure_smem((const void *)k_plan_place, smem_place)) != cudaSuccess) return e;
-    k_plan_place<<<dim3(g.M, g.L), 512, smem_place, st>>>(hist, tab, p.slot_expert, rep, p.inst_load,
-                                                          p.rank_load, p.stats, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_plan_route<<<dim3(g.R, g.L), 256, 0, st>>>(hist, tab, rep, p.route_cnt, p.inst_load, p.rank_load,
-                                                p.stats, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_plan_place, dim3(g.M, g.L), dim3(512), smem_place, st, hist, tab,
+                        p.slot_expert, rep, p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
+        return e;
+    if ((e = launch_pdl(k_plan_route, dim3(g.R, g.L), dim3(256), 0, st, hist, tab, rep, p.route_cnt,
+                        p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
+        return e;
     const bool cc = refine_colcache(g);
     const size_t smem_ref = refine_smem_bytes(g, cc);
     if ((e = ensure_smem((const void *)k_plan_refine, smem_ref)) != cudaSuccess) return e;
-    k_plan_refine<<<dim3(g.M, g.L), refine_warps(g) * 32, smem_ref, st>>>(
-        tab, p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, cc ? 1 : 0);
-    return cudaGetLastError();
+    return launch_pdl(k_plan_refine, dim3(g.M, g.L), dim3(refine_warps(g) * 32), smem_ref, st, tab,
+                      p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, cc ? 1 : 0);
 }
 
 }  // namespace topo
