@@ -152,6 +152,8 @@ struct RankSmem {
     int *base;       // [kRankWarps][E] per-warp running base: the layout position
                      //     of the next pair (single entry) or its occurrence index
     unsigned *msk;   // [kRankWarps][E] per-warp token bitmask of the round
+    int2 *walkq;     // [kRankWarps][kWalkCap] per warp: pairs of the round whose
+                     //     expert has several entries -- (occurrence, key index)
     int32_t *keys;   // [TT][kp] ids, then the instance codes, in place
 };
 
@@ -159,12 +161,13 @@ __device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
     RankSmem r;
     int *p = sm;
     r.ec = p; p += g.E;
-    r.ro = p; p += g.E + 1;
+    r.ro = p; p += g.E + 2;                         // + 1: keeps walkq 8-byte aligned
     r.ent_ce = p; p += kRankEntCap;
     r.ent_code = p; p += kRankEntCap;
     r.ent_ob = p; p += kRankEntCap;
     r.base = p; p += kRankWarps * g.E;
     r.msk = reinterpret_cast<unsigned *>(p); p += kRankWarps * g.E;
+    r.walkq = reinterpret_cast<int2 *>(p); p += 2 * kRankWarps * kWalkCap;
     r.keys = reinterpret_cast<int32_t *>(p);
     return r;
 }
@@ -273,6 +276,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     if (fast) {
         int *mybase = S.base + w * E;
         unsigned *mymsk = S.msk + w * E;
+        int2 *myq = S.walkq + w * kWalkCap;
         // pass 1: per-warp counts over its rounds, added into the next warp's
         // base (shifted by one so pass 2 is a plain prefix)
         if (w + 1 < kRankWarps) {
@@ -329,13 +333,15 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
             __syncwarp();
             int nb[KB];
             unsigned lead = 0;
+            int nq = 0;                                 // pairs queued for the entry walk
             {
                 int j = rot;
 #pragma unroll
                 for (int jj = 0; jj < KB; ++jj) {
                     nb[jj] = 0;
                     if (jj >= k) continue;
-                    int code = -1, pos = -1;
+                    int code = -1, pos = -1, occ = 0;
+                    bool defer = false;
                     if (ek[jj] >= 0) {
                         const unsigned m = mymsk[ek[jj]];
                         const int b = mybase[ek[jj]];
@@ -344,12 +350,29 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                             lead |= 1u << jj;
                             nb[jj] = b + __popc(m);
                         }
+                        occ = b + rk;
                         code = S.ec[ek[jj]];
-                        if (code >= 0) pos = b + rk;
-                        else if (code == -1) code = route_walk(b + rk, ek[jj], S, row_in_smem, re, &pos);
-                        if (code < 0) bad_state = true;
+                        if (code >= 0) pos = occ;
+                        else if (code == -1) defer = true;
+                        else bad_state = true;
                     }
-                    if (vt) {
+                    // pairs whose expert has several entries are walked after the
+                    // round, one per lane, so the walk does not diverge the warp
+                    const unsigned dm = __ballot_sync(0xffffffffu, defer);
+                    if (dm) {
+                        const int qi = nq + __popc(dm & lt_mask);
+                        if (defer) {
+                            if (qi < kWalkCap) {
+                                myq[qi] = make_int2(occ, t * kp + j);
+                            } else {                    // queue full: walk here
+                                defer = false;
+                                code = route_walk(occ, ek[jj], S, row_in_smem, re, &pos);
+                                if (code < 0) bad_state = true;
+                            }
+                        }
+                        nq += __popc(dm);
+                    }
+                    if (vt && !defer) {
                         S.keys[t * kp + j] = code;
                         if (kFused) {
                             if (code >= 0 && pos >= 0 && pos < g.npairs)
@@ -358,7 +381,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                                 bad_state = true;
                         }
                     }
-                    if (!kFused)
+                    if (!kFused && !defer)
                         pos_ws[tg.slot0 + ((t >> 5) * k + j) * 32 + lane] =
                             (vt && code >= 0) ? pos : -1;
                     j = (j + 1 == k) ? 0 : j + 1;
@@ -371,6 +394,24 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                     mybase[ek[jj]] = nb[jj];
                     mymsk[ek[jj]] = 0;
                 }
+            // the queued pairs: their key still holds the expert id
+            for (int i = lane; i < min(nq, kWalkCap); i += 32) {
+                const int2 it = myq[i];
+                const int key = it.y;
+                const int tt = key / kp, js = key - tt * kp;   // token of the tile, slot
+                int pos = -1;
+                const int code = route_walk(it.x, S.keys[key], S, row_in_smem, re, &pos);
+                if (code < 0) bad_state = true;
+                S.keys[key] = code;
+                if (kFused) {
+                    if (code >= 0 && pos >= 0 && pos < g.npairs)
+                        sorted_layer[pos] = (int32_t)(tg.p0 + tt * k + js);
+                    else if (code >= 0)
+                        bad_state = true;
+                } else {
+                    pos_ws[tg.slot0 + ((tt >> 5) * k + js) * 32 + (tt & 31)] = code >= 0 ? pos : -1;
+                }
+            }
             __syncwarp();
         }
     }
@@ -481,8 +522,8 @@ cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, in
 }  // namespace
 
 size_t rank_smem_bytes(const Geo &g) {
-    return ((size_t)2 * g.E + 1 + 3 * (size_t)kRankEntCap) * 4 + (size_t)kRankWarps * g.E * 8 +
-           (size_t)g.TT * g.kp * 4;
+    return ((size_t)2 * g.E + 2 + 3 * (size_t)kRankEntCap) * 4 + (size_t)kRankWarps * g.E * 8 +
+           (size_t)kRankWarps * kWalkCap * 8 + (size_t)g.TT * g.kp * 4;
 }
 
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,
