@@ -17,22 +17,30 @@ namespace {
 constexpr int kHistThreads = 512;
 constexpr int kHistVec = 6;          // 16-byte loads in flight per thread
 
+// Count one id; an id outside [0, E) goes to the spare counter E (dropped)
+// and raises `bad`, without a branch.
 __device__ __forceinline__ void count_id(int e, int E, int *cnt, bool &bad) {
-    if ((unsigned)e < (unsigned)E)
-        atomicAdd(&cnt[e], 1);
-    else
-        bad = true;
+    const bool ok = (unsigned)e < (unsigned)E;
+    bad |= !ok;
+    atomicAdd(&cnt[ok ? e : E], 1);
+}
+
+__device__ __forceinline__ void count4(const int4 &x, int E, int *cnt, bool &bad) {
+    count_id(x.x, E, cnt, bad);
+    count_id(x.y, E, cnt, bad);
+    count_id(x.z, E, cnt, bad);
+    count_id(x.w, E, cnt, bad);
 }
 
 __global__ void __launch_bounds__(kHistThreads, 3)
 k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, WsHeader *hdr, Geo g) {
-    extern __shared__ int cnt[];
+    extern __shared__ int cnt[];                     // [E + 1]: E = the spare counter
     const int E = g.E;
     const int tile = blockIdx.x;
     const int t = tile % g.tps;
     const int s = (tile / g.tps) % g.R;
     const int l = tile / (g.tps * g.R);
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
 
     const int tok0 = t * g.TT;
     const int ntok = max(0, min(g.TT, g.tpr - tok0));
@@ -42,28 +50,23 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, Ws
     if (head > n) head = n;
     const int4 *v = reinterpret_cast<const int4 *>(a + head);
     const int nv = (n - head) >> 2;
-    // all of this thread's vectors requested before any is counted
+    // all of this thread's vectors requested before any is counted; vectors
+    // past the end read as the spare id E
     int4 x[kHistVec];
 #pragma unroll
     for (int u = 0; u < kHistVec; ++u) {
         const int i = threadIdx.x + u * kHistThreads;
-        x[u] = i < nv ? __ldg(v + i) : make_int4(-1, -1, -1, -1);
+        x[u] = i < nv ? __ldg(v + i) : make_int4(E, E, E, E);
     }
     __syncthreads();                               // histogram zeroed
     bool bad = false;
     for (int i = threadIdx.x; i < head; i += blockDim.x) count_id(__ldg(a + i), E, cnt, bad);
     for (int j = head + nv * 4 + threadIdx.x; j < n; j += blockDim.x) count_id(__ldg(a + j), E, cnt, bad);
+    const int nmine = nv > (int)threadIdx.x ? (nv - (int)threadIdx.x + kHistThreads - 1) / kHistThreads : 0;
 #pragma unroll
-    for (int u = 0; u < kHistVec; ++u) {
-        if (threadIdx.x + u * kHistThreads >= nv) break;
-        count_id(x[u].x, E, cnt, bad); count_id(x[u].y, E, cnt, bad);
-        count_id(x[u].z, E, cnt, bad); count_id(x[u].w, E, cnt, bad);
-    }
-    for (int i = threadIdx.x + kHistVec * kHistThreads; i < nv; i += kHistThreads) {
-        const int4 y = __ldg(v + i);
-        count_id(y.x, E, cnt, bad); count_id(y.y, E, cnt, bad);
-        count_id(y.z, E, cnt, bad); count_id(y.w, E, cnt, bad);
-    }
+    for (int u = 0; u < kHistVec; ++u)
+        if (u < nmine) count4(x[u], E, cnt, bad);
+    for (int i = threadIdx.x + kHistVec * kHistThreads; i < nv; i += kHistThreads) count4(__ldg(v + i), E, cnt, bad);
     if (bad) set_error(hdr, TOPO_ERANGE);
     __syncthreads();
     int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
@@ -111,7 +114,7 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
     const int64_t tiles = (int64_t)g.L * g.R * g.tps;
     if (tiles == 0) return cudaSuccess;
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)g.E * sizeof(int);
+    const size_t smem = ((size_t)g.E + 1) * sizeof(int);
     cudaError_t e = ensure_smem((const void *)k_hist_tiles, smem);
     if (e != cudaSuccess) return e;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
