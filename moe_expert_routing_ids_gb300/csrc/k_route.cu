@@ -221,6 +221,8 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     const int k = K > 0 ? K : g.k;
     const int kp = K > 0 ? ((K & 1) ? K : K + 1) : g.kp;
     const RankSmem S = rank_smem(g, sm);
+    const int p0i = (int)tg.p0;                        // pair indices fit in int32
+    const unsigned npairs_u = (unsigned)g.npairs;
     const int32_t *ids_layer = ids + (int64_t)tg.l * g.npairs;
     int32_t *dst_layer = dst + (int64_t)tg.l * g.npairs;
     int32_t *sorted_layer = kFused ? sorted + (int64_t)tg.l * g.npairs : nullptr;
@@ -374,11 +376,9 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                     }
                     if (vt && !defer) {
                         S.keys[t * kp + j] = code;
-                        if (kFused) {
-                            if (code >= 0 && pos >= 0 && pos < g.npairs)
-                                sorted_layer[pos] = (int32_t)(tg.p0 + t * k + j);
-                            else if (code >= 0)
-                                bad_state = true;
+                        if (kFused && code >= 0) {
+                            if ((unsigned)pos < npairs_u) sorted_layer[pos] = p0i + t * k + j;
+                            else bad_state = true;
                         }
                     }
                     if (!kFused && !defer)
