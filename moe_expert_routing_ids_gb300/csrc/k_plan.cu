@@ -87,13 +87,16 @@ __global__ void k_main_tables(const int32_t *__restrict__ main_rank, int32_t *ta
 
 __global__ void __launch_bounds__(512)
 k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, int32_t *slot_expert,
-             int32_t *rep, int32_t *inst_load, int32_t *rank_load, int64_t *stats, Geo g) {
-    extern __shared__ long long keyv[];          // [E] benefit, LLONG_MIN if not a candidate
-    pdl_wait();
-    pdl_trigger();
+             int32_t *rep, int32_t *inst_load, int32_t *rank_load, int64_t *stats, Geo g, int npow) {
+    // candidates sorted by (benefit desc, expert asc) in shared memory:
+    // keyv[i] the benefit (LLONG_MIN: not a candidate), kid[i] the expert
+    extern __shared__ long long keyv[];          // [npow], then int kid[npow]
+    int *kid = reinterpret_cast<int *>(keyv + npow);
     __shared__ int ncand;
     __shared__ int64_t red[32];
     __shared__ int stat_load[kMaxRanksPerNode];
+    pdl_wait();
+    pdl_trigger();
     const int d = blockIdx.x, l = blockIdx.y;
     const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local;
     const int32_t *main_of = tab, *mains = tab + 2 * E;
@@ -101,24 +104,33 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
     if (threadIdx.x == 0) ncand = 0;
     if (threadIdx.x < rpn) stat_load[threadIdx.x] = 0;
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int64_t D = 0;
+    for (int e = threadIdx.x; e < npow; e += blockDim.x) {
+        long long key = LLONG_MIN;
+        if (e < E) {
+            int64_t D = 0;
 #pragma unroll 8
-        for (int j = 0; j < rpn; ++j) D += H[(int64_t)(d * rpn + j) * E + e];
-        const int64_t b = 2 * D * g.S_tok - g.W;
-        const bool cand = (main_of[e] / rpn != d) && b > 0;
-        keyv[e] = cand ? (long long)b : LLONG_MIN;
-        if (cand) atomicAdd(&ncand, 1);
+            for (int j = 0; j < rpn; ++j) D += H[(int64_t)(d * rpn + j) * E + e];
+            const int64_t b = 2 * D * g.S_tok - g.W;
+            if ((main_of[e] / rpn != d) && b > 0) {
+                key = (long long)b;
+                atomicAdd(&ncand, 1);
+            }
+        }
+        keyv[e] = key;
+        kid[e] = e;
     }
     int32_t *SE = slot_expert + (int64_t)l * R * ns;
     for (int i = threadIdx.x; i < rpn * ns; i += blockDim.x) SE[(int64_t)d * rpn * ns + i] = -1;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) rep[((int64_t)l * E + e) * g.M + d] = -1;
     __syncthreads();
     const int cap = rpn * ns;
+    const int placed = ncand < cap ? ncand : cap;
     int64_t repcost = 0;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int32_t code = -1;
-        const long long b = keyv[e];
-        if (b != LLONG_MIN) {
+    if (npow <= 256) {
+        // few experts: each candidate counts the candidates ahead of it
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const long long b = keyv[e];
+            if (b == LLONG_MIN) continue;
             int rank = 0;
             for (int x = 0; x < E; ++x) {
                 const long long bx = keyv[x];
@@ -127,11 +139,35 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
             if (rank < cap) {
                 const int r = d * rpn + rank % rpn, slot = rank / rpn;
                 SE[(int64_t)r * ns + slot] = e;
-                code = r * nl + g.E_R + slot;
+                rep[((int64_t)l * E + e) * g.M + d] = r * nl + g.E_R + slot;
                 repcost += cost_sr(g, main_of[e], r) * g.W;
             }
         }
-        rep[((int64_t)l * E + e) * g.M + d] = code;
+    } else {
+    // bitonic sort, descending by benefit, ascending by expert on ties
+    for (int size = 2; size <= npow; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < (npow >> 1); i += blockDim.x) {
+                const int a = 2 * i - (i & (stride - 1)), b = a + stride;
+                const long long ka = keyv[a], kb = keyv[b];
+                const int ia = kid[a], ib = kid[b];
+                const bool a_first = ka > kb || (ka == kb && ia < ib);   // a precedes b
+                const bool desc = (a & size) == 0;
+                if (desc != a_first) {
+                    keyv[a] = kb; keyv[b] = ka;
+                    kid[a] = ib; kid[b] = ia;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int rank = threadIdx.x; rank < placed; rank += blockDim.x) {
+        const int e = kid[rank];
+        const int r = d * rpn + rank % rpn, slot = rank / rpn;
+        SE[(int64_t)r * ns + slot] = e;
+        rep[((int64_t)l * E + e) * g.M + d] = r * nl + g.E_R + slot;
+        repcost += cost_sr(g, main_of[e], r) * g.W;
+    }
     }
     // static loads of the domain's ranks (mains only): each thread sums one
     // main over a strided group of sources, the groups meet in shared atomics
@@ -155,7 +191,6 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
         atomicMax(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 1]),
                   (unsigned long long)stat_load[threadIdx.x]);
     if (threadIdx.x == 0) {
-        const int placed = ncand < cap ? ncand : cap;
         atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 3]),
                   (unsigned long long)placed);
         atomicAdd(reinterpret_cast<unsigned long long *>(&stats[l * TOPO_STATS + 6]),
@@ -167,6 +202,7 @@ __global__ void __launch_bounds__(256)
 k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
              const int32_t *__restrict__ rep, int32_t *q, int32_t *inst_load, int32_t *rank_load,
              int64_t *stats, Geo g) {
+    extern __shared__ int lr[];                  // [R] this row's load per destination rank
     __shared__ int64_t red[32];
     pdl_wait();
     pdl_trigger();
@@ -178,6 +214,7 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
     int32_t *U = inst_load + (int64_t)l * R * nl;
     int32_t *Lr = rank_load + (int64_t)l * R;
     for (int i = threadIdx.x; i < R * nl; i += blockDim.x) row[i] = 0;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) lr[r] = 0;
     __syncthreads();
     const int ds = s / rpn;
     int64_t tok = 0, wsum = 0;
@@ -186,33 +223,52 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
         if (amt <= 0) return;
         row[r * nl + li] = amt;
         atomicAdd(&U[r * nl + li], amt);
-        atomicAdd(&Lr[r], amt);
+        atomicAdd(&lr[r], amt);
         tok += cost_sr(g, s, r) * amt;
     };
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int w = H[e];
-        if (w == 0) continue;
-        wsum += w;
-        const int me = main_of[e], dm = me / rpn;
-        if (dm == ds) { emit(me, main_l[e], w); continue; }
-        const int32_t *re = REP + (int64_t)e * M;
-        const int code = re[ds];
-        if (code >= 0) { emit(code / nl, code % nl, w); continue; }
-        // no instance in dom(s): every instance of e, in rank (= domain) order;
-        // all are cross-domain, so (c, r) order is rank order
-        int n = 1;
-        for (int d = 0; d < M; ++d) n += (d != dm && re[d] >= 0);
-        const int base = w / n, rem = w % n;
-        int i = 0;
-        for (int d = 0; d < M; ++d) {
-            int r, li;
-            if (d == dm) { r = me; li = main_l[e]; }
-            else if (re[d] >= 0) { r = re[d] / nl; li = re[d] % nl; }
-            else continue;
-            emit(r, li, base + (i < rem ? 1 : 0));
-            ++i;
+    // two experts per thread and pass, their table entries requested together
+    for (int e0 = threadIdx.x; e0 < E; e0 += 2 * blockDim.x) {
+        int ew[2], wv[2], me[2], ml[2], rc[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            ew[u] = e0 + u * (int)blockDim.x;
+            const bool in = ew[u] < E;
+            wv[u] = in ? __ldg(H + ew[u]) : 0;
+            me[u] = in ? __ldg(main_of + ew[u]) : 0;
+            ml[u] = in ? __ldg(main_l + ew[u]) : 0;
+            rc[u] = in ? __ldg(REP + (int64_t)ew[u] * M + ds) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int w = wv[u];
+            if (w == 0) continue;
+            wsum += w;
+            const int dm = me[u] / rpn;
+            if (dm == ds) { emit(me[u], ml[u], w); continue; }
+            if (rc[u] >= 0) { emit(rc[u] / nl, rc[u] % nl, w); continue; }
+            // no instance in dom(s): every instance of e, in rank (= domain)
+            // order; all are cross-domain, so (c, r) order is rank order
+            const int32_t *re = REP + (int64_t)ew[u] * M;
+            int n = 1;
+            for (int d = 0; d < M; ++d) n += (d != dm && __ldg(re + d) >= 0);
+            const int base = w / n, rem = w % n;
+            int i = 0;
+            for (int d = 0; d < M; ++d) {
+                int r, li;
+                if (d == dm) { r = me[u]; li = ml[u]; }
+                else {
+                    const int c = __ldg(re + d);
+                    if (c < 0) continue;
+                    r = c / nl; li = c % nl;
+                }
+                emit(r, li, base + (i < rem ? 1 : 0));
+                ++i;
+            }
         }
     }
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += blockDim.x)
+        if (lr[r]) atomicAdd(&Lr[r], lr[r]);
     const int64_t t = block_sum64(tok, red);
     const int64_t ws = block_sum64(wsum, red);
     if (threadIdx.x == 0) {
@@ -552,13 +608,16 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
     int32_t *rep = ws_at<int32_t>(ws, g.off_rep);
     if ((e = launch_main_tables(g, main_rank, ws, p.stats, g.L * TOPO_STATS, st)) != cudaSuccess)
         return e;
-    const size_t smem_place = (size_t)g.E * 8;
+    int npow = 2;
+    while (npow < g.E) npow <<= 1;
+    const size_t smem_place = (size_t)npow * 12;
     if ((e = ensure_smem((const void *)k_plan_place, smem_place)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_plan_place, dim3(g.M, g.L), dim3(512), smem_place, st, hist, tab,
-                        p.slot_expert, rep, p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
+                        p.slot_expert, rep, p.inst_load, p.rank_load, p.stats, g, npow)) != cudaSuccess)
         return e;
-    if ((e = launch_pdl(k_plan_route, dim3(g.R, g.L), dim3(256), 0, st, hist, tab, rep, p.route_cnt,
-                        p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
+    if ((e = ensure_smem((const void *)k_plan_route, (size_t)g.R * 4)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_plan_route, dim3(g.R, g.L), dim3(256), (size_t)g.R * 4, st, hist, tab, rep,
+                        p.route_cnt, p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
         return e;
     const bool cc = refine_colcache(g);
     const size_t smem_ref = refine_smem_bytes(g, cc);
