@@ -19,7 +19,6 @@ constexpr int kRankSmemTarget = 110 * 1024;        // two rank CTAs per SM
 constexpr int kSmemMax = 227 * 1024;               // per CTA on sm_103a
 constexpr int kMaxK = 64;
 constexpr int kRankEntCap = 1024;                 // routing entries of a row kept in shared memory
-constexpr int kWalkCap = 64;                      // queued multi-entry pairs per warp and round
 constexpr int kMaxRanksPerNode = 32;               // one warp lane per rank of a domain
 
 // Workspace header, 256 bytes at offset 0 of every workspace.

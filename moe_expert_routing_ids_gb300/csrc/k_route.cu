@@ -152,8 +152,6 @@ struct RankSmem {
     int *base;       // [kRankWarps][E] per-warp running base: the layout position
                      //     of the next pair (single entry) or its occurrence index
     unsigned *msk;   // [kRankWarps][E] per-warp token bitmask of the round
-    int2 *walkq;     // [kRankWarps][kWalkCap] per warp: pairs of the round whose
-                     //     expert has several entries -- (occurrence, key index)
     int32_t *keys;   // [TT][kp] ids, then the instance codes, in place
 };
 
@@ -161,13 +159,12 @@ __device__ __forceinline__ RankSmem rank_smem(const Geo &g, int *sm) {
     RankSmem r;
     int *p = sm;
     r.ec = p; p += g.E;
-    r.ro = p; p += g.E + 2;                         // + 1: keeps walkq 8-byte aligned
+    r.ro = p; p += g.E + 1;
     r.ent_ce = p; p += kRankEntCap;
     r.ent_code = p; p += kRankEntCap;
     r.ent_ob = p; p += kRankEntCap;
     r.base = p; p += kRankWarps * g.E;
     r.msk = reinterpret_cast<unsigned *>(p); p += kRankWarps * g.E;
-    r.walkq = reinterpret_cast<int2 *>(p); p += 2 * kRankWarps * kWalkCap;
     r.keys = reinterpret_cast<int32_t *>(p);
     return r;
 }
@@ -259,12 +256,24 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     for (int e = threadIdx.x; e < E; e += kRankThreads) {
         const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
         const int ne = en - b;
-        const int code = ne == 1 ? __ldg(&re[b].code) : (ne == 0 ? -2 : -1);
-        S.ec[e] = code;
-        S.ro[e] = b;
+        int code = ne == 1 ? __ldg(&re[b].code) : (ne == 0 ? -2 : -1);
         // per-warp base: tile base (+ out_base when the expert has one entry);
         // pass 1 then adds each warp's count into the following warps' bases
-        const int b0 = __ldg(tbase + e) + (ne == 1 ? __ldg(&re[b].out_base) : 0);
+        const int tb = __ldg(tbase + e);
+        int b0 = tb + (ne == 1 ? __ldg(&re[b].out_base) : 0);
+        if (ne > 1) {
+            // several entries: when the tile's occurrences [tb, te) all fall in
+            // one entry, the tile ranks e like a single-entry expert
+            const int te = tg.t + 1 < g.tps ? __ldg(tbase + E + e) : __ldg(&re[en - 1].cum_end);
+            int j = b;
+            while (j < en && tb >= __ldg(&re[j].cum_end)) ++j;
+            if (j < en && te <= __ldg(&re[j].cum_end)) {
+                code = __ldg(&re[j].code);
+                b0 = tb + __ldg(&re[j].out_base);
+            }
+        }
+        S.ec[e] = code;
+        S.ro[e] = b;
 #pragma unroll
         for (int x = 0; x < kRankWarps; ++x) {
             S.base[x * E + e] = x == 0 ? b0 : 0;
@@ -278,7 +287,6 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     if (fast) {
         int *mybase = S.base + w * E;
         unsigned *mymsk = S.msk + w * E;
-        int2 *myq = S.walkq + w * kWalkCap;
         // pass 1: per-warp counts over its rounds, added into the next warp's
         // base (shifted by one so pass 2 is a plain prefix)
         if (w + 1 < kRankWarps) {
@@ -335,15 +343,13 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
             __syncwarp();
             int nb[KB];
             unsigned lead = 0;
-            int nq = 0;                                 // pairs queued for the entry walk
             {
                 int j = rot;
 #pragma unroll
                 for (int jj = 0; jj < KB; ++jj) {
                     nb[jj] = 0;
                     if (jj >= k) continue;
-                    int code = -1, pos = -1, occ = 0;
-                    bool defer = false;
+                    int code = -1, pos = -1;
                     if (ek[jj] >= 0) {
                         const unsigned m = mymsk[ek[jj]];
                         const int b = mybase[ek[jj]];
@@ -352,36 +358,19 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                             lead |= 1u << jj;
                             nb[jj] = b + __popc(m);
                         }
-                        occ = b + rk;
                         code = S.ec[ek[jj]];
-                        if (code >= 0) pos = occ;
-                        else if (code == -1) defer = true;
-                        else bad_state = true;
+                        if (code >= 0) pos = b + rk;
+                        else if (code == -1) code = route_walk(b + rk, ek[jj], S, row_in_smem, re, &pos);
+                        if (code < 0) bad_state = true;
                     }
-                    // pairs whose expert has several entries are walked after the
-                    // round, one per lane, so the walk does not diverge the warp
-                    const unsigned dm = __ballot_sync(0xffffffffu, defer);
-                    if (dm) {
-                        const int qi = nq + __popc(dm & lt_mask);
-                        if (defer) {
-                            if (qi < kWalkCap) {
-                                myq[qi] = make_int2(occ, t * kp + j);
-                            } else {                    // queue full: walk here
-                                defer = false;
-                                code = route_walk(occ, ek[jj], S, row_in_smem, re, &pos);
-                                if (code < 0) bad_state = true;
-                            }
-                        }
-                        nq += __popc(dm);
-                    }
-                    if (vt && !defer) {
+                    if (vt) {
                         S.keys[t * kp + j] = code;
                         if (kFused && code >= 0) {
                             if ((unsigned)pos < npairs_u) sorted_layer[pos] = p0i + t * k + j;
                             else bad_state = true;
                         }
                     }
-                    if (!kFused && !defer)
+                    if (!kFused)
                         pos_ws[tg.slot0 + ((t >> 5) * k + j) * 32 + lane] =
                             (vt && code >= 0) ? pos : -1;
                     j = (j + 1 == k) ? 0 : j + 1;
@@ -394,24 +383,6 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
                     mybase[ek[jj]] = nb[jj];
                     mymsk[ek[jj]] = 0;
                 }
-            // the queued pairs: their key still holds the expert id
-            for (int i = lane; i < min(nq, kWalkCap); i += 32) {
-                const int2 it = myq[i];
-                const int key = it.y;
-                const int tt = key / kp, js = key - tt * kp;   // token of the tile, slot
-                int pos = -1;
-                const int code = route_walk(it.x, S.keys[key], S, row_in_smem, re, &pos);
-                if (code < 0) bad_state = true;
-                S.keys[key] = code;
-                if (kFused) {
-                    if (code >= 0 && pos >= 0 && pos < g.npairs)
-                        sorted_layer[pos] = (int32_t)(tg.p0 + tt * k + js);
-                    else if (code >= 0)
-                        bad_state = true;
-                } else {
-                    pos_ws[tg.slot0 + ((tt >> 5) * k + js) * 32 + (tt & 31)] = code >= 0 ? pos : -1;
-                }
-            }
             __syncwarp();
         }
     }
@@ -522,8 +493,8 @@ cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, in
 }  // namespace
 
 size_t rank_smem_bytes(const Geo &g) {
-    return ((size_t)2 * g.E + 2 + 3 * (size_t)kRankEntCap) * 4 + (size_t)kRankWarps * g.E * 8 +
-           (size_t)kRankWarps * kWalkCap * 8 + (size_t)g.TT * g.kp * 4;
+    return ((size_t)2 * g.E + 1 + 3 * (size_t)kRankEntCap) * 4 + (size_t)kRankWarps * g.E * 8 +
+           (size_t)g.TT * g.kp * 4;
 }
 
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,

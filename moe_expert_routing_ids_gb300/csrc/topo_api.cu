@@ -77,7 +77,7 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     // budget of two rank CTAs per SM and about kTilePairsTarget pairs; among
     // the admissible RW take the one with the least work per source counting
     // a fixed per-tile cost of 1.5 rounds.
-    const int64_t tables = E * (8 + 8 * kRankWarps) + (int64_t)kRankEntCap * 12 + kRankWarps * kWalkCap * 8 + 8;
+    const int64_t tables = E * (8 + 8 * kRankWarps) + (int64_t)kRankEntCap * 12;
     const int64_t round_bytes = (int64_t)kRankThreads * g->kp * 4;
     int64_t rw_max = kTilePairsTarget / ((int64_t)kRankThreads * c->k);
     const int64_t rw_smem = (kRankSmemTarget - tables) / round_bytes;
