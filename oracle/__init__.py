@@ -23,6 +23,11 @@ Parity status per function (what pins each one is in ``tests/test_oracle_*``):
             the stated readings
   reroute   pinned (hand case; per-(source, instance) counts equal q)
   layout    pinned (stable argsort; bijection; count identities)
+  permute   pinned (hand case; every token row lands k times, in its pairs'
+            positions; row sums)
+  combine   pinned (hand cases incl. round-to-nearest-even ties and the slot
+            summation order; exact round trip combine(permute(x)) == x with
+            dyadic weights; one-hot weights select a slot)
 """
 from __future__ import annotations
 
@@ -52,7 +57,7 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
                                "-Wall", "-Wextra", "-o", tmp, _SRC])
         os.replace(tmp, _LIB)
     return _LIB
@@ -75,8 +80,12 @@ def _load():
                                            i32p, i32p, i32p, i32p]
             lib.oracle_layout.argtypes = [ci, ci, ci, ci, ci, ci, cl, ci, i32p, i32p,
                                           i32p, i64p, i64p]
+            u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+            f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+            lib.oracle_permute.argtypes = [ci, ci, ci, ci, u16p, i32p, u16p]
+            lib.oracle_combine.argtypes = [ci, ci, ci, ci, u16p, i32p, f32p, u16p]
             for f in ("oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
-                      "oracle_layout"):
+                      "oracle_layout", "oracle_permute", "oracle_combine"):
                 getattr(lib, f).restype = ci
             _lib = lib
     return _lib
@@ -204,3 +213,31 @@ def layout(cfg: dict, dst_inst, n_layers: int | None = None):
     if squeeze:
         return sp[0], so[0], sc[0], st[0]
     return sp, so, sc, st
+
+
+def permute(x, sorted_pairs, k: int):
+    """Dispatch pack: y[l][pos] = x[l][sorted_pairs[l][pos] // k] (bf16 rows as
+    uint16).  x: uint16 [L, T, H]; sorted_pairs: int32 [L, T*k].  Returns
+    uint16 [L, T*k, H]."""
+    xa = np.ascontiguousarray(x, dtype=np.uint16)
+    sp = _i32(sorted_pairs)
+    L, T, H = xa.shape
+    y = np.zeros((L, T * k, H), np.uint16)
+    _check("oracle_permute", _load().oracle_permute(L, T, k, H, xa.reshape(-1), sp.reshape(-1),
+                                                    y.reshape(-1)))
+    return y
+
+
+def combine(y, sorted_pairs, w, k: int):
+    """Combine: out[l][t] = bf16(sum_j w[l][t][j] * y[l][pos(t, j)]) in float,
+    slot order, one rounding.  y: uint16 [L, T*k, H]; w: float32 [L, T, k].
+    Returns uint16 [L, T, H]."""
+    ya = np.ascontiguousarray(y, dtype=np.uint16)
+    sp = _i32(sorted_pairs)
+    wa = np.ascontiguousarray(w, dtype=np.float32)
+    L, n, H = ya.shape
+    T = n // k
+    out = np.zeros((L, T, H), np.uint16)
+    _check("oracle_combine", _load().oracle_combine(L, T, k, H, ya.reshape(-1), sp.reshape(-1),
+                                                    wa.reshape(-1), out.reshape(-1)))
+    return out

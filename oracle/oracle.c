@@ -14,6 +14,9 @@
  *   [Zyphra]  "Expert Coupling in MoE Pretraining" -- sections "Experts Are
  *             Correlated Within a Layer" and "Routing Is Also Correlated
  *             Across Layers".
+ *   [MoX]     "MoX: Efficient MoE Routing on Direct-Connect Topologies" --
+ *             §2.4 "Partial Reduction on Combine" (combine is a reduction of
+ *             the top-K expert outputs into one vector per token).
  *
  * Where the pages leave a step open, the reading taken is stated at the step.
  * Every function is a direct transcription of the step list, with no blocking,
@@ -28,6 +31,11 @@
  *   n_local = E/R + n_slot, l < E/R a main, l >= E/R replica slot l - E/R.
  *
  * Return codes: 0 ok, -1 bad argument, -2 an id outside [0, E).
+ *
+ * Floating point (permute and combine only): bf16 values are 16-bit
+ * patterns, widened to float by appending 16 zero bits and narrowed by
+ * round-to-nearest-even; products and sums are separate float operations
+ * (built with -ffp-contract=off, so no multiply-add is fused).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -612,5 +620,80 @@ int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok
         st[7] = 0;
     }
     free(count);
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Dispatch pack and combine (TopoEP Fig. 1: dispatch sends each token's
+ * activation to the ranks hosting its selected experts; [MoX] §2.4: combine
+ * reduces the token's top-K expert outputs into one vector).
+ *
+ * Readings: the send buffer is in layout order -- row pos of y holds the
+ * activation of the token of pair sorted[pos]; combine weights each expert
+ * output by the caller's gate weight w[t][j] and sums in slot order j = 0..k-1
+ * in float, rounding once to bf16.
+ * ------------------------------------------------------------------------- */
+
+static float bf16_to_float(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint16_t float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu))   /* NaN: quiet */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);                              /* to nearest, ties even */
+    return (uint16_t)(u >> 16);
+}
+
+/* y[l][pos][:] = x[l][sorted[l][pos] / k][:]   (x: [L][T][H], y: [L][T*k][H]) */
+int oracle_permute(int L, int T, int k, int H, const uint16_t *x, const int32_t *sorted,
+                   uint16_t *y) {
+    if (L < 0 || T < 0 || k < 1 || H < 1) return ORC_EINVAL;
+    const int64_t npairs = (int64_t)T * k;
+    for (int l = 0; l < L; l++)
+        for (int64_t pos = 0; pos < npairs; pos++) {
+            const int32_t p = sorted[(int64_t)l * npairs + pos];
+            if (p < 0 || p >= npairs) return ORC_EINVAL;
+            const int t = p / k;
+            memcpy(y + ((int64_t)l * npairs + pos) * H, x + ((int64_t)l * T + t) * H,
+                   sizeof(uint16_t) * (size_t)H);
+        }
+    return ORC_OK;
+}
+
+/* out[l][t][:] = bf16( sum_{j<k} w[l][t][j] * y[l][pos(t, j)][:] ), where
+ * pos(t, j) is the position of pair t*k + j in sorted[l] (sorted is a
+ * permutation of the pairs). */
+int oracle_combine(int L, int T, int k, int H, const uint16_t *y, const int32_t *sorted,
+                   const float *w, uint16_t *out) {
+    if (L < 0 || T < 0 || k < 1 || H < 1) return ORC_EINVAL;
+    const int64_t npairs = (int64_t)T * k;
+    int64_t *pos_of = (int64_t *)malloc(sizeof(int64_t) * (size_t)(npairs > 0 ? npairs : 1));
+    if (!pos_of) return ORC_EINVAL;
+    for (int l = 0; l < L; l++) {
+        for (int64_t p = 0; p < npairs; p++) pos_of[p] = -1;
+        for (int64_t pos = 0; pos < npairs; pos++) {
+            const int32_t p = sorted[(int64_t)l * npairs + pos];
+            if (p < 0 || p >= npairs || pos_of[p] >= 0) { free(pos_of); return ORC_EINVAL; }
+            pos_of[p] = pos;
+        }
+        for (int t = 0; t < T; t++)
+            for (int h = 0; h < H; h++) {
+                float acc = 0.0f;
+                for (int j = 0; j < k; j++) {
+                    const int64_t pos = pos_of[(int64_t)t * k + j];
+                    const float v = bf16_to_float(y[((int64_t)l * npairs + pos) * H + h]);
+                    const float prod = w[((int64_t)l * T + t) * k + j] * v;
+                    acc = acc + prod;
+                }
+                out[((int64_t)l * T + t) * H + h] = float_to_bf16(acc);
+            }
+    }
+    free(pos_of);
     return ORC_OK;
 }
