@@ -63,6 +63,7 @@ extern "C" {
 #define TOPO_CALL_COOCCUR 4
 #define TOPO_CALL_CHAIN 5   /* hist -> plan -> reroute -> dispatch_layout on one ws */
 #define TOPO_CALL_REROUTE_LAYOUT 6
+#define TOPO_CALL_PACK 7    /* topo_permute, topo_combine */
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -197,6 +198,38 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
                         const topo_plan_t *plan, int32_t *dst_inst, int32_t *sorted_pairs,
                         int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
                         size_t ws_bytes, cudaStream_t stream);
+
+/* Dispatch pack [TopoEP Fig. 1: dispatch sends each token's activation to the
+ * ranks hosting its selected experts].  Reading: the send buffer holds the
+ * pairs' rows in layout order, so each destination instance's rows are one
+ * contiguous segment (seg_off):
+ *   y[l][pos][:] = x[l][sorted_pairs[l][pos] / k][:]
+ * x:  device bf16 (16-bit patterns) [n_layers][T][H], 16-byte aligned.
+ * y:  device bf16 [n_layers][T*k][H], 16-byte aligned.
+ * H:  elements per row, a positive multiple of 8 (16-byte rows).
+ * sorted_pairs: device int32 [n_layers][T*k] from topo_dispatch_layout or
+ *     topo_reroute_layout (a permutation of the pairs).
+ * ws: >= topo_workspace_bytes(cfg, n_layers, TOPO_CALL_PACK) bytes (the
+ *     inverse permutation).  Rows are copied bit for bit.
+ * Device errors: TOPO_ESTATE when sorted_pairs is not a permutation (the
+ * affected tokens are skipped). */
+int topo_permute(const topo_cfg *cfg, int32_t n_layers, int32_t H, const uint16_t *x,
+                 const int32_t *sorted_pairs, uint16_t *y, void *ws, size_t ws_bytes,
+                 cudaStream_t stream);
+
+/* Combine ["MoX: Efficient MoE Routing on Direct-Connect Topologies" §2.4:
+ * combine reduces the token's top-K expert outputs into one vector].
+ * Reading: the reduction is the gate-weighted sum of the expert outputs, in
+ * float, in slot order, rounded once to bf16 (nearest, ties to even):
+ *   out[l][t][:] = bf16( sum_{j=0..k-1} w[l][t][j] * y[l][pos(t, j)][:] )
+ * where pos(t, j) is the position of pair t*k + j in sorted_pairs[l] and
+ * each product and each sum is one float operation (no fused multiply-add).
+ * y: device bf16 [n_layers][T*k][H]; w: device float [n_layers][T][k];
+ * out: device bf16 [n_layers][T][H]; alignment, H and ws as topo_permute.
+ * Device errors: TOPO_ESTATE as topo_permute. */
+int topo_combine(const topo_cfg *cfg, int32_t n_layers, int32_t H, const uint16_t *y,
+                 const int32_t *sorted_pairs, const float *w, uint16_t *out, void *ws,
+                 size_t ws_bytes, cudaStream_t stream);
 
 /* topo_hist without a caller-supplied workspace.  No passage of the pages
  * has a counterpart: it computes exactly what topo_hist computes (Omega), for

@@ -62,6 +62,7 @@ struct Geo {
     size_t off_lseg;        // int32 [L][n_keys+1]    segment offsets
     size_t off_lsend;       // int64 [L][R][R]        send counts
     size_t off_lstat;       // int64 [L][8]           layout statistics
+    size_t off_pack_inv;    // int32 [L][T*k]         position of each pair (pack workspace)
     size_t total;
 };
 
@@ -183,5 +184,9 @@ size_t row_index_smem(const Geo &g);
 size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
+cudaError_t launch_permute(const Geo &g, int H, const uint16_t *x, const int32_t *sorted, uint16_t *y,
+                           void *ws, cudaStream_t st);
+cudaError_t launch_combine(const Geo &g, int H, const uint16_t *y, const int32_t *sorted, const float *w,
+                           uint16_t *out, void *ws, cudaStream_t st);
 
 }  // namespace topo

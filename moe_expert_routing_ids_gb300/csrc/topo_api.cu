@@ -153,15 +153,35 @@ bool plan_ok(const topo_plan_t *p, const Geo &g) {
            p->rank_load && p->stats;
 }
 
+// Workspace of topo_permute / topo_combine: header + the inverse permutation.
+size_t pack_ws_bytes(Geo &g) {
+    g.off_pack_inv = sizeof(WsHeader);
+    return align_up(g.off_pack_inv + (size_t)g.L * (size_t)g.npairs * 4);
+}
+
+int pack_args(const topo_cfg *cfg, int32_t n_layers, int32_t H, const void *in, const int32_t *sorted,
+              const void *out, void *ws, size_t ws_bytes, Geo *g) {
+    int rc = make_geo(cfg, n_layers, g);
+    if (rc) return rc;
+    if (H < 8 || H % 8) return TOPO_EINVAL;
+    if (!ws) return TOPO_EINVAL;
+    if (ws_bytes < pack_ws_bytes(*g)) return TOPO_ENOSPC;
+    if (n_layers == 0 || g->npairs == 0) return TOPO_OK;
+    if (!in || !sorted || !out) return TOPO_EINVAL;
+    if (((uintptr_t)in | (uintptr_t)out) & 15) return TOPO_EINVAL;
+    return TOPO_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call) {
     if (which_call == TOPO_CALL_COOCCUR) return sizeof(WsHeader);
-    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_REROUTE_LAYOUT) return 0;
+    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_PACK) return 0;
     Geo g;
     if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
+    if (which_call == TOPO_CALL_PACK) return pack_ws_bytes(g);
     return g.total;
 }
 
@@ -245,6 +265,25 @@ int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids,
     if (ws_bytes < sizeof(WsHeader)) return TOPO_ENOSPC;
     if (L == 0) return TOPO_OK;
     return cuda_rc(launch_cooccur(L, T, E, k, ids, co, L > 1 ? tr : nullptr, ws, stream));
+}
+
+int topo_permute(const topo_cfg *cfg, int32_t n_layers, int32_t H, const uint16_t *x,
+                 const int32_t *sorted_pairs, uint16_t *y, void *ws, size_t ws_bytes,
+                 cudaStream_t stream) {
+    Geo g;
+    const int rc = pack_args(cfg, n_layers, H, x, sorted_pairs, y, ws, ws_bytes, &g);
+    if (rc || n_layers == 0 || g.npairs == 0) return rc;
+    return cuda_rc(launch_permute(g, H, x, sorted_pairs, y, ws, stream));
+}
+
+int topo_combine(const topo_cfg *cfg, int32_t n_layers, int32_t H, const uint16_t *y,
+                 const int32_t *sorted_pairs, const float *w, uint16_t *out, void *ws,
+                 size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    const int rc = pack_args(cfg, n_layers, H, y, sorted_pairs, out, ws, ws_bytes, &g);
+    if (rc || n_layers == 0 || g.npairs == 0) return rc;
+    if (!w) return TOPO_EINVAL;
+    return cuda_rc(launch_combine(g, H, y, sorted_pairs, w, out, ws, stream));
 }
 
 int topo_read_error(const void *ws) {
