@@ -386,6 +386,70 @@ def secondary_cooccur(dev, stream, hbm_peak):
             "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
 
 
+PACK_WORKLOAD_H = 7168       # hidden size of the four-layer workload (bf16 rows)
+
+
+def secondary_pack(dev, stream, hbm_peak):
+    """topo_permute and topo_combine on the first layer of the T=65536, E=256,
+    k=8, R=64 workload with H = 7168 bf16 rows: x 0.94 GB, send buffer 7.5 GB
+    (both far above L2).  Layout from the library's own chain; each call timed
+    with CUDA events, median of 5 after 2 warm-up calls."""
+    import torch
+    import moe_expert_routing_ids_gb300 as topo
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    w = W.FOUR_LAYER
+    T, k, H = w.T, w.k, PACK_WORKLOAD_H
+    P = Planner(w.plan_cfg, 1, dev, stream=stream)
+    ids = torch.as_tensor(w.ids(n_layers=1), device=dev)
+    with torch.cuda.stream(stream):
+        P.run(ids)
+    cfg = topo.make_cfg(**w.plan_cfg)
+    ws_bytes = topo.topo_workspace_bytes(cfg, 1, topo.TOPO_CALL_PACK)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(5)
+    x = (torch.randn((1, T, H), generator=g, device=dev) * 4).to(torch.bfloat16).view(torch.int16)
+    y = torch.empty((1, T * k, H), dtype=torch.int16, device=dev)
+    out = torch.empty((1, T, H), dtype=torch.int16, device=dev)
+    gw = torch.rand((1, T, k), generator=g, device=dev)
+    sp = P.buf.sorted_pairs
+
+    def timed(fn):
+        times = []
+        for i in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                fn()
+                b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                times.append(a.elapsed_time(b))
+        return statistics.median(times)
+
+    s = stream.cuda_stream
+    ms_p = timed(lambda: topo.topo_permute(cfg, 1, H, x, sp, y, ws, ws_bytes, s))
+    ms_c = timed(lambda: topo.topo_combine(cfg, 1, H, y, sp, gw, out, ws, ws_bytes, s))
+    torch.cuda.synchronize()
+    if topo.topo_read_error(ws) != 0 or P.error() != 0:
+        raise RuntimeError("device error in the pack measurement")
+    row = H * 2
+    # algorithmic: permute reads each token row once and writes it k times;
+    # combine reads the k rows and the k weights and writes one row; both also
+    # read the layout and build its inverse (12 B per pair)
+    b_p = T * row + T * k * row + 12 * T * k
+    b_c = T * k * row + T * row + 4 * T * k + 12 * T * k
+    res = {}
+    for name, ms, nb in (("permute", ms_p, b_p), ("combine", ms_c, b_c)):
+        gbs = nb / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "algorithmic_bytes": nb, "achieved_gbs": round(gbs, 1),
+                     "frac": round(gbs / hbm_peak, 4)}
+    res.update({"workload": f"{w.name} (first layer), H={H} bf16", "timing":
+                "CUDA events around one call, median of 5 after 2 warm-up calls"})
+    del y, x, out
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
@@ -459,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.skip_secondary:
         line["plan_latency"] = secondary_plan_latency(dev, stream)
         line["cooccur"] = secondary_cooccur(dev, stream, hbm)
+        line["pack"] = secondary_pack(dev, stream, hbm)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, ids)
     print(json.dumps(line), flush=True)
