@@ -28,6 +28,9 @@ Parity status per function (what pins each one is in ``tests/test_oracle_*``):
   combine   pinned (hand cases incl. round-to-nearest-even ties and the slot
             summation order; exact round trip combine(permute(x)) == x with
             dyadic weights; one-hot weights select a slot)
+  dedup     pinned (hand case; every pair covered by exactly one row; k = 1
+            keeps one row per pair; the pages' printed top-2 / top-6 row
+            savings against the closed-form expectation)
 """
 from __future__ import annotations
 
@@ -84,8 +87,10 @@ def _load():
             f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
             lib.oracle_permute.argtypes = [ci, ci, ci, ci, u16p, i32p, u16p]
             lib.oracle_combine.argtypes = [ci, ci, ci, ci, u16p, i32p, f32p, u16p]
+            u64p = np.ctypeslib.ndpointer(np.uint64, flags="C_CONTIGUOUS")
+            lib.oracle_dedup.argtypes = [ci, ci, ci, ci, ci, i32p, i32p, i32p, u64p, u64p, i64p, i64p]
             for f in ("oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
-                      "oracle_layout", "oracle_permute", "oracle_combine"):
+                      "oracle_layout", "oracle_permute", "oracle_combine", "oracle_dedup"):
                 getattr(lib, f).restype = ci
             _lib = lib
     return _lib
@@ -240,4 +245,29 @@ def combine(y, sorted_pairs, w, k: int):
     out = np.zeros((L, T, H), np.uint16)
     _check("oracle_combine", _load().oracle_combine(L, T, k, H, ya.reshape(-1), sp.reshape(-1),
                                                     wa.reshape(-1), out.reshape(-1)))
+    return out
+
+
+DEDUP_STAT_NAMES = ("rows", "pairs", "rows_remote", "pairs_remote")
+
+
+def dedup(cfg: dict, dst_inst):
+    """Deduplicated dispatch layout for dst_inst int32 [L, T*k]: dict with
+    seg [L, R+1], row_token [L, T*k], row_slots uint64 [L, T*k] (first seg[R]
+    rows used), tok_dst uint64 [L, T, ceil(R/64)], send [L, R, R] int64,
+    stats [L, 4] int64."""
+    d = _i32(dst_inst)
+    if d.ndim == 1:
+        d = d[None]
+    L = d.shape[0]
+    T, E, k, R = cfg["T"], cfg["E"], cfg["k"], cfg["R"]
+    nl = E // R + cfg["n_slot"]
+    RW = (R + 63) // 64
+    out = dict(seg=np.zeros((L, R + 1), np.int32), row_token=np.zeros((L, T * k), np.int32),
+               row_slots=np.zeros((L, T * k), np.uint64), tok_dst=np.zeros((L, T, RW), np.uint64),
+               send=np.zeros((L, R, R), np.int64), stats=np.zeros((L, 4), np.int64))
+    _check("oracle_dedup", _load().oracle_dedup(T, k, R, nl, L, d.reshape(-1),
+                                                out["seg"].reshape(-1), out["row_token"].reshape(-1),
+                                                out["row_slots"].reshape(-1), out["tok_dst"].reshape(-1),
+                                                out["send"].reshape(-1), out["stats"].reshape(-1)))
     return out

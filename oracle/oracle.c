@@ -16,7 +16,11 @@
  *             Across Layers".
  *   [MoX]     "MoX: Efficient MoE Routing on Direct-Connect Topologies" --
  *             §2.4 "Partial Reduction on Combine" (combine is a reduction of
- *             the top-K expert outputs into one vector per token).
+ *             the top-K expert outputs into one vector per token); §2 the
+ *             per-token destination bitmap.
+ *   [Zyphra]  also "Moving Correlated Experts Together" (a deduplicating
+ *             dispatcher sends a token to a GPU once, with metadata naming
+ *             the local experts that process it).
  *
  * Where the pages leave a step open, the reading taken is stated at the step.
  * Every function is a direct transcription of the step list, with no blocking,
@@ -695,5 +699,86 @@ int oracle_combine(int L, int T, int k, int H, const uint16_t *y, const int32_t 
             }
     }
     free(pos_of);
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Deduplicated dispatch layout ([Zyphra] "Moving Correlated Experts
+ * Together"; [MoX] §2 destination bitmap).  One row per (token, destination
+ * rank) instead of one per pair.
+ *
+ * Readings: rows are ordered by destination rank, then by token (so by
+ * source, tokens being source-blocked); a row carries its token and the mask
+ * of the token's slots whose instance is on that rank; the destination rank of
+ * a pair is dst_inst / n_local.
+ *
+ * Outputs per layer: seg[R+1] row offsets per destination rank; row_token and
+ * row_slots [T*k] (the first seg[R] rows used); tok_dst[T][RW] bitmap of each
+ * token's destination ranks, RW = ceil(R / 64) 64-bit words; send[R][R] rows
+ * from source s to rank r; stats {rows, pairs, rows to another rank, pairs to
+ * another rank}.
+ * ------------------------------------------------------------------------- */
+int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *dst_inst,
+                 int32_t *seg, int32_t *row_token, uint64_t *row_slots, uint64_t *tok_dst,
+                 int64_t *send, int64_t *stats) {
+    if (T < 0 || k < 1 || k > 64 || R < 1 || n_local < 1 || n_layers < 0 || T % R) return ORC_EINVAL;
+    const int64_t npairs = (int64_t)T * k;
+    const int RW = (R + 63) / 64, tpr = T / R;
+    int64_t *fill = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R + 1));
+    uint64_t *mask = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)R);
+    if (!fill || !mask) { free(fill); free(mask); return ORC_EINVAL; }
+    for (int l = 0; l < n_layers; l++) {
+        const int32_t *d = dst_inst + (int64_t)l * npairs;
+        int32_t *sg = seg + (int64_t)l * (R + 1);
+        int32_t *rt = row_token + (int64_t)l * npairs;
+        uint64_t *rs = row_slots + (int64_t)l * npairs;
+        uint64_t *td = tok_dst + (int64_t)l * T * RW;
+        int64_t *sc = send + (int64_t)l * R * R;
+        int64_t *st = stats + (int64_t)l * 4;
+        for (int64_t p = 0; p < npairs; p++)
+            if (d[p] < 0 || d[p] >= R * n_local) { free(fill); free(mask); return ORC_EINVAL; }
+        /* rows per destination rank */
+        for (int r = 0; r <= R; r++) fill[r] = 0;
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                const int r = d[(int64_t)t * k + j] / n_local;
+                int first = 1;
+                for (int i = 0; i < j; i++)
+                    if (d[(int64_t)t * k + i] / n_local == r) first = 0;
+                if (first) fill[r]++;
+            }
+        int64_t run = 0;
+        for (int r = 0; r < R; r++) {
+            const int64_t c = fill[r];
+            sg[r] = (int32_t)run;
+            fill[r] = run;
+            run += c;
+        }
+        sg[R] = (int32_t)run;
+        memset(sc, 0, sizeof(int64_t) * (size_t)R * R);
+        memset(st, 0, sizeof(int64_t) * 4);
+        memset(td, 0, sizeof(uint64_t) * (size_t)T * RW);
+        /* rows in token order within each rank */
+        for (int t = 0; t < T; t++) {
+            const int s = t / tpr;
+            for (int r = 0; r < R; r++) mask[r] = 0;
+            for (int j = 0; j < k; j++) mask[d[(int64_t)t * k + j] / n_local] |= (uint64_t)1 << j;
+            for (int r = 0; r < R; r++) {
+                if (!mask[r]) continue;
+                rt[fill[r]] = t;
+                rs[fill[r]] = mask[r];
+                fill[r]++;
+                td[(int64_t)t * RW + r / 64] |= (uint64_t)1 << (r % 64);
+                sc[(int64_t)s * R + r]++;
+                st[0]++;
+                if (r != s) st[2]++;
+            }
+            for (int j = 0; j < k; j++)
+                if (d[(int64_t)t * k + j] / n_local != s) st[3]++;
+        }
+        st[1] = npairs;
+    }
+    free(fill);
+    free(mask);
     return ORC_OK;
 }
