@@ -64,6 +64,8 @@ extern "C" {
 #define TOPO_CALL_CHAIN 5   /* hist -> plan -> reroute -> dispatch_layout on one ws */
 #define TOPO_CALL_REROUTE_LAYOUT 6
 #define TOPO_CALL_PACK 7    /* topo_permute, topo_combine */
+#define TOPO_CALL_DEDUP 8   /* topo_dedup_layout */
+#define TOPO_DEDUP_STATS 4  /* int64 deduplicated-layout statistics per layer */
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -198,6 +200,29 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
                         const topo_plan_t *plan, int32_t *dst_inst, int32_t *sorted_pairs,
                         int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, void *ws,
                         size_t ws_bytes, cudaStream_t stream);
+
+/* Deduplicated dispatch layout ["Expert Coupling in MoE Pretraining",
+ * "Moving Correlated Experts Together": a token goes to a destination rank
+ * once, with metadata naming the local experts that process it; "MoX:
+ * Efficient MoE Routing on Direct-Connect Topologies" §2: a per-token
+ * destination bitmap].  Readings: one row per (token, destination rank), the
+ * destination rank of a pair being dst_inst / n_local; rows ordered by rank,
+ * then by token; a row's metadata is the mask of the token's slots on that
+ * rank (bit j = slot j).
+ * dst_inst:  device int32 [n_layers][T*k] (topo_reroute, topo_reroute_layout).
+ * seg:       device int32 [n_layers][R+1] row offsets per destination rank.
+ * row_token: device int32 [n_layers][T*k]; row_slots: device uint64
+ *            [n_layers][T*k] (the first seg[R] entries of a layer are used).
+ * tok_dst:   device uint64 [n_layers][T][ceil(R/64)] destination-rank bitmap.
+ * send:      device int64 [n_layers][R][R] rows from source s to rank r.
+ * stats:     device int64 [n_layers][TOPO_DEDUP_STATS]: rows, pairs, rows to
+ *            another rank, pairs to another rank.
+ * Requires k <= 16 and R <= 1024 (else TOPO_EINVAL).
+ * ws: >= topo_workspace_bytes(cfg, n_layers, TOPO_CALL_DEDUP) bytes.
+ * Device errors: TOPO_ESTATE for a dst_inst value outside [0, R*n_local). */
+int topo_dedup_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst, int32_t *seg,
+                      int32_t *row_token, uint64_t *row_slots, uint64_t *tok_dst, int64_t *send,
+                      int64_t *stats, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Dispatch pack [TopoEP Fig. 1: dispatch sends each token's activation to the
  * ranks hosting its selected experts].  Reading: the send buffer holds the

@@ -25,11 +25,14 @@ TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP = -4, -5, -6
 TOPO_CALL_HIST, TOPO_CALL_PLAN, TOPO_CALL_REROUTE, TOPO_CALL_LAYOUT = 0, 1, 2, 3
 TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN, TOPO_CALL_REROUTE_LAYOUT = 4, 5, 6
 TOPO_CALL_PACK = 7
+TOPO_CALL_DEDUP = 8
+TOPO_DEDUP_STATS = 4
 TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
 EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-           "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine")
+           "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine",
+           "topo_dedup_layout")
 TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -81,13 +84,14 @@ def lib():
             L.topo_reroute_layout.argtypes = [cfgp, i32, vp, planp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_hist_noalloc.argtypes = [cfgp, i32, vp, vp, vp, vp]
             L.topo_permute.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, sz, vp]
+            L.topo_dedup_layout.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_combine.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
                       "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-                      "topo_hist_noalloc", "topo_permute", "topo_combine"):
+                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -189,6 +193,15 @@ def topo_hist_noalloc(cfg: TopoCfg, n_layers: int, ids, hist, err=None, stream=N
     err: optional device int32 that receives the device error word."""
     return _chk("topo_hist_noalloc", lib().topo_hist_noalloc(ctypes.byref(cfg), n_layers, _p(ids),
                                                              _p(hist), _p(err), _s(stream)))
+
+
+def topo_dedup_layout(cfg: TopoCfg, n_layers: int, dst_inst, seg, row_token, row_slots, tok_dst,
+                      send, stats, ws, ws_bytes: int, stream=None) -> int:
+    """Deduplicated dispatch layout: one row per (token, destination rank)."""
+    return _chk("topo_dedup_layout",
+                lib().topo_dedup_layout(ctypes.byref(cfg), n_layers, _p(dst_inst), _p(seg),
+                                        _p(row_token), _p(row_slots), _p(tok_dst), _p(send),
+                                        _p(stats), _p(ws), ws_bytes, _s(stream)))
 
 
 def topo_permute(cfg: TopoCfg, n_layers: int, H: int, x, sorted_pairs, y, ws, ws_bytes: int,

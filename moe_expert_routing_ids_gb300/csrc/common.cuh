@@ -19,6 +19,8 @@ constexpr int kRankSmemTarget = 110 * 1024;        // two rank CTAs per SM
 constexpr int kSmemMax = 227 * 1024;               // per CTA on sm_103a
 constexpr int kMaxK = 64;
 constexpr int kRankEntCap = 1024;                 // routing entries of a row kept in shared memory
+constexpr int kDedupMaxK = 16;                     // slots per token the dedup layout takes
+constexpr int kDedupMaxRanks = 1024;               // ranks the dedup layout takes
 constexpr int kMaxRanksPerNode = 32;               // one warp lane per rank of a domain
 
 // Workspace header, 256 bytes at offset 0 of every workspace.
@@ -184,6 +186,10 @@ size_t row_index_smem(const Geo &g);
 size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
+size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src);
+cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t *row_token,
+                         uint64_t *row_slots, uint64_t *tok_dst, int64_t *send, int64_t *stats, void *ws,
+                         cudaStream_t st);
 cudaError_t launch_permute(const Geo &g, int H, const uint16_t *x, const int32_t *sorted, uint16_t *y,
                            void *ws, cudaStream_t st);
 cudaError_t launch_combine(const Geo &g, int H, const uint16_t *y, const int32_t *sorted, const float *w,

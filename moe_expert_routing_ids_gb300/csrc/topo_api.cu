@@ -178,10 +178,11 @@ extern "C" {
 
 size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call) {
     if (which_call == TOPO_CALL_COOCCUR) return sizeof(WsHeader);
-    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_PACK) return 0;
+    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_DEDUP) return 0;
     Geo g;
     if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
     if (which_call == TOPO_CALL_PACK) return pack_ws_bytes(g);
+    if (which_call == TOPO_CALL_DEDUP) return dedup_ws_bytes(g, nullptr, nullptr);
     return g.total;
 }
 
@@ -265,6 +266,22 @@ int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids,
     if (ws_bytes < sizeof(WsHeader)) return TOPO_ENOSPC;
     if (L == 0) return TOPO_OK;
     return cuda_rc(launch_cooccur(L, T, E, k, ids, co, L > 1 ? tr : nullptr, ws, stream));
+}
+
+int topo_dedup_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst, int32_t *seg,
+                      int32_t *row_token, uint64_t *row_slots, uint64_t *tok_dst, int64_t *send,
+                      int64_t *stats, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (cfg->k > kDedupMaxK || cfg->R > kDedupMaxRanks) return TOPO_EINVAL;
+    if (!ws) return TOPO_EINVAL;
+    if (ws_bytes < dedup_ws_bytes(g, nullptr, nullptr)) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    if (!seg || !send || !stats || (g.npairs > 0 && (!dst_inst || !row_token || !row_slots || !tok_dst)))
+        return TOPO_EINVAL;
+    return cuda_rc(launch_dedup(g, dst_inst, seg, row_token, row_slots, tok_dst, send, stats, ws,
+                                stream));
 }
 
 int topo_permute(const topo_cfg *cfg, int32_t n_layers, int32_t H, const uint16_t *x,
