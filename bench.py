@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged
@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup"),
+                    help="run one secondary measurement alone and print it (for profiling)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds the oracle steps should take in total")
     return ap.parse_args()
@@ -450,6 +452,80 @@ def secondary_pack(dev, stream, hbm_peak):
     return res
 
 
+def secondary_dedup(P, w, dev, stream, hbm_peak):
+    """topo_dedup_layout on the destinations of the timed workload (all its
+    microbatches; dst_inst 168 MB > 129 MB L2).  The call timed with CUDA
+    events, median of 5 after 2 warm-up calls."""
+    import torch
+    import moe_expert_routing_ids_gb300 as topo
+    L, T, k, R = w.n_layers, w.T, w.k, w.R
+    RW = (R + 63) // 64
+    cfg = topo.make_cfg(**w.plan_cfg)
+    ws_bytes = topo.topo_workspace_bytes(cfg, L, topo.TOPO_CALL_DEDUP)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    o = dict(seg=torch.empty((L, R + 1), dtype=torch.int32, device=dev),
+             row_token=torch.empty((L, T * k), dtype=torch.int32, device=dev),
+             row_slots=torch.empty((L, T * k), dtype=torch.int64, device=dev),
+             tok_dst=torch.empty((L, T, RW), dtype=torch.int64, device=dev),
+             send=torch.empty((L, R, R), dtype=torch.int64, device=dev),
+             stats=torch.empty((L, topo.TOPO_DEDUP_STATS), dtype=torch.int64, device=dev))
+    s = stream.cuda_stream
+    times = []
+    for i in range(7):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            topo.topo_dedup_layout(cfg, L, P.buf.dst_inst, o["seg"], o["row_token"], o["row_slots"],
+                                   o["tok_dst"], o["send"], o["stats"], ws, ws_bytes, s)
+            b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    torch.cuda.synchronize()
+    if topo.topo_read_error(ws) != 0:
+        raise RuntimeError("device error in the deduplicated layout measurement")
+    ms = statistics.median(times)
+    st = o["stats"].cpu().numpy()
+    rows, pairs = int(st[:, 0].sum()), int(st[:, 1].sum())
+    # algorithmic: read the destinations once, write the token bitmaps and one
+    # (token, slot mask) row of 12 B per row
+    nb = 4 * pairs + 8 * L * T * RW + 12 * rows
+    gbs = nb / (ms * 1e-3) / 1e9
+    return {"workload": f"{w.name}, all {L} microbatches", "ms": round(ms, 4),
+            "rows": rows, "pairs": pairs, "rows_remote": int(st[:, 2].sum()),
+            "pairs_remote": int(st[:, 3].sum()), "pairs_per_s": round(pairs / (ms * 1e-3), 1),
+            "algorithmic_bytes": nb, "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "timing": "CUDA events around one call, median of 5 after 2 warm-up calls",
+            "gpu_launches_per_call": KERNELS_PER_CALL["dedup"]}
+
+
+def run_only(name):
+    """One secondary measurement on cuda:0, printed as its own JSON line."""
+    import torch
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    hbm, _ = peaks()
+    if name == "plan_latency":
+        res = secondary_plan_latency(dev, stream)
+    elif name == "cooccur":
+        res = secondary_cooccur(dev, stream, hbm)
+    elif name == "pack":
+        res = secondary_pack(dev, stream, hbm)
+    else:
+        w = W.STRESS
+        P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
+        with torch.cuda.stream(stream):
+            P.run(torch.as_tensor(w.ids(), device=dev))
+        torch.cuda.synchronize(dev)
+        if P.error() != 0:
+            raise RuntimeError("device error in the plan chain")
+        res = secondary_dedup(P, w, dev, stream, hbm)
+    print(json.dumps({"measurement": name, **res}), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
@@ -524,6 +600,7 @@ def run_ours(args, rank, world, local_rank):
         line["plan_latency"] = secondary_plan_latency(dev, stream)
         line["cooccur"] = secondary_cooccur(dev, stream, hbm)
         line["pack"] = secondary_pack(dev, stream, hbm)
+        line["dedup"] = secondary_dedup(P, w, dev, stream, hbm)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, ids)
     print(json.dumps(line), flush=True)
@@ -621,7 +698,11 @@ def main():
         else:
             import __graft_entry__
             __graft_entry__.build()
-            run_ours(args, rank, world, local_rank)
+            if args.only:
+                if rank == 0:
+                    run_only(args.only)
+            else:
+                run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch

@@ -6,16 +6,19 @@
 // One row per (token, destination rank), ordered by rank, then by token.  A
 // row carries its token and the mask of the token's slots whose instance is
 // on that rank (the first slot with a rank stands for the row).  Tiles of
-// kDdTile tokens inside one source, one warp per tile:
-//   k_dd_count  distinct ranks per token -> rows per (tile, rank), the
-//               token bitmaps, and the statistics
+// kDdTile tokens inside one source, one CTA per tile and one thread per token;
+// each tile's destinations are first staged slot-major in shared memory by
+// coalesced loads of the tile's contiguous run of k*tokens ints:
+//   k_dd_count  distinct ranks per token -> rows per (tile, rank), the token
+//               bitmaps, and the pairs sent to another rank
 //   k_dd_prefix per (layer, source, rank): tile counts -> exclusive prefix,
 //               total -> send counts
-//   k_dd_seg    per layer: per-source bases of every rank and the rank
-//               segment offsets
-//   k_dd_fill   rows ranked in token order inside each round of 32 tokens with
-//               a per-rank lane bitmask (popc of the lanes below), written at
-//               segment + source base + tile prefix + rank
+//   k_dd_seg    per layer: per-source bases of every rank, the rank segment
+//               offsets, and the row statistics
+//   k_dd_fill   rows ranked in token order inside the tile (per-warp lane
+//               bitmasks per rank, prefixed over warps), staged in shared
+//               memory in (rank, token) order, then written out so that
+//               consecutive threads write consecutive rows of one rank
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -23,110 +26,171 @@
 namespace topo {
 namespace {
 
-constexpr int kDdTile = 256;          // tokens per warp tile
-constexpr int kDdWarps = 8;
-constexpr int kDdMaxRW = kDedupMaxRanks / 64;   // 64-bit words of a token bitmap
+constexpr int kDdTile = 256;              // tokens per tile = threads per CTA
+constexpr int kDdWarps = kDdTile / 32;    // 32-token groups of a tile
+constexpr int kDdSegThreads = kDedupMaxRanks;
+constexpr int kDdFillCtas = 6;            // resident fill CTAs per SM the registers must allow
+
+// n / d for n < 2^32 by a multiply-high with m = floor(2^32 / d) (2^32 - 1 for
+// d = 1), which gives the quotient or one less, and one correction step
+// (the reciprocal-multiplication method of Granlund and Montgomery, "Division
+// by Invariant Integers using Multiplication", with the correction in place of
+// the rounding analysis).
+struct DdDiv {
+    unsigned d, m;
+};
+
+__host__ inline DdDiv dd_div(unsigned d) {
+    DdDiv v;
+    v.d = d;
+    v.m = d == 1 ? 0xffffffffu : (unsigned)((1ull << 32) / d);
+    return v;
+}
+
+__device__ __forceinline__ unsigned dd_quot(unsigned n, DdDiv v) {
+    unsigned q = __umulhi(n, v.m);
+    q += (n - q * v.d) >= v.d;
+    return q;
+}
 
 struct DdGeo {
     int T, k, R, nl, tpr, tps, RW, L;
     int64_t npairs;
+    DdDiv dk, dnl;
 };
 
-// Ranks of a token's k slots and, for the first slot of each rank, the mask
-// of all its slots with that rank (0 for the other slots).  KB >= k is the
-// compile-time slot count; slots k..KB-1 are empty.
+struct DdTile {
+    int l, s, tok0, ntok;
+};
+
+__device__ __forceinline__ DdTile dd_tile(const DdGeo &g) {
+    DdTile d;
+    const int64_t tile = blockIdx.x;
+    const int t = (int)(tile % g.tps);
+    d.s = (int)((tile / g.tps) % g.R);
+    d.l = (int)(tile / ((int64_t)g.tps * g.R));
+    d.tok0 = t * kDdTile;
+    d.ntok = max(0, min(kDdTile, g.tpr - d.tok0));
+    return d;
+}
+
+// The tile's pairs are one contiguous run of ntok * k ints; thread x takes the
+// elements e = u * kDdTile + x, u < KB (coalesced), all loads issued first.
 template <int KB>
-__device__ __forceinline__ void token_rows(const int32_t *d, int k, int nl, int R, int *rk,
-                                           unsigned long long *msk, bool &bad) {
+__device__ __forceinline__ void dd_load(const int32_t *__restrict__ src, int n, int *v) {
 #pragma unroll
-    for (int j = 0; j < KB; ++j) {
-        rk[j] = -1;
-        if (j < k) {
-            const int v = __ldg(d + j);
-            if ((unsigned)v < (unsigned)(R * nl)) rk[j] = v / nl;
-            else bad = true;
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-        bool first = rk[j] >= 0;
-#pragma unroll
-        for (int i = 0; i < j; ++i) first = first && rk[i] != rk[j];
-        unsigned long long m = 0;
-        if (first) {
-#pragma unroll
-            for (int i = j; i < KB; ++i) m |= (unsigned long long)(rk[i] == rk[j]) << i;
-        }
-        msk[j] = m;
+    for (int u = 0; u < KB; ++u) {
+        const int e = u * kDdTile + threadIdx.x;
+        v[u] = e < n ? __ldg(src + e) : 0;
     }
 }
 
-__device__ __forceinline__ int tile_tokens(const DdGeo &g, int t, int &tok0) {
-    tok0 = t * kDdTile;
-    return max(0, min(kDdTile, g.tpr - tok0));
+// Exclusive scan of one int per thread over the CTA; returns the thread's
+// prefix and writes the total.  Every thread of the CTA must call it.
+__device__ __forceinline__ int dd_block_scan(int v, int *warp_tot, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    total = warp_tot[nw - 1];
+    const int r = (w ? warp_tot[w - 1] : 0) + x - v;
+    __syncthreads();                                      // warp_tot reusable after return
+    return r;
 }
 
+// Element e of a tile with destination instance v: token i = e / k, slot
+// j = e % k, rank r = v / nl.  False for an instance outside [0, R*nl).
+__device__ __forceinline__ bool dd_elem(int e, int v, const DdGeo &g, int &i, int &j, int &r) {
+    i = (int)dd_quot((unsigned)e, g.dk);
+    j = e - i * g.k;
+    if ((unsigned)v >= (unsigned)(g.R * g.nl)) return false;
+    r = (int)dd_quot((unsigned)v, g.dnl);
+    return true;
+}
+
+// Rows per (tile, rank): lm[(i / 32) * R + r] gets bit i % 32 for every slot
+// of token i on rank r, so a token with several slots on one rank sets one
+// bit and the popcounts of a rank's words are its rows in the tile.  The
+// token bitmaps are built in shared memory (32-bit words, little-endian
+// halves of the 64-bit output words) and stored as the tile's contiguous run.
 template <int KB>
-__global__ void __launch_bounds__(kDdWarps * 32)
-k_dd_count(const int32_t *__restrict__ dst, int32_t *tile_cnt, unsigned long long *tok_dst,
-           int64_t *stats, WsHeader *hdr, DdGeo g, int64_t ntiles) {
-    extern __shared__ int ddc[];                           // [kDdWarps][R]
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tile = (int64_t)blockIdx.x * kDdWarps + w;
-    int *cnt = ddc + w * g.R;
-    for (int r = lane; r < g.R; r += 32) cnt[r] = 0;
-    __syncwarp();
-    if (tile >= ntiles) return;                            // whole warp (no block barrier below)
-    const int t = (int)(tile % g.tps), s = (int)((tile / g.tps) % g.R), l = (int)(tile / ((int64_t)g.tps * g.R));
-    int tok0;
-    const int ntok = tile_tokens(g, t, tok0);
-    long long rows = 0, rows_remote = 0, pairs_remote = 0;
+__global__ void __launch_bounds__(kDdTile)
+k_dd_count(const int32_t *__restrict__ dst, int32_t *__restrict__ tile_cnt,
+           unsigned long long *__restrict__ tok_dst, int64_t *stats, WsHeader *hdr, DdGeo g) {
+    extern __shared__ unsigned ddc[];
+    unsigned *lm = ddc;                                    // [kDdWarps][R] lane masks
+    unsigned *bm = ddc + kDdWarps * g.R;                   // [kDdTile][2*RW] token bitmaps
+    __shared__ int red[kDdWarps];
+    __shared__ int any_bad;
+    const DdTile d = dd_tile(g);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int n = d.ntok * g.k;
+    const int64_t tokb = (int64_t)d.s * g.tpr + d.tok0;
+    int v[KB];
+    dd_load<KB>(dst + (int64_t)d.l * g.npairs + tokb * g.k, n, v);
+    for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lm[x] = 0;
+    for (int x = tid; x < kDdTile * 2 * g.RW; x += kDdTile) bm[x] = 0;
+    if (tid == 0) any_bad = 0;
+    __syncthreads();
+    int pr = 0;
     bool bad = false;
-    for (int r0 = 0; r0 < ntok; r0 += 32) {
-        const int i = r0 + lane;
-        if (i >= ntok) continue;
-        const int64_t tok = (int64_t)s * g.tpr + tok0 + i;
-        int rk[KB];
-        unsigned long long m[KB];
-        token_rows<KB>(dst + (int64_t)l * g.npairs + tok * g.k, g.k, g.nl, g.R, rk, m, bad);
-        unsigned long long bits[kDdMaxRW];
 #pragma unroll
-        for (int x = 0; x < kDdMaxRW; ++x) bits[x] = 0;
-#pragma unroll
-        for (int j = 0; j < KB; ++j) {
-            if (rk[j] >= 0 && rk[j] != s) ++pairs_remote;
-            if (!m[j]) continue;
-            atomicAdd(&cnt[rk[j]], 1);
-            ++rows;
-            if (rk[j] != s) ++rows_remote;
-#pragma unroll
-            for (int x = 0; x < kDdMaxRW; ++x)
-                if (x == (rk[j] >> 6)) bits[x] |= 1ull << (rk[j] & 63);
+    for (int u = 0; u < KB; ++u) {
+        const int e = u * kDdTile + tid;
+        int i, j, r;
+        if (e >= n) continue;
+        if (dd_elem(e, v[u], g, i, j, r)) {
+            atomicOr(&lm[(i >> 5) * g.R + r], 1u << (i & 31));
+            atomicOr(&bm[i * 2 * g.RW + (r >> 5)], 1u << (r & 31));
+            pr += r != d.s;
+        } else {
+            bad = true;
         }
-        unsigned long long *td = tok_dst + ((int64_t)l * g.T + tok) * g.RW;
+    }
+    if (bad) any_bad = 1;
 #pragma unroll
-        for (int x = 0; x < kDdMaxRW; ++x)
-            if (x < g.RW) td[x] = bits[x];
+    for (int o = 16; o > 0; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
+    if (lane == 0) red[tid >> 5] = pr;
+    __syncthreads();
+    int32_t *out = tile_cnt + (int64_t)blockIdx.x * g.R;
+    for (int r = tid; r < g.R; r += kDdTile) {
+        int c = 0;
+#pragma unroll
+        for (int x = 0; x < kDdWarps; ++x) c += __popc(lm[x * g.R + r]);
+        out[r] = c;
     }
-    __syncwarp();
-    int32_t *out = tile_cnt + tile * g.R;
-    for (int r = lane; r < g.R; r += 32) out[r] = cnt[r];
-    for (int o = 16; o > 0; o >>= 1) {
-        rows += __shfl_xor_sync(0xffffffffu, rows, o);
-        rows_remote += __shfl_xor_sync(0xffffffffu, rows_remote, o);
-        pairs_remote += __shfl_xor_sync(0xffffffffu, pairs_remote, o);
+    // the tile's bitmaps are one contiguous run of ntok * RW words
+    unsigned long long *td = tok_dst + ((int64_t)d.l * g.T + tokb) * g.RW;
+    const int nw = d.ntok * g.RW;
+    for (int x = tid; x < nw; x += kDdTile)
+        td[x] = (unsigned long long)bm[2 * x] | ((unsigned long long)bm[2 * x + 1] << 32);
+    if (tid == 0) {
+        long long sum = 0;
+#pragma unroll
+        for (int w = 0; w < kDdWarps; ++w) sum += red[w];
+        if (sum) atomicAdd(reinterpret_cast<unsigned long long *>(stats + (int64_t)d.l * 4 + 3),
+                           (unsigned long long)sum);
+        if (any_bad) set_error(hdr, TOPO_ESTATE);
     }
-    if (lane == 0) {
-        unsigned long long *st = reinterpret_cast<unsigned long long *>(stats + (int64_t)l * 4);
-        atomicAdd(&st[0], (unsigned long long)rows);
-        atomicAdd(&st[2], (unsigned long long)rows_remote);
-        atomicAdd(&st[3], (unsigned long long)pairs_remote);
-    }
-    if (bad) set_error(hdr, TOPO_ESTATE);
 }
 
 // One thread per (layer, source, rank): tile counts -> exclusive prefix over
-// the source's tiles; the total -> send count.
+// the source's tiles (32 loads in flight per thread); the total -> send count.
 __global__ void __launch_bounds__(256)
 k_dd_prefix(int32_t *tile_cnt, int64_t *send, DdGeo g, int64_t ncols) {
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -135,120 +199,144 @@ k_dd_prefix(int32_t *tile_cnt, int64_t *send, DdGeo g, int64_t ncols) {
     const int64_t ls = c / g.R;                            // l * R + s
     int32_t *col = tile_cnt + ls * g.tps * g.R + r;
     int run = 0;
-    for (int t = 0; t < g.tps; ++t) {
-        const int v = col[(int64_t)t * g.R];
-        col[(int64_t)t * g.R] = run;
-        run += v;
+    for (int t0 = 0; t0 < g.tps; t0 += 32) {
+        int v[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) v[u] = t0 + u < g.tps ? col[(int64_t)(t0 + u) * g.R] : 0;
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+            if (t0 + u < g.tps) {
+                col[(int64_t)(t0 + u) * g.R] = run;
+                run += v[u];
+            }
     }
     send[c] = run;
 }
 
-// One CTA per layer: src_base[l][s][r] = rows to rank r from sources before s;
-// seg[l][r] = rows to ranks before r; stats[l][1] = pairs.
-__global__ void __launch_bounds__(1024)
-k_dd_seg(const int64_t *__restrict__ send, int32_t *src_base, int32_t *seg, int64_t *stats, DdGeo g) {
-    __shared__ int tot[1024];
-    __shared__ int carry;
-    const int l = blockIdx.x;
-    if (threadIdx.x == 0) {
-        carry = 0;
-        stats[(int64_t)l * 4 + 1] = g.npairs;
-    }
-    for (int r0 = 0; r0 < g.R; r0 += blockDim.x) {
-        const int r = r0 + threadIdx.x;
-        int run = 0;
-        if (r < g.R)
-            for (int s = 0; s < g.R; ++s) {
-                const int64_t i = ((int64_t)l * g.R + s) * g.R + r;
-                src_base[i] = run;
-                run += (int)send[i];
-            }
-        tot[threadIdx.x] = r < g.R ? run : 0;
-        __syncthreads();
-        if (threadIdx.x == 0) {                            // prefix of this chunk of ranks
-            int c = carry;
-            for (int x = 0; x < (int)blockDim.x && r0 + x < g.R; ++x) {
-                const int v = tot[x];
-                seg[(int64_t)l * (g.R + 1) + r0 + x] = c;
-                c += v;
-            }
-            carry = c;
+// One CTA per layer, one thread per rank r: src_base[l][s][r] = rows to rank
+// r from sources before s (32 loads in flight); seg[l][r] = rows to ranks
+// before r (CTA scan); stats[l][0..2] = rows, pairs, rows to another rank.
+__global__ void __launch_bounds__(kDdSegThreads)
+k_dd_seg(const int64_t *__restrict__ send, int32_t *__restrict__ src_base, int32_t *seg, int64_t *stats,
+         DdGeo g) {
+    __shared__ int warp_tot[32];
+    const int l = blockIdx.x, r = threadIdx.x;
+    int run = 0, local = 0;
+    if (r < g.R) {
+        const int64_t *col = send + (int64_t)l * g.R * g.R + r;
+        int32_t *sb = src_base + (int64_t)l * g.R * g.R + r;
+        for (int s0 = 0; s0 < g.R; s0 += 32) {
+            int v[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = s0 + u < g.R ? (int)col[(int64_t)(s0 + u) * g.R] : 0;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                if (s0 + u < g.R) {
+                    sb[(int64_t)(s0 + u) * g.R] = run;
+                    run += v[u];
+                    if (s0 + u == r) local = v[u];
+                }
         }
-        __syncthreads();
     }
-    if (threadIdx.x == 0) seg[(int64_t)l * (g.R + 1) + g.R] = carry;
+    int total;
+    const int pre = dd_block_scan(run, warp_tot, total);
+    int loc_total;
+    dd_block_scan(local, warp_tot, loc_total);
+    if (r < g.R) seg[(int64_t)l * (g.R + 1) + r] = pre;
+    if (r == 0) {
+        seg[(int64_t)l * (g.R + 1) + g.R] = total;
+        stats[(int64_t)l * 4 + 0] = total;
+        stats[(int64_t)l * 4 + 1] = g.npairs;
+        stats[(int64_t)l * 4 + 2] = total - loc_total;
+    }
 }
 
 template <int KB>
-__global__ void __launch_bounds__(kDdWarps * 32)
+__global__ void __launch_bounds__(kDdTile, kDdFillCtas)
 k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
-          const int32_t *__restrict__ src_base, const int32_t *__restrict__ seg, int32_t *row_token,
-          unsigned long long *row_slots, DdGeo g, int64_t ntiles) {
-    extern __shared__ int ddf[];                           // [kDdWarps][3][R]
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tile = (int64_t)blockIdx.x * kDdWarps + w;
-    if (tile >= ntiles) return;                            // whole warp
-    int *gb = ddf + w * 3 * g.R;                           // row position base per rank
-    unsigned *msk = reinterpret_cast<unsigned *>(gb + g.R);
-    int *base = gb + 2 * g.R;                              // rows already placed in this tile
-    const int t = (int)(tile % g.tps), s = (int)((tile / g.tps) % g.R), l = (int)(tile / ((int64_t)g.tps * g.R));
-    for (int r = lane; r < g.R; r += 32) {
-        gb[r] = __ldg(seg + (int64_t)l * (g.R + 1) + r) +
-                __ldg(src_base + ((int64_t)l * g.R + s) * g.R + r) + __ldg(tile_pre + tile * g.R + r);
-        msk[r] = 0;
-        base[r] = 0;
-    }
-    __syncwarp();
-    int tok0;
-    const int ntok = tile_tokens(g, t, tok0);
-    const unsigned bit = 1u << lane, lt = bit - 1u;
-    int32_t *rt = row_token + (int64_t)l * g.npairs;
-    unsigned long long *rs = row_slots + (int64_t)l * g.npairs;
-    for (int r0 = 0; r0 < ntok; r0 += 32) {
-        const int i = r0 + lane;
-        const bool vt = i < ntok;
-        const int64_t tok = (int64_t)s * g.tpr + tok0 + i;
-        int rk[KB];
-        unsigned long long m[KB];
-        bool bad = false;
-        if (vt) {
-            token_rows<KB>(dst + (int64_t)l * g.npairs + tok * g.k, g.k, g.nl, g.R, rk, m, bad);
-        } else {
+          const int32_t *__restrict__ src_base, const int32_t *__restrict__ seg,
+          int32_t *__restrict__ row_token, unsigned long long *__restrict__ row_slots, DdGeo g) {
+    extern __shared__ unsigned ddf[];
+    unsigned *lm = ddf;                                    // [kDdWarps][R] lane masks
+    int *base = reinterpret_cast<int *>(lm + kDdWarps * g.R);   // [kDdWarps][R] tile positions
+    int *dlt = base + kDdWarps * g.R;                      // [R] global - tile position
+    unsigned *srow = reinterpret_cast<unsigned *>(dlt + g.R);   // [kDdTile*KB] token | slots << 8
+    unsigned short *srk = reinterpret_cast<unsigned short *>(srow + kDdTile * KB);  // row rank
+    __shared__ int warp_tot[32];
+    const DdTile d = dd_tile(g);
+    const int tid = threadIdx.x;
+    const int n = d.ntok * g.k;
+    const int64_t tokb = (int64_t)d.s * g.tpr + d.tok0;
+    int v[KB];
+    dd_load<KB>(dst + (int64_t)d.l * g.npairs + tokb * g.k, n, v);
+    for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lm[x] = 0;
 #pragma unroll
-            for (int j = 0; j < KB; ++j) { rk[j] = -1; m[j] = 0; }
+    for (int u = 0; u < KB; ++u) srow[u * kDdTile + tid] = 0;
+    __syncthreads();
+    // element -> packed rank | token << 10 | slot << 18; -1 for padding and
+    // invalid elements (those are flagged by k_dd_count)
+    int pk[KB];
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+        const int e = u * kDdTile + tid;
+        int i = 0, j = 0, r = -1;
+        pk[u] = -1;
+        if (e < n && dd_elem(e, v[u], g, i, j, r)) {
+            pk[u] = r | (i << 10) | (j << 18);
+            atomicOr(&lm[(i >> 5) * g.R + r], 1u << (i & 31));
         }
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-            if (m[j]) atomicOr(&msk[rk[j]], bit);
-        __syncwarp();
-        int nb[KB];
-        unsigned lead = 0;
-#pragma unroll
-        for (int j = 0; j < KB; ++j) {
-            nb[j] = 0;
-            if (!m[j]) continue;
-            const unsigned mm = msk[rk[j]];
-            const int b = base[rk[j]];
-            const int rank = __popc(mm & lt);
-            if (rank == 0) {
-                lead |= 1u << j;
-                nb[j] = b + __popc(mm);
-            }
-            const int64_t pos = (int64_t)gb[rk[j]] + b + rank;
-            if (pos >= 0 && pos < g.npairs) {
-                rt[pos] = (int32_t)tok;
-                rs[pos] = m[j];
-            }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-            if ((lead >> j) & 1u) {
-                base[rk[j]] = nb[j];
-                msk[rk[j]] = 0;
-            }
-        __syncwarp();
     }
+    __syncthreads();
+    // tile positions: ranks in consecutive chunks of q per thread, scanned over the CTA
+    const int q = (g.R + kDdTile - 1) / kDdTile;
+    const int r0 = min(tid * q, g.R), r1 = min(r0 + q, g.R);
+    int mine = 0;
+    for (int r = r0; r < r1; ++r)
+#pragma unroll
+        for (int x = 0; x < kDdWarps; ++x) mine += __popc(lm[x * g.R + r]);
+    int nrows;
+    int run = dd_block_scan(mine, warp_tot, nrows);
+    const int64_t tile = blockIdx.x;
+    for (int r = r0; r < r1; ++r) {
+        dlt[r] = __ldg(seg + (int64_t)d.l * (g.R + 1) + r) +
+                 __ldg(src_base + ((int64_t)d.l * g.R + d.s) * g.R + r) +
+                 __ldg(tile_pre + tile * g.R + r) - run;
+#pragma unroll
+        for (int x = 0; x < kDdWarps; ++x) {
+            base[x * g.R + r] = run;
+            run += __popc(lm[x * g.R + r]);
+        }
+    }
+    __syncthreads();
+    // a row's position: its rank's tile base for the token's 32-group, plus
+    // the group's earlier tokens with that rank; every slot ORs its bit in
+#pragma unroll
+    for (int u = 0; u < KB; ++u)
+        if (pk[u] >= 0) {
+            const int r = pk[u] & 1023, i = (pk[u] >> 10) & 255, j = pk[u] >> 18;
+            const int x = (i >> 5) * g.R + r;
+            const int p = base[x] + __popc(lm[x] & ((1u << (i & 31)) - 1u));
+            atomicOr(&srow[p], (unsigned)i | (1u << (j + 8)));
+            srk[p] = (unsigned short)r;
+        }
+    __syncthreads();
+    // consecutive threads write consecutive rows: runs of one rank are contiguous
+    int32_t *rt = row_token + (int64_t)d.l * g.npairs;
+    unsigned long long *rs = row_slots + (int64_t)d.l * g.npairs;
+    for (int p = tid; p < nrows; p += kDdTile) {
+        const unsigned v = srow[p];
+        const int64_t pos = (int64_t)dlt[srk[p]] + p;
+        if (pos >= 0 && pos < g.npairs) {
+            rt[pos] = (int32_t)(tokb + (v & 255u));
+            rs[pos] = v >> 8;
+        }
+    }
+}
+
+template <int KB>
+size_t dd_fill_smem(const DdGeo &g) {
+    return (size_t)2 * kDdWarps * g.R * 4 + (size_t)g.R * 4 + (size_t)kDdTile * KB * 4 +
+           (size_t)kDdTile * KB * 2;
 }
 
 template <int KB>
@@ -257,23 +345,21 @@ cudaError_t run_dedup(const DdGeo &g, const int32_t *dst, int32_t *seg, int32_t 
                       int32_t *tile_cnt, int32_t *src_base, WsHeader *hdr, cudaStream_t st) {
     cudaError_t e;
     const int64_t ntiles = (int64_t)g.L * g.R * g.tps;
-    const unsigned blocks = (unsigned)((ntiles + kDdWarps - 1) / kDdWarps);
     unsigned long long *ts = reinterpret_cast<unsigned long long *>(tok_dst);
     unsigned long long *rs = reinterpret_cast<unsigned long long *>(row_slots);
     if ((e = cudaMemsetAsync(stats, 0, (size_t)g.L * 4 * 8, st)) != cudaSuccess) return e;
-    const size_t smc = (size_t)kDdWarps * g.R * 4;
+    const size_t smc = (size_t)kDdWarps * g.R * 4 + (size_t)kDdTile * 2 * g.RW * 4;
     if ((e = ensure_smem((const void *)k_dd_count<KB>, smc)) != cudaSuccess) return e;
-    k_dd_count<KB><<<blocks, kDdWarps * 32, smc, st>>>(dst, tile_cnt, ts, stats, hdr, g, ntiles);
+    k_dd_count<KB><<<(unsigned)ntiles, kDdTile, smc, st>>>(dst, tile_cnt, ts, stats, hdr, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t ncols = (int64_t)g.L * g.R * g.R;
     k_dd_prefix<<<(unsigned)((ncols + 255) / 256), 256, 0, st>>>(tile_cnt, send, g, ncols);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_dd_seg<<<g.L, 1024, 0, st>>>(send, src_base, seg, stats, g);
+    k_dd_seg<<<g.L, kDdSegThreads, 0, st>>>(send, src_base, seg, stats, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smf = (size_t)kDdWarps * 3 * g.R * 4;
+    const size_t smf = dd_fill_smem<KB>(g);
     if ((e = ensure_smem((const void *)k_dd_fill<KB>, smf)) != cudaSuccess) return e;
-    k_dd_fill<KB><<<blocks, kDdWarps * 32, smf, st>>>(dst, tile_cnt, src_base, seg, row_token, rs, g,
-                                                      ntiles);
+    k_dd_fill<KB><<<(unsigned)ntiles, kDdTile, smf, st>>>(dst, tile_cnt, src_base, seg, row_token, rs, g);
     return cudaGetLastError();
 }
 
@@ -299,6 +385,8 @@ cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t
     if (d.tps < 1) d.tps = 1;
     d.RW = (g.R + 63) / 64;
     d.npairs = g.npairs;
+    d.dk = dd_div((unsigned)(g.k > 0 ? g.k : 1));
+    d.dnl = dd_div((unsigned)g.n_local);
     size_t off_tile = 0, off_src = 0;
     dedup_ws_bytes(g, &off_tile, &off_src);
     int32_t *tile_cnt = ws_at<int32_t>(ws, off_tile);
