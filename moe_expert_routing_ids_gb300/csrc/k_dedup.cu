@@ -6,19 +6,22 @@
 // One row per (token, destination rank), ordered by rank, then by token.  A
 // row carries its token and the mask of the token's slots whose instance is
 // on that rank (the first slot with a rank stands for the row).  Tiles of
-// kDdTile tokens inside one source, one CTA per tile and one thread per token;
-// each tile's destinations are first staged slot-major in shared memory by
-// coalesced loads of the tile's contiguous run of k*tokens ints:
-//   k_dd_count  distinct ranks per token -> rows per (tile, rank), the token
-//               bitmaps, and the pairs sent to another rank
+// kDdTile tokens inside one source, one CTA per tile; thread x takes the
+// tile's (token, slot) elements x, x + kDdTile, ... of the tile's contiguous
+// run of k * tokens ints (coalesced loads, all issued before any use):
+//   k_dd_count  per-rank lane masks of the tile's 32-token groups (shared
+//               atomicOr of the token's lane bit: a token with several
+//               slots on one rank sets it once) -> rows per (tile, rank);
+//               the token bitmaps; the pairs sent to another rank
 //   k_dd_prefix per (layer, source, rank): tile counts -> exclusive prefix,
 //               total -> send counts
 //   k_dd_seg    per layer: per-source bases of every rank, the rank segment
 //               offsets, and the row statistics
-//   k_dd_fill   rows ranked in token order inside the tile (per-warp lane
-//               bitmasks per rank, prefixed over warps), staged in shared
-//               memory in (rank, token) order, then written out so that
-//               consecutive threads write consecutive rows of one rank
+//   k_dd_fill   the same lane masks, prefixed over ranks and groups (CTA
+//               scan), give each row its place in (rank, token) order inside
+//               the tile; every slot ORs its bit into the row staged in
+//               shared memory, and consecutive threads write consecutive
+//               rows, so runs of one rank leave as contiguous stores
 #include <cuda_runtime.h>
 
 #include "common.cuh"
