@@ -89,7 +89,9 @@ def _load():
             lib.oracle_combine.argtypes = [ci, ci, ci, ci, u16p, i32p, f32p, u16p]
             u64p = np.ctypeslib.ndpointer(np.uint64, flags="C_CONTIGUOUS")
             lib.oracle_dedup.argtypes = [ci, ci, ci, ci, ci, i32p, i32p, i32p, u64p, u64p, i64p, i64p]
-            for f in ("oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
+            lib.oracle_gate.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_void_p, ctypes.c_void_p,
+                                        i32p, f32p, i32p]
+            for f in ("oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
                       "oracle_layout", "oracle_permute", "oracle_combine", "oracle_dedup"):
                 getattr(lib, f).restype = ci
             _lib = lib
@@ -110,6 +112,35 @@ def _check(fn, rc, allow=(OK,)):
     if rc not in allow:
         raise OracleError(fn, rc)
     return rc
+
+
+def gate(logits, k: int, R: int, bias=None):
+    """Top-k gating and Omega [TopoEP §2.1, §6.4; O1].
+
+    logits: float32 [L, T, E] (or [T, E]), or uint16 bf16 patterns of that
+    shape.  bias: float32 [E] or None.  Returns dict with ids int32 [L, T, k],
+    scores float32 [L, T, k] (raw logits of the selected experts) and hist
+    int32 [L, R, E] (without the leading L for a 2-D input)."""
+    a = np.asarray(logits)
+    if a.dtype not in (np.float32, np.uint16):
+        raise TypeError("logits must be float32 or uint16 bf16 patterns")
+    a = np.ascontiguousarray(a)
+    squeeze = a.ndim == 2
+    if squeeze:
+        a = a[None]
+    L, T, E = a.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if b is not None and b.shape != (E,):
+        raise ValueError("bias must be float32 [E]")
+    out = dict(ids=np.zeros((L, T, k), np.int32), scores=np.zeros((L, T, k), np.float32),
+               hist=np.zeros((L, R, E), np.int32))
+    _check("oracle_gate", _load().oracle_gate(
+        T, E, k, R, L, int(a.dtype == np.uint16), a.ctypes.data_as(ctypes.c_void_p),
+        None if b is None else b.ctypes.data_as(ctypes.c_void_p), out["ids"].reshape(-1),
+        out["scores"].reshape(-1), out["hist"].reshape(-1)))
+    if squeeze:
+        out = {key: v[0] for key, v in out.items()}
+    return out
 
 
 def hist(ids, R: int, E: int):

@@ -8,7 +8,8 @@
  *
  * Sources (page title, section / equation / figure):
  *   [TopoEP]  "TopoEP: Topology-Aware Load Balancing for Expert-Parallel MoE
- *             Training" -- §4.1 (system model, Eqs. 3-4), §4.2 (constraints
+ *             Training" -- §2.1 (Top-k gating), §6.4 (synthetic routing from
+ *             biased random logits), §4.1 (system model, Eqs. 3-4), §4.2 (constraints
  *             C1-C5, Eqs. 5-8), §4.3 (two-stage solver, Eqs. 9-10, Fig. 9),
  *             §2.3 (Fig. 3 byte accounting), §5 (receive counts on the GPU).
  *   [Zyphra]  "Expert Coupling in MoE Pretraining" -- sections "Experts Are
@@ -36,7 +37,7 @@
  *
  * Return codes: 0 ok, -1 bad argument, -2 an id outside [0, E).
  *
- * Floating point (permute and combine only): bf16 values are 16-bit
+ * Floating point (gating, permute and combine only): bf16 values are 16-bit
  * patterns, widened to float by appending 16 zero bits and narrowed by
  * round-to-nearest-even; products and sums are separate float operations
  * (built with -ffp-contract=off, so no multiply-add is fused).
@@ -131,6 +132,58 @@ int oracle_hist(int T, int E, int k, int R, int n_layers, const int32_t *ids,
         }
     }
     return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O0  Top-k gating [TopoEP §2.1: for each token a trainable router selects  */
+/* the Top-k experts; §6.4: synthetic routing uses random logits with a      */
+/* fixed expert-specific bias], followed by O1 on the selected ids.          */
+/* Readings: score_{t,e} = logit_{t,e} + bias_e as one float addition (no    */
+/* addition without a bias); the k experts of the largest scores, in         */
+/* descending order; equal scores (-0 equals +0) go to the lower expert      */
+/* index; a NaN score ranks below every number, NaNs among themselves by     */
+/* index.  scores[t][j] is the raw logit of the j-th selected expert.        */
+/* logits are float32, or bf16 patterns widened by appending 16 zero bits.   */
+/* ------------------------------------------------------------------------ */
+
+/* Does score a of expert ia rank above score b of expert ib? */
+static int gate_above(float a, int ia, float b, int ib) {
+    int na = a != a, nb = b != b;
+    if (na != nb) return nb;             /* a number ranks above a NaN */
+    if (!na && a != b) return a > b;
+    return ia < ib;
+}
+
+int oracle_gate(int T, int E, int k, int R, int n_layers, int is_bf16, const void *logits,
+                const float *bias, int32_t *ids, float *scores, int32_t *hist) {
+    if (T < 0 || E < 1 || k < 1 || k > E || R < 1 || n_layers < 0 || T % R != 0)
+        return ORC_EINVAL;
+    float *raw = (float *)malloc(sizeof(float) * (size_t)E);
+    float *sc = (float *)malloc(sizeof(float) * (size_t)E);
+    char *taken = (char *)malloc((size_t)E);
+    if (!raw || !sc || !taken) { free(raw); free(sc); free(taken); return ORC_EINVAL; }
+    for (int64_t t = 0; t < (int64_t)n_layers * T; t++) {
+        for (int e = 0; e < E; e++) {
+            if (is_bf16) {
+                uint32_t w = (uint32_t)((const uint16_t *)logits)[t * E + e] << 16;
+                memcpy(&raw[e], &w, 4);
+            } else {
+                raw[e] = ((const float *)logits)[t * E + e];
+            }
+            sc[e] = bias ? raw[e] + bias[e] : raw[e];
+            taken[e] = 0;
+        }
+        for (int j = 0; j < k; j++) {
+            int best = -1;
+            for (int e = 0; e < E; e++)
+                if (!taken[e] && (best < 0 || gate_above(sc[e], e, sc[best], best))) best = e;
+            taken[best] = 1;
+            ids[t * k + j] = best;
+            scores[t * k + j] = raw[best];
+        }
+    }
+    free(raw); free(sc); free(taken);
+    return oracle_hist(T, E, k, R, n_layers, ids, hist);
 }
 
 /* ------------------------------------------------------------------------ */
