@@ -66,6 +66,10 @@ extern "C" {
 #define TOPO_CALL_PACK 7    /* topo_permute, topo_combine */
 #define TOPO_CALL_DEDUP 8   /* topo_dedup_layout */
 #define TOPO_DEDUP_STATS 4  /* int64 deduplicated-layout statistics per layer */
+#define TOPO_CALL_GATE 9    /* topo_gate_hist (the chain's workspace) */
+#define TOPO_DTYPE_F32 0    /* logits as float32 */
+#define TOPO_DTYPE_BF16 1   /* logits as bf16 bit patterns */
+#define TOPO_GATE_MAX_E 1024
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -126,6 +130,27 @@ int topo_ws_reset(void *ws, size_t ws_bytes, cudaStream_t stream);
  * Device errors: TOPO_ERANGE (the id is skipped). */
 int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t *hist,
               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Top-k gating fused with the routing matrix [TopoEP §2.1: per token the
+ * router selects the Top-k experts; §6.4: synthetic routing from random
+ * logits with a fixed expert-specific bias; Omega as in topo_hist].
+ * Readings: score[t][e] = logit[t][e] + bias[e] (one float addition; no bias
+ * when bias is NULL); ids[t] = the k experts of the largest scores, in
+ * descending order; equal scores (-0 equals +0) go to the lower expert; a NaN
+ * score ranks below every number.
+ * logits: device [n_layers][T][E], float32 (TOPO_DTYPE_F32) or bf16 bit
+ *         patterns (TOPO_DTYPE_BF16), aligned to its element size.
+ * bias:   device float32 [E] or NULL.
+ * ids:    device int32 [n_layers][T][k] (written).
+ * scores: device float32 [n_layers][T][k], the raw logits of the selected
+ *         experts, or NULL.
+ * hist:   device int32 [n_layers][R][E] (written, as topo_hist for ids).
+ * ws:     >= topo_workspace_bytes(cfg, n_layers, TOPO_CALL_GATE); receives the
+ *         tile index of ids, so topo_reroute / topo_reroute_layout may follow.
+ * Requires k <= E <= TOPO_GATE_MAX_E (else TOPO_EINVAL).  No device errors. */
+int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, int32_t logits_dtype,
+                   const float *bias, int32_t *ids, float *scores, int32_t *hist, void *ws,
+                   size_t ws_bytes, cudaStream_t stream);
 
 /* Expert co-selection and cross-layer transition counts ["Expert Coupling in
  * MoE Pretraining": within-layer correlation, cross-layer correlation]:

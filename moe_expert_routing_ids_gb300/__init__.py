@@ -26,13 +26,17 @@ TOPO_CALL_HIST, TOPO_CALL_PLAN, TOPO_CALL_REROUTE, TOPO_CALL_LAYOUT = 0, 1, 2, 3
 TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN, TOPO_CALL_REROUTE_LAYOUT = 4, 5, 6
 TOPO_CALL_PACK = 7
 TOPO_CALL_DEDUP = 8
+TOPO_CALL_GATE = 9
+TOPO_DTYPE_F32 = 0
+TOPO_DTYPE_BF16 = 1
+TOPO_GATE_MAX_E = 1024
 TOPO_DEDUP_STATS = 4
 TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
 EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
            "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine",
-           "topo_dedup_layout")
+           "topo_dedup_layout", "topo_gate_hist")
 TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -85,13 +89,14 @@ def lib():
             L.topo_hist_noalloc.argtypes = [cfgp, i32, vp, vp, vp, vp]
             L.topo_permute.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, sz, vp]
             L.topo_dedup_layout.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_gate_hist.argtypes = [cfgp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_combine.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
                       "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout"):
+                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout", "topo_gate_hist"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -193,6 +198,14 @@ def topo_hist_noalloc(cfg: TopoCfg, n_layers: int, ids, hist, err=None, stream=N
     err: optional device int32 that receives the device error word."""
     return _chk("topo_hist_noalloc", lib().topo_hist_noalloc(ctypes.byref(cfg), n_layers, _p(ids),
                                                              _p(hist), _p(err), _s(stream)))
+
+
+def topo_gate_hist(cfg: TopoCfg, n_layers: int, logits, logits_dtype: int, bias, ids, scores, hist,
+                   ws, ws_bytes: int, stream=None) -> int:
+    """Top-k gating of router logits (plus an optional expert bias) and Omega."""
+    return _chk("topo_gate_hist",
+                lib().topo_gate_hist(ctypes.byref(cfg), n_layers, _p(logits), logits_dtype, _p(bias),
+                                     _p(ids), _p(scores), _p(hist), _p(ws), ws_bytes, _s(stream)))
 
 
 def topo_dedup_layout(cfg: TopoCfg, n_layers: int, dst_inst, seg, row_token, row_slots, tok_dst,

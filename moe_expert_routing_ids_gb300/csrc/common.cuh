@@ -170,6 +170,14 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ---------------------------------------------------------------------------
 cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *ws, uint64_t fp,
                         cudaStream_t st);
+// Column prefix of the tile counts in ws (the tile index) and Omega; records
+// the hist fingerprint fp.  Shared by topo_hist and topo_gate_hist.
+cudaError_t launch_hist_prefix(const Geo &g, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st);
+// Top-k gating of logits [L][T][E] (float32, or bf16 patterns) plus bias,
+// writing ids, the selected raw logits (scores may be null) and the tile
+// counts, then launch_hist_prefix.
+cudaError_t launch_gate(const Geo &g, const void *logits, bool bf16, const float *bias, int32_t *ids,
+                        float *scores, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st);
 cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
                         const topo_plan_t &p, void *ws, cudaStream_t st);
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,

@@ -1,0 +1,306 @@
+// Top-k gating fused with the routing matrix ("TopoEP: Topology-Aware Load
+// Balancing for Expert-Parallel MoE Training" §2.1: per token the router
+// selects the Top-k experts; §6.4: synthetic routing from random logits with a
+// fixed expert-specific bias; Omega of the selection, §4.1 Eq. 3).
+//
+// score = logit + bias (one float addition); the k largest scores in
+// descending order, equal scores (-0 equals +0) to the lower expert, NaN below
+// every number.  One CTA per tile of TT tokens of one source (the tiles of
+// topo_hist), one warp per token at a time.  Lane l holds VPL scores of the
+// token: with 16-byte loads, chunk c = u * 32 + l of VEC consecutive experts;
+// otherwise experts u * 32 + l.
+//
+// Selection: the k-th largest of the 32 lane maxima (a warp bitonic sort) is
+// a lower bound tau of the k-th largest score, since k lanes each hold a
+// score >= tau.  Every score >= tau is a candidate -- typically a little more
+// than k -- and each candidate's place is the number of candidates ranking
+// above it.  When that shortcut cannot be taken (k > 32, more than
+// kGateCand candidates, or fewer than k because of NaN or padding) the warp
+// runs k rounds of an exact argmax instead.  The selected ids are counted in
+// shared memory and stored as the tile's counts; k_hist_prefix then builds
+// Omega and the tile index exactly as topo_hist does.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace topo {
+namespace {
+
+constexpr int kGateThreads = 256;
+constexpr int kGateWarps = kGateThreads / 32;
+constexpr int kGateCand = 64;               // candidate buffer per warp
+
+// Does (a, ia) rank above (b, ib)?  NaN below every number; ties by index.
+__device__ __forceinline__ bool g_above(float a, int ia, float b, int ib) {
+    const bool na = a != a, nb = b != b;
+    if (na != nb) return nb;
+    if (!na && a != b) return a > b;
+    return ia < ib;
+}
+
+template <bool BF>
+__device__ __forceinline__ float g_widen(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+// The raw logit of expert e of a token row (read again for a selected expert).
+template <bool BF>
+__device__ __forceinline__ float g_raw(const void *row, int e) {
+    if (BF) return g_widen<BF>(__ldg(reinterpret_cast<const unsigned short *>(row) + e));
+    return __ldg(reinterpret_cast<const float *>(row) + e);
+}
+
+// Raw logits of this lane's VPL slots of one token row (invalid slots 0).
+template <int VPL, bool BF, int VEC>
+__device__ __forceinline__ void g_load(const void *row, int E, int lane, float *x) {
+    if (VEC > 1) {
+#pragma unroll
+        for (int c = 0; c < VPL / VEC; ++c) {
+            const int ch = c * 32 + lane;
+            if (ch * VEC < E) {
+                if (BF) {
+                    const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(row) + ch);
+                    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        x[c * VEC + 2 * h] = __uint_as_float(q[h] << 16);
+                        x[c * VEC + 2 * h + 1] = __uint_as_float(q[h] & 0xffff0000u);
+                    }
+                } else {
+                    const float4 w = __ldcs(reinterpret_cast<const float4 *>(row) + ch);
+                    x[c * VEC] = w.x;
+                    x[c * VEC + 1] = w.y;
+                    x[c * VEC + 2] = w.z;
+                    x[c * VEC + 3] = w.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) x[c * VEC + i] = 0.f;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            const int e = u * 32 + lane;
+            x[u] = 0.f;
+            if (e < E) {
+                if (BF) x[u] = g_widen<BF>(__ldcs(reinterpret_cast<const unsigned short *>(row) + e));
+                else x[u] = __ldcs(reinterpret_cast<const float *>(row) + e);
+            }
+        }
+    }
+}
+
+template <int VPL, int VEC>
+__device__ __forceinline__ int g_expert(int u, int lane) {
+    return VEC > 1 ? ((u / VEC) * 32 + lane) * VEC + (u % VEC) : u * 32 + lane;
+}
+
+template <int VPL, bool BF, int VEC>
+__global__ void __launch_bounds__(kGateThreads, VPL >= 32 ? 2 : 3)
+k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, int32_t *__restrict__ ids,
+             float *__restrict__ scores, int32_t *__restrict__ tile_cnt, Geo g) {
+    extern __shared__ __align__(16) int gsm[];
+    float *sb = reinterpret_cast<float *>(gsm);                   // [E4] bias (E4 = E rounded up to 4)
+    const int E4 = (g.E + 3) & ~3;
+    int *cnt = gsm + E4;                                          // [E]
+    float *cs = reinterpret_cast<float *>(cnt + g.E);             // [warps][kGateCand] score
+    int *ci = reinterpret_cast<int *>(cs + kGateWarps * kGateCand);    // index
+    const int E = g.E, k = g.k;
+    const int tile = blockIdx.x;
+    const int t = tile % g.tps;
+    const int s = (tile / g.tps) % g.R;
+    const int l = tile / (g.tps * g.R);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += kGateThreads) cnt[e] = 0;
+    if (bias)
+        for (int e = threadIdx.x; e < E4; e += kGateThreads) sb[e] = e < E ? __ldg(bias + e) : 0.f;
+    float *ws = cs + w * kGateCand;
+    int *wi = ci + w * kGateCand;
+    unsigned valid = 0;                                           // this lane's slots inside [0, E)
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) valid |= (unsigned)(g_expert<VPL, VEC>(u, lane) < E) << u;
+    __syncthreads();                                              // cnt zeroed, bias staged
+
+    const int tok0 = t * g.TT;
+    const int ntok = max(0, min(g.TT, g.tpr - tok0));
+    const int64_t row0 = (int64_t)l * g.T + (int64_t)s * g.tpr + tok0;   // token row of the tile
+    const size_t esz = BF ? 2 : 4;
+    const char *base = reinterpret_cast<const char *>(logits);
+    float nx[VPL];
+    if (w < ntok) g_load<VPL, BF, VEC>(base + (size_t)(row0 + w) * E * esz, E, lane, nx);
+    for (int i = w; i < ntok; i += kGateWarps) {
+        const void *row = base + (size_t)(row0 + i) * E * esz;
+        float sc[VPL];                                            // scores, in place of the logits
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) sc[u] = nx[u];
+        if (i + kGateWarps < ntok)                                // next token in flight
+            g_load<VPL, BF, VEC>(base + (size_t)(row0 + i + kGateWarps) * E * esz, E, lane, nx);
+        if (bias) {                                               // same chunking as the loads
+            if (VEC > 1) {
+#pragma unroll
+                for (int c = 0; c < VPL / VEC; ++c) {
+                    const int ch = c * 32 + lane;
+                    if (ch * VEC < E)
+#pragma unroll
+                        for (int h = 0; h < VEC / 4; ++h) {
+                            const float4 bb = reinterpret_cast<const float4 *>(sb)[ch * (VEC / 4) + h];
+                            sc[c * VEC + 4 * h] += bb.x;
+                            sc[c * VEC + 4 * h + 1] += bb.y;
+                            sc[c * VEC + 4 * h + 2] += bb.z;
+                            sc[c * VEC + 4 * h + 3] += bb.w;
+                        }
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    if ((valid >> u) & 1u) sc[u] += sb[u * 32 + lane];
+            }
+        }
+        float m = -__int_as_float(0x7f800000);                    // -inf
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if ((valid >> u) & 1u) m = fmaxf(m, sc[u]);           // a NaN never wins fmaxf
+        // tau = k-th largest lane maximum (warp bitonic sort, descending)
+        float tau = -__int_as_float(0x7f800000);
+        if (k <= 32) {
+            float y = m;
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const float o = __shfl_xor_sync(0xffffffffu, y, stride);
+                    const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+                    y = keep_max ? fmaxf(y, o) : fminf(y, o);
+                }
+            tau = __shfl_sync(0xffffffffu, y, k - 1);
+        }
+        unsigned cm = 0;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) cm |= (unsigned)(((valid >> u) & 1u) && sc[u] >= tau) << u;
+        const int c = __popc(cm);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int n = __shfl_sync(0xffffffffu, incl, 31);
+        const int64_t tok = row0 + i;
+        int32_t *out_id = ids + tok * k;
+        float *out_sc = scores ? scores + tok * k : nullptr;
+        if (k <= 32 && n >= k && n <= kGateCand) {
+            int off = incl - c;
+#pragma unroll
+            for (int u = 0; u < VPL; ++u)
+                if ((cm >> u) & 1u) {
+                    ws[off] = sc[u];
+                    wi[off] = g_expert<VPL, VEC>(u, lane);
+                    ++off;
+                }
+            __syncwarp();
+            for (int q = lane; q < n; q += 32) {
+                const float v = ws[q];
+                const int e = wi[q];
+                int rank = 0;
+                for (int j = 0; j < n; ++j) {
+                    const float vj = ws[j];
+                    rank += vj > v || (vj == v && wi[j] < e);
+                }
+                if (rank < k) {
+                    out_id[rank] = e;
+                    if (out_sc) out_sc[rank] = bias ? g_raw<BF>(row, e) : v;
+                    atomicAdd(&cnt[e], 1);
+                }
+            }
+            __syncwarp();
+        } else {
+            // exact: k rounds of a warp argmax over the slots not yet taken
+            unsigned taken = 0;
+            for (int j = 0; j < k; ++j) {
+                float bv = 0.f;
+                int bi = -1;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    const int e = g_expert<VPL, VEC>(u, lane);
+                    if (((valid & ~taken) >> u) & 1u && (bi < 0 || g_above(sc[u], e, bv, bi))) {
+                        bv = sc[u];
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (oi >= 0 && (bi < 0 || g_above(ov, oi, bv, bi))) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    if (g_expert<VPL, VEC>(u, lane) == bi) taken |= 1u << u;
+                if (lane == 0) {
+                    out_id[j] = bi;
+                    if (out_sc) out_sc[j] = bias ? g_raw<BF>(row, bi) : bv;
+                    atomicAdd(&cnt[bi], 1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
+    for (int e = threadIdx.x; e < E; e += kGateThreads) mine[e] = cnt[e];
+}
+
+template <int VPL, bool BF, int VEC>
+cudaError_t run_gate(const Geo &g, const void *logits, const float *bias, int32_t *ids, float *scores,
+                     int32_t *tile_cnt, cudaStream_t st) {
+    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const size_t smem = (size_t)((g.E + 3) & ~3) * 4 + (size_t)g.E * 4 + (size_t)kGateWarps * kGateCand * 8;
+    cudaError_t e = ensure_smem((const void *)k_gate_tiles<VPL, BF, VEC>, smem);
+    if (e != cudaSuccess) return e;
+    k_gate_tiles<VPL, BF, VEC><<<(unsigned)tiles, kGateThreads, smem, st>>>(logits, bias, ids, scores,
+                                                                           tile_cnt, g);
+    return cudaGetLastError();
+}
+
+template <int VPL, bool BF>
+cudaError_t gate_vec(const Geo &g, const void *logits, const float *bias, int32_t *ids, float *scores,
+                     int32_t *tile_cnt, bool vec, cudaStream_t st) {
+    constexpr int V = BF ? 8 : 4;
+    if (vec && VPL % V == 0) return run_gate<VPL, BF, (VPL % V == 0 ? V : 1)>(g, logits, bias, ids, scores,
+                                                                              tile_cnt, st);
+    return run_gate<VPL, BF, 1>(g, logits, bias, ids, scores, tile_cnt, st);
+}
+
+template <bool BF>
+cudaError_t gate_vpl(const Geo &g, const void *logits, const float *bias, int32_t *ids, float *scores,
+                     int32_t *tile_cnt, bool vec, cudaStream_t st) {
+    const int vpl = (g.E + 31) / 32;
+    if (vpl <= 1) return gate_vec<1, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (vpl <= 2) return gate_vec<2, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (vpl <= 4) return gate_vec<4, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (vpl <= 8) return gate_vec<8, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (vpl <= 16) return gate_vec<16, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (vpl <= 32) return gate_vec<32, BF>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const Geo &g, const void *logits, bool bf16, const float *bias, int32_t *ids,
+                        float *scores, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st) {
+    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    if (tiles == 0) return cudaSuccess;
+    if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+    const size_t esz = bf16 ? 2 : 4;
+    const bool vec = ((uintptr_t)logits & 15) == 0 && ((size_t)g.E * esz) % 16 == 0;
+    int32_t *tile_cnt = ws_at<int32_t>(ws, g.off_tile);
+    cudaError_t e = bf16 ? gate_vpl<true>(g, logits, bias, ids, scores, tile_cnt, vec, st)
+                         : gate_vpl<false>(g, logits, bias, ids, scores, tile_cnt, vec, st);
+    if (e != cudaSuccess) return e;
+    return launch_hist_prefix(g, hist, ws, fp, st);
+}
+
+}  // namespace topo

@@ -120,9 +120,14 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     k_hist_tiles<<<(unsigned)tiles, kHistThreads, smem, st>>>(ids, ws_at<int32_t>(ws, g.off_tile), hdr, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_hist_prefix(g, hist, ws, fp, st);
+}
+
+cudaError_t launch_hist_prefix(const Geo &g, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st) {
     const int64_t cols = (int64_t)g.L * g.R * g.E;
+    if (cols == 0) return cudaSuccess;
     k_hist_prefix<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws_at<int32_t>(ws, g.off_tile), hist,
-                                                                  hdr, g, fp, cols);
+                                                                  ws_at<WsHeader>(ws, 0), g, fp, cols);
     return cudaGetLastError();
 }
 

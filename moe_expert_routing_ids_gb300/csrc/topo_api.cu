@@ -178,7 +178,7 @@ extern "C" {
 
 size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which_call) {
     if (which_call == TOPO_CALL_COOCCUR) return sizeof(WsHeader);
-    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_DEDUP) return 0;
+    if (which_call < TOPO_CALL_HIST || which_call > TOPO_CALL_GATE) return 0;
     Geo g;
     if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
     if (which_call == TOPO_CALL_PACK) return pack_ws_bytes(g);
@@ -200,6 +200,24 @@ int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
     return cuda_rc(launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream));
+}
+
+int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, int32_t logits_dtype,
+                   const float *bias, int32_t *ids, float *scores, int32_t *hist, void *ws,
+                   size_t ws_bytes, cudaStream_t stream) {
+    Geo g;
+    int rc = make_geo(cfg, n_layers, &g);
+    if (rc) return rc;
+    if (logits_dtype != TOPO_DTYPE_F32 && logits_dtype != TOPO_DTYPE_BF16) return TOPO_EINVAL;
+    if (cfg->k > cfg->E || cfg->E > TOPO_GATE_MAX_E) return TOPO_EINVAL;
+    if (!hist || !ws || (g.npairs > 0 && n_layers > 0 && (!logits || !ids))) return TOPO_EINVAL;
+    const uintptr_t esz = logits_dtype == TOPO_DTYPE_BF16 ? 2 : 4;
+    if (((uintptr_t)logits % esz) || ((uintptr_t)bias | (uintptr_t)ids | (uintptr_t)scores) % 4)
+        return TOPO_EINVAL;
+    if (ws_bytes < g.total) return TOPO_ENOSPC;
+    if (n_layers == 0) return TOPO_OK;
+    return cuda_rc(launch_gate(g, logits, logits_dtype == TOPO_DTYPE_BF16, bias, ids, scores, hist, ws,
+                               hist_fingerprint(g, ids), stream));
 }
 
 int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const topo_plan_t *plan,

@@ -9,9 +9,10 @@ import dataclasses
 
 import torch
 
-from . import (TOPO_CALL_CHAIN, TOPO_CALL_COOCCUR, TOPO_LAYOUT_STATS, TOPO_STATS, make_cfg,
-               make_plan, topo_cooccur, topo_dispatch_layout, topo_hist, topo_plan, topo_read_error,
-               topo_reroute, topo_reroute_layout, topo_workspace_bytes, topo_ws_reset)
+from . import (TOPO_CALL_CHAIN, TOPO_CALL_COOCCUR, TOPO_DTYPE_BF16, TOPO_DTYPE_F32, TOPO_LAYOUT_STATS,
+               TOPO_STATS, make_cfg, make_plan, topo_cooccur, topo_dispatch_layout, topo_gate_hist,
+               topo_hist, topo_plan, topo_read_error, topo_reroute, topo_reroute_layout,
+               topo_workspace_bytes, topo_ws_reset)
 
 
 @dataclasses.dataclass
@@ -76,6 +77,21 @@ class Planner:
     def hist(self, ids: torch.Tensor):
         topo_hist(self.cfg, self.L, ids, self.buf.hist, self.ws, self.ws_bytes, self._stream())
 
+    def gate_hist(self, logits: torch.Tensor, ids: torch.Tensor, bias: torch.Tensor | None = None,
+                  scores: torch.Tensor | None = None):
+        """Top-k gating of router logits (float32 or bfloat16 [L, T, E]) plus an
+        optional float32 expert bias into ids (int32 [L, T, k]), the selected
+        raw logits (float32 [L, T, k], optional) and the histogram; leaves the
+        tile index so that make_plan / reroute_layout(ids) can follow."""
+        if logits.dtype == torch.float32:
+            dt = TOPO_DTYPE_F32
+        elif logits.dtype == torch.bfloat16:
+            dt = TOPO_DTYPE_BF16
+        else:
+            raise TypeError("logits must be float32 or bfloat16")
+        topo_gate_hist(self.cfg, self.L, logits, dt, bias, ids, scores, self.buf.hist, self.ws,
+                       self.ws_bytes, self._stream())
+
     def make_plan(self, hist: torch.Tensor | None = None):
         h = self.buf.hist if hist is None else hist
         topo_plan(self.cfg, self.L, h, self.plan, self.ws, self.ws_bytes, self._stream())
@@ -106,6 +122,13 @@ class Planner:
             self.reroute(ids)
             self.layout()
 
+    def run_from_logits(self, logits: torch.Tensor, ids: torch.Tensor, bias: torch.Tensor | None = None,
+                        scores: torch.Tensor | None = None):
+        """Gating, plan, rerouting and dispatch layout from router logits."""
+        self.gate_hist(logits, ids, bias, scores)
+        self.make_plan()
+        self.reroute_layout(ids)
+
     def error(self) -> int:
         """Device error word (synchronises the device)."""
         torch.cuda.synchronize(self.device)
@@ -135,6 +158,13 @@ class Cooccur:
         topo_cooccur(self.L, self.T, self.E, self.k, ids, self.co,
                      self.tr if (self.tr is not None and self.L > 1) else None, self.ws,
                      self.ws_bytes, s)
+
+    def run_from_logits(self, logits: torch.Tensor, ids: torch.Tensor, bias: torch.Tensor | None = None,
+                        scores: torch.Tensor | None = None):
+        """Gating, plan, rerouting and dispatch layout from router logits."""
+        self.gate_hist(logits, ids, bias, scores)
+        self.make_plan()
+        self.reroute_layout(ids)
 
     def error(self) -> int:
         torch.cuda.synchronize(self.device)
