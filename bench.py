@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged
@@ -61,8 +61,10 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup"),
+    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate"),
                     help="run one secondary measurement alone and print it (for profiling)")
+    ap.add_argument("--microbatches", type=int, default=0,
+                    help="--only gate: microbatches of the workload to use (0 = all; 1 for ncu captures)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds the oracle steps should take in total")
     return ap.parse_args()
@@ -452,6 +454,61 @@ def secondary_pack(dev, stream, hbm_peak):
     return res
 
 
+def secondary_gate(dev, stream, hbm_peak, microbatches=0):
+    """topo_gate_hist on the T = 1048576, E = 512, k = 10, R = 128 workload, all
+    4 microbatches: router logits = standard Gumbel noise, bias = log of the
+    workload's Zipf(1.4) expert probabilities (random logits with a fixed
+    expert-specific bias), float32 (8.6 GB) and bf16 (4.3 GB), both far above
+    L2.  No score output.  Each call timed with CUDA events, median of 5 after
+    2 warm-up calls."""
+    import torch
+    import moe_expert_routing_ids_gb300 as topo
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    w = W.STRESS
+    L, T, E, k = w.n_layers, w.T, w.E, w.k
+    if microbatches:
+        L = min(L, microbatches)
+    P = Planner(w.plan_cfg, L, dev, stream=stream)
+    g = torch.Generator(device=dev).manual_seed(17)
+    x = torch.empty((L, T, E), dtype=torch.float32, device=dev)
+    x.uniform_(generator=g).clamp_(min=1e-12).log_().neg_().log_().neg_()
+    p = 1.0 / torch.arange(1, E + 1, dtype=torch.float64, device=dev) ** w.zipf_s
+    perm = torch.randperm(E, generator=g, device=dev)
+    bias = torch.log(p / p.sum())[perm].float()
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    res = {"workload": f"{w.name}, {L} microbatches", "timing":
+           "CUDA events around one call, median of 5 after 2 warm-up calls"}
+    for name in ("f32", "bf16"):
+        if name == "f32":
+            logits = x
+        else:
+            logits = x.to(torch.bfloat16)
+            del x                                   # only the bf16 copy stays referenced
+        times = []
+        for i in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                P.gate_hist(logits, ids, bias)
+                b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                times.append(a.elapsed_time(b))
+        if P.error() != 0:
+            raise RuntimeError("device error in the gating measurement")
+        ms = statistics.median(times)
+        # algorithmic: read the logits once, write the ids
+        nb = L * T * E * logits.element_size() + L * T * k * 4
+        gbs = nb / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "tokens_per_s": round(L * T / (ms * 1e-3), 1),
+                     "algorithmic_bytes": nb, "achieved_gbs": round(gbs, 1),
+                     "frac": round(gbs / hbm_peak, 4)}
+        del logits
+    res["gpu_launches_per_call"] = KERNELS_PER_CALL["gate"]
+    return res
+
+
 def secondary_dedup(P, w, dev, stream, hbm_peak):
     """topo_dedup_layout on the destinations of the timed workload (all its
     microbatches; dst_inst 168 MB > 129 MB L2).  The call timed with CUDA
@@ -499,7 +556,7 @@ def secondary_dedup(P, w, dev, stream, hbm_peak):
             "gpu_launches_per_call": KERNELS_PER_CALL["dedup"]}
 
 
-def run_only(name):
+def run_only(name, microbatches=0):
     """One secondary measurement on cuda:0, printed as its own JSON line."""
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
@@ -514,6 +571,8 @@ def run_only(name):
         res = secondary_cooccur(dev, stream, hbm)
     elif name == "pack":
         res = secondary_pack(dev, stream, hbm)
+    elif name == "gate":
+        res = secondary_gate(dev, stream, hbm, microbatches)
     else:
         w = W.STRESS
         P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
@@ -601,6 +660,7 @@ def run_ours(args, rank, world, local_rank):
         line["cooccur"] = secondary_cooccur(dev, stream, hbm)
         line["pack"] = secondary_pack(dev, stream, hbm)
         line["dedup"] = secondary_dedup(P, w, dev, stream, hbm)
+        line["gate"] = secondary_gate(dev, stream, hbm)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, ids)
     print(json.dumps(line), flush=True)
@@ -700,7 +760,7 @@ def main():
             __graft_entry__.build()
             if args.only:
                 if rank == 0:
-                    run_only(args.only)
+                    run_only(args.only, args.microbatches)
             else:
                 run_ours(args, rank, world, local_rank)
     finally:

@@ -43,7 +43,8 @@ __device__ __forceinline__ float g_widen(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
-// The raw logit of expert e of a token row (read again for a selected expert).
+// The raw logit of expert e of a token row (read again for a selected expert;
+// the row was just streamed, so it is normally still in L2).
 template <bool BF>
 __device__ __forceinline__ float g_raw(const void *row, int e) {
     if (BF) return g_widen<BF>(__ldg(reinterpret_cast<const unsigned short *>(row) + e));
@@ -96,17 +97,28 @@ __device__ __forceinline__ int g_expert(int u, int lane) {
     return VEC > 1 ? ((u / VEC) * 32 + lane) * VEC + (u % VEC) : u * 32 + lane;
 }
 
-template <int VPL, bool BF, int VEC>
+// Order key of a candidate score (never NaN) and its expert: the float's
+// sign-magnitude bits made monotone (-0 taken as +0), then the complement of
+// the expert, so that a larger key ranks above and every key is distinct.
+__device__ __forceinline__ unsigned long long g_key(float v, int e) {
+    uint32_t bits = __float_as_uint(v);
+    if (bits == 0x80000000u) bits = 0u;
+    const uint32_t k32 = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    return ((unsigned long long)k32 << 32) | (uint32_t)~e;
+}
+
+// FULL: E == 32 * VPL, every slot of every lane holds an expert.
+template <int VPL, bool BF, int VEC, bool FULL>
 __global__ void __launch_bounds__(kGateThreads, VPL >= 32 ? 2 : 3)
 k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, int32_t *__restrict__ ids,
              float *__restrict__ scores, int32_t *__restrict__ tile_cnt, Geo g) {
     extern __shared__ __align__(16) int gsm[];
-    float *sb = reinterpret_cast<float *>(gsm);                   // [E4] bias (E4 = E rounded up to 4)
-    const int E4 = (g.E + 3) & ~3;
-    int *cnt = gsm + E4;                                          // [E]
-    float *cs = reinterpret_cast<float *>(cnt + g.E);             // [warps][kGateCand] score
-    int *ci = reinterpret_cast<int *>(cs + kGateWarps * kGateCand);    // index
     const int E = g.E, k = g.k;
+    const int E4 = (E + 3) & ~3;
+    float *sb = reinterpret_cast<float *>(gsm);                   // [E4] bias
+    float *stash = sb + E4;                                       // [warps][32 * VPL] scores by expert
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(stash + kGateWarps * 32 * VPL);
+    int *cnt = reinterpret_cast<int *>(keys + kGateWarps * kGateCand);  // [E]
     const int tile = blockIdx.x;
     const int t = tile % g.tps;
     const int s = (tile / g.tps) % g.R;
@@ -115,11 +127,22 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
     for (int e = threadIdx.x; e < E; e += kGateThreads) cnt[e] = 0;
     if (bias)
         for (int e = threadIdx.x; e < E4; e += kGateThreads) sb[e] = e < E ? __ldg(bias + e) : 0.f;
-    float *ws = cs + w * kGateCand;
-    int *wi = ci + w * kGateCand;
-    unsigned valid = 0;                                           // this lane's slots inside [0, E)
+    float *wst = stash + w * 32 * VPL;
+    unsigned long long *wk = keys + w * kGateCand;
+    unsigned valid = FULL ? (VPL >= 32 ? 0xffffffffu : (1u << VPL) - 1u) : 0u;   // slots inside [0, E)
+    if (!FULL)
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) valid |= (unsigned)(g_expert<VPL, VEC>(u, lane) < E) << u;
+        for (int u = 0; u < VPL; ++u) valid |= (unsigned)(g_expert<VPL, VEC>(u, lane) < E) << u;
+    // bitonic directions of this lane, one bit per compare-exchange stage
+    unsigned kmax = 0;
+    {
+        int st = 0;
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1, ++st)
+                kmax |= (unsigned)(((lane & stride) == 0) == ((lane & size) == 0)) << st;
+    }
     __syncthreads();                                              // cnt zeroed, bias staged
 
     const int tok0 = t * g.TT;
@@ -141,7 +164,7 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
 #pragma unroll
                 for (int c = 0; c < VPL / VEC; ++c) {
                     const int ch = c * 32 + lane;
-                    if (ch * VEC < E)
+                    if (FULL || ch * VEC < E)
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             const float4 bb = reinterpret_cast<const float4 *>(sb)[ch * (VEC / 4) + h];
@@ -165,13 +188,13 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
         float tau = -__int_as_float(0x7f800000);
         if (k <= 32) {
             float y = m;
+            int st = 0;
 #pragma unroll
             for (int size = 2; size <= 32; size <<= 1)
 #pragma unroll
-                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int stride = size >> 1; stride > 0; stride >>= 1, ++st) {
                     const float o = __shfl_xor_sync(0xffffffffu, y, stride);
-                    const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
-                    y = keep_max ? fmaxf(y, o) : fminf(y, o);
+                    y = ((kmax >> st) & 1u) ? fmaxf(y, o) : fminf(y, o);
                 }
             tau = __shfl_sync(0xffffffffu, y, k - 1);
         }
@@ -190,26 +213,41 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
         int32_t *out_id = ids + tok * k;
         float *out_sc = scores ? scores + tok * k : nullptr;
         if (k <= 32 && n >= k && n <= kGateCand) {
-            int off = incl - c;
+            // the lane's scores by expert, so that its few candidates are read by index
+            if (c) {
+                if (VEC > 1) {
 #pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                if ((cm >> u) & 1u) {
-                    ws[off] = sc[u];
-                    wi[off] = g_expert<VPL, VEC>(u, lane);
-                    ++off;
+                    for (int q = 0; q < VPL / VEC; ++q) {
+                        const int ch = q * 32 + lane;
+                        if (FULL || ch * VEC < E)
+#pragma unroll
+                            for (int h = 0; h < VEC / 4; ++h)
+                                reinterpret_cast<float4 *>(wst)[ch * (VEC / 4) + h] =
+                                    make_float4(sc[q * VEC + 4 * h], sc[q * VEC + 4 * h + 1],
+                                                sc[q * VEC + 4 * h + 2], sc[q * VEC + 4 * h + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < VPL; ++u) wst[u * 32 + lane] = sc[u];
                 }
+                int off = incl - c;
+                unsigned mm = cm;
+                while (mm) {
+                    const int u = __ffs(mm) - 1;
+                    mm &= mm - 1u;
+                    const int e = g_expert<VPL, VEC>(u, lane);
+                    wk[off++] = g_key(wst[VEC > 1 ? e : u * 32 + lane], e);
+                }
+            }
             __syncwarp();
             for (int q = lane; q < n; q += 32) {
-                const float v = ws[q];
-                const int e = wi[q];
+                const unsigned long long key = wk[q];
                 int rank = 0;
-                for (int j = 0; j < n; ++j) {
-                    const float vj = ws[j];
-                    rank += vj > v || (vj == v && wi[j] < e);
-                }
+                for (int j = 0; j < n; ++j) rank += wk[j] > key;
                 if (rank < k) {
+                    const int e = (int)~(uint32_t)key;
                     out_id[rank] = e;
-                    if (out_sc) out_sc[rank] = bias ? g_raw<BF>(row, e) : v;
+                    if (out_sc) out_sc[rank] = g_raw<BF>(row, e);
                     atomicAdd(&cnt[e], 1);
                 }
             }
@@ -242,7 +280,7 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
                     if (g_expert<VPL, VEC>(u, lane) == bi) taken |= 1u << u;
                 if (lane == 0) {
                     out_id[j] = bi;
-                    if (out_sc) out_sc[j] = bias ? g_raw<BF>(row, bi) : bv;
+                    if (out_sc) out_sc[j] = g_raw<BF>(row, bi);
                     atomicAdd(&cnt[bi], 1);
                 }
             }
@@ -257,11 +295,19 @@ template <int VPL, bool BF, int VEC>
 cudaError_t run_gate(const Geo &g, const void *logits, const float *bias, int32_t *ids, float *scores,
                      int32_t *tile_cnt, cudaStream_t st) {
     const int64_t tiles = (int64_t)g.L * g.R * g.tps;
-    const size_t smem = (size_t)((g.E + 3) & ~3) * 4 + (size_t)g.E * 4 + (size_t)kGateWarps * kGateCand * 8;
-    cudaError_t e = ensure_smem((const void *)k_gate_tiles<VPL, BF, VEC>, smem);
+    const size_t smem = (size_t)((g.E + 3) & ~3) * 4 + (size_t)kGateWarps * 32 * VPL * 4 +
+                        (size_t)kGateWarps * kGateCand * 8 + (size_t)g.E * 4;
+    const bool full = g.E == 32 * VPL;
+    const void *fn = full ? (const void *)k_gate_tiles<VPL, BF, VEC, true>
+                          : (const void *)k_gate_tiles<VPL, BF, VEC, false>;
+    cudaError_t e = ensure_smem(fn, smem);
     if (e != cudaSuccess) return e;
-    k_gate_tiles<VPL, BF, VEC><<<(unsigned)tiles, kGateThreads, smem, st>>>(logits, bias, ids, scores,
-                                                                           tile_cnt, g);
+    if (full)
+        k_gate_tiles<VPL, BF, VEC, true><<<(unsigned)tiles, kGateThreads, smem, st>>>(logits, bias, ids, scores,
+                                                                                    tile_cnt, g);
+    else
+        k_gate_tiles<VPL, BF, VEC, false><<<(unsigned)tiles, kGateThreads, smem, st>>>(logits, bias, ids,
+                                                                                     scores, tile_cnt, g);
     return cudaGetLastError();
 }
 
