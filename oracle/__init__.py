@@ -91,7 +91,8 @@ def _load():
             lib.oracle_dedup.argtypes = [ci, ci, ci, ci, ci, i32p, i32p, i32p, u64p, u64p, i64p, i64p]
             lib.oracle_gate.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_void_p, ctypes.c_void_p,
                                         i32p, f32p, i32p]
-            for f in ("oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
+            lib.oracle_shuffle.argtypes = [ci, ci, ci, ci, ci, i32p, i64p, ctypes.c_void_p, i32p, i64p]
+            for f in ("oracle_shuffle", "oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
                       "oracle_layout", "oracle_permute", "oracle_combine", "oracle_dedup"):
                 getattr(lib, f).restype = ci
             _lib = lib
@@ -141,6 +142,30 @@ def gate(logits, k: int, R: int, bias=None):
     if squeeze:
         out = {key: v[0] for key, v in out.items()}
     return out
+
+
+SHUFFLE_STAT_NAMES = ("next_pairs_on_target", "next_pairs_on_source", "tokens_moved", "next_pairs")
+
+
+def shuffle(ids, tr, R: int, main_rank=None):
+    """Token-shuffle targets [Zyphra, "Moving Tokens Toward Their Next Experts"].
+
+    ids int32 [L, T, k]; tr int64 [L-1, E, E] (cooccur's transitions); main_rank
+    int32 [E] or None.  Returns (target int32 [L-1, T], stats int64 [L-1, 4])."""
+    a = _i32(ids)
+    L, T, k = a.shape
+    t = np.ascontiguousarray(tr, dtype=np.int64)
+    E = t.shape[-1] if t.size else int(a.max()) + 1
+    if L > 1 and t.shape != (L - 1, E, E):
+        raise ValueError("tr must be int64 [L-1, E, E]")
+    mr = None if main_rank is None else _i32(main_rank)
+    target = np.zeros((max(L - 1, 0), T), np.int32)
+    stats = np.zeros((max(L - 1, 0), 4), np.int64)
+    _check("oracle_shuffle", _load().oracle_shuffle(
+        L, T, E, k, R, a.reshape(-1), t.reshape(-1) if t.size else np.zeros(1, np.int64),
+        None if mr is None else mr.ctypes.data_as(ctypes.c_void_p), target.reshape(-1),
+        stats.reshape(-1)))
+    return target, stats
 
 
 def hist(ids, R: int, E: int):

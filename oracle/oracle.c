@@ -835,3 +835,71 @@ int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *
     free(mask);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Token-shuffle targets [Zyphra, "Moving Tokens Toward Their Next Experts": */
+/* the experts a token selected at one layer predict which GPU holds most of */
+/* its next experts, and the token is moved there before the next router].   */
+/* Readings: the prediction for layer l+1 uses layer l's ids and the         */
+/* transition counts tr_l (O2); the rank of an expert is its main rank       */
+/* (main_rank map, or e / (E/R) when NULL);                                  */
+/*   M_l[a][r]   = sum over experts b on rank r of tr_l[a][b],               */
+/*   score_r(t)  = sum over the token's slots j of M_l[ids_l[t][j]][r],       */
+/*   target_l[t] = the rank of the largest score; on a tie the token's own    */
+/*                 source rank src(t) if it is among the largest, else the    */
+/*                 lowest such rank.                                          */
+/* stats_l = {next-layer pairs whose expert is on target_l[t], next-layer    */
+/* pairs whose expert is on src(t), tokens with target != src, pairs}.       */
+/* ------------------------------------------------------------------------ */
+
+int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
+                   const int32_t *main_rank, int32_t *target, int64_t *stats) {
+    if (L < 0 || T < 0 || E < 1 || k < 1 || R < 1 || T % R != 0 || (!main_rank && E % R != 0))
+        return ORC_EINVAL;
+    int tpr = T / R, rc = ORC_OK;
+    int32_t *rank_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int64_t *M = (int64_t *)malloc(sizeof(int64_t) * (size_t)E * R);
+    int64_t *score = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+    if (!rank_of || !M || !score) { free(rank_of); free(M); free(score); return ORC_EINVAL; }
+    for (int e = 0; e < E; e++) {
+        rank_of[e] = main_rank ? main_rank[e] : e / (E / R);
+        if (rank_of[e] < 0 || rank_of[e] >= R) { free(rank_of); free(M); free(score); return ORC_EINVAL; }
+    }
+    for (int l = 0; l + 1 < L; l++) {
+        const int64_t *t_l = tr + (int64_t)l * E * E;
+        const int32_t *cur = ids + (int64_t)l * T * k, *nxt = ids + (int64_t)(l + 1) * T * k;
+        int64_t *st = stats + (int64_t)l * 4;
+        memset(M, 0, sizeof(int64_t) * (size_t)E * R);
+        for (int a = 0; a < E; a++)
+            for (int b = 0; b < E; b++) M[(int64_t)a * R + rank_of[b]] += t_l[(int64_t)a * E + b];
+        memset(st, 0, sizeof(int64_t) * 4);
+        for (int t = 0; t < T; t++) {
+            int s = t / tpr;
+            for (int r = 0; r < R; r++) score[r] = 0;
+            for (int j = 0; j < k; j++) {
+                int a = cur[(int64_t)t * k + j];
+                if (a < 0 || a >= E) { rc = ORC_ERANGE; continue; }
+                for (int r = 0; r < R; r++) score[r] += M[(int64_t)a * R + r];
+            }
+            int64_t mx = score[0];
+            for (int r = 1; r < R; r++)
+                if (score[r] > mx) mx = score[r];
+            int best = s;
+            if (score[s] != mx) {
+                best = 0;
+                while (score[best] != mx) best++;
+            }
+            target[(int64_t)l * T + t] = best;
+            if (best != s) st[2]++;
+            for (int j = 0; j < k; j++) {
+                int b = nxt[(int64_t)t * k + j];
+                if (b < 0 || b >= E) { rc = ORC_ERANGE; continue; }
+                if (rank_of[b] == best) st[0]++;
+                if (rank_of[b] == s) st[1]++;
+                st[3]++;
+            }
+        }
+    }
+    free(rank_of); free(M); free(score);
+    return rc;
+}
