@@ -70,6 +70,8 @@ extern "C" {
 #define TOPO_DTYPE_F32 0    /* logits as float32 */
 #define TOPO_DTYPE_BF16 1   /* logits as bf16 bit patterns */
 #define TOPO_GATE_MAX_E 1024
+#define TOPO_SHUFFLE_STATS 4
+#define TOPO_SHUFFLE_MAX_RANKS 256
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -151,6 +153,32 @@ int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t
 int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, int32_t logits_dtype,
                    const float *bias, int32_t *ids, float *scores, int32_t *hist, void *ws,
                    size_t ws_bytes, cudaStream_t stream);
+
+/* Token-shuffle targets ["Expert Coupling in MoE Pretraining", "Moving Tokens
+ * Toward Their Next Experts": a token's experts at one layer predict the GPU
+ * holding most of its next experts, and the token is moved there before the
+ * next router runs].  For each layer l < L-1 and token t:
+ *   M_l[a][r]   = sum of tr[l][a][b] over experts b with main rank r,
+ *   score_r     = sum over the token's slots j of M_l[ids[l][t][j]][r],
+ *   target[l][t] = the best rank; a tie keeps the token on its source rank
+ *                 t / (T/R) if that rank is among the best, else the lowest.
+ * ids:       device int32 [L][T][k].
+ * tr:        device int64 [L-1][E][E] (topo_cooccur's transitions, or counts
+ *            gathered elsewhere); the sums must fit int64.
+ * main_rank: device int32 [E] (experts per rank need not be equal here) or
+ *            NULL for e / (E/R).
+ * target:    device int32 [L-1][T] (written).
+ * stats:     device int64 [L-1][TOPO_SHUFFLE_STATS]: next-layer pairs whose
+ *            expert is on the target, next-layer pairs on the source rank,
+ *            tokens whose target is not their source, next-layer pairs.
+ * ws:        >= topo_shuffle_workspace_bytes(L, E, R).
+ * Requires T % R == 0, 1 <= R <= TOPO_SHUFFLE_MAX_RANKS, 1 <= k <= 64, and
+ * E % R == 0 without a map.  Device errors: TOPO_ERANGE (an id outside
+ * [0, E), skipped), TOPO_EMAP (a map entry outside [0, R), skipped). */
+size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R);
+int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, const int32_t *ids,
+                         const int64_t *tr, const int32_t *main_rank, int32_t *target, int64_t *stats,
+                         void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Expert co-selection and cross-layer transition counts ["Expert Coupling in
  * MoE Pretraining": within-layer correlation, cross-layer correlation]:

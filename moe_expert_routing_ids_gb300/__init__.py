@@ -30,13 +30,16 @@ TOPO_CALL_GATE = 9
 TOPO_DTYPE_F32 = 0
 TOPO_DTYPE_BF16 = 1
 TOPO_GATE_MAX_E = 1024
+TOPO_SHUFFLE_STATS = 4
+TOPO_SHUFFLE_MAX_RANKS = 256
 TOPO_DEDUP_STATS = 4
 TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
 EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
            "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine",
-           "topo_dedup_layout", "topo_gate_hist")
+           "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_workspace_bytes",
+           "topo_shuffle_targets")
 TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -90,13 +93,16 @@ def lib():
             L.topo_permute.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, sz, vp]
             L.topo_dedup_layout.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_gate_hist.argtypes = [cfgp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_shuffle_workspace_bytes.argtypes = [i32, i32, i32]
+            L.topo_shuffle_workspace_bytes.restype = sz
+            L.topo_shuffle_targets.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_combine.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
                       "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout", "topo_gate_hist"):
+                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_targets"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -198,6 +204,18 @@ def topo_hist_noalloc(cfg: TopoCfg, n_layers: int, ids, hist, err=None, stream=N
     err: optional device int32 that receives the device error word."""
     return _chk("topo_hist_noalloc", lib().topo_hist_noalloc(ctypes.byref(cfg), n_layers, _p(ids),
                                                              _p(hist), _p(err), _s(stream)))
+
+
+def topo_shuffle_workspace_bytes(L: int, E: int, R: int) -> int:
+    return int(lib().topo_shuffle_workspace_bytes(L, E, R))
+
+
+def topo_shuffle_targets(L: int, T: int, E: int, k: int, R: int, ids, tr, main_rank, target, stats, ws,
+                         ws_bytes: int, stream=None) -> int:
+    """Token-shuffle targets from cross-layer transition counts."""
+    return _chk("topo_shuffle_targets",
+                lib().topo_shuffle_targets(L, T, E, k, R, _p(ids), _p(tr), _p(main_rank), _p(target),
+                                           _p(stats), _p(ws), ws_bytes, _s(stream)))
 
 
 def topo_gate_hist(cfg: TopoCfg, n_layers: int, logits, logits_dtype: int, bias, ids, scores, hist,

@@ -178,6 +178,12 @@ cudaError_t launch_hist_prefix(const Geo &g, int32_t *hist, void *ws, uint64_t f
 // counts, then launch_hist_prefix.
 cudaError_t launch_gate(const Geo &g, const void *logits, bool bf16, const float *bias, int32_t *ids,
                         float *scores, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st);
+// Token-shuffle targets: ranks at most kShuffleMaxRanks.
+constexpr int kShuffleMaxRanks = 256;
+size_t shuffle_ws_bytes(int L, int E, int R);
+cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
+                           const int32_t *main_rank, int32_t *target, int64_t *stats, void *ws,
+                           cudaStream_t st);
 cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
                         const topo_plan_t &p, void *ws, cudaStream_t st);
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,

@@ -220,6 +220,26 @@ int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, in
                                hist_fingerprint(g, ids), stream));
 }
 
+size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R) {
+    if (L < 0 || E < 1 || R < 1 || R > TOPO_SHUFFLE_MAX_RANKS || E >= (1 << 26)) return 0;
+    return shuffle_ws_bytes(L, E, R);
+}
+
+int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, const int32_t *ids,
+                         const int64_t *tr, const int32_t *main_rank, int32_t *target, int64_t *stats,
+                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+    static_assert(TOPO_SHUFFLE_MAX_RANKS == kShuffleMaxRanks, "rank limit");
+    if (L < 0 || T < 0 || E < 1 || E >= (1 << 26) || k < 1 || k > kMaxK || R < 1 ||
+        R > TOPO_SHUFFLE_MAX_RANKS || T % R != 0 || (!main_rank && E % R != 0))
+        return TOPO_EINVAL;
+    if ((int64_t)L * T * k > ((int64_t)1 << 40)) return TOPO_EINVAL;
+    if (!ws) return TOPO_EINVAL;
+    if (ws_bytes < shuffle_ws_bytes(L, E, R)) return TOPO_ENOSPC;
+    if (L < 2) return TOPO_OK;
+    if (!tr || !stats || (T > 0 && (!ids || !target))) return TOPO_EINVAL;
+    return cuda_rc(launch_shuffle(L, T, E, k, R, ids, tr, main_rank, target, stats, ws, stream));
+}
+
 int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const topo_plan_t *plan,
               void *ws, size_t ws_bytes, cudaStream_t stream) {
     Geo g;

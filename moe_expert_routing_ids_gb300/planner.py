@@ -159,13 +159,6 @@ class Cooccur:
                      self.tr if (self.tr is not None and self.L > 1) else None, self.ws,
                      self.ws_bytes, s)
 
-    def run_from_logits(self, logits: torch.Tensor, ids: torch.Tensor, bias: torch.Tensor | None = None,
-                        scores: torch.Tensor | None = None):
-        """Gating, plan, rerouting and dispatch layout from router logits."""
-        self.gate_hist(logits, ids, bias, scores)
-        self.make_plan()
-        self.reroute_layout(ids)
-
     def error(self) -> int:
         torch.cuda.synchronize(self.device)
         return topo_read_error(self.ws)
