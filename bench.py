@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2, "shuffle": 2}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged
@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate"),
+    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle"),
                     help="run one secondary measurement alone and print it (for profiling)")
     ap.add_argument("--microbatches", type=int, default=0,
                     help="--only gate: microbatches of the workload to use (0 = all; 1 for ncu captures)")
@@ -390,6 +390,76 @@ def secondary_cooccur(dev, stream, hbm_peak):
             "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
 
 
+SHUFFLE_RANKS = 16           # EP16 over the co-occurrence workload's 128 experts
+
+
+def secondary_shuffle(dev, stream, hbm_peak):
+    """topo_shuffle_targets over the co-occurrence workload (8 layers of
+    262144 tokens, E = 128, k = 8) as EP16, with its own GPU transition
+    counts; L2 flushed (256 MB write) before each call; CUDA events inside one
+    captured graph per call, median of 10 after 3 warm-up replays.  Also the
+    prediction statistics of the four-layer workload, whose layers are
+    correlated."""
+    import torch
+    import moe_expert_routing_ids_gb300 as topo
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Cooccur
+    res = {}
+    for w, timed in ((W.COOCCUR, True), (W.FOUR_LAYER, False)):
+        R = SHUFFLE_RANKS if timed else w.R
+        L, T, E, k = w.n_layers, w.T, w.E, w.k
+        C = Cooccur(L, T, E, k, dev)
+        ids = torch.as_tensor(w.ids(), device=dev)
+        with torch.cuda.stream(stream):
+            C.run(ids, stream)
+        nb = topo.topo_shuffle_workspace_bytes(L, E, R)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        target = torch.empty((L - 1, T), dtype=torch.int32, device=dev)
+        stats = torch.empty((L - 1, topo.TOPO_SHUFFLE_STATS), dtype=torch.int64, device=dev)
+        s = stream.cuda_stream
+
+        def call():
+            topo.topo_shuffle_targets(L, T, E, k, R, ids, C.tr, None, target, stats, ws, nb, s)
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        if topo.topo_read_error(ws) != 0 or C.error() != 0:
+            raise RuntimeError("device error in the shuffle measurement")
+        st = stats.cpu().numpy().sum(axis=0)
+        entry = {"workload": f"{w.name} as EP{R}", "next_pairs_on_target": int(st[0]),
+                 "next_pairs_on_source": int(st[1]), "tokens_moved": int(st[2]),
+                 "next_pairs": int(st[3]),
+                 "locality_target": round(st[0] / max(st[3], 1), 4),
+                 "locality_source": round(st[1] / max(st[3], 1), 4)}
+        if timed:
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+            gev = GraphEvents(2)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                flush.fill_(1)
+                gev.record(0, stream)
+                call()
+                gev.record(1, stream)
+            times = []
+            for _ in range(13):
+                graph.replay()
+                torch.cuda.synchronize()
+                times.append(gev.elapsed(0, 1))
+            gev.close()
+            ms = statistics.median(times[3:])
+            # algorithmic: each layer's ids read as the current and as the next
+            # layer, the transitions, the targets written
+            nbytes = 2 * (L - 1) * T * k * 4 + (L - 1) * E * E * 8 + (L - 1) * T * 4
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            entry.update({"ms": round(ms, 4), "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / hbm_peak, 4), "l2": "flushed (256 MB write) before each call",
+                          "gpu_launches_per_call": KERNELS_PER_CALL["shuffle"]})
+            res["timed"] = entry
+        else:
+            res["correlated_layers"] = entry
+    return res
+
+
 PACK_WORKLOAD_H = 7168       # hidden size of the four-layer workload (bf16 rows)
 
 
@@ -573,6 +643,8 @@ def run_only(name, microbatches=0):
         res = secondary_pack(dev, stream, hbm)
     elif name == "gate":
         res = secondary_gate(dev, stream, hbm, microbatches)
+    elif name == "shuffle":
+        res = secondary_shuffle(dev, stream, hbm)
     else:
         w = W.STRESS
         P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
@@ -661,6 +733,7 @@ def run_ours(args, rank, world, local_rank):
         line["pack"] = secondary_pack(dev, stream, hbm)
         line["dedup"] = secondary_dedup(P, w, dev, stream, hbm)
         line["gate"] = secondary_gate(dev, stream, hbm)
+        line["shuffle"] = secondary_shuffle(dev, stream, hbm)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, ids)
     print(json.dumps(line), flush=True)

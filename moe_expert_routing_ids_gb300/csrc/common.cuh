@@ -106,6 +106,28 @@ __host__ __device__ inline T *ws_at(void *ws, size_t off) {
 // made while a stream is being captured into a CUDA graph, launch only.
 cudaError_t ensure_smem(const void *fn, size_t bytes);
 
+// n / d for n < 2^32 by a multiply-high with m = floor(2^32 / d) (2^32 - 1 for
+// d = 1), which gives the quotient or one less, and one correction step (the
+// reciprocal-multiplication method of Granlund and Montgomery, "Division by
+// Invariant Integers using Multiplication", with the correction in place of
+// the rounding analysis).
+struct FastDiv {
+    unsigned d, m;
+};
+
+inline FastDiv make_fast_div(unsigned d) {
+    FastDiv v;
+    v.d = d;
+    v.m = d <= 1 ? 0xffffffffu : (unsigned)((1ull << 32) / d);
+    return v;
+}
+
+__device__ __forceinline__ unsigned fast_quot(unsigned n, FastDiv v) {
+    unsigned q = __umulhi(n, v.m);
+    q += (n - q * v.d) >= v.d;
+    return q;
+}
+
 // Routing-index entry of one (source, instance) pair with a nonzero count:
 // the instance code r * n_local + l, the source's occurrences of the expert
 // routed there [cum_start, cum_end), and the layout position of occurrence

@@ -34,32 +34,10 @@ constexpr int kDdWarps = kDdTile / 32;    // 32-token groups of a tile
 constexpr int kDdSegThreads = kDedupMaxRanks;
 constexpr int kDdFillCtas = 6;            // resident fill CTAs per SM the registers must allow
 
-// n / d for n < 2^32 by a multiply-high with m = floor(2^32 / d) (2^32 - 1 for
-// d = 1), which gives the quotient or one less, and one correction step
-// (the reciprocal-multiplication method of Granlund and Montgomery, "Division
-// by Invariant Integers using Multiplication", with the correction in place of
-// the rounding analysis).
-struct DdDiv {
-    unsigned d, m;
-};
-
-__host__ inline DdDiv dd_div(unsigned d) {
-    DdDiv v;
-    v.d = d;
-    v.m = d == 1 ? 0xffffffffu : (unsigned)((1ull << 32) / d);
-    return v;
-}
-
-__device__ __forceinline__ unsigned dd_quot(unsigned n, DdDiv v) {
-    unsigned q = __umulhi(n, v.m);
-    q += (n - q * v.d) >= v.d;
-    return q;
-}
-
 struct DdGeo {
     int T, k, R, nl, tpr, tps, RW, L;
     int64_t npairs;
-    DdDiv dk, dnl;
+    FastDiv dk, dnl;
 };
 
 struct DdTile {
@@ -119,10 +97,10 @@ __device__ __forceinline__ int dd_block_scan(int v, int *warp_tot, int &total) {
 // Element e of a tile with destination instance v: token i = e / k, slot
 // j = e % k, rank r = v / nl.  False for an instance outside [0, R*nl).
 __device__ __forceinline__ bool dd_elem(int e, int v, const DdGeo &g, int &i, int &j, int &r) {
-    i = (int)dd_quot((unsigned)e, g.dk);
+    i = (int)fast_quot((unsigned)e, g.dk);
     j = e - i * g.k;
     if ((unsigned)v >= (unsigned)(g.R * g.nl)) return false;
-    r = (int)dd_quot((unsigned)v, g.dnl);
+    r = (int)fast_quot((unsigned)v, g.dnl);
     return true;
 }
 
@@ -388,8 +366,8 @@ cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t
     if (d.tps < 1) d.tps = 1;
     d.RW = (g.R + 63) / 64;
     d.npairs = g.npairs;
-    d.dk = dd_div((unsigned)(g.k > 0 ? g.k : 1));
-    d.dnl = dd_div((unsigned)g.n_local);
+    d.dk = make_fast_div((unsigned)(g.k > 0 ? g.k : 1));
+    d.dnl = make_fast_div((unsigned)g.n_local);
     size_t off_tile = 0, off_src = 0;
     dedup_ws_bytes(g, &off_tile, &off_src);
     int32_t *tile_cnt = ws_at<int32_t>(ws, off_tile);

@@ -9,10 +9,12 @@
 //                 that rank is among the best, else the lowest best rank.
 //
 // k_sh_table: one CTA per (layer, expert a) sums the row tr_l[a][.] by rank
-// (shared 64-bit atomics).  k_sh_target: a group of G lanes (G = the power of
-// two >= R, at most 32) scores one token, lane i holding ranks i, i + G, ...;
-// each slot's id is one broadcast load and its M row one contiguous read, so
-// a warp's groups read whole rows.  The best rank is a group shuffle
+// (shared 64-bit atomics).  For R <= 16, k_sh_target_t: one thread per token
+// (below).  Otherwise k_sh_target: a group of G lanes (G = the power of
+// two >= R, at most 32) scores kShIter tokens in turn, lane i holding ranks
+// i, i + G, ...; the group's lanes load a token's ids together (the next
+// token's already in flight) and pass each to all lanes by shuffle, and each
+// id's M row is one contiguous read, so a warp's groups read whole rows.  The best rank is a group shuffle
 // reduction; the next layer's slots on the target and on the source are
 // counted per lane and summed per CTA.
 #include <climits>
@@ -26,14 +28,16 @@ namespace {
 
 constexpr int kShThreads = 256;
 constexpr size_t kShSmemTable = 96 * 1024;   // largest M table staged in shared memory
+constexpr int kShIter = 16;                  // tokens per group per CTA
 
 struct ShGeo {
-    int L, T, E, k, R, tpr, er;      // er = E / R for the contiguous main map
+    int L, T, E, k, R;
+    FastDiv tpr, er;                 // tokens per source; E / R for the contiguous main map
     const int32_t *main_rank;
 };
 
 __device__ __forceinline__ int sh_rank(const ShGeo &g, int b) {
-    return g.main_rank ? __ldg(g.main_rank + b) : b / g.er;
+    return g.main_rank ? __ldg(g.main_rank + b) : (int)fast_quot((unsigned)b, g.er);
 }
 
 __global__ void __launch_bounds__(128)
@@ -58,9 +62,20 @@ k_sh_table(const int64_t *__restrict__ tr, int64_t *__restrict__ M, WsHeader *hd
     for (int r = threadIdx.x; r < g.R; r += blockDim.x) dst[r] = (int64_t)acc[r];
 }
 
-// RPL: ranks per lane (R <= G * RPL).  SMEM: the layer's table is staged in
-// shared memory (E * R * 8 bytes).
-template <int G, int RPL, bool SMEM>
+// A group's lanes hold a token's slots j = lane, lane + G, ... (KQ registers).
+template <int G, int KQ>
+__device__ __forceinline__ void sh_load_ids(const int32_t *row, int k, int gl, int *v) {
+#pragma unroll
+    for (int q = 0; q < KQ; ++q) {
+        const int j = gl + q * G;
+        v[q] = j < k ? __ldg(row + j) : -1;
+    }
+}
+
+// RPL: ranks per lane (R <= G * RPL).  KQ: slots per lane (k <= G * KQ).
+// SMEM: the layer's table is staged in shared memory (E * R * 8 bytes).
+// Each group scores kShIter tokens, the ids of the next one in flight.
+template <int G, int RPL, int KQ, bool SMEM>
 __global__ void __launch_bounds__(kShThreads)
 k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int32_t *__restrict__ target,
             int64_t *stats, WsHeader *hdr, ShGeo g, int blocks_per_layer) {
@@ -76,30 +91,50 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
     const long long *tp = SMEM ? tab : reinterpret_cast<const long long *>(Ml);
     const int lane = threadIdx.x & 31, gl = lane & (G - 1);
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
-    const int gpw = 32 / G;                                   // tokens per warp
-    const int warp = threadIdx.x >> 5;
-    const int64_t t = ((int64_t)blk * (kShThreads / 32) + warp) * gpw + lane / G;
-    long long on_tgt = 0, on_src = 0, moved = 0, pairs = 0;
+    constexpr int kGroups = kShThreads / G;                   // groups per CTA
+    const int grp = threadIdx.x / G;
+    const int64_t tok0 = (int64_t)blk * kGroups * kShIter;
+    int on_tgt = 0, on_src = 0, moved = 0, pairs = 0;           // per thread: < kShIter * KQ
     bool bad = false;
+    const int32_t *cur0 = ids + (int64_t)l * g.T * g.k;
+    const int32_t *nxt0 = ids + (int64_t)(l + 1) * g.T * g.k;
+    int ca[KQ], cb[KQ];                                       // this token's ids: layer l, l + 1
+    int64_t t = tok0 + grp;
     if (t < g.T) {
-        const int32_t *cur = ids + ((int64_t)l * g.T + t) * g.k;
-        const int32_t *nxt = ids + ((int64_t)(l + 1) * g.T + t) * g.k;
+        sh_load_ids<G, KQ>(cur0 + t * g.k, g.k, gl, ca);
+        sh_load_ids<G, KQ>(nxt0 + t * g.k, g.k, gl, cb);
+    }
+    for (int it = 0; it < kShIter && t < g.T; ++it, t += kGroups) {   // t uniform in the group
+        int a_cur[KQ], a_nxt[KQ];
+#pragma unroll
+        for (int q = 0; q < KQ; ++q) {
+            a_cur[q] = ca[q];
+            a_nxt[q] = cb[q];
+        }
+        const int64_t tn = t + kGroups;
+        if (it + 1 < kShIter && tn < g.T) {                   // the next token's ids in flight
+            sh_load_ids<G, KQ>(cur0 + tn * g.k, g.k, gl, ca);
+            sh_load_ids<G, KQ>(nxt0 + tn * g.k, g.k, gl, cb);
+        }
         long long sc[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) sc[i] = 0;
-        for (int j = 0; j < g.k; ++j) {
-            const int a = __ldg(cur + j);                    // the same address across the group
-            if ((unsigned)a >= (unsigned)g.E) {
-                bad = true;
-                continue;
-            }
-            const long long *row = tp + (int64_t)a * g.R;
 #pragma unroll
-            for (int i = 0; i < RPL; ++i) {
-                const int r = gl + i * G;
-                if (r < g.R) sc[i] += SMEM ? row[r] : __ldg(row + r);
+        for (int q = 0; q < KQ; ++q)
+            for (int jj = 0; jj < G; ++jj) {
+                if (q * G + jj >= g.k) break;
+                const int a = __shfl_sync(gmask, a_cur[q], jj, G);
+                if ((unsigned)a >= (unsigned)g.E) {
+                    bad = true;
+                    continue;
+                }
+                const long long *row = tp + (int64_t)a * g.R;
+#pragma unroll
+                for (int i = 0; i < RPL; ++i) {
+                    const int r = gl + i * G;
+                    if (r < g.R) sc[i] += SMEM ? row[r] : __ldg(row + r);
+                }
             }
-        }
         // the best (score, rank) of the lane, then of the group; lower rank on ties
         long long best = sc[0];
         int br = gl < g.R ? gl : 0;
@@ -122,17 +157,22 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
             }
         }
         // the source rank's own score, from the lane that holds it
-        const int s = (int)(t / g.tpr);
+        const int s = (int)fast_quot((unsigned)t, g.tpr);
         long long mine = 0;
 #pragma unroll
         for (int i = 0; i < RPL; ++i)
             if (gl + i * G == s) mine = sc[i];
         const long long ssc = __shfl_sync(gmask, mine, s % G, G);
         const int tg = ssc == best ? s : br;
-        if (gl == 0) target[(int64_t)l * g.T + t] = tg;
+        if (gl == 0) {
+            target[(int64_t)l * g.T + t] = tg;
+            moved += tg != s;
+        }
         // next-layer slots on the target and on the source
-        for (int j = gl; j < g.k; j += G) {
-            const int b = __ldg(nxt + j);
+#pragma unroll
+        for (int q = 0; q < KQ; ++q) {
+            const int b = a_nxt[q];
+            if (gl + q * G >= g.k) continue;
             if ((unsigned)b >= (unsigned)g.E) {
                 bad = true;
                 continue;
@@ -142,16 +182,16 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
             on_src += rb == s;
             ++pairs;
         }
-        if (gl == 0) moved = tg != s;
-    }                                   // a group past the end skips its shuffles as a whole
+    }
     if (bad) set_error(hdr, TOPO_ERANGE);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = 16; o > 0; o >>= 1) {                       // a warp's sums stay far below 2^31
         on_tgt += __shfl_xor_sync(0xffffffffu, on_tgt, o);
         on_src += __shfl_xor_sync(0xffffffffu, on_src, o);
         moved += __shfl_xor_sync(0xffffffffu, moved, o);
         pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
     }
+    const int warp = threadIdx.x >> 5;
     if (lane == 0) {
         red[0][warp] = on_tgt;
         red[1][warp] = on_src;
@@ -167,10 +207,136 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
     }
 }
 
-template <int G, int RPL>
-cudaError_t run_target(const ShGeo &g, const int32_t *ids, const int64_t *M, int32_t *target, int64_t *stats,
-                       WsHeader *hdr, cudaStream_t st) {
-    const int tok_per_block = (kShThreads / 32) * (32 / G);
+// One thread per token, for R <= 2 * RB <= 16 and k <= KV: the token's R
+// scores live in registers as RB pairs; the table rows are padded to 2 * RB
+// entries and read in 16-byte chunks, lane i starting at chunk i mod RB, so
+// that the 8 lanes of a quarter-warp read 8 different bank groups.
+template <int RB, int KV>
+__global__ void __launch_bounds__(kShThreads)
+k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int32_t *__restrict__ target,
+              int64_t *stats, WsHeader *hdr, ShGeo g, int blocks_per_layer) {
+    extern __shared__ longlong2 tab2[];                      // [E][RB]
+    __shared__ long long red[4][kShThreads / 32];
+    const int l = blockIdx.x / blocks_per_layer;
+    const int blk = blockIdx.x - l * blocks_per_layer;
+    const int64_t *Ml = M + (int64_t)l * g.E * g.R;
+    long long *tab = reinterpret_cast<long long *>(tab2);
+    for (int x = threadIdx.x; x < g.E * 2 * RB; x += kShThreads) {
+        const int a = x / (2 * RB), r = x - a * 2 * RB;
+        tab[x] = r < g.R ? __ldg(Ml + (int64_t)a * g.R + r) : 0;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    int on_tgt = 0, on_src = 0, moved = 0, pairs = 0;
+    bool bad = false;
+    const int32_t *cur0 = ids + (int64_t)l * g.T * g.k;
+    const int32_t *nxt0 = ids + (int64_t)(l + 1) * g.T * g.k;
+    const int64_t tok0 = (int64_t)blk * kShThreads * kShIter;
+    for (int it = 0; it < kShIter; ++it) {
+        const int64_t t = tok0 + (int64_t)it * kShThreads + threadIdx.x;
+        if (t >= g.T) break;
+        int a[KV], b[KV];
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+            a[j] = j < g.k ? __ldg(cur0 + t * g.k + j) : -1;
+            b[j] = j < g.k ? __ldg(nxt0 + t * g.k + j) : -1;
+        }
+        longlong2 acc[RB];
+#pragma unroll
+        for (int c = 0; c < RB; ++c) acc[c] = make_longlong2(0, 0);
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+            if (j >= g.k) break;
+            if ((unsigned)a[j] >= (unsigned)g.E) {
+                bad = true;
+                continue;
+            }
+            const longlong2 *row = tab2 + a[j] * RB;
+#pragma unroll
+            for (int c = 0; c < RB; ++c) {
+                const longlong2 v = row[(c + lane) % RB];
+                acc[c].x += v.x;
+                acc[c].y += v.y;
+            }
+        }
+        const int s = (int)fast_quot((unsigned)t, g.tpr);
+        long long best = LLONG_MIN, ssc = 0;
+        int br = 0;
+#pragma unroll
+        for (int c = 0; c < RB; ++c) {
+            const int r0 = ((c + lane) % RB) * 2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = r0 + h;
+                const long long v = h ? acc[c].y : acc[c].x;
+                if (r < g.R) {
+                    if (v > best || (v == best && r < br)) {
+                        best = v;
+                        br = r;
+                    }
+                    if (r == s) ssc = v;
+                }
+            }
+        }
+        const int tg = ssc == best ? s : br;
+        target[(int64_t)l * g.T + t] = tg;
+        moved += tg != s;
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+            if (j >= g.k) break;
+            if ((unsigned)b[j] >= (unsigned)g.E) {
+                bad = true;
+                continue;
+            }
+            const int rb = sh_rank(g, b[j]);
+            on_tgt += rb == tg;
+            on_src += rb == s;
+            ++pairs;
+        }
+    }
+    if (bad) set_error(hdr, TOPO_ERANGE);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        on_tgt += __shfl_xor_sync(0xffffffffu, on_tgt, o);
+        on_src += __shfl_xor_sync(0xffffffffu, on_src, o);
+        moved += __shfl_xor_sync(0xffffffffu, moved, o);
+        pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+    }
+    const int warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        red[0][warp] = on_tgt;
+        red[1][warp] = on_src;
+        red[2][warp] = moved;
+        red[3][warp] = pairs;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+        long long v = 0;
+        for (int w = 0; w < kShThreads / 32; ++w) v += red[threadIdx.x][w];
+        if (v) atomicAdd(reinterpret_cast<unsigned long long *>(stats + (int64_t)l * 4 + threadIdx.x),
+                         (unsigned long long)v);
+    }
+}
+
+template <int RB, int KV>
+cudaError_t run_target_t(const ShGeo &g, const int32_t *ids, const int64_t *M, int32_t *target,
+                         int64_t *stats, WsHeader *hdr, cudaStream_t st) {
+    const int tok_per_block = kShThreads * kShIter;
+    const int bpl = (g.T + tok_per_block - 1) / tok_per_block;
+    const int64_t blocks = (int64_t)(g.L - 1) * bpl;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+    const size_t tab = (size_t)g.E * RB * 16;
+    cudaError_t e = ensure_smem((const void *)k_sh_target_t<RB, KV>, tab);
+    if (e != cudaSuccess) return e;
+    k_sh_target_t<RB, KV><<<(unsigned)blocks, kShThreads, tab, st>>>(ids, M, target, stats, hdr, g, bpl);
+    return cudaGetLastError();
+}
+
+template <int G, int RPL, int KQ>
+cudaError_t run_target_kq(const ShGeo &g, const int32_t *ids, const int64_t *M, int32_t *target,
+                          int64_t *stats, WsHeader *hdr, cudaStream_t st) {
+    const int tok_per_block = (kShThreads / G) * kShIter;
     const int bpl = (g.T + tok_per_block - 1) / tok_per_block;
     const int64_t blocks = (int64_t)(g.L - 1) * bpl;
     if (blocks == 0) return cudaSuccess;
@@ -178,14 +344,22 @@ cudaError_t run_target(const ShGeo &g, const int32_t *ids, const int64_t *M, int
     const size_t tab = (size_t)g.E * g.R * 8;
     cudaError_t e;
     if (tab <= kShSmemTable) {
-        if ((e = ensure_smem((const void *)k_sh_target<G, RPL, true>, tab)) != cudaSuccess) return e;
-        k_sh_target<G, RPL, true><<<(unsigned)blocks, kShThreads, tab, st>>>(ids, M, target, stats, hdr, g,
-                                                                              bpl);
+        if ((e = ensure_smem((const void *)k_sh_target<G, RPL, KQ, true>, tab)) != cudaSuccess) return e;
+        k_sh_target<G, RPL, KQ, true><<<(unsigned)blocks, kShThreads, tab, st>>>(ids, M, target, stats, hdr,
+                                                                                  g, bpl);
     } else {
-        k_sh_target<G, RPL, false><<<(unsigned)blocks, kShThreads, 0, st>>>(ids, M, target, stats, hdr, g,
-                                                                             bpl);
+        k_sh_target<G, RPL, KQ, false><<<(unsigned)blocks, kShThreads, 0, st>>>(ids, M, target, stats, hdr,
+                                                                                 g, bpl);
     }
     return cudaGetLastError();
+}
+
+// KQ = 1 when a group's lanes cover the token's slots, else enough for k <= 64.
+template <int G, int RPL>
+cudaError_t run_target(const ShGeo &g, const int32_t *ids, const int64_t *M, int32_t *target, int64_t *stats,
+                       WsHeader *hdr, cudaStream_t st) {
+    if (g.k <= G) return run_target_kq<G, RPL, 1>(g, ids, M, target, stats, hdr, st);
+    return run_target_kq<G, RPL, (kMaxK + G - 1) / G>(g, ids, M, target, stats, hdr, st);
 }
 
 }  // namespace
@@ -201,8 +375,8 @@ cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids
     if (L < 2) return cudaSuccess;
     ShGeo g;
     g.L = L; g.T = T; g.E = E; g.k = k; g.R = R;
-    g.tpr = R > 0 && T > 0 ? T / R : 1;
-    g.er = main_rank ? 1 : E / R;
+    g.tpr = make_fast_div((unsigned)(R > 0 && T > 0 ? T / R : 1));
+    g.er = make_fast_div((unsigned)(main_rank ? 1 : E / R));
     g.main_rank = main_rank;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
     int64_t *M = ws_at<int64_t>(ws, sizeof(WsHeader));
@@ -211,6 +385,17 @@ cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids
     k_sh_table<<<(unsigned)((L - 1) * E), 128, (size_t)R * 8, st>>>(tr, M, hdr, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (T == 0) return cudaSuccess;
+    if (R <= 16 && k <= 16 && (size_t)E * 128 <= kShSmemTable) {   // one thread per token
+        const int rb = (R + 1) / 2;
+        if (k <= 8) {
+            if (rb <= 2) return run_target_t<2, 8>(g, ids, M, target, stats, hdr, st);
+            if (rb <= 4) return run_target_t<4, 8>(g, ids, M, target, stats, hdr, st);
+            return run_target_t<8, 8>(g, ids, M, target, stats, hdr, st);
+        }
+        if (rb <= 2) return run_target_t<2, 16>(g, ids, M, target, stats, hdr, st);
+        if (rb <= 4) return run_target_t<4, 16>(g, ids, M, target, stats, hdr, st);
+        return run_target_t<8, 16>(g, ids, M, target, stats, hdr, st);
+    }
     if (R <= 4) return run_target<4, 1>(g, ids, M, target, stats, hdr, st);
     if (R <= 8) return run_target<8, 1>(g, ids, M, target, stats, hdr, st);
     if (R <= 16) return run_target<16, 1>(g, ids, M, target, stats, hdr, st);
