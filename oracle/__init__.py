@@ -92,7 +92,8 @@ def _load():
             lib.oracle_gate.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_void_p, ctypes.c_void_p,
                                         i32p, f32p, i32p]
             lib.oracle_shuffle.argtypes = [ci, ci, ci, ci, ci, i32p, i64p, ctypes.c_void_p, i32p, i64p]
-            for f in ("oracle_shuffle", "oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
+            lib.oracle_place.argtypes = [ci, ci, ci, ci, i64p, i32p, i64p]
+            for f in ("oracle_place", "oracle_shuffle", "oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
                       "oracle_layout", "oracle_permute", "oracle_combine", "oracle_dedup"):
                 getattr(lib, f).restype = ci
             _lib = lib
@@ -142,6 +143,26 @@ def gate(logits, k: int, R: int, bias=None):
     if squeeze:
         out = {key: v[0] for key, v in out.items()}
     return out
+
+
+PLACE_STAT_NAMES = ("within_contiguous", "within_greedy", "within_final", "swaps")
+
+
+def place(co, R: int, max_iters: int = 0):
+    """Correlated expert placement [Zyphra, "Moving Correlated Experts Together"].
+
+    co int64 [L, E, E] (or [E, E]).  Returns (main_rank int32 [L, E], stats
+    int64 [L, 4]) (without the leading L for a 2-D input)."""
+    c = np.ascontiguousarray(co, dtype=np.int64)
+    squeeze = c.ndim == 2
+    if squeeze:
+        c = c[None]
+    L, E, _ = c.shape
+    mr = np.zeros((L, E), np.int32)
+    st = np.zeros((L, 4), np.int64)
+    _check("oracle_place", _load().oracle_place(L, E, R, max_iters, c.reshape(-1), mr.reshape(-1),
+                                                st.reshape(-1)))
+    return (mr[0], st[0]) if squeeze else (mr, st)
 
 
 SHUFFLE_STAT_NAMES = ("next_pairs_on_target", "next_pairs_on_source", "tokens_moved", "next_pairs")

@@ -903,3 +903,107 @@ int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const 
     free(rank_of); free(M); free(score);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Correlated expert placement [Zyphra, "Moving Correlated Experts           */
+/* Together": the co-selection counts form a graph over experts, which is    */
+/* partitioned across GPUs with a fixed number of experts per GPU so that    */
+/* frequently co-selected experts share a GPU].  The pages give no           */
+/* algorithm.  Readings: the weight of a pair is w(a,b) = co[a][b] +         */
+/* co[b][a] (a != b; the diagonal is ignored).  Greedy construction: ranks   */
+/* r = 0..R-1 in turn take E/R experts: first the unassigned expert with the */
+/* largest total weight, then repeatedly the unassigned expert with the      */
+/* largest weight to the rank's members.  Refinement: while some swap of two */
+/* experts on different ranks raises the within-rank weight, apply the best  */
+/* one (gain C[a][rb] - C[a][ra] + C[b][ra] - C[b][rb] - 2 w(a,b), with      */
+/* C[x][r] the weight of x to rank r's members), at most max_iters swaps     */
+/* when max_iters > 0.  Every choice takes the lowest index on ties (a       */
+/* before b for swaps, a < b).  stats = {within-rank weight of the           */
+/* contiguous map e / (E/R), after the greedy construction, final, swaps}.   */
+/* ------------------------------------------------------------------------ */
+
+static int64_t place_within(int E, const int64_t *w, const int32_t *part) {
+    int64_t s = 0;
+    for (int a = 0; a < E; a++)
+        for (int b = a + 1; b < E; b++)
+            if (part[a] == part[b]) s += w[(int64_t)a * E + b];
+    return s;
+}
+
+int oracle_place(int L, int E, int R, int max_iters, const int64_t *co, int32_t *main_rank,
+                 int64_t *stats) {
+    if (L < 0 || E < 1 || R < 1 || E % R != 0 || max_iters < 0) return ORC_EINVAL;
+    int per = E / R;
+    int64_t *w = (int64_t *)malloc(sizeof(int64_t) * (size_t)E * E);
+    int64_t *C = (int64_t *)malloc(sizeof(int64_t) * (size_t)E * R);
+    int32_t *part = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    if (!w || !C || !part) { free(w); free(C); free(part); return ORC_EINVAL; }
+    for (int l = 0; l < L; l++) {
+        const int64_t *c = co + (int64_t)l * E * E;
+        int32_t *mr = main_rank + (int64_t)l * E;
+        int64_t *st = stats + (int64_t)l * 4;
+        for (int a = 0; a < E; a++)
+            for (int b = 0; b < E; b++)
+                w[(int64_t)a * E + b] = a == b ? 0 : c[(int64_t)a * E + b] + c[(int64_t)b * E + a];
+        for (int e = 0; e < E; e++) part[e] = e / per;
+        st[0] = place_within(E, w, part);
+        /* greedy construction */
+        for (int e = 0; e < E; e++) part[e] = -1;
+        for (int r = 0; r < R; r++) {
+            int seed = -1;
+            int64_t best = 0;
+            for (int a = 0; a < E; a++) {
+                if (part[a] >= 0) continue;
+                int64_t tot = 0;
+                for (int b = 0; b < E; b++) tot += w[(int64_t)a * E + b];
+                if (seed < 0 || tot > best) { seed = a; best = tot; }
+            }
+            part[seed] = r;
+            for (int n = 1; n < per; n++) {
+                int pick = -1;
+                int64_t bc = 0;
+                for (int b = 0; b < E; b++) {
+                    if (part[b] >= 0) continue;
+                    int64_t conn = 0;
+                    for (int m = 0; m < E; m++)
+                        if (part[m] == r) conn += w[(int64_t)m * E + b];
+                    if (pick < 0 || conn > bc) { pick = b; bc = conn; }
+                }
+                part[pick] = r;
+            }
+        }
+        st[1] = place_within(E, w, part);
+        /* swap refinement */
+        for (int x = 0; x < E; x++) {
+            for (int r = 0; r < R; r++) C[(int64_t)x * R + r] = 0;
+            for (int m = 0; m < E; m++) C[(int64_t)x * R + part[m]] += w[(int64_t)x * E + m];
+        }
+        int64_t swaps = 0;
+        while (max_iters == 0 || swaps < max_iters) {
+            int ba = -1, bb = -1;
+            int64_t bg = 0;
+            for (int a = 0; a < E; a++)
+                for (int b = a + 1; b < E; b++) {
+                    int pa = part[a], pb = part[b];
+                    if (pa == pb) continue;
+                    int64_t g = C[(int64_t)a * R + pb] - C[(int64_t)a * R + pa] + C[(int64_t)b * R + pa] -
+                                C[(int64_t)b * R + pb] - 2 * w[(int64_t)a * E + b];
+                    if (g > bg) { bg = g; ba = a; bb = b; }
+                }
+            if (ba < 0) break;
+            int pa = part[ba], pb = part[bb];
+            for (int x = 0; x < E; x++) {
+                C[(int64_t)x * R + pa] += w[(int64_t)x * E + bb] - w[(int64_t)x * E + ba];
+                C[(int64_t)x * R + pb] += w[(int64_t)x * E + ba] - w[(int64_t)x * E + bb];
+            }
+            part[ba] = pb;
+            part[bb] = pa;
+            swaps++;
+        }
+        st[2] = place_within(E, w, part);
+        st[3] = swaps;
+        for (int e = 0; e < E; e++) mr[e] = part[e];
+    }
+    free(w); free(C); free(part);
+    return ORC_OK;
+}

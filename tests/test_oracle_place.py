@@ -1,0 +1,105 @@
+"""Pins of the oracle's correlated expert placement ("Expert Coupling in MoE
+Pretraining", "Moving Correlated Experts Together")."""
+from itertools import combinations
+
+import numpy as np
+
+import oracle
+
+
+def test_place_hand_cases(golden):
+    for c in golden("place_hand.json")["cases"]:
+        mr, st = oracle.place(np.array(c["co"], np.int64), c["R"])
+        assert mr.tolist() == c["main_rank"], c["notes"]
+        assert st.tolist() == c["stats"], c["notes"]
+
+
+def _within(w, part):
+    E = len(part)
+    return sum(w[a, b] for a in range(E) for b in range(a + 1, E) if part[a] == part[b])
+
+
+def _weights(co):
+    w = co + co.T
+    np.fill_diagonal(w, 0)
+    return w
+
+
+def test_result_is_balanced_swap_optimal_and_its_stats_recompute():
+    rng = np.random.default_rng(0)
+    for (E, R) in ((6, 2), (6, 3), (8, 4), (12, 3), (16, 4)):
+        for trial in range(4):
+            co = rng.integers(0, 20, size=(E, E)).astype(np.int64)
+            mr, st = oracle.place(co, R)
+            w = _weights(co)
+            assert np.all(np.bincount(mr, minlength=R) == E // R)
+            for a, b in combinations(range(E), 2):                  # no swap gains
+                if mr[a] == mr[b]:
+                    continue
+                p = mr.copy()
+                p[a], p[b] = p[b], p[a]
+                assert _within(w, p) <= _within(w, mr)
+            assert st[0] == _within(w, np.arange(E) // (E // R))
+            assert st[2] == _within(w, mr)
+            assert st[2] >= st[1]
+
+
+def test_tiny_instances_against_brute_force():
+    # the heuristic is swap-optimal, and on these tiny graphs it must also be
+    # within 15% of the best balanced partition found by enumeration
+    rng = np.random.default_rng(1)
+    E, R = 8, 2
+    for trial in range(6):
+        co = rng.integers(0, 10, size=(E, E)).astype(np.int64)
+        w = _weights(co)
+        best = 0
+        for half in combinations(range(1, E), E // 2 - 1):
+            part = np.ones(E, int)
+            part[[0, *half]] = 0
+            best = max(best, _within(w, part))
+        mr, st = oracle.place(co, R)
+        assert st[2] <= best and st[2] >= 0.85 * best
+
+
+def test_planted_groups_are_recovered():
+    rng = np.random.default_rng(2)
+    E, R = 32, 4
+    perm = rng.permutation(E)
+    group = np.empty(E, int)
+    group[perm] = np.arange(E) // 8
+    co = rng.integers(0, 3, size=(E, E)).astype(np.int64)
+    co += 40 * (group[:, None] == group[None, :])
+    mr, st = oracle.place(co, R)
+    for r in range(R):
+        assert len(set(group[mr == r])) == 1                    # each rank holds one planted group
+
+
+def test_iteration_cap():
+    c = np.array([[0, 5, 5, 5], [0, 0, 9, 0], [0, 0, 0, 0], [0, 0, 0, 0]], np.int64)
+    mr, st = oracle.place(c, 2, max_iters=1)
+    assert st[3] == 1
+    mr0, st0 = oracle.place(c, 2, max_iters=0)
+    assert st0[2] >= st[2]
+
+
+def test_correlated_placement_raises_dedup_savings():
+    # the pages report deduplication removing more rows once correlated experts
+    # share a GPU; on routing with planted expert groups it must do the same
+    from moe_expert_routing_ids_gb300 import workloads as W
+    rng = np.random.default_rng(3)
+    E, k, T, R = 64, 6, 8192, 8
+    groups = rng.permutation(E).reshape(8, 8)
+    ids = np.empty((1, T, k), np.int32)
+    for t in range(T):
+        g = groups[rng.integers(0, 8)]
+        first = rng.choice(g, size=4, replace=False)
+        rest = rng.choice(np.setdiff1d(np.arange(E), first), size=2, replace=False)
+        ids[0, t] = np.concatenate([first, rest])
+    co, _ = oracle.cooccur(ids, E)
+    mr, _ = oracle.place(co[0], R)
+    per = E // R
+
+    def saved(rank):
+        rows = sum(len(set(rank[ids[0, t]])) for t in range(T))
+        return 1 - rows / (T * k)
+    assert saved(mr) > saved(np.arange(E) // per) + 0.15
