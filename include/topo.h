@@ -72,6 +72,7 @@ extern "C" {
 #define TOPO_GATE_MAX_E 1024
 #define TOPO_SHUFFLE_STATS 4
 #define TOPO_SHUFFLE_MAX_RANKS 256
+#define TOPO_PLACE_STATS 4
 
 #define TOPO_STATS 8        /* int64 plan statistics per layer */
 #define TOPO_LAYOUT_STATS 8 /* int64 layout statistics per layer */
@@ -179,6 +180,26 @@ size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R);
 int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, const int32_t *ids,
                          const int64_t *tr, const int32_t *main_rank, int32_t *target, int64_t *stats,
                          void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Correlated expert placement ["Expert Coupling in MoE Pretraining", "Moving
+ * Correlated Experts Together": the co-selection graph partitioned across
+ * GPUs with a fixed number of experts per GPU, co-selected experts kept
+ * together].  Readings (the pages give no algorithm): w(a,b) = co[a][b] +
+ * co[b][a] for a != b; greedy construction, ranks r = 0..R-1 in turn taking
+ * E/R experts -- the unassigned expert of largest total weight, then
+ * repeatedly the unassigned expert of largest weight to the rank's members;
+ * then, while the best swap of two experts on different ranks raises the
+ * within-rank weight, apply it (at most max_iters swaps when max_iters > 0).
+ * Lowest index on every tie.
+ * co:        device int64 [L][E][E] (topo_cooccur's co-selection counts).
+ * main_rank: device int32 [L][E] (written): a map for topo_cfg.main_rank.
+ * stats:     device int64 [L][TOPO_PLACE_STATS]: within-rank weight of the
+ *            contiguous map e / (E/R), after the greedy construction, final;
+ *            swaps applied.
+ * Requires E % R == 0, E <= 1024 and E * (R + 1.5) * 8 bytes of shared memory
+ * within the device limit (else TOPO_EINVAL).  No device errors. */
+int topo_place_experts(int32_t L, int32_t E, int32_t R, int32_t max_iters, const int64_t *co,
+                       int32_t *main_rank, int64_t *stats, cudaStream_t stream);
 
 /* Expert co-selection and cross-layer transition counts ["Expert Coupling in
  * MoE Pretraining": within-layer correlation, cross-layer correlation]:

@@ -32,6 +32,7 @@ TOPO_DTYPE_BF16 = 1
 TOPO_GATE_MAX_E = 1024
 TOPO_SHUFFLE_STATS = 4
 TOPO_SHUFFLE_MAX_RANKS = 256
+TOPO_PLACE_STATS = 4
 TOPO_DEDUP_STATS = 4
 TOPO_STATS = 8
 TOPO_LAYOUT_STATS = 8
@@ -39,7 +40,7 @@ EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
            "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine",
            "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_workspace_bytes",
-           "topo_shuffle_targets")
+           "topo_shuffle_targets", "topo_place_experts")
 TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -96,13 +97,14 @@ def lib():
             L.topo_shuffle_workspace_bytes.argtypes = [i32, i32, i32]
             L.topo_shuffle_workspace_bytes.restype = sz
             L.topo_shuffle_targets.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_place_experts.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
             L.topo_combine.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
             L.topo_strerror.argtypes = [ctypes.c_int]
             L.topo_strerror.restype = ctypes.c_char_p
             for f in ("topo_ws_reset", "topo_hist", "topo_cooccur", "topo_plan", "topo_reroute",
                       "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
-                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_targets"):
+                      "topo_hist_noalloc", "topo_permute", "topo_combine", "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_targets", "topo_place_experts"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -204,6 +206,12 @@ def topo_hist_noalloc(cfg: TopoCfg, n_layers: int, ids, hist, err=None, stream=N
     err: optional device int32 that receives the device error word."""
     return _chk("topo_hist_noalloc", lib().topo_hist_noalloc(ctypes.byref(cfg), n_layers, _p(ids),
                                                              _p(hist), _p(err), _s(stream)))
+
+
+def topo_place_experts(L: int, E: int, R: int, max_iters: int, co, main_rank, stats, stream=None) -> int:
+    """Correlated expert placement from co-selection counts into a main-rank map."""
+    return _chk("topo_place_experts",
+                lib().topo_place_experts(L, E, R, max_iters, _p(co), _p(main_rank), _p(stats), _s(stream)))
 
 
 def topo_shuffle_workspace_bytes(L: int, E: int, R: int) -> int:

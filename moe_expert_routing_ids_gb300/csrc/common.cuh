@@ -206,6 +206,12 @@ size_t shuffle_ws_bytes(int L, int E, int R);
 cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
                            const int32_t *main_rank, int32_t *target, int64_t *stats, void *ws,
                            cudaStream_t st);
+// Correlated expert placement: one CTA per layer, E <= kPlaceMaxE and the
+// shared tables within kSmemMax.
+constexpr int kPlaceMaxE = 1024;
+size_t place_smem_bytes(int E, int R);
+cudaError_t launch_place(int L, int E, int R, int max_iters, const int64_t *co, int32_t *main_rank,
+                         int64_t *stats, cudaStream_t st);
 cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *hist,
                         const topo_plan_t &p, void *ws, cudaStream_t st);
 cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t *ids,

@@ -1,0 +1,200 @@
+// Correlated expert placement ("Expert Coupling in MoE Pretraining", "Moving
+// Correlated Experts Together": the co-selection counts form a graph over
+// experts, partitioned across GPUs with a fixed number of experts per GPU so
+// that frequently co-selected experts share a GPU).
+//
+// w(a,b) = co[a][b] + co[b][a] for a != b.  Greedy construction: ranks
+// r = 0..R-1 in turn take E/R experts, first the unassigned expert of largest
+// total weight, then repeatedly the unassigned expert of largest weight to the
+// rank's members.  Refinement: while the best swap of two experts on different
+// ranks gains, apply it (gain C[a][rb] - C[a][ra] + C[b][ra] - C[b][rb] -
+// 2 w(a,b), C[x][r] = weight of x to rank r's members).  Lowest index on ties.
+//
+// One CTA of kPlThreads per layer.  Each choice is a block argmax over a key
+// (value desc, index asc); the connection array of the greedy phase and the
+// C table live in shared memory, the counts are read through L1/L2.
+#include <climits>
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace topo {
+namespace {
+
+constexpr int kPlThreads = 1024;
+constexpr int kPlWarps = kPlThreads / 32;
+
+struct PlKey {
+    long long v;
+    int i;                            // ranks above any key with a larger i at equal v
+};
+
+__device__ __forceinline__ bool pl_better(const PlKey &a, const PlKey &b) {
+    return a.v > b.v || (a.v == b.v && a.i < b.i);
+}
+
+// Block-wide best key; every thread gets the result.  scratch: kPlWarps keys.
+__device__ __forceinline__ PlKey pl_block_best(PlKey k, PlKey *scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        PlKey q;
+        q.v = __shfl_xor_sync(0xffffffffu, k.v, o);
+        q.i = __shfl_xor_sync(0xffffffffu, k.i, o);
+        if (pl_better(q, k)) k = q;
+    }
+    __syncthreads();                                  // scratch free
+    if (lane == 0) scratch[w] = k;
+    __syncthreads();
+    k = scratch[0];
+    for (int x = 1; x < kPlWarps; ++x)
+        if (pl_better(scratch[x], k)) k = scratch[x];
+    return k;
+}
+
+__device__ __forceinline__ long long pl_w(const int64_t *co, int E, int a, int b) {
+    return a == b ? 0 : __ldg(co + (int64_t)a * E + b) + __ldg(co + (int64_t)b * E + a);
+}
+
+// Within-rank weight of the map in part (block sum; every thread gets it).
+__device__ long long pl_within(const int64_t *co, int E, FastDiv fe, const int *part, long long *red) {
+    long long s = 0;
+    for (int x = threadIdx.x; x < E * E; x += kPlThreads) {
+        const int a = (int)fast_quot((unsigned)x, fe), b = x - a * E;
+        if (a < b && part[a] == part[b]) s += pl_w(co, E, a, b);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    long long t = 0;
+    for (int x = 0; x < kPlWarps; ++x) t += red[x];
+    return t;
+}
+
+__global__ void __launch_bounds__(kPlThreads)
+k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int64_t *__restrict__ stats,
+        int E, int R, int max_iters, FastDiv fe) {
+    extern __shared__ long long psm[];
+    long long *conn = psm;                            // [E] greedy connection / total weight
+    long long *C = conn + E;                          // [E][R]
+    int *part = reinterpret_cast<int *>(C + (size_t)E * R);   // [E]
+    __shared__ PlKey scratch[kPlWarps];
+    __shared__ long long red[kPlWarps];
+    const int l = blockIdx.x;
+    const int64_t *co = co_all + (int64_t)l * E * E;
+    const int per = E / R;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+
+    // contiguous map, and every expert's total weight (a warp per row)
+    for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = e / per;
+    __syncthreads();
+    const long long w_contig = pl_within(co, E, fe, part, red);
+    for (int a = w; a < E; a += kPlWarps) {
+        long long s = 0;
+        for (int b = lane; b < E; b += 32) s += pl_w(co, E, a, b);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) conn[a] = s;
+    }
+    for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = -1;
+    __syncthreads();
+
+    // greedy construction; the totals move to the first E entries of C, conn is reused
+    for (int e = threadIdx.x; e < E; e += kPlThreads) C[e] = conn[e];
+    __syncthreads();
+    for (int r = 0; r < R; ++r) {
+        PlKey k{LLONG_MIN, INT_MAX};
+        for (int a = threadIdx.x; a < E; a += kPlThreads)
+            if (part[a] < 0) {
+                const PlKey q{C[a], a};
+                if (pl_better(q, k)) k = q;
+            }
+        int pick = pl_block_best(k, scratch).i;
+        __syncthreads();
+        if (threadIdx.x == 0) part[pick] = r;
+        for (int b = threadIdx.x; b < E; b += kPlThreads) conn[b] = pl_w(co, E, pick, b);
+        __syncthreads();
+        for (int n = 1; n < per; ++n) {
+            PlKey q0{LLONG_MIN, INT_MAX};
+            for (int b = threadIdx.x; b < E; b += kPlThreads)
+                if (part[b] < 0) {
+                    const PlKey q{conn[b], b};
+                    if (pl_better(q, q0)) q0 = q;
+                }
+            pick = pl_block_best(q0, scratch).i;
+            __syncthreads();
+            if (threadIdx.x == 0) part[pick] = r;
+            for (int b = threadIdx.x; b < E; b += kPlThreads) conn[b] += pl_w(co, E, pick, b);
+            __syncthreads();
+        }
+    }
+    const long long w_greedy = pl_within(co, E, fe, part, red);
+
+    // refinement: C[x][r], then best-gain swaps
+    for (int x = threadIdx.x; x < E; x += kPlThreads) {
+        long long *cx = C + (size_t)x * R;
+        for (int r = 0; r < R; ++r) cx[r] = 0;
+        for (int m = 0; m < E; ++m) cx[part[m]] += pl_w(co, E, x, m);
+    }
+    __syncthreads();
+    long long swaps = 0;
+    while (max_iters == 0 || swaps < max_iters) {
+        PlKey k{0, INT_MAX};                          // only a positive gain is taken
+        for (int x = threadIdx.x; x < E * E; x += kPlThreads) {
+            const int a = (int)fast_quot((unsigned)x, fe), b = x - a * E;
+            if (a >= b) continue;
+            const int pa = part[a], pb = part[b];
+            if (pa == pb) continue;
+            const long long g = C[(size_t)a * R + pb] - C[(size_t)a * R + pa] + C[(size_t)b * R + pa] -
+                                C[(size_t)b * R + pb] - 2 * pl_w(co, E, a, b);
+            const PlKey q{g, x};
+            if (g > 0 && pl_better(q, k)) k = q;
+        }
+        const PlKey best = pl_block_best(k, scratch);
+        if (best.i == INT_MAX) break;                 // no swap gains
+        const int ba = best.i / E, bb = best.i - ba * E;
+        const int pa = part[ba], pb = part[bb];
+        __syncthreads();                              // every thread has read part
+        for (int x = threadIdx.x; x < E; x += kPlThreads) {
+            const long long da = pl_w(co, E, x, ba), db = pl_w(co, E, x, bb);
+            C[(size_t)x * R + pa] += db - da;
+            C[(size_t)x * R + pb] += da - db;
+        }
+        if (threadIdx.x == 0) {
+            part[ba] = pb;
+            part[bb] = pa;
+        }
+        ++swaps;
+        __syncthreads();
+    }
+    const long long w_final = pl_within(co, E, fe, part, red);
+    for (int e = threadIdx.x; e < E; e += kPlThreads) main_rank[(int64_t)l * E + e] = part[e];
+    if (threadIdx.x == 0) {
+        stats[(int64_t)l * 4 + 0] = w_contig;
+        stats[(int64_t)l * 4 + 1] = w_greedy;
+        stats[(int64_t)l * 4 + 2] = w_final;
+        stats[(int64_t)l * 4 + 3] = swaps;
+    }
+}
+
+}  // namespace
+
+size_t place_smem_bytes(int E, int R) {
+    return (size_t)E * 8 + (size_t)E * R * 8 + (size_t)E * 4;
+}
+
+cudaError_t launch_place(int L, int E, int R, int max_iters, const int64_t *co, int32_t *main_rank,
+                         int64_t *stats, cudaStream_t st) {
+    if (L == 0) return cudaSuccess;
+    const size_t smem = place_smem_bytes(E, R);
+    cudaError_t e = ensure_smem((const void *)k_place, smem);
+    if (e != cudaSuccess) return e;
+    k_place<<<L, kPlThreads, smem, st>>>(co, main_rank, stats, E, R, max_iters,
+                                         make_fast_div((unsigned)E));
+    return cudaGetLastError();
+}
+
+}  // namespace topo

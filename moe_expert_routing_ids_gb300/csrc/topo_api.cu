@@ -220,6 +220,15 @@ int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, in
                                hist_fingerprint(g, ids), stream));
 }
 
+int topo_place_experts(int32_t L, int32_t E, int32_t R, int32_t max_iters, const int64_t *co,
+                       int32_t *main_rank, int64_t *stats, cudaStream_t stream) {
+    if (L < 0 || E < 1 || E > kPlaceMaxE || R < 1 || E % R != 0 || max_iters < 0) return TOPO_EINVAL;
+    if (place_smem_bytes(E, R) > kSmemMax) return TOPO_EINVAL;
+    if (L == 0) return TOPO_OK;
+    if (!co || !main_rank || !stats) return TOPO_EINVAL;
+    return cuda_rc(launch_place(L, E, R, max_iters, co, main_rank, stats, stream));
+}
+
 size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R) {
     if (L < 0 || E < 1 || R < 1 || R > TOPO_SHUFFLE_MAX_RANKS || E >= (1 << 26)) return 0;
     return shuffle_ws_bytes(L, E, R);
