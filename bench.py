@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2, "shuffle": 2}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2, "shuffle": 2, "place": 1}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged
@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle"),
+    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle", "place"),
                     help="run one secondary measurement alone and print it (for profiling)")
     ap.add_argument("--microbatches", type=int, default=0,
                     help="--only gate: microbatches of the workload to use (0 = all; 1 for ncu captures)")
@@ -391,6 +391,74 @@ def secondary_cooccur(dev, stream, hbm_peak):
 
 
 SHUFFLE_RANKS = 16           # EP16 over the co-occurrence workload's 128 experts
+PLACE_RANKS = 8              # EP8, the scale at which the pages report deduplication savings
+
+
+def secondary_place(dev, stream):
+    """topo_place_experts on the co-occurrence workload's 8 layers (E = 128)
+    at EP8: one call for all layers timed with CUDA events (median of 5 after
+    2 warm-up calls), then, for its first layer, the rows the deduplicated
+    dispatch layout sends with the contiguous and with the correlated map
+    (plan with no replica slots, so every pair goes to its expert's main
+    rank)."""
+    import torch
+    import moe_expert_routing_ids_gb300 as topo
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Cooccur, Planner
+    w = W.COOCCUR
+    L, T, E, k, R = w.n_layers, w.T, w.E, w.k, PLACE_RANKS
+    ids_np = w.ids()
+    ids = torch.as_tensor(ids_np, device=dev)
+    C = Cooccur(L, T, E, k, dev, transitions=False)
+    with torch.cuda.stream(stream):
+        C.run(ids, stream)
+    mr = torch.empty((L, E), dtype=torch.int32, device=dev)
+    st = torch.empty((L, topo.TOPO_PLACE_STATS), dtype=torch.int64, device=dev)
+    s = stream.cuda_stream
+    times = []
+    for i in range(7):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            topo.topo_place_experts(L, E, R, 0, C.co, mr, st, s)
+            b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    stn = st.cpu().numpy()
+    res = {"workload": f"{w.name} as EP{R}", "ms": round(ms, 4), "layers_in_parallel": L,
+           "within_weight_contiguous": int(stn[:, 0].sum()), "within_weight_greedy": int(stn[:, 1].sum()),
+           "within_weight_final": int(stn[:, 2].sum()), "swaps": int(stn[:, 3].sum()),
+           "timing": "CUDA events around one call for all layers, median of 5 after 2 warm-up calls",
+           "gpu_launches_per_call": KERNELS_PER_CALL["place"]}
+    # deduplication at EP8 on layer 0, contiguous against correlated placement
+    saved = {}
+    for name, m in (("contiguous", None), ("correlated", mr[0].contiguous())):
+        cfg = dict(T=T, E=E, k=k, R=R, ranks_per_node=R, n_slot=0, tok_bytes=2048, expert_bytes=1 << 20,
+                   c_intra=1, c_inter=4, max_refine_iters=0, main_rank=m)
+        P = Planner(cfg, 1, dev, stream=stream)
+        with torch.cuda.stream(stream):
+            P.run(ids[:1])
+        c = topo.make_cfg(**{**cfg, "main_rank": P.main_rank})
+        nb = topo.topo_workspace_bytes(c, 1, topo.TOPO_CALL_DEDUP)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        o = [torch.empty((1, R + 1), dtype=torch.int32, device=dev),
+             torch.empty((1, T * k), dtype=torch.int32, device=dev),
+             torch.empty((1, T * k), dtype=torch.int64, device=dev),
+             torch.empty((1, T, 1), dtype=torch.int64, device=dev),
+             torch.empty((1, R, R), dtype=torch.int64, device=dev),
+             torch.empty((1, topo.TOPO_DEDUP_STATS), dtype=torch.int64, device=dev)]
+        with torch.cuda.stream(stream):
+            topo.topo_dedup_layout(c, 1, P.buf.dst_inst, *o, ws, nb, s)
+        torch.cuda.synchronize()
+        if P.error() != 0 or topo.topo_read_error(ws) != 0:
+            raise RuntimeError("device error in the placement measurement")
+        dst = o[5].cpu().numpy()[0]
+        saved[name] = round(1 - dst[0] / dst[1], 4)
+    res["dedup_rows_saved_layer0"] = saved
+    return res
+
 
 
 def secondary_shuffle(dev, stream, hbm_peak):
@@ -645,6 +713,8 @@ def run_only(name, microbatches=0):
         res = secondary_gate(dev, stream, hbm, microbatches)
     elif name == "shuffle":
         res = secondary_shuffle(dev, stream, hbm)
+    elif name == "place":
+        res = secondary_place(dev, stream)
     else:
         w = W.STRESS
         P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
@@ -734,6 +804,7 @@ def run_ours(args, rank, world, local_rank):
         line["dedup"] = secondary_dedup(P, w, dev, stream, hbm)
         line["gate"] = secondary_gate(dev, stream, hbm)
         line["shuffle"] = secondary_shuffle(dev, stream, hbm)
+        line["place"] = secondary_place(dev, stream)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, ids)
     print(json.dumps(line), flush=True)
