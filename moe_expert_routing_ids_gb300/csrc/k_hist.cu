@@ -41,6 +41,7 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, Ws
     const int s = (tile / g.tps) % g.R;
     const int l = tile / (g.tps * g.R);
     for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
+    pdl_wait();                                    // the ids may come from the previous kernel
 
     const int tok0 = t * g.TT;
     const int ntok = max(0, min(g.TT, g.tpr - tok0));
@@ -71,6 +72,7 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, Ws
     __syncthreads();
     int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) mine[e] = cnt[e];
+    pdl_trigger();
 }
 
 // One thread per (layer, source, expert): exclusive prefix of the source's
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(256)
 k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo g, uint64_t fp,
               int64_t n_cols) {
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();
     if (c == 0) {
         hdr->hist_fp = fp;
         hdr->route_fp = 0;                      // any routing index is now stale
@@ -105,6 +108,7 @@ k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo 
         run += v;
     }
     hist[c] = run;
+    pdl_trigger();
 }
 
 }  // namespace
@@ -118,17 +122,17 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
     cudaError_t e = ensure_smem((const void *)k_hist_tiles, smem);
     if (e != cudaSuccess) return e;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
-    k_hist_tiles<<<(unsigned)tiles, kHistThreads, smem, st>>>(ids, ws_at<int32_t>(ws, g.off_tile), hdr, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_hist_tiles, dim3((unsigned)tiles), dim3(kHistThreads), smem, st, ids,
+                        ws_at<int32_t>(ws, g.off_tile), hdr, g)) != cudaSuccess)
+        return e;
     return launch_hist_prefix(g, hist, ws, fp, st);
 }
 
 cudaError_t launch_hist_prefix(const Geo &g, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st) {
     const int64_t cols = (int64_t)g.L * g.R * g.E;
     if (cols == 0) return cudaSuccess;
-    k_hist_prefix<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws_at<int32_t>(ws, g.off_tile), hist,
-                                                                  ws_at<WsHeader>(ws, 0), g, fp, cols);
-    return cudaGetLastError();
+    return launch_pdl(k_hist_prefix, dim3((unsigned)((cols + 255) / 256)), dim3(256), 0, st,
+                      ws_at<int32_t>(ws, g.off_tile), hist, ws_at<WsHeader>(ws, 0), g, fp, cols);
 }
 
 }  // namespace topo

@@ -67,6 +67,7 @@ __device__ __forceinline__ void stage_words(void *dst, const void *src, int n) {
 __global__ void __launch_bounds__(256)
 k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict__ tab, int32_t *iexp,
              unsigned *imask, WsHeader *hdr, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     const int l = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (l == 0 && i == 0) hdr->route_fp = 0;
@@ -85,6 +86,7 @@ k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict_
         if (old & bit) bad = true;                             // expert twice on one rank
     }
     if (bad) set_error(hdr, TOPO_ESTATE);
+    pdl_trigger();
 }
 
 // Exclusive scan of one (count, sum) pair per thread over the CTA; returns
@@ -136,6 +138,7 @@ __device__ __forceinline__ int lower_idx(const int *a, int n, int v) {
 __global__ void __launch_bounds__(256)
 k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask, int32_t *ioff_g,
             int32_t *ilist, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     extern __shared__ __align__(16) int sml[];
     __shared__ int warp_tot[32];
     const int l = blockIdx.y, E = g.E, nk = g.n_keys, nl = g.n_local;
@@ -166,6 +169,7 @@ k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask
     int j = ioff[e] + __popc(m[r >> 5] & ((1u << (r & 31)) - 1u));
     for (int w = 0; w < (r >> 5); ++w) j += __popc(m[w]);
     ilist[(int64_t)l * nk + j] = i;
+    pdl_trigger();
 }
 
 // Routing index of one source row: per expert, its nonzero instances in rank
@@ -178,6 +182,7 @@ k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask
 __global__ void __launch_bounds__(256)
 k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff_g,
             const int32_t *__restrict__ ilist_g, int32_t *roff, Entry *rent, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     extern __shared__ __align__(16) int smi[];
     __shared__ int2 warp_tot2[32];
     __shared__ int cbase[256], vbase[256];
@@ -241,6 +246,7 @@ k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff_g,
             vs += v;
         }
     }
+    pdl_trigger();
 }
 
 // Column prefix of q over sources (stored only where q != 0) and column
@@ -249,6 +255,7 @@ k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff_g,
 // shared memory.
 __global__ void __launch_bounds__(256)
 k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     __shared__ int part[8][33];
     const int l = blockIdx.y;
     const int lane = threadIdx.x & 31, ch = threadIdx.x >> 5;
@@ -284,6 +291,7 @@ k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
             run += v[u];
         }
     }
+    pdl_trigger();
 }
 
 // Segment offsets (exclusive prefix of the column totals); zeroes the layout
@@ -291,6 +299,7 @@ k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
 // totals, the runs' sums are scanned once, then each run is written out.
 __global__ void __launch_bounds__(1024)
 k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     __shared__ int warp_tot[32];
     __shared__ int sums[1024];
     const int l = blockIdx.x;
@@ -328,6 +337,7 @@ k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g
         }
     }
     if (threadIdx.x == 0) o[n] = total;
+    pdl_trigger();
 }
 
 // Per-entry output bases; send counts and locality statistics from the
@@ -335,6 +345,7 @@ k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g
 __global__ void __launch_bounds__(256)
 k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__restrict__ soff,
               const int32_t *__restrict__ lseg, int64_t *lsend, int64_t *lstat, Geo g) {
+    pdl_wait();                                  // the previous kernel's outputs
     extern __shared__ long long sc[];            // [R]
     __shared__ long long red[4][32];
     const int s = blockIdx.x, l = blockIdx.y, R = g.R, nl = g.n_local;
@@ -378,6 +389,7 @@ k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__re
             atomicAdd(reinterpret_cast<unsigned long long *>(&st[3 + threadIdx.x]),
                       (unsigned long long)(t * g.S_tok));
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -397,35 +409,34 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     if ((e = cudaMemsetAsync(ws_at<unsigned>(ws, g.off_imask), 0, (size_t)g.L * g.E * RW * 4, st)) !=
         cudaSuccess)
         return e;
-    k_inst_index<<<dim3((g.n_keys + 255) / 256, g.L), 256, 0, st>>>(
+    if ((e = launch_pdl(k_inst_index, dim3((g.n_keys + 255) / 256, g.L), dim3(256), 0, st,
         p.slot_expert, main_rank ? ws_at<int32_t>(ws, g.off_main) : nullptr,
-        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask), hdr, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask), hdr, g)) != cudaSuccess)
+        return e;
     const size_t smem_list = ((size_t)g.E * RW + g.E + 1) * 4;
     if ((e = ensure_smem((const void *)k_inst_list, smem_list)) != cudaSuccess) return e;
-    k_inst_list<<<dim3((g.n_keys + 255) / 256, g.L), 256, smem_list, st>>>(
+    if ((e = launch_pdl(k_inst_list, dim3((g.n_keys + 255) / 256, g.L), dim3(256), smem_list, st,
         ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask), ws_at<int32_t>(ws, g.off_ioff),
-        ws_at<int32_t>(ws, g.off_ilist), g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ws_at<int32_t>(ws, g.off_ilist), g)) != cudaSuccess)
+        return e;
     const size_t smem_row = row_index_smem(g);
     if ((e = ensure_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;
-    k_row_index<<<dim3(g.R, g.L), 256, smem_row, st>>>(
+    if ((e = launch_pdl(k_row_index, dim3(g.R, g.L), dim3(256), smem_row, st,
         p.route_cnt, ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
-        ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_lay_cols<<<dim3((g.n_keys + 31) / 32, g.L), 256, 0, st>>>(
-        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_lay_seg<<<g.L, 1024, 0, st>>>(ws_at<int32_t>(ws, g.off_ccnt), ws_at<int32_t>(ws, g.off_lseg),
-                                    ws_at<int64_t>(ws, g.off_lstat), g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), g)) != cudaSuccess)
+        return e;
+    if ((e = launch_pdl(k_lay_cols, dim3((g.n_keys + 31) / 32, g.L), dim3(256), 0, st,
+        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), g)) != cudaSuccess)
+        return e;
+    if ((e = launch_pdl(k_lay_seg, dim3(g.L), dim3(1024), 0, st, ws_at<int32_t>(ws, g.off_ccnt),
+                        ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lstat), g)) != cudaSuccess)
+        return e;
     const size_t smem_e = (size_t)g.R * 8;
     if ((e = ensure_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
-    k_lay_entries<<<dim3(g.R, g.L), 256, smem_e, st>>>(
+    return launch_pdl(k_lay_entries, dim3(g.R, g.L), dim3(256), smem_e, st,
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), ws_at<int32_t>(ws, g.off_soff),
         ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
         ws_at<int64_t>(ws, g.off_lstat), g);
-    return cudaGetLastError();
 }
 
 }  // namespace topo

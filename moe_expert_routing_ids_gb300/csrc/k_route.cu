@@ -205,6 +205,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
               const int32_t *__restrict__ roff, const Entry *__restrict__ rent, int32_t *dst,
               int32_t *pos_ws, int32_t *sorted, WsHeader *hdr, Geo g, uint64_t hist_fp,
               uint64_t route_part) {
+    pdl_wait();                                  // the previous kernel's outputs
     constexpr int KB = K > 0 ? K : KMAX;
     extern __shared__ int sm[];
     __shared__ int ok;
@@ -399,12 +400,14 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     }
     if (bad_id) set_error(hdr, TOPO_ERANGE);
     if (bad_state) set_error(hdr, TOPO_ESTATE);
+    pdl_trigger();
 }
 
 // Layout from the positions topo_reroute stored: sorted[pos] = pair.
 __global__ void __launch_bounds__(256)
 k_layout_scatter(const int32_t *__restrict__ pos_ws, int32_t *sorted, WsHeader *hdr, Geo g,
                  uint64_t route_part) {
+    pdl_wait();                                  // the previous kernel's outputs
     __shared__ int ok;
     if (!check_fp(hdr, 0, true, route_part, &ok)) {
         if (threadIdx.x == 0) set_error(hdr, TOPO_ESTATE);
@@ -425,6 +428,7 @@ k_layout_scatter(const int32_t *__restrict__ pos_ws, int32_t *sorted, WsHeader *
         out[v] = (int32_t)(tg.p0 + (int64_t)t * k + j);
     }
     if (bad) set_error(hdr, TOPO_ESTATE);
+    pdl_trigger();
 }
 
 // Copy the small layout outputs computed by the prep kernels.
@@ -432,6 +436,7 @@ __global__ void __launch_bounds__(256)
 k_lay_copy(const int32_t *__restrict__ lseg, const int64_t *__restrict__ lsend,
            const int64_t *__restrict__ lstat, int32_t *seg_off, int64_t *send_counts,
            int64_t *layout_stats, const WsHeader *hdr, Geo g, uint64_t route_part, int check) {
+    pdl_wait();                                  // the previous kernel's outputs
     __shared__ int ok;
     if (check && !check_fp(hdr, 0, true, route_part, &ok)) return;
     const int64_t nseg = (int64_t)g.L * (g.n_keys + 1);
@@ -444,6 +449,7 @@ k_lay_copy(const int32_t *__restrict__ lseg, const int64_t *__restrict__ lsend,
         else if (i < nseg + nsend) send_counts[i - nseg] = lsend[i - nseg];
         else layout_stats[i - nseg - nsend] = lstat[i - nseg - nsend];
     }
+    pdl_trigger();
 }
 
 template <bool kFused>
@@ -472,11 +478,10 @@ cudaError_t launch_tiles(const Geo &g, const int32_t *ids, int32_t *dst, int32_t
     cudaError_t e;
     if ((e = ensure_smem((const void *)kern, smem)) != cudaSuccess) return e;
     const int64_t tiles = (int64_t)g.L * g.R * g.tps;
-    kern<<<(unsigned)tiles, kRankThreads, smem, st>>>(
+    return launch_pdl(kern, dim3((unsigned)tiles), dim3(kRankThreads), smem, st,
         ids, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_roff),
         ws_at<Entry>(ws, g.off_rent), dst, ws_at<int32_t>(ws, g.off_pos), sorted,
         ws_at<WsHeader>(ws, 0), g, hist_fp, route_part);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
@@ -484,10 +489,9 @@ cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, in
     const int64_t n = (int64_t)g.L * (g.n_keys + 1 + (int64_t)g.R * g.R + TOPO_LAYOUT_STATS);
     const int64_t want = (n + 255) / 256;
     const int blocks = (int)(want < 1024 ? want : 1024);
-    k_lay_copy<<<blocks, 256, 0, st>>>(ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
-                                       ws_at<int64_t>(ws, g.off_lstat), seg_off, send_counts,
-                                       layout_stats, ws_at<WsHeader>(ws, 0), g, route_part, check);
-    return cudaGetLastError();
+    return launch_pdl(k_lay_copy, dim3(blocks), dim3(256), 0, st, ws_at<int32_t>(ws, g.off_lseg),
+                      ws_at<int64_t>(ws, g.off_lsend), ws_at<int64_t>(ws, g.off_lstat), seg_off, send_counts,
+                      layout_stats, ws_at<WsHeader>(ws, 0), g, route_part, check);
 }
 
 }  // namespace
@@ -509,9 +513,9 @@ cudaError_t launch_layout(const Geo &g, int32_t *sorted, int32_t *seg_off, int64
                           int64_t *layout_stats, void *ws, uint64_t route_part, cudaStream_t st) {
     cudaError_t e;
     const int64_t tiles = (int64_t)g.L * g.R * g.tps;
-    k_layout_scatter<<<(unsigned)tiles, 256, 0, st>>>(ws_at<int32_t>(ws, g.off_pos), sorted,
-                                                      ws_at<WsHeader>(ws, 0), g, route_part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_layout_scatter, dim3((unsigned)tiles), dim3(256), 0, st, ws_at<int32_t>(ws, g.off_pos),
+                        sorted, ws_at<WsHeader>(ws, 0), g, route_part)) != cudaSuccess)
+        return e;
     return launch_copy(g, seg_off, send_counts, layout_stats, ws, route_part, 1, st);
 }
 
