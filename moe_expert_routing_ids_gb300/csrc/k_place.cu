@@ -10,9 +10,11 @@
 // ranks gains, apply it (gain C[a][rb] - C[a][ra] + C[b][ra] - C[b][rb] -
 // 2 w(a,b), C[x][r] = weight of x to rank r's members).  Lowest index on ties.
 //
-// One CTA of kPlThreads per layer.  Each choice is a block argmax over a key
-// (value desc, index asc); the connection array of the greedy phase and the
-// C table live in shared memory, the counts are read through L1/L2.
+// One CTA of kPlThreads per layer.  Each choice takes the best key (value
+// desc, index asc): the greedy choices are warp argmaxes made by one warp,
+// the swap choice a block argmax over all pairs.  The symmetrised weights are
+// staged in shared memory when E <= kPlSmemE (else read through L1/L2), with
+// the connection array and the C table.
 #include <climits>
 
 #include <cuda_runtime.h>
@@ -24,6 +26,7 @@ namespace {
 
 constexpr int kPlThreads = 1024;
 constexpr int kPlWarps = kPlThreads / 32;
+constexpr int kPlSmemE = 128;         // up to this E the weights are staged in shared memory
 
 struct PlKey {
     long long v;
@@ -53,16 +56,35 @@ __device__ __forceinline__ PlKey pl_block_best(PlKey k, PlKey *scratch) {
     return k;
 }
 
-__device__ __forceinline__ long long pl_w(const int64_t *co, int E, int a, int b) {
-    return a == b ? 0 : __ldg(co + (int64_t)a * E + b) + __ldg(co + (int64_t)b * E + a);
+// Best key over a warp (every lane gets it).
+__device__ __forceinline__ PlKey pl_warp_best(PlKey k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        PlKey q;
+        q.v = __shfl_xor_sync(0xffffffffu, k.v, o);
+        q.i = __shfl_xor_sync(0xffffffffu, k.i, o);
+        if (pl_better(q, k)) k = q;
+    }
+    return k;
 }
 
+// Pair weights: from the staged matrix W (E x E) when present, else from co.
+struct PlW {
+    const int64_t *co;
+    const long long *W;
+    int E;
+    __device__ __forceinline__ long long operator()(int a, int b) const {
+        if (W) return W[a * E + b];
+        return a == b ? 0 : __ldg(co + (int64_t)a * E + b) + __ldg(co + (int64_t)b * E + a);
+    }
+};
+
 // Within-rank weight of the map in part (block sum; every thread gets it).
-__device__ long long pl_within(const int64_t *co, int E, FastDiv fe, const int *part, long long *red) {
+__device__ long long pl_within(const PlW &wt, int E, FastDiv fe, const int *part, long long *red) {
     long long s = 0;
     for (int x = threadIdx.x; x < E * E; x += kPlThreads) {
         const int a = (int)fast_quot((unsigned)x, fe), b = x - a * E;
-        if (a < b && part[a] == part[b]) s += pl_w(co, E, a, b);
+        if (a < b && part[a] == part[b]) s += wt(a, b);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -76,10 +98,12 @@ __device__ long long pl_within(const int64_t *co, int E, FastDiv fe, const int *
 
 __global__ void __launch_bounds__(kPlThreads)
 k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int64_t *__restrict__ stats,
-        int E, int R, int max_iters, FastDiv fe) {
+        int E, int R, int max_iters, FastDiv fe, int staged) {
     extern __shared__ long long psm[];
-    long long *conn = psm;                            // [E] greedy connection / total weight
-    long long *C = conn + E;                          // [E][R]
+    long long *W = psm;                               // [E][E] when staged
+    long long *conn = psm + (staged ? (size_t)E * E : 0);   // [E] greedy connection
+    long long *tot = conn + E;                        // [E] total weight
+    long long *C = tot + E;                           // [E][R]
     int *part = reinterpret_cast<int *>(C + (size_t)E * R);   // [E]
     __shared__ PlKey scratch[kPlWarps];
     __shared__ long long red[kPlWarps];
@@ -87,57 +111,64 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
     const int64_t *co = co_all + (int64_t)l * E * E;
     const int per = E / R;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (staged)
+        for (int x = threadIdx.x; x < E * E; x += kPlThreads) {
+            const int a = (int)fast_quot((unsigned)x, fe), b = x - a * E;
+            W[x] = a == b ? 0 : __ldg(co + (int64_t)a * E + b) + __ldg(co + (int64_t)b * E + a);
+        }
+    const PlW wt{co, staged ? W : nullptr, E};
 
     // contiguous map, and every expert's total weight (a warp per row)
     for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = e / per;
     __syncthreads();
-    const long long w_contig = pl_within(co, E, fe, part, red);
+    const long long w_contig = pl_within(wt, E, fe, part, red);
     for (int a = w; a < E; a += kPlWarps) {
         long long s = 0;
-        for (int b = lane; b < E; b += 32) s += pl_w(co, E, a, b);
+        for (int b = lane; b < E; b += 32) s += wt(a, b);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) conn[a] = s;
+        if (lane == 0) tot[a] = s;
     }
     for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = -1;
     __syncthreads();
 
-    // greedy construction; the totals move to the first E entries of C, conn is reused
-    for (int e = threadIdx.x; e < E; e += kPlThreads) C[e] = conn[e];
-    __syncthreads();
-    for (int r = 0; r < R; ++r) {
-        PlKey k{LLONG_MIN, INT_MAX};
-        for (int a = threadIdx.x; a < E; a += kPlThreads)
-            if (part[a] < 0) {
-                const PlKey q{C[a], a};
-                if (pl_better(q, k)) k = q;
-            }
-        int pick = pl_block_best(k, scratch).i;
-        __syncthreads();
-        if (threadIdx.x == 0) part[pick] = r;
-        for (int b = threadIdx.x; b < E; b += kPlThreads) conn[b] = pl_w(co, E, pick, b);
-        __syncthreads();
-        for (int n = 1; n < per; ++n) {
-            PlKey q0{LLONG_MIN, INT_MAX};
-            for (int b = threadIdx.x; b < E; b += kPlThreads)
-                if (part[b] < 0) {
-                    const PlKey q{conn[b], b};
-                    if (pl_better(q, q0)) q0 = q;
+    // greedy construction by one warp: each choice is a warp argmax
+    if (w == 0) {
+        for (int r = 0; r < R; ++r) {
+            PlKey k{LLONG_MIN, INT_MAX};
+            for (int a = lane; a < E; a += 32)
+                if (part[a] < 0) {
+                    const PlKey q{tot[a], a};
+                    if (pl_better(q, k)) k = q;
                 }
-            pick = pl_block_best(q0, scratch).i;
-            __syncthreads();
-            if (threadIdx.x == 0) part[pick] = r;
-            for (int b = threadIdx.x; b < E; b += kPlThreads) conn[b] += pl_w(co, E, pick, b);
-            __syncthreads();
+            int pick = pl_warp_best(k).i;
+            __syncwarp();
+            if (lane == 0) part[pick] = r;
+            for (int b = lane; b < E; b += 32) conn[b] = wt(pick, b);
+            __syncwarp();
+            for (int n = 1; n < per; ++n) {
+                PlKey q0{LLONG_MIN, INT_MAX};
+                for (int b = lane; b < E; b += 32)
+                    if (part[b] < 0) {
+                        const PlKey q{conn[b], b};
+                        if (pl_better(q, q0)) q0 = q;
+                    }
+                pick = pl_warp_best(q0).i;
+                __syncwarp();
+                if (lane == 0) part[pick] = r;
+                for (int b = lane; b < E; b += 32) conn[b] += wt(pick, b);
+                __syncwarp();
+            }
         }
     }
-    const long long w_greedy = pl_within(co, E, fe, part, red);
+    __syncthreads();
+    const long long w_greedy = pl_within(wt, E, fe, part, red);
 
     // refinement: C[x][r], then best-gain swaps
     for (int x = threadIdx.x; x < E; x += kPlThreads) {
         long long *cx = C + (size_t)x * R;
         for (int r = 0; r < R; ++r) cx[r] = 0;
-        for (int m = 0; m < E; ++m) cx[part[m]] += pl_w(co, E, x, m);
+        for (int m = 0; m < E; ++m) cx[part[m]] += wt(x, m);
     }
     __syncthreads();
     long long swaps = 0;
@@ -149,7 +180,7 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
             const int pa = part[a], pb = part[b];
             if (pa == pb) continue;
             const long long g = C[(size_t)a * R + pb] - C[(size_t)a * R + pa] + C[(size_t)b * R + pa] -
-                                C[(size_t)b * R + pb] - 2 * pl_w(co, E, a, b);
+                                C[(size_t)b * R + pb] - 2 * wt(a, b);
             const PlKey q{g, x};
             if (g > 0 && pl_better(q, k)) k = q;
         }
@@ -159,7 +190,7 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
         const int pa = part[ba], pb = part[bb];
         __syncthreads();                              // every thread has read part
         for (int x = threadIdx.x; x < E; x += kPlThreads) {
-            const long long da = pl_w(co, E, x, ba), db = pl_w(co, E, x, bb);
+            const long long da = wt(x, ba), db = wt(x, bb);
             C[(size_t)x * R + pa] += db - da;
             C[(size_t)x * R + pb] += da - db;
         }
@@ -170,7 +201,7 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
         ++swaps;
         __syncthreads();
     }
-    const long long w_final = pl_within(co, E, fe, part, red);
+    const long long w_final = pl_within(wt, E, fe, part, red);
     for (int e = threadIdx.x; e < E; e += kPlThreads) main_rank[(int64_t)l * E + e] = part[e];
     if (threadIdx.x == 0) {
         stats[(int64_t)l * 4 + 0] = w_contig;
@@ -182,18 +213,20 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
 
 }  // namespace
 
-size_t place_smem_bytes(int E, int R) {
-    return (size_t)E * 8 + (size_t)E * R * 8 + (size_t)E * 4;
+size_t place_smem_bytes(int E, int R) {       // without the staged weights
+    return (size_t)2 * E * 8 + (size_t)E * R * 8 + (size_t)E * 4;
 }
 
 cudaError_t launch_place(int L, int E, int R, int max_iters, const int64_t *co, int32_t *main_rank,
                          int64_t *stats, cudaStream_t st) {
     if (L == 0) return cudaSuccess;
-    const size_t smem = place_smem_bytes(E, R);
+    size_t smem = place_smem_bytes(E, R);
+    const int staged = E <= kPlSmemE && smem + (size_t)E * E * 8 <= kSmemMax;
+    if (staged) smem += (size_t)E * E * 8;
     cudaError_t e = ensure_smem((const void *)k_place, smem);
     if (e != cudaSuccess) return e;
     k_place<<<L, kPlThreads, smem, st>>>(co, main_rank, stats, E, R, max_iters,
-                                         make_fast_div((unsigned)E));
+                                         make_fast_div((unsigned)E), staged);
     return cudaGetLastError();
 }
 
