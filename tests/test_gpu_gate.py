@@ -195,3 +195,18 @@ def test_gate_full_size_sampled():
     assert np.array_equal(got, want["ids"][0])
     assert np.array_equal(sc[0, rows].cpu().numpy().view(np.uint32), want["scores"][0].view(np.uint32))
     assert np.array_equal(P.buf.hist.cpu().numpy(), oracle.hist(ids.cpu().numpy(), w.R, E))
+
+
+@gpu
+def test_gate_of_an_empty_batch_and_no_layers():
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    cfg = _cfg(0, 16, 2, 4, 2, 1)
+    P = Planner(cfg, 2, dev)
+    x = torch.zeros((2, 0, 16), dtype=torch.float32, device=dev)
+    ids = torch.zeros((2, 0, 2), dtype=torch.int32, device=dev)
+    P.gate_hist(x, ids)
+    assert P.error() == 0
+    assert not P.buf.hist.cpu().numpy().any()
+    c = topo.make_cfg(**cfg)
+    topo.topo_gate_hist(c, 0, None, topo.TOPO_DTYPE_F32, None, None, None, P.buf.hist, P.ws, P.ws_bytes)

@@ -111,3 +111,9 @@ def test_placement_from_gpu_cooccurrence_feeds_the_plan_chain():
     got = P.numpy()
     assert np.array_equal(got["slot_expert"], p["slot_expert"])
     assert np.array_equal(got["dst_inst"], d)
+
+
+@gpu
+def test_place_of_no_layers_is_a_no_op():
+    _dev()
+    topo.topo_place_experts(0, 16, 4, 0, None, None, None)

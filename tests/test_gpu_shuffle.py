@@ -117,3 +117,15 @@ def test_shuffle_flags_bad_ids_and_maps():
     mr[3] = 4
     _, _, err = run_shuffle(ids, tr, 4, mr, dev)
     assert err == topo.TOPO_EMAP
+
+
+@gpu
+def test_shuffle_with_one_layer_or_no_tokens_is_a_no_op():
+    dev = _dev()
+    nb = topo.topo_shuffle_workspace_bytes(1, 16, 4)
+    ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device=dev)
+    topo.topo_shuffle_targets(1, 64, 16, 2, 4, None, None, None, None, None, ws, ws.numel())
+    ids = np.zeros((3, 0, 2), np.int32)
+    tr = np.zeros((2, 16, 16), np.int64)
+    t, st, err = run_shuffle(ids, tr, 4, None, dev)
+    assert err == 0 and t.shape == (2, 0) and not st.any()
