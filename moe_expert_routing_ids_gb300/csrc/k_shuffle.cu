@@ -14,9 +14,9 @@
 // two >= R, at most 32) scores kShIter tokens in turn, lane i holding ranks
 // i, i + G, ...; the group's lanes load a token's ids together (the next
 // token's already in flight) and pass each to all lanes by shuffle, and each
-// id's M row is one contiguous read, so a warp's groups read whole rows.  The best rank is a group shuffle
-// reduction; the next layer's slots on the target and on the source are
-// counted per lane and summed per CTA.
+// id's M row is one contiguous read, so a warp's groups read whole rows.  The
+// best rank is a group shuffle reduction; the next layer's slots on the target
+// and on the source are counted per lane and summed per CTA.
 #include <climits>
 
 #include <cuda_runtime.h>
@@ -29,6 +29,7 @@ namespace {
 constexpr int kShThreads = 256;
 constexpr size_t kShSmemTable = 96 * 1024;   // largest M table staged in shared memory
 constexpr int kShIter = 16;                  // tokens per group per CTA
+constexpr int kShIterT = 4;                  // tokens per thread per CTA (one thread per token)
 
 struct ShGeo {
     int L, T, E, k, R;
@@ -41,7 +42,8 @@ __device__ __forceinline__ int sh_rank(const ShGeo &g, int b) {
 }
 
 __global__ void __launch_bounds__(128)
-k_sh_table(const int64_t *__restrict__ tr, int64_t *__restrict__ M, WsHeader *hdr, ShGeo g) {
+k_sh_table(const int64_t *__restrict__ tr, int64_t *__restrict__ M, int32_t *__restrict__ M32, int *wide,
+           WsHeader *hdr, ShGeo g) {
     extern __shared__ unsigned long long acc[];              // [R]
     const int row = blockIdx.x;                              // l * E + a
     for (int r = threadIdx.x; r < g.R; r += blockDim.x) acc[r] = 0;
@@ -59,7 +61,15 @@ k_sh_table(const int64_t *__restrict__ tr, int64_t *__restrict__ M, WsHeader *hd
     if (bad) set_error(hdr, TOPO_EMAP);
     __syncthreads();
     int64_t *dst = M + (int64_t)row * g.R;
-    for (int r = threadIdx.x; r < g.R; r += blockDim.x) dst[r] = (int64_t)acc[r];
+    int32_t *dst32 = M32 + (int64_t)row * g.R;
+    const long long lim = INT_MAX / g.k;                     // k int32 additions cannot overflow
+    for (int r = threadIdx.x; r < g.R; r += blockDim.x) {
+        const long long v = (long long)acc[r];
+        dst[r] = v;
+        const bool fits = v <= lim && v >= -lim;
+        dst32[r] = fits ? (int32_t)v : 0;
+        if (!fits) atomicOr(wide, 1);
+    }
 }
 
 // A group's lanes hold a token's slots j = lane, lane + G, ... (KQ registers).
@@ -208,42 +218,50 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
 }
 
 // One thread per token, for R <= 2 * RB <= 16 and k <= KV: the token's R
-// scores live in registers as RB pairs; the table rows are padded to 2 * RB
-// entries and read in 16-byte chunks, lane i starting at chunk i mod RB, so
-// that the 8 lanes of a quarter-warp read 8 different bank groups.
-template <int RB, int KV>
-__global__ void __launch_bounds__(kShThreads)
-k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int32_t *__restrict__ target,
-              int64_t *stats, WsHeader *hdr, ShGeo g, int blocks_per_layer) {
-    extern __shared__ longlong2 tab2[];                      // [E][RB]
-    __shared__ long long red[4][kShThreads / 32];
-    const int l = blockIdx.x / blocks_per_layer;
-    const int blk = blockIdx.x - l * blocks_per_layer;
-    const int64_t *Ml = M + (int64_t)l * g.E * g.R;
-    long long *tab = reinterpret_cast<long long *>(tab2);
-    for (int x = threadIdx.x; x < g.E * 2 * RB; x += kShThreads) {
-        const int a = x / (2 * RB), r = x - a * 2 * RB;
-        tab[x] = r < g.R ? __ldg(Ml + (int64_t)a * g.R + r) : 0;
-    }
-    __syncthreads();
+// scores live in registers; the table rows are padded to P = 2 * RB entries
+// and read in 16-byte chunks, lane i starting at chunk i mod the chunk count,
+// so that the 8 lanes of a quarter-warp read different bank groups.  The
+// scores are int32 when the table kernel found every entry small enough for
+// k additions (flag *wide clear), else int64: half or all of the reads.
+template <int RB, int KV, typename S>
+__device__ __forceinline__ void sh_thread_tokens(const int32_t *__restrict__ ids, const S *tab,
+                                                 int32_t *__restrict__ target, int l, int64_t tok0,
+                                                 const ShGeo &g, int &on_tgt, int &on_src, int &moved,
+                                                 int &pairs, bool &bad) {
+    constexpr int P = 2 * RB;
+    constexpr int CPR = 16 / (int)sizeof(S);                 // ranks per 16-byte chunk
+    constexpr int NCH = P / CPR;
     const int lane = threadIdx.x & 31;
-    int on_tgt = 0, on_src = 0, moved = 0, pairs = 0;
-    bool bad = false;
+    const uint4 *tab4 = reinterpret_cast<const uint4 *>(tab);
     const int32_t *cur0 = ids + (int64_t)l * g.T * g.k;
     const int32_t *nxt0 = ids + (int64_t)(l + 1) * g.T * g.k;
-    const int64_t tok0 = (int64_t)blk * kShThreads * kShIter;
-    for (int it = 0; it < kShIter; ++it) {
+    // 16-byte id loads when every token's slots start 16-byte aligned
+    const bool vec = (g.k & 3) == 0 && ((reinterpret_cast<uintptr_t>(ids) & 15) == 0);
+    for (int it = 0; it < kShIterT; ++it) {
         const int64_t t = tok0 + (int64_t)it * kShThreads + threadIdx.x;
         if (t >= g.T) break;
         int a[KV], b[KV];
+        if (vec) {
 #pragma unroll
-        for (int j = 0; j < KV; ++j) {
-            a[j] = j < g.k ? __ldg(cur0 + t * g.k + j) : -1;
-            b[j] = j < g.k ? __ldg(nxt0 + t * g.k + j) : -1;
+            for (int j = 0; j < KV; j += 4) {
+                int4 x = make_int4(-1, -1, -1, -1), y = x;
+                if (j < g.k) {
+                    x = __ldg(reinterpret_cast<const int4 *>(cur0 + t * g.k + j));
+                    y = __ldg(reinterpret_cast<const int4 *>(nxt0 + t * g.k + j));
+                }
+                a[j] = x.x; a[j + 1] = x.y; a[j + 2] = x.z; a[j + 3] = x.w;
+                b[j] = y.x; b[j + 1] = y.y; b[j + 2] = y.z; b[j + 3] = y.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < KV; ++j) {
+                a[j] = j < g.k ? __ldg(cur0 + t * g.k + j) : -1;
+                b[j] = j < g.k ? __ldg(nxt0 + t * g.k + j) : -1;
+            }
         }
-        longlong2 acc[RB];
+        S acc[P];
 #pragma unroll
-        for (int c = 0; c < RB; ++c) acc[c] = make_longlong2(0, 0);
+        for (int c = 0; c < P; ++c) acc[c] = 0;
 #pragma unroll
         for (int j = 0; j < KV; ++j) {
             if (j >= g.k) break;
@@ -251,26 +269,33 @@ k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, in
                 bad = true;
                 continue;
             }
-            const longlong2 *row = tab2 + a[j] * RB;
+            const uint4 *row = tab4 + a[j] * NCH;
 #pragma unroll
-            for (int c = 0; c < RB; ++c) {
-                const longlong2 v = row[(c + lane) % RB];
-                acc[c].x += v.x;
-                acc[c].y += v.y;
+            for (int c = 0; c < NCH; ++c) {
+                const uint4 v = row[(c + lane) % NCH];
+                if constexpr (sizeof(S) == 8) {
+                    acc[c * CPR] += (S)(((unsigned long long)v.y << 32) | v.x);
+                    acc[c * CPR + 1] += (S)(((unsigned long long)v.w << 32) | v.z);
+                } else {
+                    acc[c * CPR] += (S)(int)v.x;
+                    acc[c * CPR + 1] += (S)(int)v.y;
+                    acc[c * CPR + 2] += (S)(int)v.z;
+                    acc[c * CPR + 3] += (S)(int)v.w;
+                }
             }
         }
         const int s = (int)fast_quot((unsigned)t, g.tpr);
-        long long best = LLONG_MIN, ssc = 0;
-        int br = 0;
+        S best = 0, ssc = 0;
+        int br = -1;
 #pragma unroll
-        for (int c = 0; c < RB; ++c) {
-            const int r0 = ((c + lane) % RB) * 2;
+        for (int c = 0; c < NCH; ++c) {
+            const int r0 = ((c + lane) % NCH) * CPR;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < CPR; ++h) {
                 const int r = r0 + h;
-                const long long v = h ? acc[c].y : acc[c].x;
+                const S v = acc[c * CPR + h];
                 if (r < g.R) {
-                    if (v > best || (v == best && r < br)) {
+                    if (br < 0 || v > best || (v == best && r < br)) {
                         best = v;
                         br = r;
                     }
@@ -294,6 +319,45 @@ k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, in
             ++pairs;
         }
     }
+}
+
+template <int RB, int KV>
+__global__ void __launch_bounds__(kShThreads, 3)
+k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, const int32_t *__restrict__ M32,
+              const int *__restrict__ wide, int32_t *__restrict__ target, int64_t *stats, WsHeader *hdr, ShGeo g,
+              int blocks_per_layer) {
+    extern __shared__ uint4 tabs[];                          // [E][2 * RB] scores of the chosen width
+    __shared__ long long red[4][kShThreads / 32];
+    constexpr int P = 2 * RB;
+    const int l = blockIdx.x / blocks_per_layer;
+    const int blk = blockIdx.x - l * blocks_per_layer;
+    const bool w64 = __ldg(wide) != 0;                       // uniform over the launch
+    if (w64) {
+        long long *tab = reinterpret_cast<long long *>(tabs);
+        const int64_t *Ml = M + (int64_t)l * g.E * g.R;
+        for (int x = threadIdx.x; x < g.E * P; x += kShThreads) {
+            const int a = x / P, r = x - a * P;
+            tab[x] = r < g.R ? __ldg(Ml + (int64_t)a * g.R + r) : 0;
+        }
+    } else {
+        int *tab = reinterpret_cast<int *>(tabs);
+        const int32_t *Ml = M32 + (int64_t)l * g.E * g.R;
+        for (int x = threadIdx.x; x < g.E * P; x += kShThreads) {
+            const int a = x / P, r = x - a * P;
+            tab[x] = r < g.R ? __ldg(Ml + (int64_t)a * g.R + r) : 0;
+        }
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    int on_tgt = 0, on_src = 0, moved = 0, pairs = 0;
+    bool bad = false;
+    const int64_t tok0 = (int64_t)blk * kShThreads * kShIterT;
+    if (w64)
+        sh_thread_tokens<RB, KV, long long>(ids, reinterpret_cast<const long long *>(tabs), target, l, tok0, g,
+                                            on_tgt, on_src, moved, pairs, bad);
+    else
+        sh_thread_tokens<RB, KV, int>(ids, reinterpret_cast<const int *>(tabs), target, l, tok0, g, on_tgt,
+                                      on_src, moved, pairs, bad);
     if (bad) set_error(hdr, TOPO_ERANGE);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -319,17 +383,18 @@ k_sh_target_t(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, in
 }
 
 template <int RB, int KV>
-cudaError_t run_target_t(const ShGeo &g, const int32_t *ids, const int64_t *M, int32_t *target,
-                         int64_t *stats, WsHeader *hdr, cudaStream_t st) {
-    const int tok_per_block = kShThreads * kShIter;
+cudaError_t run_target_t(const ShGeo &g, const int32_t *ids, const int64_t *M, const int32_t *M32,
+                         const int *wide, int32_t *target, int64_t *stats, WsHeader *hdr, cudaStream_t st) {
+    const int tok_per_block = kShThreads * kShIterT;
     const int bpl = (g.T + tok_per_block - 1) / tok_per_block;
     const int64_t blocks = (int64_t)(g.L - 1) * bpl;
     if (blocks == 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    const size_t tab = (size_t)g.E * RB * 16;
+    const size_t tab = (size_t)g.E * RB * 16;                // room for the int64 table
     cudaError_t e = ensure_smem((const void *)k_sh_target_t<RB, KV>, tab);
     if (e != cudaSuccess) return e;
-    k_sh_target_t<RB, KV><<<(unsigned)blocks, kShThreads, tab, st>>>(ids, M, target, stats, hdr, g, bpl);
+    k_sh_target_t<RB, KV><<<(unsigned)blocks, kShThreads, tab, st>>>(ids, M, M32, wide, target, stats, hdr, g,
+                                                                      bpl);
     return cudaGetLastError();
 }
 
@@ -364,9 +429,11 @@ cudaError_t run_target(const ShGeo &g, const int32_t *ids, const int64_t *M, int
 
 }  // namespace
 
+// Workspace: header, the int32 "wide" flag (own 256 bytes), the int64 table,
+// its int32 copy.
 size_t shuffle_ws_bytes(int L, int E, int R) {
-    const size_t table = (size_t)(L > 1 ? L - 1 : 0) * E * R * 8;
-    return sizeof(WsHeader) + ((table + 255) & ~size_t(255));
+    const size_t n = (size_t)(L > 1 ? L - 1 : 0) * E * R;
+    return sizeof(WsHeader) + 256 + ((n * 8 + 255) & ~size_t(255)) + ((n * 4 + 255) & ~size_t(255));
 }
 
 cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
@@ -379,22 +446,26 @@ cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids
     g.er = make_fast_div((unsigned)(main_rank ? 1 : E / R));
     g.main_rank = main_rank;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
-    int64_t *M = ws_at<int64_t>(ws, sizeof(WsHeader));
+    const size_t n = (size_t)(L - 1) * E * R;
+    int *wide = ws_at<int>(ws, sizeof(WsHeader));
+    int64_t *M = ws_at<int64_t>(ws, sizeof(WsHeader) + 256);
+    int32_t *M32 = ws_at<int32_t>(ws, sizeof(WsHeader) + 256 + ((n * 8 + 255) & ~size_t(255)));
     cudaError_t e = cudaMemsetAsync(stats, 0, (size_t)(L - 1) * 4 * 8, st);
     if (e != cudaSuccess) return e;
-    k_sh_table<<<(unsigned)((L - 1) * E), 128, (size_t)R * 8, st>>>(tr, M, hdr, g);
+    if ((e = cudaMemsetAsync(wide, 0, sizeof(int), st)) != cudaSuccess) return e;
+    k_sh_table<<<(unsigned)((L - 1) * E), 128, (size_t)R * 8, st>>>(tr, M, M32, wide, hdr, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (T == 0) return cudaSuccess;
     if (R <= 16 && k <= 16 && (size_t)E * 128 <= kShSmemTable) {   // one thread per token
         const int rb = (R + 1) / 2;
         if (k <= 8) {
-            if (rb <= 2) return run_target_t<2, 8>(g, ids, M, target, stats, hdr, st);
-            if (rb <= 4) return run_target_t<4, 8>(g, ids, M, target, stats, hdr, st);
-            return run_target_t<8, 8>(g, ids, M, target, stats, hdr, st);
+            if (rb <= 2) return run_target_t<2, 8>(g, ids, M, M32, wide, target, stats, hdr, st);
+            if (rb <= 4) return run_target_t<4, 8>(g, ids, M, M32, wide, target, stats, hdr, st);
+            return run_target_t<8, 8>(g, ids, M, M32, wide, target, stats, hdr, st);
         }
-        if (rb <= 2) return run_target_t<2, 16>(g, ids, M, target, stats, hdr, st);
-        if (rb <= 4) return run_target_t<4, 16>(g, ids, M, target, stats, hdr, st);
-        return run_target_t<8, 16>(g, ids, M, target, stats, hdr, st);
+        if (rb <= 2) return run_target_t<2, 16>(g, ids, M, M32, wide, target, stats, hdr, st);
+        if (rb <= 4) return run_target_t<4, 16>(g, ids, M, M32, wide, target, stats, hdr, st);
+        return run_target_t<8, 16>(g, ids, M, M32, wide, target, stats, hdr, st);
     }
     if (R <= 4) return run_target<4, 1>(g, ids, M, target, stats, hdr, st);
     if (R <= 8) return run_target<8, 1>(g, ids, M, target, stats, hdr, st);

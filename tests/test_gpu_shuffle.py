@@ -129,3 +129,17 @@ def test_shuffle_with_one_layer_or_no_tokens_is_a_no_op():
     tr = np.zeros((2, 16, 16), np.int64)
     t, st, err = run_shuffle(ids, tr, 4, None, dev)
     assert err == 0 and t.shape == (2, 0) and not st.any()
+
+
+@gpu
+@pytest.mark.parametrize("R", [4, 16, 64])
+def test_shuffle_with_counts_too_large_for_int32_scores(R):
+    dev = _dev()
+    rng = np.random.default_rng(R)
+    L, T, E, k = 2, 64 * 16, 64, 6
+    ids = _ids(rng, L, T, E, k)
+    tr = rng.integers(0, 1 << 40, size=(L - 1, E, E)).astype(np.int64)
+    t, st, err = run_shuffle(ids, tr, R, None, dev)
+    assert err == 0
+    et, est = oracle.shuffle(ids, tr, R)
+    assert np.array_equal(t, et) and np.array_equal(st, est)
