@@ -796,7 +796,10 @@ def run_ours(args, rank, world, local_rank):
     if clk:
         line["clocks"] = clk
     if not args.skip_e2e:
-        line["e2e"] = e2e(P, w, ids, dev, stream, max(3, min(args.steps, 20)))
+        n_e2e = max(3, min(args.steps, 20))
+        line["e2e"] = e2e(P, w, ids, dev, stream, n_e2e)
+        line["e2e_full_outputs"] = e2e(P, w, ids, dev, stream, n_e2e, _outputs,
+                                       "every plan and layout output (dst_inst, sorted_pairs, tables)")
     if not args.skip_secondary:
         line["plan_latency"] = secondary_plan_latency(dev, stream)
         line["cooccur"] = secondary_cooccur(dev, stream, hbm)
@@ -816,10 +819,18 @@ def _outputs(Q):
             b.rank_load, b.stats]
 
 
-def e2e(P, w, ids, dev, stream, steps):
+def _result(Q):
+    """The step's result read back by the host: the plan and layout statistics
+    and the rank loads (the plan and layout themselves stay on the device for
+    the dispatch that consumes them)."""
+    b = Q.buf
+    return [b.stats, b.layout_stats, b.rank_load]
+
+
+def e2e(P, w, ids, dev, stream, steps, outputs=_result, what="the plan and layout statistics"):
     """Same metric through host buffers.  Every step copies its ids in from
-    pinned host memory, runs the three calls, and copies the plan and layout
-    outputs back to pinned host memory.  Steps are pipelined over two slots
+    pinned host memory, runs the three calls, and copies `outputs` back to
+    pinned host memory.  Steps are pipelined over two slots
     (two planners, two device input buffers): step i's input copy and step
     i-1's output copy overlap step i's compute, on their own streams.  Timed
     from before the first input copy to after the last output copy."""
@@ -827,7 +838,7 @@ def e2e(P, w, ids, dev, stream, steps):
     from moe_expert_routing_ids_gb300.planner import Planner
     Ps = [P, Planner(w.plan_cfg, w.n_layers, dev, stream=stream)]
     h_ids = torch.from_numpy(ids).pin_memory()
-    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in _outputs(Q)] for Q in Ps]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs(Q)] for Q in Ps]
     d_ids = [torch.empty(ids.shape, dtype=torch.int32, device=dev) for _ in Ps]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     in_done = [torch.cuda.Event() for _ in Ps]
@@ -848,7 +859,7 @@ def e2e(P, w, ids, dev, stream, steps):
         run_done[k].record(stream)
         s_out.wait_event(run_done[k])
         with torch.cuda.stream(s_out):
-            for h, d in zip(h_out[k], _outputs(Q)):
+            for h, d in zip(h_out[k], outputs(Q)):
                 h.copy_(d, non_blocking=True)
         out_done[k].record(s_out)
 
@@ -867,8 +878,9 @@ def e2e(P, w, ids, dev, stream, steps):
             raise RuntimeError("device error in the end-to-end run")
     return {"value": ids.size / (ms * 1e-3), "unit": "pairs/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(ids.nbytes),
-            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in _outputs(P))),
-            "steps": steps, "pipeline": "2 slots; input copy, compute, output copy on 3 streams"}
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outputs(P))),
+            "read_back": what, "steps": steps,
+            "pipeline": "2 slots; input copy, compute, output copy on 3 streams"}
 
 
 def cpu_baseline(w, ids):
