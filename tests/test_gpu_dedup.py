@@ -155,3 +155,18 @@ def test_dedup_flags_an_instance_out_of_range():
     d[0, 17] = 12
     got, err = run_dedup(cfg, 1, torch.as_tensor(d, device=dev), dev)
     assert err == topo.TOPO_ESTATE
+
+
+@gpu
+def test_dedup_full_size_stress_workload():
+    # the T = 1048576, E = 512, k = 10, R = 128 workload, all 4 microbatches, as
+    # bench.py times it: every output against the oracle
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    w = W.STRESS
+    P = Planner(w.plan_cfg, w.n_layers, dev)
+    P.run(torch.as_tensor(w.ids(), device=dev))
+    assert P.error() == 0
+    got, err = run_dedup(w.plan_cfg, w.n_layers, P.buf.dst_inst, dev)
+    assert err == 0
+    assert_same(got, oracle.dedup(w.plan_cfg, P.buf.dst_inst.cpu().numpy()))

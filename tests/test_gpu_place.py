@@ -117,3 +117,18 @@ def test_placement_from_gpu_cooccurrence_feeds_the_plan_chain():
 def test_place_of_no_layers_is_a_no_op():
     _dev()
     topo.topo_place_experts(0, 16, 4, 0, None, None, None)
+
+
+@gpu
+def test_place_full_size_cooccurrence_workload():
+    # all 8 layers of the co-occurrence workload at EP8, as bench.py times it
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Cooccur
+    dev = _dev()
+    w = W.COOCCUR
+    C = Cooccur(w.n_layers, w.T, w.E, w.k, dev, transitions=False)
+    C.run(torch.as_tensor(w.ids(), device=dev))
+    assert C.error() == 0
+    mr, st = run_place(C.co, 8, dev)
+    emr, est = oracle.place(C.co.cpu().numpy(), 8)
+    assert np.array_equal(mr, emr) and np.array_equal(st, est)

@@ -143,3 +143,21 @@ def test_shuffle_with_counts_too_large_for_int32_scores(R):
     assert err == 0
     et, est = oracle.shuffle(ids, tr, R)
     assert np.array_equal(t, et) and np.array_equal(st, est)
+
+
+@gpu
+def test_shuffle_full_size_cooccurrence_workload():
+    # the 8-layer, 262144-token, E = 128, k = 8 workload as EP16, as bench.py
+    # times it, with its own GPU transition counts
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Cooccur
+    dev = _dev()
+    w = W.COOCCUR
+    ids = w.ids()
+    C = Cooccur(w.n_layers, w.T, w.E, w.k, dev)
+    C.run(torch.as_tensor(ids, device=dev))
+    assert C.error() == 0
+    t, st, err = run_shuffle(ids, C.tr, 16, None, dev)
+    assert err == 0
+    et, est = oracle.shuffle(ids, C.tr.cpu().numpy(), 16)
+    assert np.array_equal(t, et) and np.array_equal(st, est)
