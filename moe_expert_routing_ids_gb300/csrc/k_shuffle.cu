@@ -9,8 +9,10 @@
 //                 that rank is among the best, else the lowest best rank.
 //
 // k_sh_table: one CTA per (layer, expert a) sums the row tr_l[a][.] by rank
-// (shared 64-bit atomics).  For R <= 16, k_sh_target_t: one thread per token
-// (below).  Otherwise k_sh_target: a group of G lanes (G = the power of
+// (shared 64-bit atomics), writes it as int64 and as int32, and flags the call
+// when some entry is too large for k int32 additions.  For R <= 16,
+// k_sh_target_t: one thread per token (below), int32 scores unless flagged.
+// Otherwise k_sh_target: a group of G lanes (G = the power of
 // two >= R, at most 32) scores kShIter tokens in turn, lane i holding ranks
 // i, i + G, ...; the group's lanes load a token's ids together (the next
 // token's already in flight) and pass each to all lanes by shuffle, and each
