@@ -501,7 +501,7 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    if (remaining <= 0) break;
+                    if (remaining <= 0 || base + 32 * u >= R) break;   // no source left to take from
                     const int s = base + 32 * u + lane;
                     const int incl = warp_incl_scan(v[u]);
                     const int excl = incl - v[u];
