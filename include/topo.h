@@ -189,7 +189,8 @@ int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, 
  * E/R experts -- the unassigned expert of largest total weight, then
  * repeatedly the unassigned expert of largest weight to the rank's members;
  * then, while the best swap of two experts on different ranks raises the
- * within-rank weight, apply it (at most max_iters swaps when max_iters > 0).
+ * within-rank weight, apply it (at most max_iters swaps when max_iters > 0,
+ * and never more than 2^20).
  * Lowest index on every tie.
  * co:        device int64 [L][E][E] (topo_cooccur's co-selection counts).
  * main_rank: device int32 [L][E] (written): a map for topo_cfg.main_rank.

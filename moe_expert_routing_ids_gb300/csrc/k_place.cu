@@ -27,6 +27,7 @@ namespace {
 constexpr int kPlThreads = 1024;
 constexpr int kPlWarps = kPlThreads / 32;
 constexpr int kPlSmemE = 128;         // up to this E the weights are staged in shared memory
+constexpr long long kPlaceSwapCap = 1 << 20;   // swaps at most (each raises the weight; a bound on time)
 
 struct PlKey {
     long long v;
@@ -172,7 +173,7 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
     }
     __syncthreads();
     long long swaps = 0;
-    while (max_iters == 0 || swaps < max_iters) {
+    while ((max_iters == 0 || swaps < max_iters) && swaps < kPlaceSwapCap) {
         PlKey k{0, INT_MAX};                          // only a positive gain is taken
         for (int x = threadIdx.x; x < E * E; x += kPlThreads) {
             const int a = (int)fast_quot((unsigned)x, fe), b = x - a * E;

@@ -917,7 +917,7 @@ int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const 
 /* experts on different ranks raises the within-rank weight, apply the best  */
 /* one (gain C[a][rb] - C[a][ra] + C[b][ra] - C[b][rb] - 2 w(a,b), with      */
 /* C[x][r] the weight of x to rank r's members), at most max_iters swaps     */
-/* when max_iters > 0.  Every choice takes the lowest index on ties (a       */
+/* when max_iters > 0 and never more than 2^20 (a bound on time).  Every choice takes the lowest index on ties (a       */
 /* before b for swaps, a < b).  stats = {within-rank weight of the           */
 /* contiguous map e / (E/R), after the greedy construction, final, swaps}.   */
 /* ------------------------------------------------------------------------ */
@@ -979,7 +979,7 @@ int oracle_place(int L, int E, int R, int max_iters, const int64_t *co, int32_t 
             for (int m = 0; m < E; m++) C[(int64_t)x * R + part[m]] += w[(int64_t)x * E + m];
         }
         int64_t swaps = 0;
-        while (max_iters == 0 || swaps < max_iters) {
+        while ((max_iters == 0 || swaps < max_iters) && swaps < (1 << 20)) {
             int ba = -1, bb = -1;
             int64_t bg = 0;
             for (int a = 0; a < E; a++)
