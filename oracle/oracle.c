@@ -917,9 +917,10 @@ int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const 
 /* experts on different ranks raises the within-rank weight, apply the best  */
 /* one (gain C[a][rb] - C[a][ra] + C[b][ra] - C[b][rb] - 2 w(a,b), with      */
 /* C[x][r] the weight of x to rank r's members), at most max_iters swaps     */
-/* when max_iters > 0 and never more than 2^20 (a bound on time).  Every choice takes the lowest index on ties (a       */
-/* before b for swaps, a < b).  stats = {within-rank weight of the           */
-/* contiguous map e / (E/R), after the greedy construction, final, swaps}.   */
+/* when max_iters > 0 and never more than 2^20 (a bound on time).  Every     */
+/* choice takes the lowest index on ties (a before b for swaps, a < b).      */
+/* stats = {within-rank weight of the contiguous map e / (E/R), after the    */
+/* greedy construction, final, swaps}.                                       */
 /* ------------------------------------------------------------------------ */
 
 static int64_t place_within(int E, const int64_t *w, const int32_t *part) {
