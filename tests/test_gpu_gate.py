@@ -98,6 +98,11 @@ CASES = {
     "e100_k5_bf16_unaligned_rows": (_cfg(4 * 100, 100, 5, 4, 2, 1), 1, "bf16", True),
     "e64_k40_exact_path": (_cfg(2 * 64, 64, 40, 2, 2, 1), 1, "f32", True),
     "e256_k32": (_cfg(8 * 40, 256, 32, 8, 8, 1), 1, "f32", False),
+    # 16 lanes per token (128 < E <= 512, k <= 16) at its edges, and k = 17 just past them
+    "e129_k16_f32_unaligned_rows": (_cfg(3 * 150, 129, 16, 3, 3, 1), 1, "f32", True),
+    "e130_k16_bf16_scalar_rows": (_cfg(2 * 150, 130, 16, 2, 2, 1), 1, "bf16", True),
+    "e384_k17_f32": (_cfg(4 * 150, 384, 17, 4, 2, 1), 1, "f32", True),
+    "e448_k1_bf16_three_layers": (_cfg(2 * 131, 448, 1, 2, 2, 1), 3, "bf16", False),
 }
 
 
@@ -125,22 +130,25 @@ def test_gate_without_scores_output():
 
 @gpu
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_gate_ties_signed_zeros_and_nans(dt):
+@pytest.mark.parametrize("E", [96, 200, 512])      # 32 lanes per token; 16 lanes, ragged; 16, full
+def test_gate_ties_signed_zeros_and_nans(dt, E):
     dev = _dev()
     rng = np.random.default_rng(7)
-    cfg = _cfg(4 * 256, 96, 6, 4, 2, 1)
-    x = rng.integers(-2, 3, size=(1, 1024, 96)).astype(np.float32)   # > 64 candidates: exact path
+    cfg = _cfg(4 * 256, E, 6, 4, 2, 1)
+    x = rng.integers(-2, 3, size=(1, 1024, E)).astype(np.float32)    # > 64 candidates: exact path
     x[rng.random(x.shape) < 0.1] = -0.0
     x[rng.random(x.shape) < 0.05] = np.nan
     x[0, 5, :] = np.nan                                             # all NaN
-    x[0, 9, :90] = np.nan                                           # exactly k numbers left
+    x[0, 9, :E - 6] = np.nan                                        # exactly k numbers left
+    x[0, 10, E - 7:] = np.nan                                       # k + 1, all in the last lanes
     x[0, 11, 3] = np.inf
     x[0, 12, :] = -np.inf
-    x[0, 100:200] = _gumbel(rng, (100, 96))                         # fast path rows
+    x[0, 100:200] = _gumbel(rng, (100, E))                          # fast path rows
+    x[0, 300] = 0.0                                                 # all equal
     if dt == "bf16":
         x = _bf16(x)
     _check(cfg, 1, x, None, dev)
-    _check(cfg, 1, x, np.zeros(96, np.float32), dev)               # +0 bias: -0 + 0 = +0
+    _check(cfg, 1, x, np.zeros(E, np.float32), dev)                # +0 bias: -0 + 0 = +0
 
 
 @gpu
