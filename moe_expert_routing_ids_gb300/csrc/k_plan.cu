@@ -337,6 +337,7 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
     pdl_trigger();
     __shared__ Key kbuf[kRefineMaxWarps];
     __shared__ int cbuf[kRefineMaxWarps];
+    __shared__ int lbuf[kRefineMaxWarps];
     const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nthr = blockDim.x, nwarp = nthr >> 5;
     const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
@@ -405,6 +406,7 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
         const int jb = __ffs(__ballot_sync(0xffffffffu, myL == Lb)) - 1;
         Key best{0ull, 0ull, 0u};
         int bc = 0;                              // packed (lb << 5 | jt) of best
+        int blt = -1;                            // its local index on jt, -1: a new replica
         int lb = c_lb0, jt = c_jt0;
         for (int c = tid; c < ncand; c += nthr) {
             if (jt != jb) {
@@ -435,6 +437,7 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
                         if (key_gt(k, best)) {
                             best = k;
                             bc = (lb << 5) | jt;
+                            blt = lt;
                         }
                     }
                 }
@@ -450,30 +453,33 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
         wk.b = __shfl_sync(0xffffffffu, best.b, wl);
         wk.c = __shfl_sync(0xffffffffu, best.c, wl);
         int wc = __shfl_sync(0xffffffffu, bc, wl);
+        int wlt = __shfl_sync(0xffffffffu, blt, wl);
         if (nwarp > 1) {
             if (lane == 0) {
                 kbuf[w] = wk;
                 cbuf[w] = wc;
+                lbuf[w] = wlt;
             }
             __syncthreads();
             wk = kbuf[0];
             wc = cbuf[0];
+            wlt = lbuf[0];
             for (int x = 1; x < nwarp; ++x)
                 if (key_gt(kbuf[x], wk)) {
                     wk = kbuf[x];
                     wc = cbuf[x];
+                    wlt = lbuf[x];
                 }
         }
         if (wk.a == 0) break;                   // uniform: every thread saw the same keys
         if (w == 0) {
             const int delta = (int)(wk.a >> 32);
             const int blb = wc >> 5, bjt = wc & 31;
-            const int e = xe[jb * nl + blb];
+            const int e = (int)((~wk.c) >> 5);
             const int xcv = xc[jb * nl + blb];
             const int rb = r0 + jb, rt = r0 + bjt;
-            int lt = hl[bjt * E + e];
-            const bool is_new = lt < 0;
-            if (is_new) lt = ER + used[bjt];
+            const bool is_new = wlt < 0;
+            const int lt = is_new ? ER + used[bjt] : wlt;
             const int m_rt = min(*qcell(rt, jb, blb), delta);
             int remaining = delta - m_rt;
             __syncwarp();
