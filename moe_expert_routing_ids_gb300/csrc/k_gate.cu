@@ -112,7 +112,7 @@ __device__ __forceinline__ unsigned long long g_key(float v, int e) {
 // G lanes per token (32 / G tokens per warp at a time); FULL: E == G * VPL,
 // every slot of every lane holds an expert.
 template <int VPL, int G, bool BF, int VEC, bool FULL>
-__global__ void __launch_bounds__(kGateThreads, VPL >= 32 ? 2 : 3)
+__global__ void __launch_bounds__(kGateThreads, 3)
 k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, int32_t *__restrict__ ids,
              float *__restrict__ scores, int32_t *__restrict__ tile_cnt, Geo g) {
     constexpr int kGroups = kGateThreads / G;                  // token groups per CTA
@@ -156,15 +156,10 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
     const int64_t row0 = (int64_t)l * g.T + (int64_t)s * g.tpr + tok0;   // token row of the tile
     const size_t esz = BF ? 2 : 4;
     const char *base = reinterpret_cast<const char *>(logits);
-    float nx[VPL];
-    if (grp < ntok) g_load<VPL, G, BF, VEC>(base + (size_t)(row0 + grp) * E * esz, E, gl, nx);
     for (int i = grp; i < ntok; i += kGroups) {                  // i uniform in the group
         const void *row = base + (size_t)(row0 + i) * E * esz;
         float sc[VPL];                                            // scores, in place of the logits
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) sc[u] = nx[u];
-        if (i + kGroups < ntok)                                   // next token in flight
-            g_load<VPL, G, BF, VEC>(base + (size_t)(row0 + i + kGroups) * E * esz, E, gl, nx);
+        g_load<VPL, G, BF, VEC>(row, E, gl, sc);
         if (bias) {                                               // same chunking as the loads
             if (VEC > 1) {
 #pragma unroll
