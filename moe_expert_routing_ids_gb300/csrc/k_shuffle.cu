@@ -31,7 +31,7 @@ namespace {
 constexpr int kShThreads = 256;
 constexpr size_t kShSmemTable = 96 * 1024;   // largest M table staged in shared memory
 constexpr int kShIter = 16;                  // tokens per group per CTA
-constexpr int kShIterT = 4;                  // tokens per thread per CTA (one thread per token)
+constexpr int kShIterT = 8;                  // tokens per thread per CTA (one thread per token)
 
 struct ShGeo {
     int L, T, E, k, R;
