@@ -12,7 +12,10 @@
 //
 // One CTA of kPlThreads per layer.  Each choice takes the best key (value
 // desc, index asc): the greedy choices are warp argmaxes made by one warp,
-// the swap choice a block argmax over all pairs.  The symmetrised weights are
+// the swap choice a block argmax over all pairs.  When every pair weight lies
+// in [0, 2^36) -- always so for co-selection counts -- the greedy sums stay
+// below 2^47 and a key packs into 64 bits (value << 16 | 0xffff - index), so
+// that a warp argmax is two 32-bit max reductions.  The symmetrised weights are
 // staged in shared memory when E <= kPlSmemE (else read through L1/L2), with
 // the connection array and the C table.
 #include <climits>
@@ -28,6 +31,7 @@ constexpr int kPlThreads = 1024;
 constexpr int kPlWarps = kPlThreads / 32;
 constexpr int kPlSmemE = 128;         // up to this E the weights are staged in shared memory
 constexpr long long kPlaceSwapCap = 1 << 20;   // swaps at most (each raises the weight; a bound on time)
+constexpr long long kPlPackedW = 1ll << 36;    // pair weights below this: packed greedy keys
 
 struct PlKey {
     long long v;
@@ -67,6 +71,13 @@ __device__ __forceinline__ PlKey pl_warp_best(PlKey k) {
         if (pl_better(q, k)) k = q;
     }
     return k;
+}
+
+// Index of the best packed key over a warp (every lane gets it); key 0: none.
+__device__ __forceinline__ int pl_warp_best_packed(unsigned long long key) {
+    const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(key >> 32));
+    const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(key >> 32) == hi ? (unsigned)key : 0u);
+    return 0xffff - (int)(lo & 0xffffu);
 }
 
 // Pair weights: from the staged matrix W (E x E) when present, else from co.
@@ -123,38 +134,50 @@ k_place(const int64_t *__restrict__ co_all, int32_t *__restrict__ main_rank, int
     for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = e / per;
     __syncthreads();
     const long long w_contig = pl_within(wt, E, fe, part, red);
+    bool wide = false;                                // a weight outside [0, kPlPackedW)
     for (int a = w; a < E; a += kPlWarps) {
         long long s = 0;
-        for (int b = lane; b < E; b += 32) s += wt(a, b);
+        for (int b = lane; b < E; b += 32) {
+            const long long v = wt(a, b);
+            wide |= v < 0 || v >= kPlPackedW;
+            s += v;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (lane == 0) tot[a] = s;
     }
     for (int e = threadIdx.x; e < E; e += kPlThreads) part[e] = -1;
-    __syncthreads();
+    const bool packed = !__syncthreads_or(wide);     // uniform; also the barrier
 
-    // greedy construction by one warp: each choice is a warp argmax
-    if (w == 0) {
-        for (int r = 0; r < R; ++r) {
-            PlKey k{LLONG_MIN, INT_MAX};
+    // greedy construction by one warp: each choice is a warp argmax over the
+    // unassigned experts of val (tot, then the connection to the rank)
+    auto choose = [&](const long long *val) -> int {
+        if (packed) {
+            unsigned long long key = 0;
             for (int a = lane; a < E; a += 32)
                 if (part[a] < 0) {
-                    const PlKey q{tot[a], a};
-                    if (pl_better(q, k)) k = q;
+                    const unsigned long long q = ((unsigned long long)val[a] << 16) | (unsigned)(0xffff - a);
+                    key = q > key ? q : key;
                 }
-            int pick = pl_warp_best(k).i;
+            return pl_warp_best_packed(key);
+        }
+        PlKey k{LLONG_MIN, INT_MAX};
+        for (int a = lane; a < E; a += 32)
+            if (part[a] < 0) {
+                const PlKey q{val[a], a};
+                if (pl_better(q, k)) k = q;
+            }
+        return pl_warp_best(k).i;
+    };
+    if (w == 0) {
+        for (int r = 0; r < R; ++r) {
+            int pick = choose(tot);
             __syncwarp();
             if (lane == 0) part[pick] = r;
             for (int b = lane; b < E; b += 32) conn[b] = wt(pick, b);
             __syncwarp();
             for (int n = 1; n < per; ++n) {
-                PlKey q0{LLONG_MIN, INT_MAX};
-                for (int b = lane; b < E; b += 32)
-                    if (part[b] < 0) {
-                        const PlKey q{conn[b], b};
-                        if (pl_better(q, q0)) q0 = q;
-                    }
-                pick = pl_warp_best(q0).i;
+                pick = choose(conn);
                 __syncwarp();
                 if (lane == 0) part[pick] = r;
                 for (int b = lane; b < E; b += 32) conn[b] += wt(pick, b);

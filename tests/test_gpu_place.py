@@ -84,6 +84,24 @@ def test_place_matches_the_oracle(name):
 
 
 @gpu
+@pytest.mark.parametrize("kind", ["wide", "negative"])
+def test_place_weights_outside_the_packed_key_range(kind):
+    # pair weights >= 2^36 or < 0 take the general (value, index) key path
+    dev = _dev()
+    rng = np.random.default_rng(5)
+    E, R = 64, 8
+    if kind == "wide":
+        co = rng.integers(0, 50, size=(1, E, E)).astype(np.int64)
+        co += (1 << 40) * (rng.random((1, E, E)) < 0.05)
+    else:
+        co = rng.integers(-30, 50, size=(1, E, E)).astype(np.int64)
+    mr, st = run_place(co, R, dev)
+    emr, est = oracle.place(co, R)
+    assert np.array_equal(mr, emr)
+    assert np.array_equal(st, est)
+
+
+@gpu
 def test_placement_from_gpu_cooccurrence_feeds_the_plan_chain():
     from moe_expert_routing_ids_gb300 import workloads as W
     from moe_expert_routing_ids_gb300.planner import Cooccur, Planner
