@@ -102,6 +102,29 @@ def profiled_traffic(call: str, units: int):
     return rec["dram_bytes"] * units / rec["units"]
 
 
+def host_info() -> dict:
+    """The host the oracle baseline ran on: logical CPUs and CPU model."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip().lower() in ("model name", "cpu model", "hardware"):
+                    model = val.strip()
+                    break
+    except OSError:
+        pass
+    if not model:                                  # Arm kernels list no model name; lscpu does
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            model = next((l.split(":", 1)[1].strip() for l in out.splitlines()
+                          if l.lower().startswith("model name")), "")
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
+
+
 def max_over_ranks(x: float, device="cpu") -> float:
     """The largest x over the ranks of the default process group (x itself
     without one): the job's time is its slowest rank's."""
@@ -267,7 +290,7 @@ def run_reference(args, rank):
                        "ranks_per_node": w.ranks_per_node, "n_slot": w.n_slot,
                        "microbatches": w.n_layers, "tokens_per_step": t_s,
                        "parallelism": "replicas"},
-            "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": 1, "kind": "oracle", "host": host_info(),
                              "sample": sample},
             "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -892,7 +915,7 @@ def cpu_baseline(w, ids):
         secs += s
         pairs += p
         n += 1
-    return {"value": pairs / secs, "unit": "pairs/s", "cores": 1, "kind": "oracle",
+    return {"value": pairs / secs, "unit": "pairs/s", "cores": 1, "kind": "oracle", "host": host_info(),
             "sample": f"{n} microbatch(es) of the workload, {pairs} pairs, oracle chain "
                       f"hist+plan+reroute+layout single-threaded, {secs:.1f} s"}
 
