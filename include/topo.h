@@ -79,21 +79,28 @@ extern "C" {
 
 /* Problem configuration (TopoEP §4.1: N_slot, C, S_tok, ||W_e||, main(e)). */
 typedef struct {
-    int32_t T;                /* tokens per layer; T % R == 0; T*k <= 2^31-1 */
-    int32_t E;                /* logical experts; E % R == 0 */
-    int32_t k;                /* expert choices per token (Top-k) */
+    int32_t T;                /* tokens per layer; T >= 0, T % R == 0; T*k <= 2^31-1 */
+    int32_t E;                /* logical experts; E % R == 0, E < 2^26 */
+    int32_t k;                /* expert choices per token (Top-k), 1..64 */
     int32_t R;                /* expert-parallel ranks; R % ranks_per_node == 0 */
-    int32_t ranks_per_node;   /* ranks per NVLink domain */
-    int32_t n_slot;           /* replica slots per rank (C3) */
-    int64_t tok_bytes;        /* S_tok: bytes of one routed activation (>= 0) */
-    int64_t expert_bytes;     /* ||W_e||: parameter bytes of one expert (>= 0) */
+    int32_t ranks_per_node;   /* ranks per NVLink domain, 1..32 */
+    int32_t n_slot;           /* replica slots per rank (C3), >= 0; R*n_slot <= 2^20
+                                 and E/R + n_slot <= 32767 */
+    int64_t tok_bytes;        /* S_tok: bytes of one routed activation, >= 0,
+                                 tok_bytes * c_inter < 2^31 */
+    int64_t expert_bytes;     /* ||W_e||: parameter bytes of one expert, >= 0,
+                                 expert_bytes * c_inter < 2^40 (so every cost
+                                 product is exact in int64) */
     int32_t c_intra;          /* integer per-byte cost inside a domain, >= 1 */
     int32_t c_inter;          /* integer per-byte cost across domains, >= c_intra */
-    int32_t max_refine_iters; /* cap on refinement commits per domain; 0 = none */
+    int32_t max_refine_iters; /* cap on refinement commits per domain, >= 0; 0 = none */
     int32_t reserved;         /* must be 0 */
     const int32_t *main_rank; /* device [E] main rank of each expert, or NULL for
                                  e / (E/R); each rank must own exactly E/R mains */
 } topo_cfg;
+/* A cfg that breaks one of these rules, or whose E, R, ranks_per_node and
+ * n_slot exceed the kernels' shared memory (227 KB per CTA), is invalid:
+ * topo_workspace_bytes returns 0 and every call returns TOPO_EINVAL. */
 
 /* Plan outputs (TopoEP §4.2 decision variables x and q, loads U and L).
  * All device pointers, caller-allocated, layer-major. */
