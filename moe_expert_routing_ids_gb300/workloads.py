@@ -245,3 +245,23 @@ def random_small(seed: int, T: int, E: int, k: int, n_layers: int = 1, s: float 
         rng = rng_for(1000 + seed, l)
         out[l] = topk_without_replacement(rng, zipf_probs(E, s, rng.permutation(E)), T, k)
     return out
+
+
+def gumbel_logits(seed: int, L: int, T: int, E: int, chunk: int = 1 << 16) -> np.ndarray:
+    """Router logits float32 [L, T, E]: standard Gumbel noise (the "random
+    logits" of TopoEP §6.4), drawn in token chunks so the float64 draw never
+    holds more than `chunk` rows."""
+    out = np.empty((L, T, E), np.float32)
+    for l in range(L):
+        rng = rng_for(seed, l)
+        for a in range(0, T, chunk):
+            b = min(T, a + chunk)
+            out[l, a:b] = rng.gumbel(size=(b - a, E))
+    return out
+
+
+def zipf_bias(seed: int, E: int, s: float) -> np.ndarray:
+    """Fixed expert-specific bias float32 [E]: log of Zipf(s) probabilities
+    over a seeded expert order (TopoEP §6.4)."""
+    rng = rng_for(seed, 1 << 20)
+    return np.log(zipf_probs(E, s, rng.permutation(E))).astype(np.float32)

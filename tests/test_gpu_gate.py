@@ -178,31 +178,34 @@ def test_gate_feeds_the_plan_chain():
 
 
 @gpu
-def test_gate_full_size_sampled():
-    # one microbatch of the T = 1048576, E = 512, k = 10, R = 128 workload:
-    # sampled tokens against the oracle, the histogram against the GPU's own ids
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gate_full_size_every_token(dtype):
+    # one whole microbatch of the T = 1048576, E = 512, k = 10, R = 128
+    # workload (Gumbel logits plus a log-Zipf(1.4) bias): every token's ids and
+    # selected logits, and Omega, against the oracle
     from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
     dev = _dev()
     w = W.STRESS
     cfg = dict(w.plan_cfg)
     T, E, k = w.T, w.E, w.k
-    g = torch.Generator(device=dev).manual_seed(11)
-    u = torch.rand((1, T, E), generator=g, device=dev).clamp_(1e-12, 1.0)
-    x = -torch.log(-torch.log(u))
-    bias = torch.log(torch.distributions.Dirichlet(torch.full((E,), 0.3, device=dev)).sample() + 1e-9)
-    from moe_expert_routing_ids_gb300.planner import Planner
+    x = W.gumbel_logits(23, 1, T, E)
+    if dtype == "bf16":
+        x = (x.view(np.uint32) >> 16).astype(np.uint16)          # bf16 patterns of the logits
+        xd = torch.as_tensor(x.view(np.int16), device=dev).view(torch.bfloat16)
+    else:
+        xd = torch.as_tensor(x, device=dev)
+    bias = W.zipf_bias(23, E, w.zipf_s)
     P = Planner(cfg, 1, dev)
     ids = torch.empty((1, T, k), dtype=torch.int32, device=dev)
     sc = torch.empty((1, T, k), dtype=torch.float32, device=dev)
-    P.gate_hist(x, ids, bias.float(), sc)
+    P.gate_hist(xd, ids, torch.as_tensor(bias, device=dev), sc)
     assert P.error() == 0
-    rows = np.sort(np.random.default_rng(0).choice(T, 3000, replace=False))
-    xs = x[0, rows].cpu().numpy()[None]
-    want = oracle.gate(xs, k, 1, bias=bias.float().cpu().numpy())
-    got = ids[0, rows].cpu().numpy()
-    assert np.array_equal(got, want["ids"][0])
-    assert np.array_equal(sc[0, rows].cpu().numpy().view(np.uint32), want["scores"][0].view(np.uint32))
-    assert np.array_equal(P.buf.hist.cpu().numpy(), oracle.hist(ids.cpu().numpy(), w.R, E))
+    del xd
+    want = oracle.gate(x, k, w.R, bias=bias)
+    assert np.array_equal(ids.cpu().numpy(), want["ids"])
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), want["scores"].view(np.uint32))
+    assert np.array_equal(P.buf.hist.cpu().numpy(), want["hist"])
 
 
 @gpu

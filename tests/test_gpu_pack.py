@@ -114,3 +114,46 @@ def test_pack_flags_a_layout_that_is_not_a_permutation():
     _, _, err = _run_pack(cfg, L, H, sp, _bf16_bits(rng, (1, 256, H)),
                           np.ones((1, 256, 2), np.float32), dev)
     assert err == topo.TOPO_ESTATE
+
+
+@gpu
+def test_permute_and_combine_at_the_benchmarked_size():
+    # the first layer of the T = 65536, E = 256, k = 8, R = 64 workload with
+    # H = 7168 bf16 rows (x 0.94 GB, send buffer 7.5 GB), the size the
+    # benchmark times.  The layout comes from the oracle chain; the GPU runs on
+    # whole rows and every byte is compared, in blocks of columns (both
+    # operations act on each column independently).
+    from moe_expert_routing_ids_gb300 import workloads as W
+    dev = _dev()
+    w = W.FOUR_LAYER
+    cfg = dict(w.plan_cfg)
+    T, k, H = w.T, w.k, 7168
+    ids = w.ids(n_layers=1)
+    h = oracle.hist(ids, w.R, w.E)
+    pl = oracle.plan(cfg, h)
+    sp, _, _, _ = oracle.layout(cfg, oracle.reroute(cfg, ids, pl))
+    sp = sp.reshape(1, T * k)
+    rng = np.random.default_rng(71)
+    x = _bf16_bits(rng, (1, T, H))
+    wts = rng.random((1, T, k)).astype(np.float32)
+    c = topo.make_cfg(**cfg)
+    ws_bytes = topo.topo_workspace_bytes(c, 1, topo.TOPO_CALL_PACK)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    d_sp = torch.as_tensor(sp, device=dev)
+    d_x = torch.as_tensor(x.view(np.int16), device=dev)
+    y = torch.empty((1, T * k, H), dtype=torch.int16, device=dev)
+    topo.topo_permute(c, 1, H, d_x, d_sp, y, ws, ws_bytes)
+    out = torch.empty((1, T, H), dtype=torch.int16, device=dev)
+    topo.topo_combine(c, 1, H, y, d_sp, torch.as_tensor(wts, device=dev), out, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert topo.topo_read_error(ws) == 0
+    del d_x
+    out_h = out.cpu().numpy().view(np.uint16)
+    step = 512
+    for a in range(0, H, step):
+        xa = np.ascontiguousarray(x[:, :, a:a + step])
+        ya = oracle.permute(xa, sp, k)
+        got = y[:, :, a:a + step].contiguous().cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, ya), f"permute, columns {a}..{a + step}"
+        oa = oracle.combine(ya, sp, wts, k)
+        assert np.array_equal(out_h[:, :, a:a + step], oa), f"combine, columns {a}..{a + step}"

@@ -103,3 +103,33 @@ def test_correlated_placement_raises_dedup_savings():
         rows = sum(len(set(rank[ids[0, t]])) for t in range(T))
         return 1 - rows / (T * k)
     assert saved(mr) > saved(np.arange(E) // per) + 0.15
+
+
+SWAP_CAP = 1 << 20
+
+
+def test_the_swap_cap_does_not_bind():
+    # Every applied swap raises the integer within-rank weight by at least 1,
+    # and no balanced map holds more than W+ = the sum of the positive pair
+    # weights, so at most W+ - (greedy within-rank weight) swaps can follow
+    # the construction.  Where that is below 2^20 the cap cannot change the
+    # result; elsewhere a run that stops below 2^20 swaps stopped because no
+    # swap gains, which is the rule without a cap.
+    rng = np.random.default_rng(9)
+    for (E, R) in ((8, 2), (16, 4), (32, 8), (64, 8)):
+        co = rng.integers(0, 50, size=(E, E)).astype(np.int64)
+        mr, st = oracle.place(co, R)
+        w = _weights(co)
+        w_plus = int(np.triu(np.maximum(w, 0), 1).sum())
+        assert st[3] <= w_plus - st[1] < SWAP_CAP
+    # the co-occurrence workload (8 layers, T = 262144, E = 128, k = 8) at EP8
+    # and EP16, the placements the benchmark and the GPU parity tests run
+    from moe_expert_routing_ids_gb300 import workloads as W
+    w = W.COOCCUR
+    co = oracle.cooccur(w.ids(), w.E, transitions=False)
+    co = co[0] if isinstance(co, tuple) else co
+    for R in (8, 16):
+        for layer in range(w.n_layers):
+            mr, st = oracle.place(co[layer], R)
+            assert st[3] < SWAP_CAP
+            assert st[2] - st[1] >= st[3]                      # each swap gained >= 1

@@ -1,10 +1,12 @@
 """topo_hist_noalloc: the histogram with the library's fixed scratch array
-must give exactly what topo_hist gives with an allocated workspace, call
-after call, and must refuse shapes whose scratch does not fit."""
+must give exactly what topo_hist gives with an allocated workspace, and what
+the CPU oracle gives, call after call, and must refuse shapes whose scratch
+does not fit."""
 import numpy as np
 import pytest
 
 import moe_expert_routing_ids_gb300 as topo
+import oracle
 from moe_expert_routing_ids_gb300 import workloads as W
 
 
@@ -67,8 +69,10 @@ def test_hist_noalloc_matches_topo_hist_twice_in_a_row():
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         outs.append((hist.cpu().numpy(), _hist_with_workspace(torch, cfg, L, d_ids, stream)))
-    for got, want in outs:
+    for (got, want), (cfg, L, ids) in zip(outs, cases):
         np.testing.assert_array_equal(got, want)
+        # and the oracle's Omega (Eq. 3), independently of both GPU paths
+        np.testing.assert_array_equal(got, oracle.hist(ids, cfg.R, cfg.E))
     # the same shape once more, after the other: identical again
     cfg, L, ids = cases[0]
     d_ids = torch.as_tensor(np.ascontiguousarray(ids, dtype=np.int32), device=dev)
