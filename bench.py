@@ -61,7 +61,8 @@ def parse():
     ap.add_argument("--skip-secondary", action="store_true", help="only the main line's fields")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle", "place"),
+    ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle", "place",
+                                       "configs", "solver"),
                     help="run one secondary measurement alone and print it (for profiling)")
     ap.add_argument("--microbatches", type=int, default=0,
                     help="--only gate: microbatches of the workload to use (0 = all; 1 for ncu captures)")
@@ -413,6 +414,153 @@ def secondary_cooccur(dev, stream, hbm_peak):
             "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
 
 
+L2_BYTES = 129 << 20
+
+
+def plan_quality(w, stats, lstats, hist):
+    """Plan-quality and locality figures of one call over all its layers, the
+    numbers the pages judge a plan by: rank-load imbalance max/mean (TopoEP §6
+    Fig. 10, Fig. 13b), the share of token-expert assignments that cross
+    nodes and the share served by replicas (Fig. 16), and the intra- and
+    inter-node dispatch bytes (§2.3 Fig. 3).  stats / lstats: the plan and
+    layout statistics [L, 8]; hist: Omega [L, R, E], used only for the static
+    placement's inter-node share (every pair on its expert's main rank)."""
+    L = stats.shape[0]
+    pairs = w.T * w.k * L
+    mean = stats[:, 7] / w.R
+    e_r = w.E // w.R
+    dom_src = np.arange(w.R) // w.ranks_per_node
+    dom_main = (np.arange(w.E) // e_r) // w.ranks_per_node
+    cross = dom_src[:, None] != dom_main[None, :]
+    static_inter = int(sum(int(hist[l][cross].sum()) for l in range(L)))
+    return {
+        "L_max": stats[:, 0].tolist(), "L_max_static": stats[:, 1].tolist(),
+        "imbalance_max_over_mean": [round(float(a / m), 4) if m else None for a, m in zip(stats[:, 0], mean)],
+        "imbalance_static": [round(float(a / m), 4) if m else None for a, m in zip(stats[:, 1], mean)],
+        "replicas": int(stats[:, 2].sum()), "replicas_inter_node_stage": int(stats[:, 3].sum()),
+        "refine_commits": int(stats[:, 4].sum()),
+        "inter_node_pairs_frac": round(float(lstats[:, 2].sum()) / max(pairs, 1), 5),
+        "inter_node_pairs_frac_static": round(static_inter / max(pairs, 1), 5),
+        "replica_served_pairs_frac": round(float(lstats[:, 6].sum()) / max(pairs, 1), 5),
+        "pairs_local_intra_inter": [int(lstats[:, i].sum()) for i in (0, 1, 2)],
+        "bytes_local_intra_inter": [int(lstats[:, i].sum()) for i in (3, 4, 5)],
+        "T_token": int(stats[:, 5].sum()), "T_replica": int(stats[:, 6].sum())}
+
+
+def oracle_chain_stats(w, ids):
+    """The oracle's plan and layout statistics and Omega for the same ids."""
+    import oracle
+    cfg = w.plan_cfg
+    h = oracle.hist(ids, w.R, w.E)
+    p = oracle.plan(cfg, h)
+    d = oracle.reroute(cfg, ids, p)
+    _, _, _, st = oracle.layout(cfg, d)
+    return np.asarray(p["stats"]).reshape(-1, 8), np.asarray(st).reshape(-1, 8), h
+
+
+def config_lines(dev, stream, hbm_peak, check_oracle=True):
+    """Every plan workload (the T=4096 E=8, T=16384 E=64, four-layer and stress
+    configurations): the whole chain hist -> plan -> reroute_layout timed as
+    200 steps after 20 warm-up steps (TopoEP §6.3 protocol) in CUDA graphs with
+    event nodes between the calls; pairs/s, per-layer plan latency, %HBM
+    where the ids exceed L2 (else the replayed steps are L2-resident and only
+    latency is reported); and the plan-quality figures, checked equal to the
+    oracle's on the same ids."""
+    import torch
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    out = {}
+    for w in W.PLAN_WORKLOADS:
+        ids = w.ids()
+        d_ids = torch.as_tensor(ids, device=dev)
+        P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                P.run(d_ids)
+        if P.error() != 0:
+            raise RuntimeError(f"device error on {w.name}")
+        total, n, per_call = time_chain(P, d_ids, 200, stream)
+        if P.error() != 0:
+            raise RuntimeError(f"device error on {w.name}")
+        ms = total / n
+        pairs = int(ids.size)
+        b = P.numpy()
+        entry = {"pairs": pairs, "layers": w.n_layers, "ms_per_step": round(ms, 5),
+                 "pairs_per_s": round(pairs / (ms * 1e-3), 1),
+                 "us_per_call": {c: round(per_call[c] * 1e3, 2) for c in CALLS},
+                 "plan_us_per_layer": round(per_call["plan"] * 1e3 / w.n_layers, 2),
+                 "ids_bytes": int(ids.nbytes)}
+        if ids.nbytes > L2_BYTES:
+            entry["hbm_frac"] = {c: round(BYTES_PER_PAIR[c] * pairs / (per_call[c] * 1e-3) / 1e9 / hbm_peak, 4)
+                                 for c in BYTES_PER_PAIR}
+        else:
+            entry["hbm_frac"] = None
+            entry["l2"] = "ids fit in L2: latency only"
+        entry["quality"] = plan_quality(w, b["stats"], b["layout_stats"], b["hist"])
+        if check_oracle:
+            ost, olst, oh = oracle_chain_stats(w, ids)
+            entry["quality_equals_oracle"] = bool(np.array_equal(ost, b["stats"]) and
+                                                  np.array_equal(olst, b["layout_stats"]) and
+                                                  np.array_equal(oh, b["hist"]))
+        out[w.name] = entry
+        del P, d_ids
+    return out
+
+
+def solver_sweep(dev, stream):
+    """topo_plan latency shaped like TopoEP §6.3 Fig. 11: (a) E = 640, Top-8,
+    EP 8..128; (b) EP 32 over a 16x range of expert counts.  Each point: one
+    hist, 20 warm-up plan calls, then 200 calls in one CUDA graph, mean per
+    call; the oracle's plan of the same Omega timed beside it (one call,
+    single-threaded), and the plan's imbalance."""
+    import torch
+    import oracle
+    from moe_expert_routing_ids_gb300 import workloads as W
+    from moe_expert_routing_ids_gb300.planner import Planner
+    res = {}
+    for label, pts in (("rank_scaling_e640", W.SOLVER_RANKS), ("expert_scaling_r32", W.SOLVER_EXPERTS)):
+        rows = []
+        for w in pts:
+            ids = w.ids()
+            P = Planner(w.plan_cfg, 1, dev, stream=stream)
+            d_ids = torch.as_tensor(ids, device=dev)
+            with torch.cuda.stream(stream):
+                P.hist(d_ids)
+                for _ in range(20):
+                    P.make_plan()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(200):
+                    P.make_plan()
+            graph.replay()
+            torch.cuda.synchronize()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                graph.replay()
+                z.record(stream)
+            z.synchronize()
+            us = a.elapsed_time(z) * 1e3 / 200
+            if P.error() != 0:
+                raise RuntimeError(f"device error on {w.name}")
+            st = P.buf.stats.cpu().numpy()[0]
+            h = oracle.hist(ids, w.R, w.E)
+            t0 = time.perf_counter()
+            ost = oracle.plan(w.plan_cfg, h)["stats"].reshape(-1)
+            o_us = (time.perf_counter() - t0) * 1e6
+            rows.append({"E": w.E, "R": w.R, "T": w.T, "us": round(us, 2), "oracle_us": round(o_us, 1),
+                         "imbalance": round(float(st[0] / (st[7] / w.R)), 4),
+                         "imbalance_static": round(float(st[1] / (st[7] / w.R)), 4),
+                         "replicas": int(st[2]), "refine_commits": int(st[4]),
+                         "stats_equal_oracle": bool(np.array_equal(st, ost))})
+            del graph, P, d_ids
+        res[label] = rows
+    res["setup"] = ("Top-8, n_slot 2, 4096 tokens per rank, 8 ranks per node, Zipf(1.2), hidden 2048, "
+                    "intermediate 768; 200 calls after 20 warm-ups, mean")
+    return res
+
+
 SHUFFLE_RANKS = 16           # EP16 over the co-occurrence workload's 128 experts
 PLACE_RANKS = 8              # EP8, the scale at which the pages report deduplication savings
 
@@ -538,9 +686,11 @@ def secondary_shuffle(dev, stream, hbm_peak):
                 times.append(gev.elapsed(0, 1))
             gev.close()
             ms = statistics.median(times[3:])
-            # algorithmic: each layer's ids read as the current and as the next
-            # layer, the transitions, the targets written
-            nbytes = 2 * (L - 1) * T * k * 4 + (L - 1) * E * E * 8 + (L - 1) * T * 4
+            # algorithmic: every layer's ids read once (a layer is the next
+            # layer of one prediction and the current layer of the following
+            # one, but its bytes need to leave HBM only once), the
+            # transitions, the targets written
+            nbytes = L * T * k * 4 + (L - 1) * E * E * 8 + (L - 1) * T * 4
             gbs = nbytes / (ms * 1e-3) / 1e9
             entry.update({"ms": round(ms, 4), "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
                           "frac": round(gbs / hbm_peak, 4), "l2": "flushed (256 MB write) before each call",
@@ -738,6 +888,10 @@ def run_only(name, microbatches=0):
         res = secondary_shuffle(dev, stream, hbm)
     elif name == "place":
         res = secondary_place(dev, stream)
+    elif name == "configs":
+        res = {"configs": config_lines(dev, stream, hbm)}
+    elif name == "solver":
+        res = solver_sweep(dev, stream)
     else:
         w = W.STRESS
         P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
@@ -824,6 +978,8 @@ def run_ours(args, rank, world, local_rank):
         line["e2e_full_outputs"] = e2e(P, w, ids, dev, stream, n_e2e, _outputs,
                                        "every plan and layout output (dst_inst, sorted_pairs, tables)")
     if not args.skip_secondary:
+        line["configs"] = config_lines(dev, stream, hbm)
+        line["solver_latency"] = solver_sweep(dev, stream)
         line["plan_latency"] = secondary_plan_latency(dev, stream)
         line["cooccur"] = secondary_cooccur(dev, stream, hbm)
         line["pack"] = secondary_pack(dev, stream, hbm)

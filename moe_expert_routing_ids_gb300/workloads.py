@@ -265,3 +265,20 @@ def zipf_bias(seed: int, E: int, s: float) -> np.ndarray:
     over a seeded expert order (TopoEP §6.4)."""
     rng = rng_for(seed, 1 << 20)
     return np.log(zipf_probs(E, s, rng.permutation(E))).astype(np.float32)
+
+
+def _solver_point(seed: int, E: int, R: int) -> Workload:
+    return Workload(seed, f"t{4096 * R}_e{E}_k8_r{R}", "plan", "zipf", T=4096 * R, E=E, k=8,
+                    n_layers=1, R=R, ranks_per_node=8, n_slot=2, hidden=2048, intermediate=768,
+                    zipf_s=1.2)
+
+
+# Solver-latency sweeps shaped like TopoEP §6.3 Fig. 11: Top-8 routing with two
+# replica slots per rank (the setting §6.2 adopts after Fig. 10), 4096 tokens
+# per source rank, 8 ranks per node, Zipf(1.2) over a seeded expert order,
+# hidden 2048 / intermediate 768 (the Qwen3-30B-A3B row of Table 1, whose
+# expert is the 9 MiB of Fig. 3).  (a) E = 640 over EP 8..128; (b) EP 32 over
+# a 16x range of expert counts.
+SOLVER_RANKS = tuple(_solver_point(600 + i, 640, R) for i, R in enumerate((8, 16, 32, 64, 128)))
+SOLVER_EXPERTS = tuple(_solver_point(700 + i, E, 32)
+                       for i, E in enumerate((64, 128, 256, 512, 640, 1024)))
