@@ -76,7 +76,11 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, Ws
 }
 
 // One thread per (layer, source, expert): exclusive prefix of the source's
-// tile counts in place, and the source's total into Omega.
+// tile counts in place, and the source's total into Omega.  The column is
+// read in chunks of kPrefixChunk tiles, every load of a chunk issued before
+// any of its stores, so no load waits behind a store.
+constexpr int kPrefixChunk = 16;
+
 __global__ void __launch_bounds__(256)
 k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo g, uint64_t fp,
               int64_t n_cols) {
@@ -88,24 +92,20 @@ k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo 
     }
     if (c >= n_cols) return;
     const int E = g.E;
-    const int64_t row = c / E, e = c - row * E;  // row = l * R + s
-    int32_t *col = tile_cnt + row * g.tps * E + e;
+    const unsigned row = (unsigned)(c / E);       // l * R + s
+    const int e = (int)(c - (int64_t)row * E);
+    int32_t *col = tile_cnt + (int64_t)row * g.tps * E + e;
     int run = 0;
-    int u = 0;
-    for (; u + 8 <= g.tps; u += 8) {
-        int v[8];
+    for (int u0 = 0; u0 < g.tps; u0 += kPrefixChunk) {
+        const int m = min(kPrefixChunk, g.tps - u0);
+        int v[kPrefixChunk];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = col[(int64_t)(u + q) * E];
+        for (int q = 0; q < kPrefixChunk; ++q) v[q] = q < m ? col[(int64_t)(u0 + q) * E] : 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            col[(int64_t)(u + q) * E] = run;
+        for (int q = 0; q < kPrefixChunk; ++q) {
+            if (q < m) col[(int64_t)(u0 + q) * E] = run;
             run += v[q];
         }
-    }
-    for (; u < g.tps; ++u) {
-        const int v = col[(int64_t)u * E];
-        col[(int64_t)u * E] = run;
-        run += v;
     }
     hist[c] = run;
     pdl_trigger();
