@@ -658,7 +658,7 @@ def secondary_shuffle(dev, stream, hbm_peak):
         s = stream.cuda_stream
 
         def call():
-            topo.topo_shuffle_targets(L, T, E, k, R, ids, C.tr, None, target, stats, ws, nb, s)
+            topo.topo_shuffle_targets(L, T, E, k, R, ids, C.tr, None, None, target, stats, ws, nb, s)
         with torch.cuda.stream(stream):
             call()
         torch.cuda.synchronize()

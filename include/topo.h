@@ -9,8 +9,11 @@
  * and, for the correlation statistics, "Expert Coupling in MoE Pretraining".
  *
  * Model.  R expert-parallel ranks form M = R / ranks_per_node NVLink domains
- * (dom(r) = r / ranks_per_node).  Token t of a layer belongs to source rank
- * src(t) = t / (T / R) (equal contiguous blocks).  Pair p = t*k + j is the
+ * (dom(r) = r / ranks_per_node).  Each rank routes its own local tokens
+ * (TopoEP §2.1): the tokens of a layer are the ranks' blocks one after the
+ * other, token t belonging to source rank src(t) = the s with
+ * rank_offsets[s] <= t < rank_offsets[s+1] (equal blocks of T / R tokens
+ * when rank_offsets is NULL).  Pair p = t*k + j is the
  * j-th expert choice of token t.  Expert e has its main instance on rank
  * main(e) (= e / (E/R) by default, or main_rank[e]) with local index l < E/R
  * (ascending e among the rank's mains); each rank also has n_slot replica
@@ -54,6 +57,7 @@ extern "C" {
 #define TOPO_ERANGE (-4)   /* device: an expert id outside [0, E) */
 #define TOPO_ESTATE (-5)   /* device: ws does not hold the index this call needs */
 #define TOPO_EMAP (-6)     /* device: main_rank is not a balanced map onto [0, R) */
+#define TOPO_EOFFSETS (-7) /* device: rank_offsets is not 0 = o[0] <= o[1] <= ... <= o[R] = T */
 
 /* Workspace needs per call (argument `which_call` of topo_workspace_bytes). */
 #define TOPO_CALL_HIST 0
@@ -79,7 +83,8 @@ extern "C" {
 
 /* Problem configuration (TopoEP §4.1: N_slot, C, S_tok, ||W_e||, main(e)). */
 typedef struct {
-    int32_t T;                /* tokens per layer; T >= 0, T % R == 0; T*k <= 2^31-1 */
+    int32_t T;                /* tokens per layer; T >= 0, T*k <= 2^31-1; T % R == 0
+                                 when rank_offsets is NULL */
     int32_t E;                /* logical experts; E % R == 0, E < 2^26 */
     int32_t k;                /* expert choices per token (Top-k), 1..64 */
     int32_t R;                /* expert-parallel ranks; R % ranks_per_node == 0 */
@@ -97,6 +102,14 @@ typedef struct {
     int32_t reserved;         /* must be 0 */
     const int32_t *main_rank; /* device [E] main rank of each expert, or NULL for
                                  e / (E/R); each rank must own exactly E/R mains */
+    const int64_t *rank_offsets; /* device int64 [R+1] token offsets of the source
+                                 ranks' blocks (the same for every layer), or NULL
+                                 for equal blocks of T / R tokens.  Must satisfy
+                                 0 = o[0] <= o[1] <= ... <= o[R] = T; a source may
+                                 be empty.  Checked on the device by the calls that
+                                 read tokens (topo_hist, topo_gate_hist,
+                                 topo_dedup_layout; TOPO_EOFFSETS).  The calls of one
+                                 chain must be given the same pointer. */
 } topo_cfg;
 /* A cfg that breaks one of these rules, or whose E, R, ranks_per_node and
  * n_slot exceed the kernels' shared memory (227 KB per CTA), is invalid:
@@ -137,7 +150,8 @@ int topo_ws_reset(void *ws, size_t ws_bytes, cudaStream_t stream);
  * hist: device int32 [n_layers][R][E].
  * ws:   device; also receives the per-tile expert-count index that
  *       topo_reroute and topo_dispatch_layout read for these ids.
- * Device errors: TOPO_ERANGE (the id is skipped). */
+ * Device errors: TOPO_ERANGE (the id is skipped), TOPO_EOFFSETS (nothing is
+ * counted). */
 int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t *hist,
               void *ws, size_t ws_bytes, cudaStream_t stream);
 
@@ -169,24 +183,28 @@ int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, in
  *   M_l[a][r]   = sum of tr[l][a][b] over experts b with main rank r,
  *   score_r     = sum over the token's slots j of M_l[ids[l][t][j]][r],
  *   target[l][t] = the best rank; a tie keeps the token on its source rank
- *                 t / (T/R) if that rank is among the best, else the lowest.
+ *                 src(t) if that rank is among the best, else the lowest.
  * ids:       device int32 [L][T][k].
  * tr:        device int64 [L-1][E][E] (topo_cooccur's transitions, or counts
  *            gathered elsewhere); the sums must fit int64.
  * main_rank: device int32 [E] (experts per rank need not be equal here) or
  *            NULL for e / (E/R).
+ * rank_offsets: device int64 [R+1] source blocks as in topo_cfg, or NULL for
+ *            equal blocks of T / R tokens.
  * target:    device int32 [L-1][T] (written).
  * stats:     device int64 [L-1][TOPO_SHUFFLE_STATS]: next-layer pairs whose
  *            expert is on the target, next-layer pairs on the source rank,
  *            tokens whose target is not their source, next-layer pairs.
  * ws:        >= topo_shuffle_workspace_bytes(L, E, R).
- * Requires T % R == 0, 1 <= R <= TOPO_SHUFFLE_MAX_RANKS, 1 <= k <= 64, and
- * E % R == 0 without a map.  Device errors: TOPO_ERANGE (an id outside
- * [0, E), skipped), TOPO_EMAP (a map entry outside [0, R), skipped). */
+ * Requires T % R == 0 without rank_offsets, 1 <= R <= TOPO_SHUFFLE_MAX_RANKS,
+ * 1 <= k <= 64, and E % R == 0 without a map.  Device errors: TOPO_ERANGE (an
+ * id outside [0, E), skipped), TOPO_EMAP (a map entry outside [0, R),
+ * skipped), TOPO_EOFFSETS (rank_offsets out of order). */
 size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R);
 int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, const int32_t *ids,
-                         const int64_t *tr, const int32_t *main_rank, int32_t *target, int64_t *stats,
-                         void *ws, size_t ws_bytes, cudaStream_t stream);
+                         const int64_t *tr, const int32_t *main_rank, const int64_t *rank_offsets,
+                         int32_t *target, int64_t *stats, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
 
 /* Correlated expert placement ["Expert Coupling in MoE Pretraining", "Moving
  * Correlated Experts Together": the co-selection graph partitioned across
@@ -301,7 +319,8 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
  *            another rank, pairs to another rank.
  * Requires k <= 16 and R <= 1024 (else TOPO_EINVAL).
  * ws: >= topo_workspace_bytes(cfg, n_layers, TOPO_CALL_DEDUP) bytes.
- * Device errors: TOPO_ESTATE for a dst_inst value outside [0, R*n_local). */
+ * Device errors: TOPO_ESTATE for a dst_inst value outside [0, R*n_local),
+ * TOPO_EOFFSETS. */
 int topo_dedup_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_inst, int32_t *seg,
                       int32_t *row_token, uint64_t *row_slots, uint64_t *tok_dst, int64_t *send,
                       int64_t *stats, void *ws, size_t ws_bytes, cudaStream_t stream);

@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtopoep.so")
 
 TOPO_OK, TOPO_EINVAL, TOPO_ENOSPC, TOPO_ECUDA = 0, -1, -2, -3
-TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP = -4, -5, -6
+TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP, TOPO_EOFFSETS = -4, -5, -6, -7
 TOPO_CALL_HIST, TOPO_CALL_PLAN, TOPO_CALL_REROUTE, TOPO_CALL_LAYOUT = 0, 1, 2, 3
 TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN, TOPO_CALL_REROUTE_LAYOUT = 4, 5, 6
 TOPO_CALL_PACK = 7
@@ -57,7 +57,8 @@ class TopoCfg(ctypes.Structure):
                 ("n_slot", ctypes.c_int32), ("tok_bytes", ctypes.c_int64),
                 ("expert_bytes", ctypes.c_int64), ("c_intra", ctypes.c_int32),
                 ("c_inter", ctypes.c_int32), ("max_refine_iters", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("main_rank", ctypes.c_void_p)]
+                ("reserved", ctypes.c_int32), ("main_rank", ctypes.c_void_p),
+                ("rank_offsets", ctypes.c_void_p)]
 
 
 class TopoPlan(ctypes.Structure):
@@ -96,7 +97,7 @@ def lib():
             L.topo_gate_hist.argtypes = [cfgp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_shuffle_workspace_bytes.argtypes = [i32, i32, i32]
             L.topo_shuffle_workspace_bytes.restype = sz
-            L.topo_shuffle_targets.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_shuffle_targets.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_place_experts.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
             L.topo_combine.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.topo_read_error.argtypes = [vp]
@@ -133,10 +134,11 @@ def _chk(fn, rc):
 
 
 def make_cfg(T, E, k, R, ranks_per_node, n_slot, tok_bytes=0, expert_bytes=0, c_intra=1,
-             c_inter=4, max_refine_iters=0, main_rank=None, **_ignored) -> TopoCfg:
-    """topo_cfg from plain values; main_rank is a device pointer/tensor or None."""
+             c_inter=4, max_refine_iters=0, main_rank=None, rank_offsets=None, **_ignored) -> TopoCfg:
+    """topo_cfg from plain values; main_rank (int32 [E]) and rank_offsets
+    (int64 [R+1]) are device pointers/tensors or None."""
     return TopoCfg(T, E, k, R, ranks_per_node, n_slot, tok_bytes, expert_bytes, c_intra, c_inter,
-                   max_refine_iters, 0, _p(main_rank))
+                   max_refine_iters, 0, _p(main_rank), _p(rank_offsets))
 
 
 def make_plan(slot_expert, route_cnt, inst_load, rank_load, stats) -> TopoPlan:
@@ -218,12 +220,12 @@ def topo_shuffle_workspace_bytes(L: int, E: int, R: int) -> int:
     return int(lib().topo_shuffle_workspace_bytes(L, E, R))
 
 
-def topo_shuffle_targets(L: int, T: int, E: int, k: int, R: int, ids, tr, main_rank, target, stats, ws,
-                         ws_bytes: int, stream=None) -> int:
+def topo_shuffle_targets(L: int, T: int, E: int, k: int, R: int, ids, tr, main_rank, rank_offsets, target,
+                         stats, ws, ws_bytes: int, stream=None) -> int:
     """Token-shuffle targets from cross-layer transition counts."""
     return _chk("topo_shuffle_targets",
-                lib().topo_shuffle_targets(L, T, E, k, R, _p(ids), _p(tr), _p(main_rank), _p(target),
-                                           _p(stats), _p(ws), ws_bytes, _s(stream)))
+                lib().topo_shuffle_targets(L, T, E, k, R, _p(ids), _p(tr), _p(main_rank), _p(rank_offsets),
+                                           _p(target), _p(stats), _p(ws), ws_bytes, _s(stream)))
 
 
 def topo_gate_hist(cfg: TopoCfg, n_layers: int, logits, logits_dtype: int, bias, ids, scores, hist,

@@ -12,6 +12,7 @@ namespace topo {
 // (TT = 32 * kRankWarps * RW, RW rounds of 32 tokens per warp), so tiles never
 // straddle a source and every token's k pairs sit in one tile.  hist, reroute
 // and layout share the tiling: the tile index topo_hist leaves is per tile.
+// Tiles are numbered source by source within a layer (see tile_ref).
 constexpr int kRankWarps = 8;
 constexpr int kRankThreads = kRankWarps * 32;
 constexpr int kTilePairsTarget = 16384;            // pairs per tile aimed for
@@ -36,8 +37,14 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 // Geometry of one call, derived on the host and passed by value to kernels.
 struct Geo {
     int32_t T, E, k, R, rpn, n_slot, M, E_R, n_local, L;
-    int32_t tps;            // tiles per source rank
-    int32_t tpr;            // tokens per source rank
+    int32_t tps;            // tiles per source rank (equal blocks)
+    int32_t tpr;            // tokens per source rank (equal blocks)
+    int32_t ntl;            // tiles per layer: R * tps, or ceil(T / TT) + R with
+                            //   rank_offsets (a bound: sources hold whole tiles)
+    const int64_t *roff;    // device [R+1] token offsets of the sources, or null
+                            //   for equal blocks of tpr tokens
+    const int32_t *tfirst;  // device [R+1] first tile of each source (rank_offsets
+                            //   only; set per call from the workspace)
     int32_t TT, RW;         // tokens per tile, rounds of 32 tokens per warp
     int32_t kp;             // shared-memory stride of a token's ids (k, made odd)
     uint32_t kmagic;        // ceil(2^32 / k) for k >= 2: i / k == umulhi(i, kmagic), i < 2^26
@@ -65,6 +72,7 @@ struct Geo {
     size_t off_lsend;       // int64 [L][R][R]        send counts
     size_t off_lstat;       // int64 [L][8]           layout statistics
     size_t off_pack_inv;    // int32 [L][T*k]         position of each pair (pack workspace)
+    size_t off_first;       // int32 [R+1]            first tile of each source (rank_offsets)
     size_t total;
 };
 
@@ -73,6 +81,72 @@ __host__ __device__ inline int dom_of(int r, int rpn) { return r / rpn; }
 __host__ __device__ inline int64_t cost_sr(const Geo &g, int s, int r) {
     if (s == r) return 0;
     return (s / g.rpn == r / g.rpn) ? g.c_intra : g.c_inter;
+}
+
+// Source blocks and tiles.  Token t of a layer belongs to the source s with
+// off[s] <= t < off[s+1], where off = rank_offsets, or s * tpr for equal
+// blocks.  Tiles of TT tokens never straddle a source and are numbered source
+// by source: tile = s * tps + t for equal blocks; with rank_offsets, source s
+// owns tiles [first[s], first[s+1]) (first[] built per call by
+// launch_tile_first), and tiles from first[R] to ntl are empty.
+struct TileRef {
+    int s, t;          // source, tile within the source (s < 0: an empty tile)
+    int tok0, ntok;    // first token (within the layer) and token count
+    bool last;         // the source's last tile
+};
+
+// roff: the offsets or null; tpr: tokens per source for equal blocks.
+__device__ __forceinline__ TileRef tile_ref(const int64_t *roff, int R, int tpr, const int32_t *first,
+                                            int TT, int tps, int tile) {
+    TileRef r;
+    if (!roff) {
+        r.s = tile / tps;
+        r.t = tile - r.s * tps;
+        r.tok0 = r.s * tpr + r.t * TT;
+        r.ntok = max(0, min(TT, tpr - r.t * TT));
+        r.last = r.t + 1 == tps;
+        return r;
+    }
+    // the last source whose first tile is <= tile (binary search over first[])
+    const int nt = __ldg(first + R);
+    if (tile >= nt) {
+        r.s = -1; r.t = 0; r.tok0 = 0; r.ntok = 0; r.last = true;
+        return r;
+    }
+    int lo = 0, hi = R - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(first + mid) <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    r.s = lo;
+    r.t = tile - __ldg(first + lo);
+    const int64_t b = __ldg(roff + lo), e = __ldg(roff + lo + 1);
+    r.tok0 = (int)b + r.t * TT;
+    r.ntok = max(0, min(TT, (int)(e - r.tok0)));
+    r.last = tile + 1 == __ldg(first + lo + 1);
+    return r;
+}
+
+__device__ __forceinline__ TileRef tile_ref(const Geo &g, const int32_t *first, int TT, int tps, int tile) {
+    return tile_ref(g.roff, g.R, g.tpr, first, TT, tps, tile);
+}
+
+// Tiles [*b, *e) of source s.
+__device__ __forceinline__ void source_tiles(const int64_t *roff, const int32_t *first, int tps, int s,
+                                             int *b, int *e) {
+    if (!roff) {
+        *b = s * tps;
+        *e = *b + tps;
+    } else {
+        *b = __ldg(first + s);
+        *e = __ldg(first + s + 1);
+    }
+}
+
+__device__ __forceinline__ void source_tiles(const Geo &g, const int32_t *first, int tps, int s, int *b,
+                                             int *e) {
+    source_tiles(g.roff, first, tps, s, b, e);
 }
 
 // Record the first device error in the header (sticky).
@@ -160,6 +234,11 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
                         cudaStream_t st);
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st);
+// first[s] = first tile of source s for tiles of TT tokens over g.roff, and
+// first[R] = the tile count; checks that the offsets partition [0, T] in
+// order (TOPO_EOFFSETS in hdr otherwise, with every tile left empty).
+// Defined in k_hist.cu.
+cudaError_t launch_tile_first(const Geo &g, int TT, int32_t *first, WsHeader *hdr, cudaStream_t st);
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may
 // start while the previous kernel of the stream is still finishing: it must
@@ -204,8 +283,8 @@ cudaError_t launch_gate(const Geo &g, const void *logits, bool bf16, const float
 constexpr int kShuffleMaxRanks = 256;
 size_t shuffle_ws_bytes(int L, int E, int R);
 cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
-                           const int32_t *main_rank, int32_t *target, int64_t *stats, void *ws,
-                           cudaStream_t st);
+                           const int32_t *main_rank, const int64_t *rank_offsets, int32_t *target,
+                           int64_t *stats, void *ws, cudaStream_t st);
 // Correlated expert placement: one CTA per layer, E <= kPlaceMaxE and the
 // shared tables within kSmemMax.
 constexpr int kPlaceMaxE = 1024;
@@ -228,7 +307,7 @@ size_t row_index_smem(const Geo &g);
 size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
-size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src);
+size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src, size_t *off_first);
 cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t *row_token,
                          uint64_t *row_slots, uint64_t *tok_dst, int64_t *send, int64_t *stats, void *ws,
                          cudaStream_t st);

@@ -36,22 +36,25 @@ constexpr int kDdFillCtas = 6;            // resident fill CTAs per SM the regis
 
 struct DdGeo {
     int T, k, R, nl, tpr, tps, RW, L;
+    int ntl;                   // tiles per layer (R * tps, or ceil(T / kDdTile) + R)
+    const int64_t *roff;       // source offsets or null (equal blocks)
+    const int32_t *first;      // first tile of each source (with roff)
     int64_t npairs;
     FastDiv dk, dnl;
 };
 
 struct DdTile {
-    int l, s, tok0, ntok;
+    int l, s, tok0, ntok;      // tok0: first token of the tile within the layer
 };
 
 __device__ __forceinline__ DdTile dd_tile(const DdGeo &g) {
     DdTile d;
-    const int64_t tile = blockIdx.x;
-    const int t = (int)(tile % g.tps);
-    d.s = (int)((tile / g.tps) % g.R);
-    d.l = (int)(tile / ((int64_t)g.tps * g.R));
-    d.tok0 = t * kDdTile;
-    d.ntok = max(0, min(kDdTile, g.tpr - d.tok0));
+    d.l = (int)(blockIdx.x / g.ntl);
+    const int tile = (int)(blockIdx.x - (unsigned)d.l * g.ntl);
+    const TileRef r = tile_ref(g.roff, g.R, g.tpr, g.first, kDdTile, g.tps, tile);
+    d.s = r.s;
+    d.tok0 = r.tok0;
+    d.ntok = r.ntok;
     return d;
 }
 
@@ -119,9 +122,10 @@ k_dd_count(const int32_t *__restrict__ dst, int32_t *__restrict__ tile_cnt,
     __shared__ int red[kDdWarps];
     __shared__ int any_bad;
     const DdTile d = dd_tile(g);
+    if (d.s < 0) return;                                   // past the last source's tiles
     const int tid = threadIdx.x, lane = tid & 31;
     const int n = d.ntok * g.k;
-    const int64_t tokb = (int64_t)d.s * g.tpr + d.tok0;
+    const int64_t tokb = d.tok0;
     int v[KB];
     dd_load<KB>(dst + (int64_t)d.l * g.npairs + tokb * g.k, n, v);
     for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lm[x] = 0;
@@ -178,15 +182,19 @@ k_dd_prefix(int32_t *tile_cnt, int64_t *send, DdGeo g, int64_t ncols) {
     if (c >= ncols) return;
     const int r = (int)(c % g.R);
     const int64_t ls = c / g.R;                            // l * R + s
-    int32_t *col = tile_cnt + ls * g.tps * g.R + r;
+    const int l = (int)(ls / g.R), s = (int)(ls - (int64_t)l * g.R);
+    int tb, te;
+    source_tiles(g.roff, g.first, g.tps, s, &tb, &te);
+    const int nt = te - tb;
+    int32_t *col = tile_cnt + ((int64_t)l * g.ntl + tb) * g.R + r;
     int run = 0;
-    for (int t0 = 0; t0 < g.tps; t0 += 32) {
+    for (int t0 = 0; t0 < nt; t0 += 32) {
         int v[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) v[u] = t0 + u < g.tps ? col[(int64_t)(t0 + u) * g.R] : 0;
+        for (int u = 0; u < 32; ++u) v[u] = t0 + u < nt ? col[(int64_t)(t0 + u) * g.R] : 0;
 #pragma unroll
         for (int u = 0; u < 32; ++u)
-            if (t0 + u < g.tps) {
+            if (t0 + u < nt) {
                 col[(int64_t)(t0 + u) * g.R] = run;
                 run += v[u];
             }
@@ -245,9 +253,10 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
     unsigned short *srk = reinterpret_cast<unsigned short *>(srow + kDdTile * KB);  // row rank
     __shared__ int warp_tot[32];
     const DdTile d = dd_tile(g);
+    if (d.s < 0) return;                                   // past the last source's tiles
     const int tid = threadIdx.x;
     const int n = d.ntok * g.k;
-    const int64_t tokb = (int64_t)d.s * g.tpr + d.tok0;
+    const int64_t tokb = d.tok0;
     int v[KB];
     dd_load<KB>(dst + (int64_t)d.l * g.npairs + tokb * g.k, n, v);
     for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lm[x] = 0;
@@ -325,7 +334,7 @@ cudaError_t run_dedup(const DdGeo &g, const int32_t *dst, int32_t *seg, int32_t 
                       uint64_t *row_slots, uint64_t *tok_dst, int64_t *send, int64_t *stats,
                       int32_t *tile_cnt, int32_t *src_base, WsHeader *hdr, cudaStream_t st) {
     cudaError_t e;
-    const int64_t ntiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t ntiles = (int64_t)g.L * g.ntl;
     unsigned long long *ts = reinterpret_cast<unsigned long long *>(tok_dst);
     unsigned long long *rs = reinterpret_cast<unsigned long long *>(row_slots);
     if ((e = cudaMemsetAsync(stats, 0, (size_t)g.L * 4 * 8, st)) != cudaSuccess) return e;
@@ -346,13 +355,27 @@ cudaError_t run_dedup(const DdGeo &g, const int32_t *dst, int32_t *seg, int32_t 
 
 }  // namespace
 
-size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src) {
+namespace {
+
+int dd_tps(const Geo &g) {
     const int tps = (g.tpr + kDdTile - 1) / kDdTile;
-    const size_t a = sizeof(WsHeader);
-    const size_t b = (a + (size_t)g.L * g.R * (tps > 0 ? tps : 1) * g.R * 4 + 255) & ~size_t(255);
+    return tps > 0 ? tps : 1;
+}
+
+int64_t dd_ntl(const Geo &g) {
+    return g.roff ? ((int64_t)g.T + kDdTile - 1) / kDdTile + g.R : (int64_t)g.R * dd_tps(g);
+}
+
+}  // namespace
+
+size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src, size_t *off_first) {
+    const size_t f = sizeof(WsHeader);
+    const size_t a = (f + (size_t)(g.R + 1) * 4 + 255) & ~size_t(255);
+    const size_t b = (a + (size_t)g.L * dd_ntl(g) * g.R * 4 + 255) & ~size_t(255);
     const size_t c = (b + (size_t)g.L * g.R * g.R * 4 + 255) & ~size_t(255);
     if (off_tile) *off_tile = a;
     if (off_src) *off_src = b;
+    if (off_first) *off_first = f;
     return c;
 }
 
@@ -362,17 +385,25 @@ cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t
                          cudaStream_t st) {
     DdGeo d;
     d.T = g.T; d.k = g.k; d.R = g.R; d.nl = g.n_local; d.tpr = g.tpr; d.L = g.L;
-    d.tps = (g.tpr + kDdTile - 1) / kDdTile;
-    if (d.tps < 1) d.tps = 1;
+    d.tps = dd_tps(g);
+    const int64_t ntl = dd_ntl(g);
+    if ((int64_t)g.L * ntl > INT32_MAX) return cudaErrorInvalidValue;
+    d.ntl = (int)ntl;
+    d.roff = g.roff;
     d.RW = (g.R + 63) / 64;
     d.npairs = g.npairs;
     d.dk = make_fast_div((unsigned)(g.k > 0 ? g.k : 1));
     d.dnl = make_fast_div((unsigned)g.n_local);
-    size_t off_tile = 0, off_src = 0;
-    dedup_ws_bytes(g, &off_tile, &off_src);
+    size_t off_tile = 0, off_src = 0, off_first = 0;
+    dedup_ws_bytes(g, &off_tile, &off_src, &off_first);
     int32_t *tile_cnt = ws_at<int32_t>(ws, off_tile);
     int32_t *src_base = ws_at<int32_t>(ws, off_src);
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
+    d.first = ws_at<int32_t>(ws, off_first);
+    if (g.roff) {
+        const cudaError_t e = launch_tile_first(g, kDdTile, ws_at<int32_t>(ws, off_first), hdr, st);
+        if (e != cudaSuccess) return e;
+    }
 #define TOPO_DD(KB) run_dedup<KB>(d, dst, seg, row_token, row_slots, tok_dst, send, stats, tile_cnt, src_base, hdr, st)
     if (g.k <= 1) return TOPO_DD(1);
     if (g.k <= 2) return TOPO_DD(2);

@@ -123,10 +123,8 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
     float *stash = sb + E4;                                       // [groups][G * VPL] scores by expert
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(stash + kGroups * G * VPL);
     int *cnt = reinterpret_cast<int *>(keys + kGroups * kGateCand);   // [E]
-    const int tile = blockIdx.x;
-    const int t = tile % g.tps;
-    const int s = (tile / g.tps) % g.R;
-    const int l = tile / (g.tps * g.R);
+    const int l = blockIdx.x / g.ntl;
+    const int tile = blockIdx.x - l * g.ntl;
     const int lane = threadIdx.x & 31, gl = lane & (G - 1);
     const int grp = threadIdx.x / G;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
@@ -151,9 +149,10 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
     }
     __syncthreads();                                              // cnt zeroed, bias staged
 
-    const int tok0 = t * g.TT;
-    const int ntok = max(0, min(g.TT, g.tpr - tok0));
-    const int64_t row0 = (int64_t)l * g.T + (int64_t)s * g.tpr + tok0;   // token row of the tile
+    const TileRef tr = tile_ref(g, g.tfirst, g.TT, g.tps, tile);
+    if (tr.s < 0) return;                                         // past the last source's tiles
+    const int ntok = tr.ntok;
+    const int64_t row0 = (int64_t)l * g.T + tr.tok0;              // token row of the tile
     const size_t esz = BF ? 2 : 4;
     const char *base = reinterpret_cast<const char *>(logits);
     for (int i = grp; i < ntok; i += kGroups) {                  // i uniform in the group
@@ -289,7 +288,7 @@ k_gate_tiles(const void *__restrict__ logits, const float *__restrict__ bias, in
         }
     }
     __syncthreads();
-    int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
+    int32_t *mine = tile_cnt + ((int64_t)l * g.ntl + tile) * E;
     for (int e = threadIdx.x; e < E; e += kGateThreads) mine[e] = cnt[e];
 }
 
@@ -297,7 +296,7 @@ template <int VPL, int G, bool BF, int VEC>
 cudaError_t run_gate(const Geo &g, const void *logits, const float *bias, int32_t *ids, float *scores,
                      int32_t *tile_cnt, cudaStream_t st) {
     constexpr int kGroups = kGateThreads / G;
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t tiles = (int64_t)g.L * g.ntl;
     const size_t smem = (size_t)((g.E + 3) & ~3) * 4 + (size_t)kGroups * G * VPL * 4 +
                         (size_t)kGroups * kGateCand * 8 + (size_t)g.E * 4;
     const bool full = g.E == G * VPL;
@@ -347,13 +346,17 @@ cudaError_t gate_vpl(const Geo &g, const void *logits, const float *bias, int32_
 
 cudaError_t launch_gate(const Geo &g, const void *logits, bool bf16, const float *bias, int32_t *ids,
                         float *scores, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st) {
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t tiles = (int64_t)g.L * g.ntl;
     if (tiles == 0) return cudaSuccess;
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
     const size_t esz = bf16 ? 2 : 4;
     const bool vec = ((uintptr_t)logits & 15) == 0 && ((size_t)g.E * esz) % 16 == 0;
     int32_t *tile_cnt = ws_at<int32_t>(ws, g.off_tile);
-    cudaError_t e = bf16 ? gate_vpl<true>(g, logits, bias, ids, scores, tile_cnt, vec, st)
+    cudaError_t e;
+    if (g.roff &&
+        (e = launch_tile_first(g, g.TT, ws_at<int32_t>(ws, g.off_first), ws_at<WsHeader>(ws, 0), st)) != cudaSuccess)
+        return e;
+    e = bf16 ? gate_vpl<true>(g, logits, bias, ids, scores, tile_cnt, vec, st)
                          : gate_vpl<false>(g, logits, bias, ids, scores, tile_cnt, vec, st);
     if (e != cudaSuccess) return e;
     return launch_hist_prefix(g, hist, ws, fp, st);

@@ -36,16 +36,18 @@ __global__ void __launch_bounds__(kHistThreads, 3)
 k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, WsHeader *hdr, Geo g) {
     extern __shared__ int cnt[];                     // [E + 1]: E = the spare counter
     const int E = g.E;
-    const int tile = blockIdx.x;
-    const int t = tile % g.tps;
-    const int s = (tile / g.tps) % g.R;
-    const int l = tile / (g.tps * g.R);
+    const int l = blockIdx.x / g.ntl;
+    const int tile = blockIdx.x - l * g.ntl;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
-    pdl_wait();                                    // the ids may come from the previous kernel
-
-    const int tok0 = t * g.TT;
-    const int ntok = max(0, min(g.TT, g.tpr - tok0));
-    const int32_t *a = ids + (int64_t)l * g.npairs + ((int64_t)s * g.tpr + tok0) * g.k;
+    pdl_wait();                                    // the ids (and the tile table) may come
+                                                   // from the previous kernels
+    const TileRef tr = tile_ref(g, g.tfirst, g.TT, g.tps, tile);
+    if (tr.s < 0) {                                // past the last source's tiles
+        pdl_trigger();
+        return;
+    }
+    const int ntok = tr.ntok;
+    const int32_t *a = ids + (int64_t)l * g.npairs + (int64_t)tr.tok0 * g.k;
     const int n = ntok * g.k;
     int head = (int)(((16 - ((uintptr_t)a & 15)) & 15) >> 2);
     if (head > n) head = n;
@@ -70,8 +72,57 @@ k_hist_tiles(const int32_t *__restrict__ ids, int32_t *__restrict__ tile_cnt, Ws
     for (int i = threadIdx.x + kHistVec * kHistThreads; i < nv; i += kHistThreads) count4(__ldg(v + i), E, cnt, bad);
     if (bad) set_error(hdr, TOPO_ERANGE);
     __syncthreads();
-    int32_t *mine = tile_cnt + (((int64_t)l * g.R + s) * g.tps + t) * E;
+    int32_t *mine = tile_cnt + ((int64_t)l * g.ntl + tile) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) mine[e] = cnt[e];
+    pdl_trigger();
+}
+
+// first[s] for tiles of TT tokens over the source offsets, one CTA: the
+// sources' tile counts ceil(len / TT), scanned in chunks of the block; the
+// offsets are checked (0 first, T last, never decreasing).  On a bad table
+// every first[] is 0, so every tile is empty, and TOPO_EOFFSETS is raised.
+constexpr int kFirstThreads = 1024;
+
+__global__ void __launch_bounds__(kFirstThreads)
+k_tile_first(const int64_t *__restrict__ off, int32_t *first, WsHeader *hdr, int R, int T, int TT) {
+    __shared__ int wsum[kFirstThreads / 32];
+    __shared__ int carry, bad;
+    pdl_wait();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        bad = (__ldg(off) != 0 || __ldg(off + R) != (int64_t)T);
+    }
+    __syncthreads();
+    for (int s0 = 0; s0 < R; s0 += kFirstThreads) {
+        const int s = s0 + threadIdx.x;
+        int c = 0;
+        if (s < R) {
+            const int64_t len = __ldg(off + s + 1) - __ldg(off + s);
+            if (len < 0 || len > T) bad = 1;
+            else c = (int)((len + TT - 1) / TT);
+        }
+        int inc = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += y;
+        }
+        if (lane == 31) wsum[w] = inc;
+        __syncthreads();
+        int before = carry;
+        for (int x = 0; x < w; ++x) before += wsum[x];
+        if (s < R) first[s] = before + inc - c;
+        __syncthreads();
+        if (threadIdx.x == kFirstThreads - 1) carry = before + inc;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) first[R] = carry;
+    __syncthreads();
+    if (bad) {
+        for (int s = threadIdx.x; s <= R; s += kFirstThreads) first[s] = 0;
+        if (threadIdx.x == 0) set_error(hdr, TOPO_EOFFSETS);
+    }
     pdl_trigger();
 }
 
@@ -94,10 +145,14 @@ k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo 
     const int E = g.E;
     const unsigned row = (unsigned)(c / E);       // l * R + s
     const int e = (int)(c - (int64_t)row * E);
-    int32_t *col = tile_cnt + (int64_t)row * g.tps * E + e;
+    const int l = (int)(row / (unsigned)g.R), s = (int)(row - (unsigned)l * g.R);
+    int tb, te;
+    source_tiles(g, g.tfirst, g.tps, s, &tb, &te);
+    int32_t *col = tile_cnt + ((int64_t)l * g.ntl + tb) * E + e;
+    const int nt = te - tb;
     int run = 0;
-    for (int u0 = 0; u0 < g.tps; u0 += kPrefixChunk) {
-        const int m = min(kPrefixChunk, g.tps - u0);
+    for (int u0 = 0; u0 < nt; u0 += kPrefixChunk) {
+        const int m = min(kPrefixChunk, nt - u0);
         int v[kPrefixChunk];
 #pragma unroll
         for (int q = 0; q < kPrefixChunk; ++q) v[q] = q < m ? col[(int64_t)(u0 + q) * E] : 0;
@@ -113,15 +168,21 @@ k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo 
 
 }  // namespace
 
+cudaError_t launch_tile_first(const Geo &g, int TT, int32_t *first, WsHeader *hdr, cudaStream_t st) {
+    return launch_pdl(k_tile_first, dim3(1), dim3(kFirstThreads), 0, st, g.roff, first, hdr, g.R, g.T, TT);
+}
+
 cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *ws, uint64_t fp,
                         cudaStream_t st) {
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t tiles = (int64_t)g.L * g.ntl;
     if (tiles == 0) return cudaSuccess;
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = ((size_t)g.E + 1) * sizeof(int);
     cudaError_t e = ensure_smem((const void *)k_hist_tiles, smem);
     if (e != cudaSuccess) return e;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
+    if (g.roff && (e = launch_tile_first(g, g.TT, ws_at<int32_t>(ws, g.off_first), hdr, st)) != cudaSuccess)
+        return e;
     if ((e = launch_pdl(k_hist_tiles, dim3((unsigned)tiles), dim3(kHistThreads), smem, st, ids,
                         ws_at<int32_t>(ws, g.off_tile), hdr, g)) != cudaSuccess)
         return e;

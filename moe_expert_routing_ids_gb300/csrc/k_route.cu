@@ -36,21 +36,25 @@ namespace {
 
 struct TileGeo {
     int l, s, t;
-    int ntok;        // tokens in this tile
+    int ntok;        // tokens in this tile (0: an empty tile, s < 0 possible)
+    bool last;       // the source's last tile
+    int64_t row;     // the tile's row of the tile index: l * ntl + tile
     int64_t p0;      // first pair of the tile within its layer
     int64_t slot0;   // base of the tile in the position array (TT * k entries)
 };
 
 __device__ __forceinline__ TileGeo tile_geo(const Geo &g) {
     TileGeo tg;
-    const int tile = blockIdx.x;
-    tg.t = tile % g.tps;
-    tg.s = (tile / g.tps) % g.R;
-    tg.l = tile / (g.tps * g.R);
-    const int tok0 = tg.t * g.TT;
-    tg.ntok = max(0, min(g.TT, g.tpr - tok0));
-    tg.p0 = ((int64_t)tg.s * g.tpr + tok0) * g.k;
-    tg.slot0 = (int64_t)tile * g.TT * g.k;
+    tg.l = blockIdx.x / g.ntl;
+    const int tile = blockIdx.x - tg.l * g.ntl;
+    const TileRef r = tile_ref(g, g.tfirst, g.TT, g.tps, tile);
+    tg.s = r.s;
+    tg.t = r.t;
+    tg.ntok = r.ntok;
+    tg.last = r.last;
+    tg.row = blockIdx.x;
+    tg.p0 = (int64_t)r.tok0 * g.k;
+    tg.slot0 = (int64_t)blockIdx.x * g.TT * g.k;
     return tg;
 }
 
@@ -215,6 +219,10 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     }
     if (!kFused && blockIdx.x == 0 && threadIdx.x == 0) hdr->route_fp = fp_mix(hist_fp, route_part);
     const TileGeo tg = tile_geo(g);
+    if (tg.ntok == 0) {                          // an empty tile: no pairs, no tables
+        pdl_trigger();
+        return;
+    }
     const int E = g.E;
     const int k = K > 0 ? K : g.k;
     const int kp = K > 0 ? ((K & 1) ? K : K + 1) : g.kp;
@@ -224,7 +232,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     const int32_t *ids_layer = ids + (int64_t)tg.l * g.npairs;
     int32_t *dst_layer = dst + (int64_t)tg.l * g.npairs;
     int32_t *sorted_layer = kFused ? sorted + (int64_t)tg.l * g.npairs : nullptr;
-    const int32_t *tbase = tile_idx + (((int64_t)tg.l * g.R + tg.s) * g.tps + tg.t) * E;
+    const int32_t *tbase = tile_idx + tg.row * E;
     const int32_t *ro = roff + ((int64_t)tg.l * g.R + tg.s) * (E + 1);
     const Entry *re = rent + ((int64_t)tg.l * g.R + tg.s) * g.n_inst_cap;
     bool bad_id = false, bad_state = false;
@@ -265,7 +273,7 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
         if (ne > 1) {
             // several entries: when the tile's occurrences [tb, te) all fall in
             // one entry, the tile ranks e like a single-entry expert
-            const int te = tg.t + 1 < g.tps ? __ldg(tbase + E + e) : __ldg(&re[en - 1].cum_end);
+            const int te = !tg.last ? __ldg(tbase + E + e) : __ldg(&re[en - 1].cum_end);
             int j = b;
             while (j < en && tb >= __ldg(&re[j].cum_end)) ++j;
             if (j < en && te <= __ldg(&re[j].cum_end)) {
@@ -417,6 +425,10 @@ k_layout_scatter(const int32_t *__restrict__ pos_ws, int32_t *sorted, WsHeader *
     const int k = g.k;
     const int n = g.TT * k;
     int32_t *out = sorted + (int64_t)tg.l * g.npairs;
+    if (tg.ntok == 0) {
+        pdl_trigger();
+        return;
+    }
     bool bad = false;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         const int wr = div_k(g, i >> 5);   // (i / 32) / k
@@ -477,7 +489,7 @@ cudaError_t launch_tiles(const Geo &g, const int32_t *ids, int32_t *dst, int32_t
     const size_t smem = rank_smem_bytes(g);
     cudaError_t e;
     if ((e = ensure_smem((const void *)kern, smem)) != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t tiles = (int64_t)g.L * g.ntl;
     return launch_pdl(kern, dim3((unsigned)tiles), dim3(kRankThreads), smem, st,
         ids, ws_at<int32_t>(ws, g.off_tile), ws_at<int32_t>(ws, g.off_roff),
         ws_at<Entry>(ws, g.off_rent), dst, ws_at<int32_t>(ws, g.off_pos), sorted,
@@ -512,7 +524,7 @@ cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t
 cudaError_t launch_layout(const Geo &g, int32_t *sorted, int32_t *seg_off, int64_t *send_counts,
                           int64_t *layout_stats, void *ws, uint64_t route_part, cudaStream_t st) {
     cudaError_t e;
-    const int64_t tiles = (int64_t)g.L * g.R * g.tps;
+    const int64_t tiles = (int64_t)g.L * g.ntl;
     if ((e = launch_pdl(k_layout_scatter, dim3((unsigned)tiles), dim3(256), 0, st, ws_at<int32_t>(ws, g.off_pos),
                         sorted, ws_at<WsHeader>(ws, 0), g, route_part)) != cudaSuccess)
         return e;

@@ -37,7 +37,28 @@ struct ShGeo {
     int L, T, E, k, R;
     FastDiv tpr, er;                 // tokens per source; E / R for the contiguous main map
     const int32_t *main_rank;
+    const int64_t *roff;             // source offsets [R+1], or null for equal blocks
 };
+
+// Source rank of token t: t / tpr for equal blocks, else the last s with
+// roff[s] <= t (an empty source never holds a token).
+__device__ __forceinline__ int sh_src(const ShGeo &g, int64_t t) {
+    if (!g.roff) return (int)fast_quot((unsigned)t, g.tpr);
+    int lo = 0, hi = g.R - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(g.roff + mid) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The offsets must run from 0 to T without decreasing.
+__global__ void k_sh_check_offsets(const int64_t *__restrict__ roff, int R, int T, WsHeader *hdr) {
+    bool bad = threadIdx.x == 0 && (__ldg(roff) != 0 || __ldg(roff + R) != (int64_t)T);
+    for (int s = threadIdx.x; s < R; s += blockDim.x) bad |= __ldg(roff + s + 1) < __ldg(roff + s);
+    if (bad) set_error(hdr, TOPO_EOFFSETS);
+}
 
 __device__ __forceinline__ int sh_rank(const ShGeo &g, int b) {
     return g.main_rank ? __ldg(g.main_rank + b) : (int)fast_quot((unsigned)b, g.er);
@@ -169,7 +190,7 @@ k_sh_target(const int32_t *__restrict__ ids, const int64_t *__restrict__ M, int3
             }
         }
         // the source rank's own score, from the lane that holds it
-        const int s = (int)fast_quot((unsigned)t, g.tpr);
+        const int s = sh_src(g, t);
         long long mine = 0;
 #pragma unroll
         for (int i = 0; i < RPL; ++i)
@@ -286,7 +307,7 @@ __device__ __forceinline__ void sh_thread_tokens(const int32_t *__restrict__ ids
                 }
             }
         }
-        const int s = (int)fast_quot((unsigned)t, g.tpr);
+        const int s = sh_src(g, t);
         S best = 0, ssc = 0;
         int br = -1;
 #pragma unroll
@@ -439,15 +460,21 @@ size_t shuffle_ws_bytes(int L, int E, int R) {
 }
 
 cudaError_t launch_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
-                           const int32_t *main_rank, int32_t *target, int64_t *stats, void *ws,
-                           cudaStream_t st) {
+                           const int32_t *main_rank, const int64_t *rank_offsets, int32_t *target,
+                           int64_t *stats, void *ws, cudaStream_t st) {
     if (L < 2) return cudaSuccess;
     ShGeo g;
     g.L = L; g.T = T; g.E = E; g.k = k; g.R = R;
-    g.tpr = make_fast_div((unsigned)(R > 0 && T > 0 ? T / R : 1));
+    g.tpr = make_fast_div((unsigned)(R > 0 && T / R > 0 ? T / R : 1));
     g.er = make_fast_div((unsigned)(main_rank ? 1 : E / R));
     g.main_rank = main_rank;
+    g.roff = rank_offsets;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
+    if (rank_offsets) {
+        k_sh_check_offsets<<<1, 256, 0, st>>>(rank_offsets, R, T, hdr);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const size_t n = (size_t)(L - 1) * E * R;
     int *wide = ws_at<int>(ws, sizeof(WsHeader));
     int64_t *M = ws_at<int64_t>(ws, sizeof(WsHeader) + 256);

@@ -41,7 +41,8 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     if (c->T < 0 || c->E < 1 || c->k < 1 || c->R < 1 || c->ranks_per_node < 1 || c->n_slot < 0)
         return TOPO_EINVAL;
     if (c->ranks_per_node > kMaxRanksPerNode) return TOPO_EINVAL;
-    if (c->R % c->ranks_per_node || c->E % c->R || c->T % c->R) return TOPO_EINVAL;
+    if (c->R % c->ranks_per_node || c->E % c->R) return TOPO_EINVAL;
+    if (!c->rank_offsets && c->T % c->R) return TOPO_EINVAL;
     if ((int64_t)c->T * c->k > INT32_MAX) return TOPO_EINVAL;
     if (c->tok_bytes < 0 || c->expert_bytes < 0 || c->c_intra < 1 || c->c_inter < c->c_intra)
         return TOPO_EINVAL;
@@ -68,7 +69,10 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     g->n_local = (int32_t)nl; g->L = n_layers;
     g->c_intra = c->c_intra; g->c_inter = c->c_inter; g->max_iters = c->max_refine_iters;
     g->S_tok = c->tok_bytes; g->W = c->expert_bytes;
-    g->tpr = c->T / c->R;
+    g->roff = c->rank_offsets;
+    // tokens per source: exact for equal blocks; with rank_offsets the
+    // average, which only steers the tile size below
+    g->tpr = c->rank_offsets ? (c->T + c->R - 1) / c->R : c->T / c->R;
     g->pps = (int64_t)g->tpr * c->k;
     g->npairs = (int64_t)c->T * c->k;
     g->kp = (c->k & 1) ? c->k : c->k + 1;
@@ -98,11 +102,16 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     g->RW = (int32_t)best_rw;
     g->TT = kRankThreads * g->RW;
     g->tps = g->tpr == 0 ? 1 : (g->tpr + g->TT - 1) / g->TT;
+    // tiles per layer: a source of n tokens holds ceil(n / TT) tiles, at most
+    // n / TT + 1, so ceil(T / TT) + R bound them for any offsets
+    g->ntl = c->rank_offsets ? (int32_t)((c->T + (int64_t)g->TT - 1) / g->TT + c->R) : c->R * g->tps;
+    if ((int64_t)n_layers * g->ntl > INT32_MAX) return TOPO_EINVAL;
     g->n_inst_cap = c->E + c->R * c->n_slot;
     g->n_keys = c->R * g->n_local;
     const size_t L = (size_t)n_layers;
-    const size_t tiles = L * (size_t)R * g->tps;
+    const size_t tiles = L * (size_t)g->ntl;
     size_t off = sizeof(WsHeader);
+    g->off_first = off; off = align_up(off + (size_t)(R + 1) * 4);
     g->off_tile = off;  off = align_up(off + tiles * E * 4);
     g->off_pos = off;   off = align_up(off + tiles * g->TT * c->k * 4);
     g->off_main = off;  off = align_up(off + 3 * E * 4);
@@ -124,6 +133,9 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? TOPO_OK : TOPO_ECUDA; }
 
+// The per-call table of each source's first tile lives in the workspace.
+void bind_ws(Geo &g, void *ws) { g.tfirst = ws_at<int32_t>(ws, g.off_first); }
+
 uint64_t hist_fingerprint(const Geo &g, const int32_t *ids) {
     uint64_t h = fp_mix(0x48495354ull, (uint64_t)g.T);
     h = fp_mix(h, (uint64_t)g.E);
@@ -131,6 +143,7 @@ uint64_t hist_fingerprint(const Geo &g, const int32_t *ids) {
     h = fp_mix(h, (uint64_t)g.R);
     h = fp_mix(h, (uint64_t)g.L);
     h = fp_mix(h, (uint64_t)g.tps);
+    h = fp_mix(h, (uint64_t)(uintptr_t)g.roff);
     return fp_mix(h, (uint64_t)(uintptr_t)ids);
 }
 
@@ -182,7 +195,7 @@ size_t topo_workspace_bytes(const topo_cfg *cfg, int32_t n_layers, int32_t which
     Geo g;
     if (make_geo(cfg, n_layers, &g) != TOPO_OK) return 0;
     if (which_call == TOPO_CALL_PACK) return pack_ws_bytes(g);
-    if (which_call == TOPO_CALL_DEDUP) return dedup_ws_bytes(g, nullptr, nullptr);
+    if (which_call == TOPO_CALL_DEDUP) return dedup_ws_bytes(g, nullptr, nullptr, nullptr);
     return g.total;
 }
 
@@ -199,6 +212,7 @@ int topo_hist(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, int32_t
     if (!hist || !ws || (!ids && g.npairs > 0 && n_layers > 0)) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
+    bind_ws(g, ws);
     return cuda_rc(launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream));
 }
 
@@ -216,6 +230,7 @@ int topo_gate_hist(const topo_cfg *cfg, int32_t n_layers, const void *logits, in
         return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
+    bind_ws(g, ws);
     return cuda_rc(launch_gate(g, logits, logits_dtype == TOPO_DTYPE_BF16, bias, ids, scores, hist, ws,
                                hist_fingerprint(g, ids), stream));
 }
@@ -235,18 +250,19 @@ size_t topo_shuffle_workspace_bytes(int32_t L, int32_t E, int32_t R) {
 }
 
 int topo_shuffle_targets(int32_t L, int32_t T, int32_t E, int32_t k, int32_t R, const int32_t *ids,
-                         const int64_t *tr, const int32_t *main_rank, int32_t *target, int64_t *stats,
-                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+                         const int64_t *tr, const int32_t *main_rank, const int64_t *rank_offsets,
+                         int32_t *target, int64_t *stats, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
     static_assert(TOPO_SHUFFLE_MAX_RANKS == kShuffleMaxRanks, "rank limit");
     if (L < 0 || T < 0 || E < 1 || E >= (1 << 26) || k < 1 || k > kMaxK || R < 1 ||
-        R > TOPO_SHUFFLE_MAX_RANKS || T % R != 0 || (!main_rank && E % R != 0))
+        R > TOPO_SHUFFLE_MAX_RANKS || (!rank_offsets && T % R != 0) || (!main_rank && E % R != 0))
         return TOPO_EINVAL;
     if ((int64_t)L * T * k > ((int64_t)1 << 40)) return TOPO_EINVAL;
     if (!ws) return TOPO_EINVAL;
     if (ws_bytes < shuffle_ws_bytes(L, E, R)) return TOPO_ENOSPC;
     if (L < 2) return TOPO_OK;
     if (!tr || !stats || (T > 0 && (!ids || !target))) return TOPO_EINVAL;
-    return cuda_rc(launch_shuffle(L, T, E, k, R, ids, tr, main_rank, target, stats, ws, stream));
+    return cuda_rc(launch_shuffle(L, T, E, k, R, ids, tr, main_rank, rank_offsets, target, stats, ws, stream));
 }
 
 int topo_plan(const topo_cfg *cfg, int32_t n_layers, const int32_t *hist, const topo_plan_t *plan,
@@ -269,6 +285,7 @@ int topo_reroute(const topo_cfg *cfg, int32_t n_layers, const int32_t *ids, cons
         return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
+    bind_ws(g, ws);
     return cuda_rc(launch_reroute(g, cfg->main_rank, ids, *plan, dst_inst, ws, hist_fingerprint(g, ids),
                                   route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
 }
@@ -284,6 +301,7 @@ int topo_dispatch_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *d
     if ((!dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
+    bind_ws(g, ws);
     return cuda_rc(launch_layout(g, sorted_pairs, seg_off, send_counts, layout_stats, ws,
                                  route_fingerprint(g, *plan, dst_inst, cfg->main_rank), stream));
 }
@@ -299,6 +317,7 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
     if ((!ids || !dst_inst || !sorted_pairs) && g.npairs > 0 && n_layers > 0) return TOPO_EINVAL;
     if (ws_bytes < g.total) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
+    bind_ws(g, ws);
     return cuda_rc(launch_reroute_layout(g, cfg->main_rank, ids, *plan, dst_inst, sorted_pairs, seg_off,
                                          send_counts, layout_stats, ws, hist_fingerprint(g, ids),
                                          stream));
@@ -323,7 +342,7 @@ int topo_dedup_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *dst_
     if (rc) return rc;
     if (cfg->k > kDedupMaxK || cfg->R > kDedupMaxRanks) return TOPO_EINVAL;
     if (!ws) return TOPO_EINVAL;
-    if (ws_bytes < dedup_ws_bytes(g, nullptr, nullptr)) return TOPO_ENOSPC;
+    if (ws_bytes < dedup_ws_bytes(g, nullptr, nullptr, nullptr)) return TOPO_ENOSPC;
     if (n_layers == 0) return TOPO_OK;
     if (!seg || !send || !stats || (g.npairs > 0 && (!dst_inst || !row_token || !row_slots || !tok_dst)))
         return TOPO_EINVAL;
@@ -366,6 +385,7 @@ const char *topo_strerror(int code) {
         case TOPO_ERANGE: return "expert id outside [0, E)";
         case TOPO_ESTATE: return "workspace does not hold the index this call needs";
         case TOPO_EMAP: return "main_rank is not a balanced map onto the ranks";
+        case TOPO_EOFFSETS: return "rank_offsets is not an ordered partition of the tokens";
         default: return "unknown error";
     }
 }
@@ -410,15 +430,17 @@ extern "C" int topo_hist_noalloc(const topo_cfg *cfg, int32_t n_layers, const in
     int rc = make_geo(cfg, n_layers, &g);
     if (rc) return rc;
     if (!hist || (!ids && g.npairs > 0 && n_layers > 0)) return TOPO_EINVAL;
-    // Compact layout: header, tile counts (the histogram kernels touch no
-    // other region).
-    const size_t tiles = (size_t)n_layers * g.R * g.tps;
-    g.off_tile = sizeof(WsHeader);
+    // Compact layout: header, the sources' first tiles, tile counts (the
+    // histogram kernels touch no other region).
+    const size_t tiles = (size_t)n_layers * g.ntl;
+    g.off_first = sizeof(WsHeader);
+    g.off_tile = align_up(g.off_first + (size_t)(g.R + 1) * 4);
     g.total = align_up(g.off_tile + tiles * g.E * sizeof(int32_t));
     if (g.total > TOPO_HIST_NOALLOC_SCRATCH_BYTES) return TOPO_ENOSPC;
     void *ws = nullptr;
     cudaError_t e = noalloc_scratch(&ws);
     if (e != cudaSuccess) return TOPO_ECUDA;
+    bind_ws(g, ws);
     e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), stream);     // error word starts at 0
     if (e == cudaSuccess && n_layers > 0)
         e = launch_hist(g, ids, hist, ws, hist_fingerprint(g, ids), stream);

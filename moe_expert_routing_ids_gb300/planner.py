@@ -34,7 +34,8 @@ class Planner:
     """Owns the workspace and output buffers of one problem shape.
 
     cfg: dict with T, E, k, R, ranks_per_node, n_slot, tok_bytes, expert_bytes,
-    c_intra, c_inter, optional max_refine_iters and main_rank (device int32
+    c_intra, c_inter, optional max_refine_iters, rank_offsets (int64 [R+1]
+    token offsets of the sources, device tensor or array, or None) and main_rank (device int32
     tensor or None)."""
 
     def __init__(self, cfg: dict, n_layers: int, device="cuda", stream=None):
@@ -44,7 +45,10 @@ class Planner:
         self.main_rank = cfg.get("main_rank")
         if self.main_rank is not None and not isinstance(self.main_rank, torch.Tensor):
             self.main_rank = torch.as_tensor(self.main_rank, dtype=torch.int32, device=self.device)
-        self.cfg = make_cfg(**{**cfg, "main_rank": self.main_rank})
+        self.rank_offsets = cfg.get("rank_offsets")
+        if self.rank_offsets is not None and not isinstance(self.rank_offsets, torch.Tensor):
+            self.rank_offsets = torch.as_tensor(self.rank_offsets, dtype=torch.int64, device=self.device)
+        self.cfg = make_cfg(**{**cfg, "main_rank": self.main_rank, "rank_offsets": self.rank_offsets})
         self.stream = stream
         T, E, k, R, ns = cfg["T"], cfg["E"], cfg["k"], cfg["R"], cfg["n_slot"]
         nl = E // R + ns

@@ -74,24 +74,24 @@ def _load():
             i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
             i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
             ci, cl = ctypes.c_int, ctypes.c_int64
-            lib.oracle_hist.argtypes = [ci, ci, ci, ci, ci, i32p, i32p]
+            vp = ctypes.c_void_p
+            lib.oracle_hist.argtypes = [ci, ci, ci, ci, ci, vp, i32p, i32p]
             lib.oracle_cooccur.argtypes = [ci, ci, ci, ci, i32p, i64p, ctypes.c_void_p]
             lib.oracle_plan.argtypes = [ci, ci, ci, ci, ci, ci, cl, cl, cl, cl, ci,
                                         ctypes.c_void_p, ci, i32p, i32p, i32p, i32p,
                                         i32p, i64p]
-            lib.oracle_reroute.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_void_p, ci,
+            lib.oracle_reroute.argtypes = [ci, ci, ci, ci, ci, ci, vp, vp, ci,
                                            i32p, i32p, i32p, i32p]
-            lib.oracle_layout.argtypes = [ci, ci, ci, ci, ci, ci, cl, ci, i32p, i32p,
+            lib.oracle_layout.argtypes = [ci, ci, ci, ci, ci, ci, cl, vp, ci, i32p, i32p,
                                           i32p, i64p, i64p]
             u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
             f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
             lib.oracle_permute.argtypes = [ci, ci, ci, ci, u16p, i32p, u16p]
             lib.oracle_combine.argtypes = [ci, ci, ci, ci, u16p, i32p, f32p, u16p]
             u64p = np.ctypeslib.ndpointer(np.uint64, flags="C_CONTIGUOUS")
-            lib.oracle_dedup.argtypes = [ci, ci, ci, ci, ci, i32p, i32p, i32p, u64p, u64p, i64p, i64p]
-            lib.oracle_gate.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_void_p, ctypes.c_void_p,
-                                        i32p, f32p, i32p]
-            lib.oracle_shuffle.argtypes = [ci, ci, ci, ci, ci, i32p, i64p, ctypes.c_void_p, i32p, i64p]
+            lib.oracle_dedup.argtypes = [ci, ci, ci, ci, vp, ci, i32p, i32p, i32p, u64p, u64p, i64p, i64p]
+            lib.oracle_gate.argtypes = [ci, ci, ci, ci, ci, vp, ci, vp, vp, i32p, f32p, i32p]
+            lib.oracle_shuffle.argtypes = [ci, ci, ci, ci, ci, i32p, i64p, vp, vp, i32p, i64p]
             lib.oracle_place.argtypes = [ci, ci, ci, ci, i64p, i32p, i64p]
             for f in ("oracle_place", "oracle_shuffle", "oracle_gate", "oracle_hist", "oracle_cooccur", "oracle_plan", "oracle_reroute",
                       "oracle_layout", "oracle_permute", "oracle_combine", "oracle_dedup"):
@@ -110,13 +110,21 @@ def _i32(a):
     return np.ascontiguousarray(a, dtype=np.int32)
 
 
+def _offsets(rank_offsets):
+    """(keep-alive array, pointer) for int64 [R+1] source offsets, or (None, None)."""
+    if rank_offsets is None:
+        return None, None
+    o = np.ascontiguousarray(rank_offsets, dtype=np.int64)
+    return o, o.ctypes.data_as(ctypes.c_void_p)
+
+
 def _check(fn, rc, allow=(OK,)):
     if rc not in allow:
         raise OracleError(fn, rc)
     return rc
 
 
-def gate(logits, k: int, R: int, bias=None):
+def gate(logits, k: int, R: int, bias=None, rank_offsets=None):
     """Top-k gating and Omega [TopoEP §2.1, §6.4; O1].
 
     logits: float32 [L, T, E] (or [T, E]), or uint16 bf16 patterns of that
@@ -136,8 +144,9 @@ def gate(logits, k: int, R: int, bias=None):
         raise ValueError("bias must be float32 [E]")
     out = dict(ids=np.zeros((L, T, k), np.int32), scores=np.zeros((L, T, k), np.float32),
                hist=np.zeros((L, R, E), np.int32))
+    keep, op = _offsets(rank_offsets)
     _check("oracle_gate", _load().oracle_gate(
-        T, E, k, R, L, int(a.dtype == np.uint16), a.ctypes.data_as(ctypes.c_void_p),
+        T, E, k, R, L, op, int(a.dtype == np.uint16), a.ctypes.data_as(ctypes.c_void_p),
         None if b is None else b.ctypes.data_as(ctypes.c_void_p), out["ids"].reshape(-1),
         out["scores"].reshape(-1), out["hist"].reshape(-1)))
     if squeeze:
@@ -168,11 +177,12 @@ def place(co, R: int, max_iters: int = 0):
 SHUFFLE_STAT_NAMES = ("next_pairs_on_target", "next_pairs_on_source", "tokens_moved", "next_pairs")
 
 
-def shuffle(ids, tr, R: int, main_rank=None):
+def shuffle(ids, tr, R: int, main_rank=None, rank_offsets=None):
     """Token-shuffle targets [Zyphra, "Moving Tokens Toward Their Next Experts"].
 
     ids int32 [L, T, k]; tr int64 [L-1, E, E] (cooccur's transitions); main_rank
-    int32 [E] or None.  Returns (target int32 [L-1, T], stats int64 [L-1, 4])."""
+    int32 [E] or None; rank_offsets int64 [R+1] or None (equal blocks).
+    Returns (target int32 [L-1, T], stats int64 [L-1, 4])."""
     a = _i32(ids)
     L, T, k = a.shape
     t = np.ascontiguousarray(tr, dtype=np.int64)
@@ -182,24 +192,27 @@ def shuffle(ids, tr, R: int, main_rank=None):
     mr = None if main_rank is None else _i32(main_rank)
     target = np.zeros((max(L - 1, 0), T), np.int32)
     stats = np.zeros((max(L - 1, 0), 4), np.int64)
+    keep, op = _offsets(rank_offsets)
     _check("oracle_shuffle", _load().oracle_shuffle(
         L, T, E, k, R, a.reshape(-1), t.reshape(-1) if t.size else np.zeros(1, np.int64),
-        None if mr is None else mr.ctypes.data_as(ctypes.c_void_p), target.reshape(-1),
+        None if mr is None else mr.ctypes.data_as(ctypes.c_void_p), op, target.reshape(-1),
         stats.reshape(-1)))
     return target, stats
 
 
-def hist(ids, R: int, E: int):
+def hist(ids, R: int, E: int, rank_offsets=None):
     """Routing matrix Omega [TopoEP §4.1, Eq. 3].
 
-    ids: int32 [L, T, k] or [T, k].  Returns int32 [L, R, E] (or [R, E])."""
+    ids: int32 [L, T, k] or [T, k]; rank_offsets: int64 [R+1] token offsets of
+    the sources, or None for equal blocks.  Returns int32 [L, R, E] (or [R, E])."""
     a = _i32(ids)
     squeeze = a.ndim == 2
     if squeeze:
         a = a[None]
     L, T, k = a.shape
     out = np.zeros((L, R, E), np.int32)
-    _check("oracle_hist", _load().oracle_hist(T, E, k, R, L, a.reshape(-1), out.reshape(-1)))
+    keep, op = _offsets(rank_offsets)
+    _check("oracle_hist", _load().oracle_hist(T, E, k, R, L, op, a.reshape(-1), out.reshape(-1)))
     return out[0] if squeeze else out
 
 
@@ -225,7 +238,8 @@ def plan(cfg: dict, hist_arr, max_refine_iters: int | None = None):
     """Two-stage plan [TopoEP §4.3] for each layer of hist int32 [L, R, E].
 
     cfg keys: T, E, k, R, ranks_per_node, n_slot, tok_bytes, expert_bytes,
-    c_intra, c_inter, optional max_refine_iters, optional main_rank.
+    c_intra, c_inter, optional max_refine_iters, optional main_rank (the
+    plan reads only Omega, so rank_offsets plays no part here).
     Returns dict of numpy arrays: slot_expert [L,R,n_slot], route_cnt
     [L,R,R,n_local], inst_load [L,R,n_local], rank_load [L,R], stats [L,8]."""
     h = _i32(hist_arr)
@@ -265,11 +279,12 @@ def reroute(cfg: dict, ids, plan_out: dict):
     se = _i32(plan_out["slot_expert"]).reshape(L, -1)
     q = _i32(plan_out["route_cnt"]).reshape(L, -1)
     keep, mp = _main_ptr(cfg.get("main_rank"))
+    keep_o, op = _offsets(cfg.get("rank_offsets"))
     dst = np.zeros((L, T * k), np.int32)
     rc = _load().oracle_reroute(T, cfg["E"], k, cfg["R"], cfg["ranks_per_node"], cfg["n_slot"],
-                                mp, L, a.reshape(-1), se.reshape(-1), q.reshape(-1),
+                                mp, op, L, a.reshape(-1), se.reshape(-1), q.reshape(-1),
                                 dst.reshape(-1))
-    del keep
+    del keep, keep_o
     _check("oracle_reroute", rc)
     return dst[0] if squeeze else dst
 
@@ -288,8 +303,9 @@ def layout(cfg: dict, dst_inst, n_layers: int | None = None):
     so = np.zeros((L, R * nl + 1), np.int32)
     sc = np.zeros((L, R, R), np.int64)
     st = np.zeros((L, 8), np.int64)
+    keep, op = _offsets(cfg.get("rank_offsets"))
     _check("oracle_layout", _load().oracle_layout(T, E, k, R, cfg["ranks_per_node"], cfg["n_slot"],
-                                                  cfg["tok_bytes"], L, d.reshape(-1),
+                                                  cfg["tok_bytes"], op, L, d.reshape(-1),
                                                   sp.reshape(-1), so.reshape(-1),
                                                   sc.reshape(-1), st.reshape(-1)))
     if squeeze:
@@ -343,7 +359,8 @@ def dedup(cfg: dict, dst_inst):
     out = dict(seg=np.zeros((L, R + 1), np.int32), row_token=np.zeros((L, T * k), np.int32),
                row_slots=np.zeros((L, T * k), np.uint64), tok_dst=np.zeros((L, T, RW), np.uint64),
                send=np.zeros((L, R, R), np.int64), stats=np.zeros((L, 4), np.int64))
-    _check("oracle_dedup", _load().oracle_dedup(T, k, R, nl, L, d.reshape(-1),
+    keep, op = _offsets(cfg.get("rank_offsets"))
+    _check("oracle_dedup", _load().oracle_dedup(T, k, R, nl, op, L, d.reshape(-1),
                                                 out["seg"].reshape(-1), out["row_token"].reshape(-1),
                                                 out["row_slots"].reshape(-1), out["tok_dst"].reshape(-1),
                                                 out["send"].reshape(-1), out["stats"].reshape(-1)))

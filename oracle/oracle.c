@@ -28,8 +28,11 @@
  * fusion or reordering.  Integers only; 64-bit where a product may overflow.
  *
  * Conventions shared with the inputs (not with any other code):
- *   pair p = t*k + j; source rank src(t) = t / (T/R) (equal contiguous token
- *   blocks, T % R == 0); domain dom(r) = r / ranks_per_node;
+ *   pair p = t*k + j; each rank routes its own local tokens [TopoEP §2.1],
+ *   the ranks' blocks lying one after the other: source rank src(t) = the s
+ *   with off[s] <= t < off[s+1] for the caller's offsets off[0..R]
+ *   (0 = off[0] <= ... <= off[R] = T), or t / (T/R) for equal blocks when no
+ *   offsets are given (T % R == 0); domain dom(r) = r / ranks_per_node;
  *   main(e) = e / (E/R) with local index e % (E/R) unless a main_rank map is
  *   given, in which case the local index of e is the number of experts e' < e
  *   with the same main rank; an instance (r, l) is packed as r*n_local + l,
@@ -76,12 +79,40 @@ static int64_t cost(const Problem *P, int s, int r) {
     return P->c_inter;
 }
 
+/* src[t] for t < T: the source rank of every token, from the offsets off
+ * (R+1 values) or, when off is NULL, from equal blocks of T/R tokens.  An
+ * offset table that is not 0 = off[0] <= off[1] <= ... <= off[R] = T, or
+ * equal blocks that do not divide T, are argument errors. */
+static int token_sources(int T, int R, const int64_t *off, int32_t *src) {
+    if (T < 0 || R < 1) return ORC_EINVAL;
+    if (!off) {
+        if (T % R != 0) return ORC_EINVAL;
+        for (int t = 0; t < T; t++) src[t] = t / (T / R);
+        return ORC_OK;
+    }
+    if (off[0] != 0 || off[R] != T) return ORC_EINVAL;
+    for (int s = 0; s < R; s++) {
+        if (off[s + 1] < off[s]) return ORC_EINVAL;
+        for (int64_t t = off[s]; t < off[s + 1]; t++) src[t] = s;
+    }
+    return ORC_OK;
+}
+
+static int32_t *sources_or_null(int T, int R, const int64_t *off) {
+    int32_t *src = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    if (src && token_sources(T, R, off, src) != ORC_OK) {
+        free(src);
+        return NULL;
+    }
+    return src;
+}
+
 static int problem_init(Problem *P, int T, int E, int k, int R, int rpn,
                         int n_slot, int64_t S_tok, int64_t W, int64_t c_intra,
                         int64_t c_inter, int max_iters, const int32_t *main_rank) {
     memset(P, 0, sizeof *P);
     if (T < 0 || E < 1 || k < 1 || R < 1 || rpn < 1 || n_slot < 0) return ORC_EINVAL;
-    if (R % rpn != 0 || E % R != 0 || T % R != 0) return ORC_EINVAL;
+    if (R % rpn != 0 || E % R != 0) return ORC_EINVAL;
     if (S_tok < 0 || W < 0 || c_intra < 1 || c_inter < c_intra || max_iters < 0) return ORC_EINVAL;
     P->T = T; P->E = E; P->k = k; P->R = R; P->rpn = rpn; P->n_slot = n_slot;
     P->S_tok = S_tok; P->W = W; P->c_intra = c_intra; P->c_inter = c_inter;
@@ -113,17 +144,18 @@ static void problem_free(Problem *P) {
 /* select expert e.                                                           */
 /* ------------------------------------------------------------------------ */
 
-int oracle_hist(int T, int E, int k, int R, int n_layers, const int32_t *ids,
-                int32_t *hist) {
-    if (T < 0 || E < 1 || k < 1 || R < 1 || n_layers < 0 || T % R != 0) return ORC_EINVAL;
-    int tpr = T / R;  /* tokens per source rank */
+int oracle_hist(int T, int E, int k, int R, int n_layers, const int64_t *rank_offsets,
+                const int32_t *ids, int32_t *hist) {
+    if (T < 0 || E < 1 || k < 1 || R < 1 || n_layers < 0) return ORC_EINVAL;
+    int32_t *src = sources_or_null(T, R, rank_offsets);
+    if (!src) return ORC_EINVAL;
     int rc = ORC_OK;
     for (int l = 0; l < n_layers; l++) {
         const int32_t *id = ids + (int64_t)l * T * k;
         int32_t *h = hist + (int64_t)l * R * E;
         memset(h, 0, sizeof(int32_t) * (size_t)R * E);
         for (int t = 0; t < T; t++) {
-            int s = t / tpr;
+            int s = src[t];
             for (int j = 0; j < k; j++) {
                 int e = id[(int64_t)t * k + j];
                 if (e < 0 || e >= E) { rc = ORC_ERANGE; continue; }
@@ -131,6 +163,7 @@ int oracle_hist(int T, int E, int k, int R, int n_layers, const int32_t *ids,
             }
         }
     }
+    free(src);
     return rc;
 }
 
@@ -154,10 +187,9 @@ static int gate_above(float a, int ia, float b, int ib) {
     return ia < ib;
 }
 
-int oracle_gate(int T, int E, int k, int R, int n_layers, int is_bf16, const void *logits,
-                const float *bias, int32_t *ids, float *scores, int32_t *hist) {
-    if (T < 0 || E < 1 || k < 1 || k > E || R < 1 || n_layers < 0 || T % R != 0)
-        return ORC_EINVAL;
+int oracle_gate(int T, int E, int k, int R, int n_layers, const int64_t *rank_offsets, int is_bf16,
+                const void *logits, const float *bias, int32_t *ids, float *scores, int32_t *hist) {
+    if (T < 0 || E < 1 || k < 1 || k > E || R < 1 || n_layers < 0) return ORC_EINVAL;
     float *raw = (float *)malloc(sizeof(float) * (size_t)E);
     float *sc = (float *)malloc(sizeof(float) * (size_t)E);
     char *taken = (char *)malloc((size_t)E);
@@ -183,7 +215,7 @@ int oracle_gate(int T, int E, int k, int R, int n_layers, int is_bf16, const voi
         }
     }
     free(raw); free(sc); free(taken);
-    return oracle_hist(T, E, k, R, n_layers, ids, hist);
+    return oracle_hist(T, E, k, R, n_layers, rank_offsets, ids, hist);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -572,13 +604,18 @@ int oracle_plan(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok,
 /* ------------------------------------------------------------------------ */
 
 int oracle_reroute(int T, int E, int k, int R, int rpn, int n_slot,
-                   const int32_t *main_rank, int n_layers, const int32_t *ids,
-                   const int32_t *slot_expert, const int32_t *route_cnt,
+                   const int32_t *main_rank, const int64_t *rank_offsets, int n_layers,
+                   const int32_t *ids, const int32_t *slot_expert, const int32_t *route_cnt,
                    int32_t *dst_inst) {
     Problem P;
     int rc = problem_init(&P, T, E, k, R, rpn, n_slot, 0, 0, 1, 1, 0, main_rank);
     if (rc != ORC_OK || n_layers < 0) { problem_free(&P); return ORC_EINVAL; }
-    int tpr = T / R;
+    /* first token of each source */
+    int64_t *beg = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R + 1));
+    int32_t *src = sources_or_null(T, R, rank_offsets);
+    if (!beg || !src) { free(beg); free(src); problem_free(&P); return ORC_EINVAL; }
+    for (int s = 0; s <= R; s++) beg[s] = rank_offsets ? rank_offsets[s] : (int64_t)s * (T / R);
+    free(src);
     int64_t npairs = (int64_t)T * k;
     int32_t *occ = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
     int *host = (int *)malloc(sizeof(int) * (size_t)R * E);
@@ -597,7 +634,7 @@ int oracle_reroute(int T, int E, int k, int R, int rpn, int n_slot,
             }
         for (int s = 0; s < R; s++) {
             memset(occ, 0, sizeof(int32_t) * (size_t)E);
-            for (int64_t p = (int64_t)s * tpr * k; p < (int64_t)(s + 1) * tpr * k; p++) {
+            for (int64_t p = beg[s] * k; p < beg[s + 1] * k; p++) {
                 int e = id[p];
                 dst[p] = -1;
                 if (e < 0 || e >= E) { rc = ORC_ERANGE; continue; }
@@ -613,7 +650,7 @@ int oracle_reroute(int T, int E, int k, int R, int rpn, int n_slot,
             }
         }
     }
-    free(occ); free(host);
+    free(occ); free(host); free(beg);
     problem_free(&P);
     return rc;
 }
@@ -632,12 +669,14 @@ int oracle_reroute(int T, int E, int k, int R, int rpn, int n_slot,
 /* ------------------------------------------------------------------------ */
 
 int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok,
-                  int n_layers, const int32_t *dst_inst, int32_t *sorted_pairs,
-                  int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats) {
+                  const int64_t *rank_offsets, int n_layers, const int32_t *dst_inst,
+                  int32_t *sorted_pairs, int32_t *seg_off, int64_t *send_counts,
+                  int64_t *layout_stats) {
     if (T < 0 || E < 1 || k < 1 || R < 1 || rpn < 1 || n_slot < 0) return ORC_EINVAL;
-    if (R % rpn != 0 || E % R != 0 || T % R != 0 || n_layers < 0) return ORC_EINVAL;
+    if (R % rpn != 0 || E % R != 0 || n_layers < 0) return ORC_EINVAL;
     int E_R = E / R, n_local = E_R + n_slot, nkeys = R * n_local;
-    int tpr = T / R;
+    int32_t *src = sources_or_null(T, R, rank_offsets);
+    if (!src) return ORC_EINVAL;
     int64_t npairs = (int64_t)T * k;
     int64_t *count = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nkeys + 1));
     for (int l = 0; l < n_layers; l++) {
@@ -647,7 +686,7 @@ int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok
         int64_t *sc = send_counts + (int64_t)l * R * R;
         int64_t *st = layout_stats + (int64_t)l * 8;
         for (int64_t p = 0; p < npairs; p++)
-            if (key[p] < 0 || key[p] >= nkeys) { free(count); return ORC_EINVAL; }
+            if (key[p] < 0 || key[p] >= nkeys) { free(count); free(src); return ORC_EINVAL; }
         /* counting sort: count, exclusive prefix, stable placement */
         memset(count, 0, sizeof(int64_t) * (size_t)(nkeys + 1));
         for (int64_t p = 0; p < npairs; p++) count[key[p]]++;
@@ -663,7 +702,7 @@ int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok
         memset(sc, 0, sizeof(int64_t) * (size_t)R * R);
         memset(st, 0, sizeof(int64_t) * 8);
         for (int64_t p = 0; p < npairs; p++) {
-            int s = (int)((p / k) / tpr);
+            int s = src[p / k];
             int r = key[p] / n_local, li = key[p] % n_local;
             sc[(int64_t)s * R + r]++;
             if (s == r) st[0]++;
@@ -677,6 +716,7 @@ int oracle_layout(int T, int E, int k, int R, int rpn, int n_slot, int64_t S_tok
         st[7] = 0;
     }
     free(count);
+    free(src);
     return ORC_OK;
 }
 
@@ -771,15 +811,17 @@ int oracle_combine(int L, int T, int k, int H, const uint16_t *y, const int32_t 
  * from source s to rank r; stats {rows, pairs, rows to another rank, pairs to
  * another rank}.
  * ------------------------------------------------------------------------- */
-int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *dst_inst,
-                 int32_t *seg, int32_t *row_token, uint64_t *row_slots, uint64_t *tok_dst,
-                 int64_t *send, int64_t *stats) {
-    if (T < 0 || k < 1 || k > 64 || R < 1 || n_local < 1 || n_layers < 0 || T % R) return ORC_EINVAL;
+int oracle_dedup(int T, int k, int R, int n_local, const int64_t *rank_offsets, int n_layers,
+                 const int32_t *dst_inst, int32_t *seg, int32_t *row_token, uint64_t *row_slots,
+                 uint64_t *tok_dst, int64_t *send, int64_t *stats) {
+    if (T < 0 || k < 1 || k > 64 || R < 1 || n_local < 1 || n_layers < 0) return ORC_EINVAL;
     const int64_t npairs = (int64_t)T * k;
-    const int RW = (R + 63) / 64, tpr = T / R;
+    const int RW = (R + 63) / 64;
+    int32_t *src = sources_or_null(T, R, rank_offsets);
+    if (!src) return ORC_EINVAL;
     int64_t *fill = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R + 1));
     uint64_t *mask = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)R);
-    if (!fill || !mask) { free(fill); free(mask); return ORC_EINVAL; }
+    if (!fill || !mask) { free(fill); free(mask); free(src); return ORC_EINVAL; }
     for (int l = 0; l < n_layers; l++) {
         const int32_t *d = dst_inst + (int64_t)l * npairs;
         int32_t *sg = seg + (int64_t)l * (R + 1);
@@ -789,7 +831,7 @@ int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *
         int64_t *sc = send + (int64_t)l * R * R;
         int64_t *st = stats + (int64_t)l * 4;
         for (int64_t p = 0; p < npairs; p++)
-            if (d[p] < 0 || d[p] >= R * n_local) { free(fill); free(mask); return ORC_EINVAL; }
+            if (d[p] < 0 || d[p] >= R * n_local) { free(fill); free(mask); free(src); return ORC_EINVAL; }
         /* rows per destination rank */
         for (int r = 0; r <= R; r++) fill[r] = 0;
         for (int t = 0; t < T; t++)
@@ -813,7 +855,7 @@ int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *
         memset(td, 0, sizeof(uint64_t) * (size_t)T * RW);
         /* rows in token order within each rank */
         for (int t = 0; t < T; t++) {
-            const int s = t / tpr;
+            const int s = src[t];
             for (int r = 0; r < R; r++) mask[r] = 0;
             for (int j = 0; j < k; j++) mask[d[(int64_t)t * k + j] / n_local] |= (uint64_t)1 << j;
             for (int r = 0; r < R; r++) {
@@ -833,6 +875,7 @@ int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *
     }
     free(fill);
     free(mask);
+    free(src);
     return ORC_OK;
 }
 
@@ -853,17 +896,19 @@ int oracle_dedup(int T, int k, int R, int n_local, int n_layers, const int32_t *
 /* ------------------------------------------------------------------------ */
 
 int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const int64_t *tr,
-                   const int32_t *main_rank, int32_t *target, int64_t *stats) {
-    if (L < 0 || T < 0 || E < 1 || k < 1 || R < 1 || T % R != 0 || (!main_rank && E % R != 0))
-        return ORC_EINVAL;
-    int tpr = T / R, rc = ORC_OK;
+                   const int32_t *main_rank, const int64_t *rank_offsets, int32_t *target,
+                   int64_t *stats) {
+    if (L < 0 || T < 0 || E < 1 || k < 1 || R < 1 || (!main_rank && E % R != 0)) return ORC_EINVAL;
+    int rc = ORC_OK;
+    int32_t *src = sources_or_null(T, R, rank_offsets);
+    if (!src) return ORC_EINVAL;
     int32_t *rank_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
     int64_t *M = (int64_t *)malloc(sizeof(int64_t) * (size_t)E * R);
     int64_t *score = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
-    if (!rank_of || !M || !score) { free(rank_of); free(M); free(score); return ORC_EINVAL; }
+    if (!rank_of || !M || !score) { free(rank_of); free(M); free(score); free(src); return ORC_EINVAL; }
     for (int e = 0; e < E; e++) {
         rank_of[e] = main_rank ? main_rank[e] : e / (E / R);
-        if (rank_of[e] < 0 || rank_of[e] >= R) { free(rank_of); free(M); free(score); return ORC_EINVAL; }
+        if (rank_of[e] < 0 || rank_of[e] >= R) { free(rank_of); free(M); free(score); free(src); return ORC_EINVAL; }
     }
     for (int l = 0; l + 1 < L; l++) {
         const int64_t *t_l = tr + (int64_t)l * E * E;
@@ -874,7 +919,7 @@ int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const 
             for (int b = 0; b < E; b++) M[(int64_t)a * R + rank_of[b]] += t_l[(int64_t)a * E + b];
         memset(st, 0, sizeof(int64_t) * 4);
         for (int t = 0; t < T; t++) {
-            int s = t / tpr;
+            int s = src[t];
             for (int r = 0; r < R; r++) score[r] = 0;
             for (int j = 0; j < k; j++) {
                 int a = cur[(int64_t)t * k + j];
@@ -900,7 +945,7 @@ int oracle_shuffle(int L, int T, int E, int k, int R, const int32_t *ids, const 
             }
         }
     }
-    free(rank_of); free(M); free(score);
+    free(rank_of); free(M); free(score); free(src);
     return rc;
 }
 

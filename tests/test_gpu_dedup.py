@@ -170,3 +170,23 @@ def test_dedup_full_size_stress_workload():
     got, err = run_dedup(w.plan_cfg, w.n_layers, P.buf.dst_inst, dev)
     assert err == 0
     assert_same(got, oracle.dedup(w.plan_cfg, P.buf.dst_inst.cpu().numpy()))
+
+
+@gpu
+@pytest.mark.parametrize("lens", [[700, 0, 1300, 257, 0, 900, 1840, 3], [5000] + [0] * 7,
+                                  [1, 2, 3, 4, 5, 6, 7, 4972]], ids=["ragged", "one_source", "tiny_heads"])
+def test_dedup_with_unequal_source_blocks(lens):
+    # destinations from the oracle chain over unequal blocks (TopoEP §2.1);
+    # rows, send counts and remote counts are per source block
+    dev = _dev()
+    T, E, k, R = 5000, 64, 6, 8
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    cfg = dict(_cfg(T, E, k, R, 4, 3), rank_offsets=off)
+    ids = W.random_small(61, T, E, k, 2, s=1.3)
+    h = oracle.hist(ids, R, E, rank_offsets=off)
+    d = oracle.reroute(cfg, ids, oracle.plan(cfg, h))
+    want = oracle.dedup(cfg, d)
+    gcfg = dict(cfg, rank_offsets=torch.as_tensor(off, device=dev))
+    got, err = run_dedup(gcfg, 2, torch.as_tensor(d, device=dev), dev)
+    assert err == 0
+    assert_same(got, want)

@@ -69,7 +69,7 @@ def run_gate(cfg, L, logits, bias, dev, with_scores=True):
 
 def _check(cfg, L, logits, bias, dev, with_scores=True):
     P, ids, sc = run_gate(cfg, L, logits, bias, dev, with_scores)
-    want = oracle.gate(logits, cfg["k"], cfg["R"], bias=bias)
+    want = oracle.gate(logits, cfg["k"], cfg["R"], bias=bias, rank_offsets=cfg.get("rank_offsets"))
     assert np.array_equal(ids.cpu().numpy(), want["ids"])
     if with_scores:
         assert np.array_equal(sc.cpu().numpy().view(np.uint32), want["scores"].view(np.uint32))
@@ -221,3 +221,28 @@ def test_gate_of_an_empty_batch_and_no_layers():
     assert not P.buf.hist.cpu().numpy().any()
     c = topo.make_cfg(**cfg)
     topo.topo_gate_hist(c, 0, None, topo.TOPO_DTYPE_F32, None, None, None, P.buf.hist, P.ws, P.ws_bytes)
+
+
+@gpu
+def test_gate_with_unequal_source_blocks():
+    # Omega and the tile index over unequal blocks (one empty), then the
+    # whole chain from the gated ids against the oracle
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    T, E, k, R = 3000, 256, 8, 8
+    off = np.array([0, 100, 100, 1700, 1701, 2200, 2900, 2999, 3000], np.int64)
+    cfg = dict(_cfg(T, E, k, R, 4, 8), rank_offsets=off)
+    rng = np.random.default_rng(12)
+    x = _gumbel(rng, (2, T, E))
+    bias = rng.standard_normal(E).astype(np.float32)
+    P, ids = _check(cfg, 2, x, bias, dev)
+    P.make_plan()
+    P.reroute_layout(ids)
+    assert P.error() == 0
+    g = oracle.gate(x, k, R, bias=bias, rank_offsets=off)
+    pl = oracle.plan(cfg, g["hist"])
+    d = oracle.reroute(cfg, g["ids"], pl)
+    sp, so, sc, st = oracle.layout(cfg, d)
+    got = P.numpy()
+    for key, v in dict(dst_inst=d, sorted_pairs=sp, seg_off=so, send_counts=sc, layout_stats=st).items():
+        assert np.array_equal(got[key], v), key

@@ -28,7 +28,9 @@ def gpu_chain(cfg, ids, fused=True):
     dev = _dev()
     L = ids.shape[0]
     mr = cfg.get("main_rank")
-    gcfg = dict(cfg, main_rank=None if mr is None else torch.as_tensor(mr, dtype=torch.int32, device=dev))
+    ro = cfg.get("rank_offsets")
+    gcfg = dict(cfg, main_rank=None if mr is None else torch.as_tensor(mr, dtype=torch.int32, device=dev),
+                rank_offsets=None if ro is None else torch.as_tensor(ro, dtype=torch.int64, device=dev))
     P = Planner(gcfg, L, dev)
     d_ids = torch.as_tensor(ids, device=dev).contiguous()
     P.run(d_ids, fused=fused)
@@ -39,7 +41,7 @@ def gpu_chain(cfg, ids, fused=True):
 
 def oracle_chain(cfg, ids):
     L = ids.shape[0]
-    h = oracle.hist(ids, cfg["R"], cfg["E"])
+    h = oracle.hist(ids, cfg["R"], cfg["E"], rank_offsets=cfg.get("rank_offsets"))
     p = oracle.plan(cfg, h)
     d = oracle.reroute(cfg, ids, p)
     sp, so, sc, st = oracle.layout(cfg, d)
@@ -115,6 +117,60 @@ EDGE = {
     "repeated_ids_in_a_token": (_cfg(8 * 700, 16, 4, 8, 4, 2, S=256, Wb=5_000),
                                 lambda c: _with_repeats(W.random_small(16, c["T"], c["E"], c["k"], 1, s=1.2))),
 }
+
+
+def _offsets(T, lens):
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    assert off[-1] == T
+    return off
+
+
+def _ragged(T, R, seed):
+    """Unequal source blocks: random cut points (some sources may be empty)."""
+    rng = np.random.default_rng(seed)
+    return np.concatenate([[0], np.sort(rng.integers(0, T + 1, R - 1)), [T]]).astype(np.int64)
+
+
+# Unequal source blocks (TopoEP §2.1: each rank routes its own local tokens).
+OFFSETS = {
+    # ragged cut points over several tiles per source, two layers
+    "ragged_blocks": (_cfg(8 * 3001, 16, 3, 8, 4, 2, S=64, Wb=10_000),
+                      lambda c: W.random_small(41, c["T"], c["E"], c["k"], 2, s=1.3),
+                      lambda c: _ragged(c["T"], c["R"], 1)),
+    # an empty source in the middle and one at the end
+    "empty_sources": (_cfg(7000, 32, 4, 8, 2, 4, S=256, Wb=5_000),
+                      lambda c: W.random_small(42, c["T"], c["E"], c["k"], 1, s=1.2),
+                      lambda c: _offsets(c["T"], [900, 1100, 0, 1500, 1200, 1300, 1000, 0])),
+    # one source holding most tokens (many tiles), the others a few each
+    "one_heavy_source": (_cfg(40_000, 64, 6, 16, 8, 6, S=512, Wb=40_000),
+                         lambda c: W.random_small(43, c["T"], c["E"], c["k"], 1, s=1.4),
+                         lambda c: _offsets(c["T"], [3] * 7 + [40_000 - 3 * 15] + [3] * 8)),
+    # k = 10 over E = 512, R = 128 (the stress kernel path), ragged blocks
+    "ragged_k10_r128": (_cfg(128 * 1200 + 77, 512, 10, 128, 8, 16, S=14336, Wb=66_060_288),
+                        lambda c: W.random_small(44, c["T"], c["E"], c["k"], 2, s=1.4),
+                        lambda c: _ragged(c["T"], c["R"], 2)),
+    # repeated ids inside a token with unequal blocks (the exact path)
+    "ragged_repeats": (_cfg(8 * 700 + 5, 16, 4, 8, 4, 2, S=256, Wb=5_000),
+                       lambda c: _with_repeats(W.random_small(45, c["T"], c["E"], c["k"], 1, s=1.2)),
+                       lambda c: _ragged(c["T"], c["R"], 3)),
+    "no_tokens": (_cfg(0, 8, 2, 4, 2, 1), lambda c: np.zeros((1, 0, 2), np.int32),
+                  lambda c: np.zeros(5, np.int64)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(OFFSETS))
+def test_unequal_source_blocks(name):
+    cfg, mk, mo = OFFSETS[name]
+    cfg = dict(cfg, rank_offsets=mo(cfg))
+    check(cfg, mk(cfg))
+
+
+def test_bad_offsets_set_the_error_word():
+    cfg = _cfg(800, 16, 2, 4, 2, 1, S=64, Wb=1000)
+    ids = W.random_small(46, 800, 16, 2, 1)
+    for bad in ([0, 300, 200, 500, 800], [0, 200, 400, 600, 799], [5, 200, 400, 600, 800]):
+        gpu, err = gpu_chain(dict(cfg, rank_offsets=np.array(bad, np.int64)), ids)
+        assert err == -7, (bad, err)
 
 
 def _with_repeats(ids):

@@ -20,10 +20,10 @@ def test_shuffle_arguments_are_checked_on_the_host():
     bad = [(2, 64, 16, 2, 257), (2, 66, 16, 2, 4), (2, 64, 18, 2, 4), (2, 64, 16, 0, 4), (2, 64, 16, 65, 4)]
     for (L, T, E, k, R) in bad:
         with pytest.raises(topo.TopoError) as ex:
-            topo.topo_shuffle_targets(L, T, E, k, R, a, a, None, a, a, a, 1 << 20)
+            topo.topo_shuffle_targets(L, T, E, k, R, a, a, None, None, a, a, a, 1 << 20)
         assert ex.value.code == topo.TOPO_EINVAL
     with pytest.raises(topo.TopoError) as ex:
-        topo.topo_shuffle_targets(2, 64, 16, 2, 4, a, a, None, a, a, a, need - 1)
+        topo.topo_shuffle_targets(2, 64, 16, 2, 4, a, a, None, None, a, a, a, need - 1)
     assert ex.value.code == topo.TOPO_ENOSPC
 
 
@@ -37,7 +37,7 @@ def _dev():
     return torch.device("cuda:0")
 
 
-def run_shuffle(ids, tr, R, main_rank, dev):
+def run_shuffle(ids, tr, R, main_rank, dev, rank_offsets=None):
     L, T, k = ids.shape
     E = tr.shape[-1]
     nb = topo.topo_shuffle_workspace_bytes(L, E, R)
@@ -45,9 +45,10 @@ def run_shuffle(ids, tr, R, main_rank, dev):
     d_ids = torch.as_tensor(ids, device=dev)
     d_tr = tr if isinstance(tr, torch.Tensor) else torch.as_tensor(tr, device=dev)
     mr = None if main_rank is None else torch.as_tensor(main_rank, device=dev)
+    roff = None if rank_offsets is None else torch.as_tensor(np.asarray(rank_offsets, np.int64), device=dev)
     target = torch.full((L - 1, T), -7, dtype=torch.int32, device=dev)
     stats = torch.full((L - 1, topo.TOPO_SHUFFLE_STATS), -7, dtype=torch.int64, device=dev)
-    topo.topo_shuffle_targets(L, T, E, k, R, d_ids, d_tr, mr, target, stats, ws, nb)
+    topo.topo_shuffle_targets(L, T, E, k, R, d_ids, d_tr, mr, roff, target, stats, ws, nb)
     torch.cuda.synchronize()
     return target.cpu().numpy(), stats.cpu().numpy(), topo.topo_read_error(ws)
 
@@ -124,7 +125,7 @@ def test_shuffle_with_one_layer_or_no_tokens_is_a_no_op():
     dev = _dev()
     nb = topo.topo_shuffle_workspace_bytes(1, 16, 4)
     ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device=dev)
-    topo.topo_shuffle_targets(1, 64, 16, 2, 4, None, None, None, None, None, ws, ws.numel())
+    topo.topo_shuffle_targets(1, 64, 16, 2, 4, None, None, None, None, None, None, ws, ws.numel())
     ids = np.zeros((3, 0, 2), np.int32)
     tr = np.zeros((2, 16, 16), np.int64)
     t, st, err = run_shuffle(ids, tr, 4, None, dev)
@@ -161,3 +162,24 @@ def test_shuffle_full_size_cooccurrence_workload():
     assert err == 0
     et, est = oracle.shuffle(ids, C.tr.cpu().numpy(), 16)
     assert np.array_equal(t, et) and np.array_equal(st, est)
+
+
+@gpu
+def test_shuffle_with_unequal_source_blocks():
+    # the tie rule and the statistics use each token's own source block
+    dev = _dev()
+    rng = np.random.default_rng(21)
+    L, T, E, k = 3, 3000, 64, 4
+    for R, lens in ((8, [10, 0, 1990, 300, 200, 0, 499, 1]), (64, None)):
+        if lens is None:
+            cuts = np.sort(rng.integers(0, T + 1, R - 1))
+            off = np.concatenate([[0], cuts, [T]]).astype(np.int64)
+        else:
+            off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        ids = _ids(rng, L, T, E, k)
+        tr = rng.integers(0, 3, size=(L - 1, E, E)).astype(np.int64)     # many ties
+        tg, st, err = run_shuffle(ids, tr, R, None, dev, rank_offsets=off)
+        assert err == 0
+        want_t, want_s = oracle.shuffle(ids, tr, R, rank_offsets=off)
+        assert np.array_equal(tg, want_t)
+        assert np.array_equal(st, want_s)

@@ -84,6 +84,29 @@ def test_hist_noalloc_matches_topo_hist_twice_in_a_row():
 
 
 @pytest.mark.gpu
+def test_hist_noalloc_with_unequal_source_blocks():
+    # the table of each source's first tile lives in the fixed array too
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    dev = torch.device("cuda:0")
+    T, E, k, R = 9000, 32, 4, 8
+    off = np.array([0, 3000, 3000, 3001, 6000, 6100, 8000, 8999, 9000], np.int64)
+    d_off = torch.as_tensor(off, device=dev)
+    cfg = topo.make_cfg(T=T, E=E, k=k, R=R, ranks_per_node=4, n_slot=1, tok_bytes=64,
+                        expert_bytes=1 << 10, rank_offsets=d_off)
+    ids = W.random_small(seed=12, T=T, E=E, k=k, n_layers=2)
+    d_ids = torch.as_tensor(ids, device=dev)
+    hist = torch.empty((2, R, E), dtype=torch.int32, device=dev)
+    err = torch.full((1,), -99, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        topo.topo_hist_noalloc(cfg, 2, d_ids, hist, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        np.testing.assert_array_equal(hist.cpu().numpy(), oracle.hist(ids, R, E, rank_offsets=off))
+
+
+@pytest.mark.gpu
 def test_hist_noalloc_reports_out_of_range_ids():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
