@@ -43,12 +43,12 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 1, "dedup": 4, "gate": 2, "shuffle": 2, "place": 1}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 8, "cooccur": 2, "dedup": 4, "gate": 2, "shuffle": 2, "place": 1}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged
 CALL_SOURCE = {"hist": ("k_hist.cu",), "plan": ("k_plan.cu",),
-               "reroute_layout": ("k_prep.cu", "k_route.cu"), "cooccur": ("k_cooccur.cu",)}
+               "reroute_layout": ("k_prep.cu", "k_route.cu"), "cooccur": ("k_cooccur_mma.cu",)}
 CALL_KERNEL = {"hist": "k_hist_tiles", "reroute_layout": "k_route_tiles", "cooccur": "k_cooccur"}
 
 
@@ -381,35 +381,65 @@ def secondary_plan_latency(dev, stream):
             "target_us": 50, "timing": "200 calls in one CUDA graph"}
 
 
+def bf16_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s, burst) and its kind."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def secondary_cooccur(dev, stream, hbm_peak):
+    """topo_cooccur on the L = 8, T = 262144, E = 128, k = 8 workload, L2
+    flushed before each call, median of 10 after 3 warm-up replays: the
+    tensor-core path (count tiles in e4m3, tcgen05.mma into float32 tensor
+    memory) against its dense-contraction FLOPs and the fp8 peak (the
+    measured bf16 peak x 2, the nominal fp8 : bf16 ratio), and the same call
+    on the shared-atomic kernels beside it."""
     import torch
     from moe_expert_routing_ids_gb300 import workloads as W
     from moe_expert_routing_ids_gb300.planner import Cooccur
     w = W.COOCCUR
-    C = Cooccur(w.n_layers, w.T, w.E, w.k, dev)
     ids = torch.as_tensor(w.ids(), device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    gev = GraphEvents(2)
-    with torch.cuda.stream(stream):
-        C.run(ids, stream)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        flush.fill_(1)                          # evict the ids from L2 (64 MiB < L2)
-        gev.record(0, stream)
-        C.run(ids, stream)
-        gev.record(1, stream)
-    times = []
-    for _ in range(13):
-        graph.replay()
+    out = {}
+    for tc in (True, False):
+        C = Cooccur(w.n_layers, w.T, w.E, w.k, dev, tensor_cores=tc)
+        gev = GraphEvents(2)
+        with torch.cuda.stream(stream):
+            C.run(ids, stream)
         torch.cuda.synchronize()
-        times.append(gev.elapsed(0, 1))
-    gev.close()
-    ms = statistics.median(times[3:])
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            flush.fill_(1)                          # evict the ids from L2 (64 MiB < L2)
+            gev.record(0, stream)
+            C.run(ids, stream)
+            gev.record(1, stream)
+        times = []
+        for _ in range(13):
+            graph.replay()
+            torch.cuda.synchronize()
+            times.append(gev.elapsed(0, 1))
+        gev.close()
+        if C.error() != 0:
+            raise RuntimeError("device error in the co-occurrence measurement")
+        out[tc] = statistics.median(times[3:])
+        del graph, C
+    ms = out[True]
     nbytes = w.n_layers * w.T * w.k * 4 + (2 * w.n_layers - 1) * w.E * w.E * 8
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": w.name, "ms": round(ms, 4), "algorithmic_bytes": nbytes,
-            "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+    # dense contraction the tensor cores run: M = 128 experts, N = 256 (co and
+    # tr together) for layers with a successor, 128 for the last, K = T
+    flops = sum(2 * 128 * (256 if l + 1 < w.n_layers else 128) * w.T for l in range(w.n_layers))
+    bf16, kind = bf16_peak()
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "ms": round(ms, 4), "path": "tensor cores (tcgen05, e4m3 counts, fp32 accumulate)",
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+            "tensor_roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": 2 * bf16,
+                                "unit": "TFLOP/s", "frac": round(tflops / (2 * bf16), 4),
+                                "peak_kind": f"{kind} bf16 x 2 (fp8)", "flops": flops},
+            "atomics_ms": round(out[False], 4),
             "l2": "flushed (256 MB write) before each call",
             "traffic": profiled_traffic("cooccur", w.n_layers * w.T * w.k)}
 

@@ -58,6 +58,7 @@ extern "C" {
 #define TOPO_ESTATE (-5)   /* device: ws does not hold the index this call needs */
 #define TOPO_EMAP (-6)     /* device: main_rank is not a balanced map onto [0, R) */
 #define TOPO_EOFFSETS (-7) /* device: rank_offsets is not 0 = o[0] <= o[1] <= ... <= o[R] = T */
+#define TOPO_ETIMEOUT (-8) /* device: a bounded wait inside a kernel expired */
 
 /* Workspace needs per call (argument `which_call` of topo_workspace_bytes). */
 #define TOPO_CALL_HIST 0
@@ -238,6 +239,18 @@ int topo_place_experts(int32_t L, int32_t E, int32_t R, int32_t max_iters, const
  * Device errors: TOPO_ERANGE. */
 int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids, int64_t *co,
                  int64_t *tr, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace that lets topo_cooccur run on the tensor cores: the counts are
+ * the contractions co_l = C_l^T C_l and tr_l = C_l^T C_{l+1} of the T x E
+ * count matrices, computed by tcgen05.mma on count tiles (exact: counts are
+ * small integers and every per-tile sum stays below 2^24 in the float32
+ * accumulator) when E <= 128 and k <= 16.  It holds the header and int32
+ * partial matrices of about 152 token chunks; with a smaller workspace
+ * (TOPO_CALL_COOCCUR bytes) topo_cooccur counts with integer shared-memory
+ * atomics instead, with the same results.  Device errors of the tensor-core
+ * path: TOPO_ERANGE (the id is dropped), TOPO_ETIMEOUT (a bounded wait for
+ * the tensor core expired; outputs unspecified). */
+size_t topo_cooccur_workspace_bytes(int32_t L, int32_t T, int32_t E, int32_t k);
 
 /* Two-stage topology-aware replication plan [TopoEP §4.3, Eqs. 9-10], one per
  * layer of hist (device int32 [n_layers][R][E]), following these rules:

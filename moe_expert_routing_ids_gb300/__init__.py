@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtopoep.so")
 
 TOPO_OK, TOPO_EINVAL, TOPO_ENOSPC, TOPO_ECUDA = 0, -1, -2, -3
-TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP, TOPO_EOFFSETS = -4, -5, -6, -7
+TOPO_ERANGE, TOPO_ESTATE, TOPO_EMAP, TOPO_EOFFSETS, TOPO_ETIMEOUT = -4, -5, -6, -7, -8
 TOPO_CALL_HIST, TOPO_CALL_PLAN, TOPO_CALL_REROUTE, TOPO_CALL_LAYOUT = 0, 1, 2, 3
 TOPO_CALL_COOCCUR, TOPO_CALL_CHAIN, TOPO_CALL_REROUTE_LAYOUT = 4, 5, 6
 TOPO_CALL_PACK = 7
@@ -40,7 +40,7 @@ EXPORTS = ("topo_workspace_bytes", "topo_ws_reset", "topo_hist", "topo_cooccur",
            "topo_reroute", "topo_dispatch_layout", "topo_reroute_layout", "topo_read_error",
            "topo_strerror", "topo_hist_noalloc", "topo_permute", "topo_combine",
            "topo_dedup_layout", "topo_gate_hist", "topo_shuffle_workspace_bytes",
-           "topo_shuffle_targets", "topo_place_experts")
+           "topo_shuffle_targets", "topo_place_experts", "topo_cooccur_workspace_bytes")
 TOPO_HIST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -95,6 +95,8 @@ def lib():
             L.topo_permute.argtypes = [cfgp, i32, i32, vp, vp, vp, vp, sz, vp]
             L.topo_dedup_layout.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.topo_gate_hist.argtypes = [cfgp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+            L.topo_cooccur_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.topo_cooccur_workspace_bytes.restype = sz
             L.topo_shuffle_workspace_bytes.argtypes = [i32, i32, i32]
             L.topo_shuffle_workspace_bytes.restype = sz
             L.topo_shuffle_targets.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -218,6 +220,11 @@ def topo_place_experts(L: int, E: int, R: int, max_iters: int, co, main_rank, st
 
 def topo_shuffle_workspace_bytes(L: int, E: int, R: int) -> int:
     return int(lib().topo_shuffle_workspace_bytes(L, E, R))
+
+
+def topo_cooccur_workspace_bytes(L: int, T: int, E: int, k: int) -> int:
+    """Workspace bytes that let topo_cooccur use the tensor cores."""
+    return int(lib().topo_cooccur_workspace_bytes(L, T, E, k))
 
 
 def topo_shuffle_targets(L: int, T: int, E: int, k: int, R: int, ids, tr, main_rank, rank_offsets, target,

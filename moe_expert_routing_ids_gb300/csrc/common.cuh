@@ -307,6 +307,16 @@ size_t row_index_smem(const Geo &g);
 size_t rank_smem_bytes(const Geo &g);
 cudaError_t launch_cooccur(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
                            void *ws, cudaStream_t st);
+// Tensor-core co-occurrence (k_cooccur_mma.cu): E <= 128 and k <= 16, units
+// of at most kMaxCoocTokens tokens (a cell's sum stays below 2^24), about
+// kCoocUnitsTarget units per call; int32 partials per unit in the workspace.
+constexpr int kMaxCoocTokens = 65536;
+constexpr int kCoocUnitsTarget = 152;
+bool cooccur_mma_applies(int L, int T, int E, int k);
+void cooccur_mma_units(int L, int T, int *nchunks, int *chunk);
+size_t cooccur_mma_ws_bytes(int L, int T, int E, int k);
+cudaError_t launch_cooccur_mma(int L, int T, int E, int k, const int32_t *ids, int64_t *co, int64_t *tr,
+                               void *ws, cudaStream_t st);
 size_t dedup_ws_bytes(const Geo &g, size_t *off_tile, size_t *off_src, size_t *off_first);
 cudaError_t launch_dedup(const Geo &g, const int32_t *dst, int32_t *seg, int32_t *row_token,
                          uint64_t *row_slots, uint64_t *tok_dst, int64_t *send, int64_t *stats, void *ws,

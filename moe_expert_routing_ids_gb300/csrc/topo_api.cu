@@ -323,6 +323,11 @@ int topo_reroute_layout(const topo_cfg *cfg, int32_t n_layers, const int32_t *id
                                          stream));
 }
 
+size_t topo_cooccur_workspace_bytes(int32_t L, int32_t T, int32_t E, int32_t k) {
+    if (L < 0 || T < 0 || E < 1 || k < 1) return 0;
+    return cooccur_mma_ws_bytes(L, T, E, k);
+}
+
 int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids, int64_t *co,
                  int64_t *tr, void *ws, size_t ws_bytes, cudaStream_t stream) {
     if (L < 0 || T < 0 || E < 1 || k < 1 || !ws) return TOPO_EINVAL;
@@ -331,6 +336,8 @@ int topo_cooccur(int32_t L, int32_t T, int32_t E, int32_t k, const int32_t *ids,
     if (L > 0 && T > 0 && !ids) return TOPO_EINVAL;
     if (ws_bytes < sizeof(WsHeader)) return TOPO_ENOSPC;
     if (L == 0) return TOPO_OK;
+    if (cooccur_mma_applies(L, T, E, k) && ws_bytes >= cooccur_mma_ws_bytes(L, T, E, k))
+        return cuda_rc(launch_cooccur_mma(L, T, E, k, ids, co, L > 1 ? tr : nullptr, ws, stream));
     return cuda_rc(launch_cooccur(L, T, E, k, ids, co, L > 1 ? tr : nullptr, ws, stream));
 }
 
@@ -386,6 +393,7 @@ const char *topo_strerror(int code) {
         case TOPO_ESTATE: return "workspace does not hold the index this call needs";
         case TOPO_EMAP: return "main_rank is not a balanced map onto the ranks";
         case TOPO_EOFFSETS: return "rank_offsets is not an ordered partition of the tokens";
+        case TOPO_ETIMEOUT: return "a bounded wait inside a kernel expired";
         default: return "unknown error";
     }
 }

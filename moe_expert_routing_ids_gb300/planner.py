@@ -10,7 +10,8 @@ import dataclasses
 import torch
 
 from . import (TOPO_CALL_CHAIN, TOPO_CALL_COOCCUR, TOPO_DTYPE_BF16, TOPO_DTYPE_F32, TOPO_LAYOUT_STATS,
-               TOPO_STATS, make_cfg, make_plan, topo_cooccur, topo_dispatch_layout, topo_gate_hist,
+               TOPO_STATS, make_cfg, make_plan, topo_cooccur, topo_cooccur_workspace_bytes,
+               topo_dispatch_layout, topo_gate_hist,
                topo_hist, topo_plan, topo_read_error, topo_reroute, topo_reroute_layout,
                topo_workspace_bytes, topo_ws_reset)
 
@@ -146,13 +147,16 @@ class Planner:
 
 
 class Cooccur:
-    """Buffers for topo_cooccur on [L, T, k] ids."""
+    """Buffers for topo_cooccur on [L, T, k] ids.  tensor_cores: give the call
+    the workspace of its tensor-core path (used when E <= 128 and k <= 16);
+    False keeps the header-only workspace and the shared-atomic kernels."""
 
-    def __init__(self, L: int, T: int, E: int, k: int, device="cuda", transitions=True):
+    def __init__(self, L: int, T: int, E: int, k: int, device="cuda", transitions=True, tensor_cores=True):
         self.L, self.T, self.E, self.k = L, T, E, k
         dev = torch.device(device)
         self.device = dev
-        self.ws_bytes = topo_workspace_bytes(None, 0, TOPO_CALL_COOCCUR)
+        self.ws_bytes = (topo_cooccur_workspace_bytes(L, T, E, k) if tensor_cores
+                         else topo_workspace_bytes(None, 0, TOPO_CALL_COOCCUR))
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.co = torch.empty((L, E, E), dtype=torch.int64, device=dev)
         self.tr = torch.empty((max(L - 1, 0), E, E), dtype=torch.int64, device=dev) if transitions else None

@@ -216,11 +216,13 @@ def test_repeat_runs_are_byte_identical():
 
 # ---------------------------------------------------------------- co-occurrence
 
-def gpu_cooccur(ids, E, transitions=True):
+def gpu_cooccur(ids, E, transitions=True, tensor_cores=True):
+    """tensor_cores: the workspace of the tcgen05 path (used for E <= 128,
+    k <= 16); False: the shared-atomic kernels."""
     from moe_expert_routing_ids_gb300.planner import Cooccur
     dev = _dev()
     L, T, k = ids.shape
-    C = Cooccur(L, T, E, k, dev, transitions)
+    C = Cooccur(L, T, E, k, dev, transitions, tensor_cores=tensor_cores)
     C.run(torch.as_tensor(ids, device=dev).contiguous())
     err = C.error()
     co = C.co.cpu().numpy()
@@ -228,21 +230,27 @@ def gpu_cooccur(ids, E, transitions=True):
     return co, tr, err
 
 
-def test_cooccur_full_size():
+PATHS = pytest.mark.parametrize("tc", [True, False], ids=["tensor_cores", "atomics"])
+
+
+@PATHS
+def test_cooccur_full_size(tc):
     w = W.COOCCUR
     ids = w.ids()
-    co, tr, err = gpu_cooccur(ids, w.E)
+    co, tr, err = gpu_cooccur(ids, w.E, tensor_cores=tc)
     assert err == 0
     oco, otr = oracle.cooccur(ids, w.E)
     assert np.array_equal(co, oco)
     assert np.array_equal(tr, otr)
 
 
+@PATHS
 @pytest.mark.parametrize("L,T,E,k", [(3, 5000, 16, 4), (1, 3000, 32, 8), (2, 1, 8, 2),
-                                     (2, 777, 40, 20), (2, 900, 300, 6), (4, 2048, 128, 16)])
-def test_cooccur_shapes(L, T, E, k):
+                                     (2, 777, 40, 20), (2, 900, 300, 6), (4, 2048, 128, 16),
+                                     (3, 70_000, 128, 10), (2, 4096, 127, 3), (5, 257, 64, 1)])
+def test_cooccur_shapes(L, T, E, k, tc):
     ids = W.random_small(T + E + k, T, E, k, L, s=1.1)
-    co, tr, err = gpu_cooccur(ids, E)
+    co, tr, err = gpu_cooccur(ids, E, tensor_cores=tc)
     assert err == 0
     oco, otr = oracle.cooccur(ids, E)
     assert np.array_equal(co, oco)
@@ -250,11 +258,25 @@ def test_cooccur_shapes(L, T, E, k):
         assert np.array_equal(tr, otr)
 
 
-def test_cooccur_repeated_ids():
+@PATHS
+def test_cooccur_repeated_ids(tc):
     ids = np.array([[[1, 1, 2], [0, 0, 0]], [[0, 2, 2], [1, 2, 1]]], np.int32)
-    co, tr, err = gpu_cooccur(ids, 3)
+    co, tr, err = gpu_cooccur(ids, 3, tensor_cores=tc)
     oco, otr = oracle.cooccur(ids, 3)
     assert err == 0 and np.array_equal(co, oco) and np.array_equal(tr, otr)
+
+
+def test_cooccur_tensor_core_sums_are_exact():
+    # counts up to 16 per token (k = 16 over E = 8), products up to 256, and
+    # each unit's float32 accumulator summing ~1800 tokens: cells far above
+    # 2^14 with arbitrary low bits must come out exact
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, 8, size=(2, 131072, 16)).astype(np.int32)
+    ids[:, ::3, :] = rng.integers(0, 2, size=(2, ids[:, ::3, :].shape[1], 16))
+    co, tr, err = gpu_cooccur(ids, 8, tensor_cores=True)
+    oco, otr = oracle.cooccur(ids, 8)
+    assert err == 0 and oco.max() > (1 << 20)
+    assert np.array_equal(co, oco) and np.array_equal(tr, otr)
 
 
 @pytest.mark.parametrize("L,T,E,k", [(2, 3001, 159, 10), (2, 1500, 160, 8), (3, 2000, 64, 6),
@@ -268,22 +290,24 @@ def test_cooccur_shapes_around_the_shared_memory_limit(L, T, E, k):
     assert np.array_equal(co, oco) and np.array_equal(tr, otr)
 
 
-def test_cooccur_repeated_ids_exact_k():
+@PATHS
+def test_cooccur_repeated_ids_exact_k(tc):
     rng = np.random.default_rng(3)
     ids = rng.integers(0, 5, size=(3, 700, 4)).astype(np.int32)   # many repeats per token
-    co, tr, err = gpu_cooccur(ids, 5)
+    co, tr, err = gpu_cooccur(ids, 5, tensor_cores=tc)
     oco, otr = oracle.cooccur(ids, 5)
     assert err == 0 and np.array_equal(co, oco) and np.array_equal(tr, otr)
 
 
+@PATHS
 @pytest.mark.parametrize("k", [8, 3])
-def test_cooccur_out_of_range_id_is_dropped_and_flagged(k):
+def test_cooccur_out_of_range_id_is_dropped_and_flagged(k, tc):
     from moe_expert_routing_ids_gb300 import TOPO_ERANGE
     E = 32
     ids = W.random_small(9, 600, E, k, 2)
     ids[0, 17, 1] = E + 5
     ids[1, 40, k - 1] = -1
-    co, tr, err = gpu_cooccur(ids, E)
+    co, tr, err = gpu_cooccur(ids, E, tensor_cores=tc)
     assert err == TOPO_ERANGE
     # the same counts as with the bad ids moved to a spare expert E and dropped
     spare = ids.copy()
@@ -292,9 +316,10 @@ def test_cooccur_out_of_range_id_is_dropped_and_flagged(k):
     assert np.array_equal(co, oco[:, :E, :E]) and np.array_equal(tr, otr[:, :E, :E])
 
 
-def test_cooccur_without_transitions():
+@PATHS
+def test_cooccur_without_transitions(tc):
     ids = W.random_small(5, 1000, 16, 4, 3)
-    co, tr, err = gpu_cooccur(ids, 16, transitions=False)
+    co, tr, err = gpu_cooccur(ids, 16, transitions=False, tensor_cores=tc)
     assert err == 0 and tr is None
     assert np.array_equal(co, oracle.cooccur(ids, 16, transitions=False))
 
