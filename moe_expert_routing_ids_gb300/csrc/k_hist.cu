@@ -126,43 +126,63 @@ k_tile_first(const int64_t *__restrict__ off, int32_t *first, WsHeader *hdr, int
     pdl_trigger();
 }
 
-// One thread per (layer, source, expert): exclusive prefix of the source's
-// tile counts in place, and the source's total into Omega.  The column is
-// read in chunks of kPrefixChunk tiles, every load of a chunk issued before
+// One thread per (layer, source, group of V experts): exclusive prefix of
+// the source's tile counts in place, and the source's totals into Omega.  V =
+// 4 (16-byte loads and stores) when E is a multiple of 4, else 1.  The column
+// is read in chunks of kPrefixChunk tiles, every load of a chunk issued before
 // any of its stores, so no load waits behind a store.
 constexpr int kPrefixChunk = 16;
 
+template <int V>
+struct IntV;
+template <>
+struct IntV<1> {
+    using T = int;
+    __device__ static void add(int &a, int b) { a += b; }
+};
+template <>
+struct IntV<4> {
+    using T = int4;
+    __device__ static void add(int4 &a, int4 b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; }
+};
+
+template <int V>
 __global__ void __launch_bounds__(256)
 k_hist_prefix(int32_t *tile_cnt, int32_t *__restrict__ hist, WsHeader *hdr, Geo g, uint64_t fp,
               int64_t n_cols) {
-    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    using Vt = typename IntV<V>::T;
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // column group
     pdl_wait();
     if (c == 0) {
         hdr->hist_fp = fp;
         hdr->route_fp = 0;                      // any routing index is now stale
     }
     if (c >= n_cols) return;
-    const int E = g.E;
-    const unsigned row = (unsigned)(c / E);       // l * R + s
-    const int e = (int)(c - (int64_t)row * E);
+    const int EV = g.E / V;
+    const unsigned row = (unsigned)(c / EV);      // l * R + s
+    const int ev = (int)(c - (int64_t)row * EV);
     const int l = (int)(row / (unsigned)g.R), s = (int)(row - (unsigned)l * g.R);
     int tb, te;
     source_tiles(g, g.tfirst, g.tps, s, &tb, &te);
-    int32_t *col = tile_cnt + ((int64_t)l * g.ntl + tb) * E + e;
+    Vt *col = reinterpret_cast<Vt *>(tile_cnt + ((int64_t)l * g.ntl + tb) * g.E) + ev;
     const int nt = te - tb;
-    int run = 0;
+    Vt run;
+    memset(&run, 0, sizeof run);
     for (int u0 = 0; u0 < nt; u0 += kPrefixChunk) {
         const int m = min(kPrefixChunk, nt - u0);
-        int v[kPrefixChunk];
-#pragma unroll
-        for (int q = 0; q < kPrefixChunk; ++q) v[q] = q < m ? col[(int64_t)(u0 + q) * E] : 0;
+        Vt v[kPrefixChunk];
 #pragma unroll
         for (int q = 0; q < kPrefixChunk; ++q) {
-            if (q < m) col[(int64_t)(u0 + q) * E] = run;
-            run += v[q];
+            if (q < m) v[q] = col[(int64_t)(u0 + q) * EV];
+            else memset(&v[q], 0, sizeof(Vt));
+        }
+#pragma unroll
+        for (int q = 0; q < kPrefixChunk; ++q) {
+            if (q < m) col[(int64_t)(u0 + q) * EV] = run;
+            IntV<V>::add(run, v[q]);
         }
     }
-    hist[c] = run;
+    reinterpret_cast<Vt *>(hist)[c] = run;
     pdl_trigger();
 }
 
@@ -192,7 +212,12 @@ cudaError_t launch_hist(const Geo &g, const int32_t *ids, int32_t *hist, void *w
 cudaError_t launch_hist_prefix(const Geo &g, int32_t *hist, void *ws, uint64_t fp, cudaStream_t st) {
     const int64_t cols = (int64_t)g.L * g.R * g.E;
     if (cols == 0) return cudaSuccess;
-    return launch_pdl(k_hist_prefix, dim3((unsigned)((cols + 255) / 256)), dim3(256), 0, st,
+    // 16-byte groups need E % 4 == 0 and a 16-byte aligned Omega (the tile
+    // index region is 256-byte aligned)
+    if (g.E % 4 == 0 && ((uintptr_t)hist & 15) == 0)
+        return launch_pdl(k_hist_prefix<4>, dim3((unsigned)((cols / 4 + 255) / 256)), dim3(256), 0, st,
+                          ws_at<int32_t>(ws, g.off_tile), hist, ws_at<WsHeader>(ws, 0), g, fp, cols / 4);
+    return launch_pdl(k_hist_prefix<1>, dim3((unsigned)((cols + 255) / 256)), dim3(256), 0, st,
                       ws_at<int32_t>(ws, g.off_tile), hist, ws_at<WsHeader>(ws, 0), g, fp, cols);
 }
 
