@@ -628,7 +628,31 @@ def secondary_place(dev, stream):
             times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     stn = st.cpu().numpy()
+    # the swap phase: uniform random co-selection counts (no planted groups),
+    # where the greedy map leaves gainful swaps; stats checked against the oracle
+    import oracle
+    co_r = W.random_cooccur(31, L, E)
+    d_co = torch.as_tensor(co_r, device=dev)
+    mr2 = torch.empty_like(mr)
+    st2 = torch.empty_like(st)
+    t_sw = []
+    for i in range(7):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            topo.topo_place_experts(L, E, R, 0, d_co, mr2, st2, s)
+            b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            t_sw.append(a.elapsed_time(b))
+    st_r = st2.cpu().numpy()
+    mr_o, st_o = oracle.place(co_r, R)
+    swaps = {"workload": f"uniform random counts, {L} layers, E = {E}, EP{R}",
+             "ms": round(statistics.median(t_sw), 4), "swaps": int(st_r[:, 3].sum()),
+             "within_weight_greedy": int(st_r[:, 1].sum()), "within_weight_final": int(st_r[:, 2].sum()),
+             "equals_oracle": bool(np.array_equal(st_r, st_o) and np.array_equal(mr2.cpu().numpy(), mr_o))}
     res = {"workload": f"{w.name} as EP{R}", "ms": round(ms, 4), "layers_in_parallel": L,
+           "swap_phase": swaps,
            "within_weight_contiguous": int(stn[:, 0].sum()), "within_weight_greedy": int(stn[:, 1].sum()),
            "within_weight_final": int(stn[:, 2].sum()), "swaps": int(stn[:, 3].sum()),
            "timing": "CUDA events around one call for all layers, median of 5 after 2 warm-up calls",

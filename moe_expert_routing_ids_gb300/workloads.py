@@ -282,3 +282,10 @@ def _solver_point(seed: int, E: int, R: int) -> Workload:
 SOLVER_RANKS = tuple(_solver_point(600 + i, 640, R) for i, R in enumerate((8, 16, 32, 64, 128)))
 SOLVER_EXPERTS = tuple(_solver_point(700 + i, E, 32)
                        for i, E in enumerate((64, 128, 256, 512, 640, 1024)))
+
+
+def random_cooccur(seed: int, L: int, E: int, hi: int = 1000) -> np.ndarray:
+    """Co-selection counts int64 [L, E, E] with independent uniform entries in
+    [0, hi): a graph without planted groups, on which the greedy placement
+    leaves gainful swaps."""
+    return np.stack([rng_for(seed, l).integers(0, hi, size=(E, E)) for l in range(L)]).astype(np.int64)
