@@ -157,7 +157,7 @@ __device__ __forceinline__ void load_token(const int32_t *src, int k, bool valid
 }
 
 // True when the token's k ids are pairwise different (the Top-k case).  For
-// eight ids below 256 the comparisons run four bytes at a time: packed words
+// eight ids below 128 the comparisons run four bytes at a time: packed words
 // A (ids 0-3) and B (ids 4-7) against their byte rotations cover every pair.
 template <int KT>
 __device__ __forceinline__ bool distinct_ids(const int (&v)[KT > 0 ? KT : kMaxKIds], int k) {
@@ -166,13 +166,15 @@ __device__ __forceinline__ bool distinct_ids(const int (&v)[KT > 0 ? KT : kMaxKI
         unsigned hi = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) hi |= (unsigned)v[j];
-        if (hi < 256u) {
+        if (hi < 128u) {
+            // x ^ y has a zero byte exactly where two packed ids are equal; a
+            // zero byte of z shows in (z - 0x01..) & ~z & 0x80.. (ids < 128)
             const unsigned A = (unsigned)v[0] | ((unsigned)v[1] << 8) | ((unsigned)v[2] << 16) | ((unsigned)v[3] << 24);
             const unsigned B = (unsigned)v[4] | ((unsigned)v[5] << 8) | ((unsigned)v[6] << 16) | ((unsigned)v[7] << 24);
-            const unsigned eq = __vcmpeq4(A, __funnelshift_l(A, A, 8)) | __vcmpeq4(A, __funnelshift_l(A, A, 16)) |
-                                __vcmpeq4(B, __funnelshift_l(B, B, 8)) | __vcmpeq4(B, __funnelshift_l(B, B, 16)) |
-                                __vcmpeq4(A, B) | __vcmpeq4(A, __funnelshift_l(B, B, 8)) |
-                                __vcmpeq4(A, __funnelshift_l(B, B, 16)) | __vcmpeq4(A, __funnelshift_l(B, B, 24));
+            auto zb = [](unsigned z) { return (z - 0x01010101u) & ~z & 0x80808080u; };
+            const unsigned r1 = __funnelshift_l(B, B, 8), r2 = __funnelshift_l(B, B, 16), r3 = __funnelshift_l(B, B, 24);
+            const unsigned eq = zb(A ^ __funnelshift_l(A, A, 8)) | zb(A ^ __funnelshift_l(A, A, 16)) |
+                                zb(B ^ r1) | zb(B ^ r2) | zb(A ^ B) | zb(A ^ r1) | zb(A ^ r2) | zb(A ^ r3);
             return eq == 0u;
         }
     }
