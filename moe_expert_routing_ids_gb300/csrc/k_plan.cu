@@ -5,7 +5,7 @@
 //                   b = 2 D S_tok - ||W|| (Eq. 9) and the inter-node placement
 //   k_plan_route    one CTA per (source, layer): the even split of omega_{s,e}
 //                   over the chosen instances; U and L by integer atomics
-//   k_plan_refine   one warp per (domain, layer): intra-node refinement (Eq. 10)
+//   k_plan_refine   one CTA per (domain, layer): intra-node refinement (Eq. 10)
 //
 // Inter-node placement in closed form: every rank of a domain starts with no
 // used slot, so placing candidates one by one on the rank with the fewest used
@@ -303,8 +303,9 @@ __device__ __forceinline__ bool key_gt(const Key &x, const Key &y) {
     return x.c > y.c;
 }
 
-// Lanes holding the warp's largest key: five 32-bit redux steps, each
-// keeping only the lanes that tie on every word so far.
+// Lanes holding the warp's largest key: up to five 32-bit redux steps, each
+// keeping only the lanes that tie on every word so far, ending once one lane
+// is left.
 __device__ __forceinline__ unsigned warp_argmax_lanes(const Key &k) {
     unsigned live = 0xffffffffu;
     const unsigned words[5] = {(unsigned)(k.a >> 32), (unsigned)k.a, (unsigned)(k.b >> 32),
@@ -314,260 +315,400 @@ __device__ __forceinline__ unsigned warp_argmax_lanes(const Key &k) {
         const bool in = (live >> (threadIdx.x & 31)) & 1u;
         const unsigned m = __reduce_max_sync(0xffffffffu, in ? words[i] : 0u);
         live = __ballot_sync(0xffffffffu, in && words[i] == m);
+        if ((live & (live - 1)) == 0) break;    // one lane left (uniform)
     }
     return live;
 }
 
 constexpr int kRefineMaxWarps = 8;
+constexpr int kRefineCpl = 4;        // candidates a thread evaluates in one batch
+constexpr int kScanPerLane = 8;      // sources a lane takes per block of the commit scan
 
-// One CTA per (domain, layer) refines the domain (TopoEP §4.3, Eq. 10).
-// Candidates (instance at the busiest rank x other rank of the domain) are
-// spread over the CTA's warps; each warp reduces with redux/ballot steps, the
-// warps' winners meet in shared memory (skipped with one warp, which then
-// runs barrier-free), and warp 0 commits.  The domain's columns of q (every
-// source, the domain's ranks) live in shared memory when they fit
-// (colcache), else in global memory -- updated there by atomic adds that do
-// not wait, and re-read past L1 -- with the domain's own sources mirrored in
-// shared memory for the candidate costs.
-__global__ void __launch_bounds__(kRefineMaxWarps * 32)
-k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
-              int32_t *rank_load, int64_t *stats, Geo g, int colcache) {
-    extern __shared__ int sm[];
-    pdl_wait();
-    pdl_trigger();
+// Row stride of the refinement CTA's q table: the sources it holds, made odd.
+__host__ __device__ __forceinline__ int refine_row_stride(const Geo &g, bool all_src) {
+    return (all_src ? g.R : g.rpn) | 1;
+}
+
+// Offset (in ints, 16-byte aligned) of the q table in the refinement CTA's
+// shared memory, after the per-rank and per-instance arrays and hl.
+__host__ __device__ __forceinline__ int refine_q_offset(const Geo &g) {
+    const int head = 2 * g.rpn + 4 * g.rpn * g.n_local + (g.rpn * g.E + 1) / 2;
+    return (head + 3) & ~3;
+}
+
+
+// Shared-memory state of one refinement CTA.  The domain's cells of q are held
+// transposed -- row (j, li) of the domain's instance over sources -- with an
+// odd row stride, so that reading one row across a warp, or writing one
+// source's cells down the rows, meets distinct banks.
+struct RefState {
+    int *Lr;        // [rpn] rank loads
+    int *used;      // [rpn] used slots
+    int *U;         // [rpn][nl] instance loads
+    int *xe;        // [rpn][nl] expert of each instance, -1: none
+    int *xc;        // [rpn][nl] main rank of that expert, or -1 - main rank when it is in another domain
+    int *dirty;     // [rpn][nl] row changed: written back to q at the end
+    short *hl;      // [rpn][E] local index of expert e on rank j, or -1
+    int *qc;        // [rpn][nl][RS] q of sources src0 .. src0 + RS - 1 (all, or the domain's own)
+    int RS, src0, r0;
+    int32_t *Q;     // this layer's q [R][R][nl]
+    int32_t *SE;    // this layer's slot experts [R][n_slot]
+};
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;\n" ::: "memory");
+}
+
+// The domain's cells of q for sources [s_begin, s_end) into the transposed
+// table: 4-byte asynchronous copies, all issued here; cp_async_wait_all()
+// completes them.
+__device__ void load_q(const RefState &x, const Geo &g, int s_begin, int s_end) {
+    const int nl = g.n_local, n = g.rpn * nl, nthr = blockDim.x;
+    const int64_t total = (int64_t)(s_end - s_begin) * n;
+    int s = (int)threadIdx.x / n, i = (int)threadIdx.x % n;
+    const int ds = nthr / n, di = nthr % n;
+    for (int64_t f = threadIdx.x; f < total; f += nthr) {
+        cp_async4(&x.qc[(size_t)i * x.RS + s], x.Q + ((int64_t)(s_begin + s) * g.R + x.r0) * nl + i);
+        s += ds;
+        i += di;
+        if (i >= n) { i -= n; ++s; }
+    }
+}
+
+// The refinement loop (TopoEP §4.3, Eq. 10) over the state in shared memory.
+// kAll: qc holds every source; else only the domain's own sources, the others
+// read from and updated in global memory (atomic adds that do not wait, reads
+// past L1).
+template <bool kAll>
+__device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int *iters_out, int64_t *tokd_out,
+                                            int64_t *repd_out) {
     __shared__ Key kbuf[kRefineMaxWarps];
     __shared__ int cbuf[kRefineMaxWarps];
     __shared__ int lbuf[kRefineMaxWarps];
-    const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nthr = blockDim.x, nwarp = nthr >> 5;
     const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
-    const int32_t *main_of = tab, *mains = tab + 2 * E;
-    int *Lr = sm;                               // [rpn]
-    int *used = Lr + rpn;                       // [rpn]
-    int *U = used + rpn;                        // [rpn][nl]
-    int *xe = U + rpn * nl;                     // [rpn][nl] expert of each instance
-    int *xc = xe + rpn * nl;                    // [rpn][nl] main rank of that expert, or
-                                                //   -1 - main rank when it is in another domain
-    // colcache: qc[s][j][l] for every source s; else qc[js][j][l] for the
-    // domain's own sources only
-    int *qc = xc + rpn * nl;
-    const int nsrc = colcache ? R : rpn;
-    short *hl = reinterpret_cast<short *>(qc + nsrc * rpn * nl);   // [rpn][E] local index or -1
-    const int r0 = d * rpn;
-    const int src0 = colcache ? 0 : r0;         // source index of qc's first row
-    int32_t *Q = q + (int64_t)l * R * R * nl;
-    int32_t *SE = slot_expert + (int64_t)l * R * ns;
-
-    for (int j = tid; j < rpn; j += nthr) {
-        Lr[j] = rank_load[(int64_t)l * R + r0 + j];
-        int u = 0;
-        while (u < ns && SE[(int64_t)(r0 + j) * ns + u] >= 0) ++u;
-        used[j] = u;
-    }
-    for (int i = tid; i < rpn * E; i += nthr) hl[i] = -1;
-    __syncthreads();
-    for (int i = tid; i < rpn * nl; i += nthr) {
-        const int j = i / nl, li = i % nl, r = r0 + j;
-        U[i] = inst_load[((int64_t)l * R + r) * nl + li];
-        const int e = li < ER ? mains[r * ER + li] : SE[(int64_t)r * ns + (li - ER)];
-        xe[i] = e;
-        if (e >= 0) {
-            hl[j * E + e] = (short)li;
-            const int m = main_of[e];
-            xc[i] = (m / rpn == d) ? m : -1 - m;
-        } else {
-            xc[i] = 0;
-        }
-    }
-    for (int i = tid; i < nsrc * rpn * nl; i += nthr) {
-        const int sr = i / (rpn * nl), rest = i % (rpn * nl);
-        qc[i] = Q[(int64_t)(src0 + sr) * R * nl + (int64_t)r0 * nl + rest];
-    }
-    __syncthreads();
-
-    auto qcell = [&](int s, int j, int li) -> int * { return &qc[((s - src0) * rpn + j) * nl + li]; };
-    // per-byte cost of a replica on rank r0 + jt of the expert whose main class is xcv
-    auto repl_cost = [&](int xcv, int jt) -> int64_t {
-        if (xcv < 0) return g.c_inter;
-        return xcv == r0 + jt ? 0 : g.c_intra;
-    };
-
-    int iters = 0;
-    int64_t tokd = 0, repd = 0;
+    int *Lr = x.Lr, *used = x.used, *U = x.U, *xe = x.xe, *xc = x.xc, *qc = x.qc;
+    short *hl = x.hl;
+    const int RS = x.RS, r0 = x.r0, src0 = x.src0;
+    int32_t *Q = x.Q;
+    const int64_t tok_cost = 2 * g.S_tok * g.c_intra;     // per token moved off or onto its own rank
+    const int64_t w_intra = (int64_t)g.c_intra * g.W, w_inter = (int64_t)g.c_inter * g.W;
     const int ncand = nl * rpn;
     // this thread's first candidate (lb, jt) and the stride in (lb, jt) form
     const int c_lb0 = tid / rpn, c_jt0 = tid % rpn;
     const int s_lb = nthr / rpn, s_jt = nthr % rpn;
+    int iters = 0;
+    int64_t tokd = 0, repd = 0;
     constexpr int kHardCap = 1 << 24;   // commits provably end; guards a corrupted state only
     while ((g.max_iters == 0 || iters < g.max_iters) && iters < kHardCap) {
         // busiest rank, lowest index on ties (every warp computes it)
         const int myL = lane < rpn ? Lr[lane] : -1;
         const int Lb = __reduce_max_sync(0xffffffffu, myL);
         const int jb = __ffs(__ballot_sync(0xffffffffu, myL == Lb)) - 1;
+        const int col_b = r0 + jb - src0;
         Key best{0ull, 0ull, 0u};
         int bc = 0;                              // packed (lb << 5 | jt) of best
         int blt = -1;                            // its local index on jt, -1: a new replica
         int lb = c_lb0, jt = c_jt0;
-        for (int c = tid; c < ncand; c += nthr) {
-            if (jt != jb) {
-                const int Ub = U[jb * nl + lb];
-                const int e = xe[jb * nl + lb];
-                const int xcv = xc[jb * nl + lb];
-                const int Lt = Lr[jt];
-                const int usedt = used[jt];
-                const int q_rt = *qcell(r0 + jt, jb, lb);
-                const int q_rb = *qcell(r0 + jb, jb, lb);
-                if (Ub > 0 && e >= 0) {
-                    const int lt = hl[jt * E + e];
-                    const bool is_new = lt < 0;
-                    const int half = (Lb - Lt) >> 1;
-                    const int delta = Ub < half ? Ub : half;
-                    if (delta >= 1 && (!is_new || usedt < ns)) {
-                        const int m_rt = q_rt < delta ? q_rt : delta;
-                        const int rest = delta - m_rt;
-                        const int others = Ub - q_rt - q_rb;
-                        const int m_o = others < rest ? others : rest;
-                        const int m_rb = rest - m_o;
-                        const int64_t cst = 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt) +
-                                            (is_new ? repl_cost(xcv, jt) * g.W : 0);
-                        Key k;
-                        k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)Lt);
-                        k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
-                        k.c = ~(((unsigned)e << 5) | (unsigned)jt);
-                        if (key_gt(k, best)) {
-                            best = k;
-                            bc = (lb << 5) | jt;
-                            blt = lt;
-                        }
+        for (int c0 = tid; c0 < ncand; c0 += kRefineCpl * nthr) {
+            // every load of the batch issued before any is used
+            int cl[kRefineCpl], cj[kRefineCpl], ub[kRefineCpl], ev[kRefineCpl], xv[kRefineCpl];
+            int lt[kRefineCpl], ldt[kRefineCpl], ut[kRefineCpl], qt[kRefineCpl], qb[kRefineCpl];
+#pragma unroll
+            for (int i = 0; i < kRefineCpl; ++i) {
+                const bool ok = c0 + i * nthr < ncand && jt != jb;
+                const int row = jb * nl + lb;
+                cl[i] = lb;
+                cj[i] = jt;
+                ub[i] = ok ? U[row] : 0;         // 0: no candidate
+                ev[i] = ok ? xe[row] : -1;
+                xv[i] = ok ? xc[row] : 0;
+                qt[i] = ok ? qc[row * RS + (r0 + jt - src0)] : 0;
+                qb[i] = ok ? qc[row * RS + col_b] : 0;
+                ldt[i] = Lr[jt];
+                ut[i] = used[jt];
+                lb += s_lb;
+                jt += s_jt;
+                if (jt >= rpn) { jt -= rpn; ++lb; }
+            }
+#pragma unroll
+            for (int i = 0; i < kRefineCpl; ++i) lt[i] = (ub[i] > 0 && ev[i] >= 0) ? hl[cj[i] * E + ev[i]] : -1;
+#pragma unroll
+            for (int i = 0; i < kRefineCpl; ++i) {
+                const bool is_new = lt[i] < 0;
+                const int half = (Lb - ldt[i]) >> 1;
+                const int delta = ub[i] < half ? ub[i] : half;
+                if (ub[i] > 0 && ev[i] >= 0 && delta >= 1 && (!is_new || ut[i] < ns)) {
+                    const int m_rt = qt[i] < delta ? qt[i] : delta;
+                    const int rest = delta - m_rt;
+                    const int others = ub[i] - qt[i] - qb[i];
+                    const int m_o = others < rest ? others : rest;
+                    const int m_rb = rest - m_o;
+                    const int64_t repl = !is_new ? 0 : xv[i] < 0 ? w_inter : xv[i] == r0 + cj[i] ? 0 : w_intra;
+                    const int64_t cst = tok_cost * (int64_t)(m_rb - m_rt) + repl;
+                    Key k;
+                    k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)ldt[i]);
+                    k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
+                    k.c = ~(((unsigned)ev[i] << 5) | (unsigned)cj[i]);
+                    if (key_gt(k, best)) {
+                        best = k;
+                        bc = (cl[i] << 5) | cj[i];
+                        blt = lt[i];
                     }
                 }
             }
-            lb += s_lb;
-            jt += s_jt;
-            if (jt >= rpn) { jt -= rpn; ++lb; }
         }
         const unsigned win = warp_argmax_lanes(best);
         const int wl = __ffs(win) - 1;
         Key wk;
         wk.a = __shfl_sync(0xffffffffu, best.a, wl);
-        wk.b = __shfl_sync(0xffffffffu, best.b, wl);
         wk.c = __shfl_sync(0xffffffffu, best.c, wl);
         int wc = __shfl_sync(0xffffffffu, bc, wl);
         int wlt = __shfl_sync(0xffffffffu, blt, wl);
         if (nwarp > 1) {
+            // the warps' winners: every thread reads all of them, then a tree
+            wk.b = __shfl_sync(0xffffffffu, best.b, wl);
             if (lane == 0) {
                 kbuf[w] = wk;
                 cbuf[w] = wc;
                 lbuf[w] = wlt;
             }
             __syncthreads();
-            wk = kbuf[0];
-            wc = cbuf[0];
-            wlt = lbuf[0];
-            for (int x = 1; x < nwarp; ++x)
-                if (key_gt(kbuf[x], wk)) {
-                    wk = kbuf[x];
-                    wc = cbuf[x];
-                    wlt = lbuf[x];
+            Key kk[kRefineMaxWarps];
+            int cc[kRefineMaxWarps], ll[kRefineMaxWarps];
+#pragma unroll
+            for (int v = 0; v < kRefineMaxWarps; ++v) {
+                if (v < nwarp) {
+                    kk[v] = kbuf[v];
+                    cc[v] = cbuf[v];
+                    ll[v] = lbuf[v];
+                } else {
+                    kk[v] = Key{0ull, 0ull, 0u};
+                    cc[v] = 0;
+                    ll[v] = -1;
                 }
+            }
+#pragma unroll
+            for (int st = 1; st < kRefineMaxWarps; st <<= 1)
+#pragma unroll
+                for (int v = 0; v + st < kRefineMaxWarps; v += 2 * st)
+                    if (key_gt(kk[v + st], kk[v])) {
+                        kk[v] = kk[v + st];
+                        cc[v] = cc[v + st];
+                        ll[v] = ll[v + st];
+                    }
+            wk = kk[0];
+            wc = cc[0];
+            wlt = ll[0];
         }
         if (wk.a == 0) break;                   // uniform: every thread saw the same keys
         if (w == 0) {
             const int delta = (int)(wk.a >> 32);
             const int blb = wc >> 5, bjt = wc & 31;
             const int e = (int)((~wk.c) >> 5);
-            const int xcv = xc[jb * nl + blb];
+            const int rowb = jb * nl + blb;
+            const int xcv = xc[rowb];
             const int rb = r0 + jb, rt = r0 + bjt;
             const bool is_new = wlt < 0;
             const int lt = is_new ? ER + used[bjt] : wlt;
-            const int m_rt = min(*qcell(rt, jb, blb), delta);
+            const int rowt = bjt * nl + lt;
+            int *qB = qc + rowb * RS, *qT = qc + rowt * RS;      // indexed by source - src0
+            const int m_rt = min(qB[rt - src0], delta);
             int remaining = delta - m_rt;
             __syncwarp();
             if (is_new) {
-                repd += repl_cost(xcv, bjt) * g.W;
+                repd += xcv < 0 ? w_inter : xcv == rt ? 0 : w_intra;
                 if (lane == 0) {
                     used[bjt] += 1;
                     hl[bjt * E + e] = (short)lt;
-                    xe[bjt * nl + lt] = e;
-                    xc[bjt * nl + lt] = xcv;
-                    SE[(int64_t)rt * ns + (lt - ER)] = e;
+                    xe[rowt] = e;
+                    xc[rowt] = xcv;
+                    x.SE[(int64_t)rt * ns + (lt - ER)] = e;
                 }
             }
-            // other sources, ascending, skipping r_t and r_b: a block of 256
-            // sources' q values is requested at once, then scanned 32 at a time
-            for (int base = 0; base < R && remaining > 0; base += 256) {
-                int v[8];
+            // other sources, ascending, skipping r_t and r_b: blocks of up to
+            // 32 * kScanPerLane sources, each lane holding a run of consecutive
+            // ones, so one warp scan of the runs' sums places every take
+            for (int base = 0; base < R && remaining > 0; base += 32 * kScanPerLane) {
+                const int nb = min(32 * kScanPerLane, R - base);
+                const int per = (nb + 31) >> 5;
+                const int s0 = base + lane * per;
+                int v[kScanPerLane];
+                int sum = 0;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int s = base + 32 * u + lane;
-                    const bool in = s < R && s != rt && s != rb;
-                    const bool cached = colcache || (s >= r0 && s < r0 + rpn);
-                    v[u] = in ? (cached ? *qcell(s, jb, blb) : __ldcg(&Q[((int64_t)s * R + rb) * nl + blb]))
-                              : 0;
+                for (int u = 0; u < kScanPerLane; ++u) {
+                    const int s = s0 + u;
+                    const bool in = u < per && s < base + nb && s != rt && s != rb;
+                    const bool cached = kAll || (s >= r0 && s < r0 + rpn);
+                    v[u] = !in ? 0 : cached ? qB[s - src0] : __ldcg(&Q[((int64_t)s * R + rb) * nl + blb]);
+                    sum += v[u];
                 }
+                const int incl = warp_incl_scan(sum);
+                int left = remaining - (incl - sum);     // still to take where this lane's run starts
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (remaining <= 0 || base + 32 * u >= R) break;   // no source left to take from
-                    const int s = base + 32 * u + lane;
-                    const int incl = warp_incl_scan(v[u]);
-                    const int excl = incl - v[u];
-                    int take = remaining - excl;
-                    take = take < 0 ? 0 : (take > v[u] ? v[u] : take);
+                for (int u = 0; u < kScanPerLane; ++u) {
+                    const int take = left <= 0 ? 0 : (left < v[u] ? left : v[u]);
+                    left -= v[u];
                     if (take > 0) {
-                        if (colcache || (s >= r0 && s < r0 + rpn)) {
-                            *qcell(s, jb, blb) -= take;
-                            *qcell(s, bjt, lt) += take;
+                        const int s = s0 + u;
+                        if (kAll || (s >= r0 && s < r0 + rpn)) {
+                            qB[s - src0] -= take;
+                            qT[s - src0] += take;
                         }
-                        if (!colcache) {   // no return value: the lane does not wait
+                        if (!kAll) {   // no return value: the lane does not wait
                             atomicAdd(&Q[((int64_t)s * R + rb) * nl + blb], -take);
                             atomicAdd(&Q[((int64_t)s * R + rt) * nl + lt], take);
                         }
                     }
-                    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-                    remaining -= tot < remaining ? tot : remaining;
                 }
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                remaining -= tot < remaining ? tot : remaining;
             }
             const int m_rb = remaining;
-            __syncwarp();
-            if (lane == 0) {
-                if (m_rt > 0) {
-                    *qcell(rt, jb, blb) -= m_rt;
-                    *qcell(rt, bjt, lt) += m_rt;
-                    if (!colcache) {
-                        atomicAdd(&Q[((int64_t)rt * R + rb) * nl + blb], -m_rt);
-                        atomicAdd(&Q[((int64_t)rt * R + rt) * nl + lt], m_rt);
-                    }
+            // r_t's and r_b's cells, the loads: three lanes, disjoint cells
+            if (lane == 0 && m_rt > 0) {
+                qB[rt - src0] -= m_rt;
+                qT[rt - src0] += m_rt;
+                if (!kAll) {
+                    atomicAdd(&Q[((int64_t)rt * R + rb) * nl + blb], -m_rt);
+                    atomicAdd(&Q[((int64_t)rt * R + rt) * nl + lt], m_rt);
                 }
-                if (m_rb > 0) {
-                    *qcell(rb, jb, blb) -= m_rb;
-                    *qcell(rb, bjt, lt) += m_rb;
-                    if (!colcache) {
-                        atomicAdd(&Q[((int64_t)rb * R + rb) * nl + blb], -m_rb);
-                        atomicAdd(&Q[((int64_t)rb * R + rt) * nl + lt], m_rb);
-                    }
+            }
+            if (lane == 1 && m_rb > 0) {
+                qB[rb - src0] -= m_rb;
+                qT[rb - src0] += m_rb;
+                if (!kAll) {
+                    atomicAdd(&Q[((int64_t)rb * R + rb) * nl + blb], -m_rb);
+                    atomicAdd(&Q[((int64_t)rb * R + rt) * nl + lt], m_rb);
                 }
-                U[jb * nl + blb] -= delta;
-                U[bjt * nl + lt] += delta;
+            }
+            if (lane == 2) {
+                U[rowb] -= delta;
+                U[rowt] += delta;
                 Lr[jb] -= delta;
                 Lr[bjt] += delta;
+                x.dirty[rowb] = 1;
+                x.dirty[rowt] = 1;
             }
-            tokd += 2 * g.S_tok * g.c_intra * (int64_t)(m_rb - m_rt);
+            tokd += tok_cost * (int64_t)(m_rb - m_rt);
             __syncwarp();
         }
         ++iters;
         if (nwarp > 1) __syncthreads();
     }
-    // write back the domain's state and statistics
-    if (nwarp > 1) __syncthreads();
-    if (colcache)
-        for (int i = tid; i < R * rpn * nl; i += nthr) {
-            const int sr = i / (rpn * nl), rest = i % (rpn * nl);
-            Q[(int64_t)sr * R * nl + (int64_t)r0 * nl + rest] = qc[i];
+    *iters_out = iters;
+    *tokd_out = tokd;
+    *repd_out = repd;
+}
+
+// One CTA per (domain, layer) refines the domain (TopoEP §4.3, Eq. 10).
+// Candidates (instance at the busiest rank x other rank of the domain) are
+// spread over the CTA's warps, a few per thread with their loads batched; each
+// warp reduces with redux/ballot steps, the warps' winners meet in shared
+// memory (skipped with one warp, which then runs barrier-free), and warp 0
+// commits.  The domain's rows of q (every source, the domain's instances) live
+// in shared memory when they fit (all_src), else only the domain's own
+// sources do and the rest stays in global memory.
+__global__ void __launch_bounds__(kRefineMaxWarps * 32)
+k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
+              int32_t *rank_load, int64_t *stats, Geo g, int all_src) {
+    extern __shared__ __align__(16) int sm[];
+    const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nthr = blockDim.x;
+    const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
+    const int32_t *main_of = tab, *mains = tab + 2 * E;
+    RefState x;
+    x.Lr = sm;
+    x.used = x.Lr + rpn;
+    x.U = x.used + rpn;
+    x.xe = x.U + rpn * nl;
+    x.xc = x.xe + rpn * nl;
+    x.dirty = x.xc + rpn * nl;
+    x.hl = reinterpret_cast<short *>(x.dirty + rpn * nl);
+    x.qc = sm + refine_q_offset(g);
+    x.r0 = d * rpn;
+    x.src0 = all_src ? 0 : x.r0;
+    x.RS = refine_row_stride(g, all_src);
+    x.Q = q + (int64_t)l * R * R * nl;
+    x.SE = slot_expert + (int64_t)l * R * ns;
+    const int r0 = x.r0;
+
+    // Before the wait, what the main tables and the placement kernel wrote:
+    // this grid starts only once every CTA of the routing kernel has passed
+    // its own wait, so those kernels have completed and their writes are
+    // visible (read past L1).  used[j]: the slots before the first empty one.
+    for (int i = tid; i < rpn * E; i += nthr) x.hl[i] = -1;
+    for (int j = tid; j < rpn; j += nthr) x.used[j] = ns;
+    __syncthreads();
+    for (int i = tid; i < rpn * ns; i += nthr) {
+        const int j = i / ns, u = i - j * ns;
+        if (__ldcg(&x.SE[(int64_t)(r0 + j) * ns + u]) < 0) atomicMin(&x.used[j], u);
+    }
+    for (int i = tid; i < rpn * nl; i += nthr) {
+        const int j = i / nl, li = i - j * nl, r = r0 + j;
+        x.dirty[i] = 0;
+        const int e = li < ER ? __ldcg(&mains[r * ER + li]) : __ldcg(&x.SE[(int64_t)r * ns + (li - ER)]);
+        x.xe[i] = e;
+        if (e >= 0) {
+            x.hl[j * E + e] = (short)li;
+            const int m = __ldcg(&main_of[e]);
+            x.xc[i] = (m / rpn == d) ? m : -1 - m;
+        } else {
+            x.xc[i] = 0;
         }
-    for (int j = tid; j < rpn; j += nthr) rank_load[(int64_t)l * R + r0 + j] = Lr[j];
-    for (int i = tid; i < rpn * nl; i += nthr) inst_load[((int64_t)l * R + r0) * nl + i] = U[i];
+    }
+    // the routing kernel's output: q (asynchronous copies), U and L
+    pdl_wait();
+    pdl_trigger();
+    if (all_src) load_q(x, g, 0, R);
+    else load_q(x, g, r0, r0 + rpn);
+    for (int j = tid; j < rpn; j += nthr) x.Lr[j] = rank_load[(int64_t)l * R + r0 + j];
+    for (int i = tid; i < rpn * nl; i += nthr) x.U[i] = inst_load[((int64_t)l * R + r0) * nl + i];
+    cp_async_wait_all();
+    __syncthreads();
+
+    int iters;
+    int64_t tokd, repd;
+    if (all_src) refine_loop<true>(x, g, &iters, &tokd, &repd);
+    else refine_loop<false>(x, g, &iters, &tokd, &repd);
+
+    // write back the domain's state and statistics; q's changed rows only
+    // (without all_src, q in global memory is already current): warp 0 lists
+    // them (over xe, no longer needed), then a thread per row writes it
+    __shared__ int n_dirty;
+    __syncthreads();
+    if (all_src) {
+        int *list = x.xe;
+        if (w == 0) {
+            int n = 0;
+            for (int base = 0; base < rpn * nl; base += 32) {
+                const int row = base + lane;
+                const bool dv = row < rpn * nl && x.dirty[row];
+                const unsigned b = __ballot_sync(0xffffffffu, dv);
+                if (dv) list[n + __popc(b & ((1u << lane) - 1u))] = row;
+                n += __popc(b);
+            }
+            if (lane == 0) n_dirty = n;
+        }
+        __syncthreads();
+        for (int k = tid; k < n_dirty; k += nthr) {
+            const int row = list[k], j = row / nl, li = row - j * nl;
+            int32_t *dst = x.Q + (int64_t)(r0 + j) * nl + li;
+            const int *src = x.qc + row * x.RS;
+#pragma unroll 4
+            for (int s = 0; s < R; ++s) dst[(int64_t)s * R * nl] = src[s];
+        }
+    }
+    for (int j = tid; j < rpn; j += nthr) rank_load[(int64_t)l * R + r0 + j] = x.Lr[j];
+    for (int i = tid; i < rpn * nl; i += nthr) inst_load[((int64_t)l * R + r0) * nl + i] = x.U[i];
     if (w == 0) {
-        int lmax = lane < rpn ? Lr[lane] : 0, nused = lane < rpn ? used[lane] : 0;
+        int lmax = lane < rpn ? x.Lr[lane] : 0, nused = lane < rpn ? x.used[lane] : 0;
         for (int o = 16; o > 0; o >>= 1) {
             lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
             nused += __shfl_xor_sync(0xffffffffu, nused, o);
@@ -585,21 +726,19 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
 
 }  // namespace
 
-// Shared memory of the refinement kernel; colcache: all sources' columns.
-size_t refine_smem_bytes(const Geo &g, bool colcache) {
-    const size_t nsrc = colcache ? (size_t)g.R : (size_t)g.rpn;
-    return (2 * (size_t)g.rpn + 3 * (size_t)g.rpn * g.n_local + nsrc * g.rpn * g.n_local) * 4 +
-           (size_t)g.rpn * g.E * 2;
+// Shared memory of the refinement kernel; all_src: every source's rows of q.
+size_t refine_smem_bytes(const Geo &g, bool all_src) {
+    return ((size_t)refine_q_offset(g) + (size_t)g.rpn * g.n_local * refine_row_stride(g, all_src)) * 4;
 }
 
-// Warps of the refinement CTA: about two candidates per lane, at most 8.
+// Warps of the refinement CTA: about kRefineCpl candidates per thread, at most 8.
 int refine_warps(const Geo &g) {
     const int ncand = g.n_local * g.rpn;
-    int w = (ncand + 31) / 32;                      // one warp per 32 candidates (measured best)
+    int w = (ncand + 32 * kRefineCpl - 1) / (32 * kRefineCpl);
     return w < 1 ? 1 : (w > kRefineMaxWarps ? kRefineMaxWarps : w);
 }
 
-bool refine_colcache(const Geo &g) { return refine_smem_bytes(g, true) <= 160 * 1024; }
+bool refine_all_sources(const Geo &g) { return refine_smem_bytes(g, true) <= 200 * 1024; }
 
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st) {
@@ -625,11 +764,11 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
     if ((e = launch_pdl(k_plan_route, dim3(g.R, g.L), dim3(256), (size_t)g.R * 4, st, hist, tab, rep,
                         p.route_cnt, p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
         return e;
-    const bool cc = refine_colcache(g);
-    const size_t smem_ref = refine_smem_bytes(g, cc);
+    const bool all_src = refine_all_sources(g);
+    const size_t smem_ref = refine_smem_bytes(g, all_src);
     if ((e = ensure_smem((const void *)k_plan_refine, smem_ref)) != cudaSuccess) return e;
     return launch_pdl(k_plan_refine, dim3(g.M, g.L), dim3(refine_warps(g) * 32), smem_ref, st, tab,
-                      p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, cc ? 1 : 0);
+                      p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, all_src ? 1 : 0);
 }
 
 }  // namespace topo
