@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -323,10 +324,26 @@ __device__ __forceinline__ unsigned warp_argmax_lanes(const Key &k) {
 constexpr int kRefineMaxWarps = 8;
 constexpr int kRefineCpl = 4;        // candidates a thread evaluates in one batch
 constexpr int kScanPerLane = 8;      // sources a lane takes per block of the commit scan
+constexpr int kRefineSmem = kSmemMax - 4096;   // dynamic shared memory beside the kernel's static arrays
 
-// Row stride of the refinement CTA's q table: the sources it holds, made odd.
-__host__ __device__ __forceinline__ int refine_row_stride(const Geo &g, bool all_src) {
-    return (all_src ? g.R : g.rpn) | 1;
+// Where the refinement CTA keeps the domain's cells of q:
+//   kQAll     every source's rows, int32, in shared memory
+//   kQAll16   every source's rows as 16-bit counts (exact while each source's
+//             cells in the domain sum to at most 65535, checked at load: a
+//             move keeps its source and stays in the domain, so no cell can
+//             exceed that sum); a CTA failing the check falls back to kQOwn
+//   kQOwnFetch the domain's own sources' rows in shared memory, the rest in
+//             global memory (atomic adds that do not wait, reads past L1),
+//             the busiest rank's rows fetched into shared memory each iteration
+//   kQOwn     the same, the commit reading the rows from global memory
+enum RefineQ : int { kQOwn = 0, kQAll = 1, kQOwnFetch = 2, kQAll16 = 3 };
+
+// Row stride (elements) of the refinement CTA's q table: the sources it holds,
+// made odd in 32-bit words so that one source's cells down the rows meet
+// distinct banks.
+__host__ __device__ __forceinline__ int refine_row_stride(const Geo &g, int qmode) {
+    if (qmode == kQAll16) return 2 * (((g.R + 1) / 2) | 1);
+    return (qmode == kQAll ? g.R : g.rpn) | 1;
 }
 
 // Offset (in ints, 16-byte aligned) of the q table in the refinement CTA's
@@ -336,11 +353,16 @@ __host__ __device__ __forceinline__ int refine_q_offset(const Geo &g) {
     return (head + 3) & ~3;
 }
 
+// Ints the q table takes (16-byte multiple).
+__host__ __device__ __forceinline__ int refine_q_ints(const Geo &g, int qmode) {
+    const int64_t el = (int64_t)g.rpn * g.n_local * refine_row_stride(g, qmode);
+    const int64_t ints = qmode == kQAll16 ? (el + 1) / 2 : el;
+    return (int)((ints + 3) & ~int64_t(3));
+}
 
 // Shared-memory state of one refinement CTA.  The domain's cells of q are held
-// transposed -- row (j, li) of the domain's instance over sources -- with an
-// odd row stride, so that reading one row across a warp, or writing one
-// source's cells down the rows, meets distinct banks.
+// transposed -- row (j, li) of the domain's instance over sources -- so that
+// the commit reads and updates one row across the warp.
 struct RefState {
     int *Lr;        // [rpn] rank loads
     int *used;      // [rpn] used slots
@@ -349,7 +371,8 @@ struct RefState {
     int *xc;        // [rpn][nl] main rank of that expert, or -1 - main rank when it is in another domain
     int *dirty;     // [rpn][nl] row changed: written back to q at the end
     short *hl;      // [rpn][E] local index of expert e on rank j, or -1
-    int *qc;        // [rpn][nl][RS] q of sources src0 .. src0 + RS - 1 (all, or the domain's own)
+    void *qc;       // [rpn][nl][RS] q of sources src0 .. src0 + RS - 1 (int32, or uint16 in kQAll16)
+    int *pf;        // [nl][R] the busiest rank's rows of q, fetched each iteration (kQOwnFetch)
     int RS, src0, r0;
     int32_t *Q;     // this layer's q [R][R][nl]
     int32_t *SE;    // this layer's slot experts [R][n_slot]
@@ -360,131 +383,260 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;\n" ::: "memory");
 }
 
-// The domain's cells of q for sources [s_begin, s_end) into the transposed
-// table: 4-byte asynchronous copies, all issued here; cp_async_wait_all()
-// completes them.
+// The domain's int32 cells of q for sources [s_begin, s_end) into the
+// transposed table: 4-byte asynchronous copies, all issued here;
+// cp_async_wait_all() completes them.
 __device__ void load_q(const RefState &x, const Geo &g, int s_begin, int s_end) {
     const int nl = g.n_local, n = g.rpn * nl, nthr = blockDim.x;
+    int *qc = static_cast<int *>(x.qc);
     const int64_t total = (int64_t)(s_end - s_begin) * n;
     int s = (int)threadIdx.x / n, i = (int)threadIdx.x % n;
     const int ds = nthr / n, di = nthr % n;
     for (int64_t f = threadIdx.x; f < total; f += nthr) {
-        cp_async4(&x.qc[(size_t)i * x.RS + s], x.Q + ((int64_t)(s_begin + s) * g.R + x.r0) * nl + i);
+        cp_async4(&qc[(size_t)i * x.RS + s], x.Q + ((int64_t)(s_begin + s) * g.R + x.r0) * nl + i);
         s += ds;
         i += di;
         if (i >= n) { i -= n; ++s; }
     }
 }
 
+// Every source's cells of the domain into the 16-bit table (kQAll16).  Only a
+// rank's first E_R + used[j] instances can hold tokens (an instance without an
+// expert routes nothing), and for one (source, rank) they are contiguous in q:
+// those runs, rounded up to whole 16-byte pieces, go by asynchronous copies
+// into an int32 staging area (sources in chunks that fit), then into the
+// table (zeroed by the caller), summing each source's cells.  Returns true (to every thread)
+// when every source's sum fits 16 bits.
+__device__ bool load_q16(const RefState &x, const Geo &g, int *stage, int stage_ints) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int R = g.R, rpn = g.rpn, nl = g.n_local, ER = g.E_R;
+    uint16_t *qc = static_cast<uint16_t *>(x.qc);
+    __shared__ int run0[kMaxRanksPerNode + 1];   // staging offset of rank j's run in a source's piece
+    __shared__ int over;
+    int *ssum = stage;                          // [R] per-source sums, then the staging pieces
+    int *pieces = stage + ((R + 3) & ~3);
+    const int piece_room = stage_ints - ((R + 3) & ~3);
+    const bool vec = (nl & 3) == 0 && ((uintptr_t)x.Q & 15) == 0;
+    if (tid == 0) {
+        int o = 0;
+        for (int j = 0; j < rpn; ++j) {
+            run0[j] = o;
+            o += (ER + x.used[j] + 3) & ~3;
+        }
+        run0[rpn] = o;
+        over = 0;
+    }
+    for (int s = tid; s < R; s += nthr) ssum[s] = 0;
+    __syncthreads();
+    const int SP = run0[rpn];                   // ints per source in the staging area
+    const int chunk = SP > 0 ? piece_room / SP : R;
+    if (chunk < 1) return false;                // no room: the caller falls back
+    for (int c0 = 0; c0 < R; c0 += chunk) {
+        const int cs = min(chunk, R - c0);
+        // a thread per (source, rank) run: its copies, then (after the wait)
+        // its cells into the table and its sum
+        for (int f = tid; f < cs * rpn; f += nthr) {
+            const int sl = f / rpn, j = f - sl * rpn;
+            const int live = ER + x.used[j];
+            const int32_t *src = x.Q + ((int64_t)(c0 + sl) * R + x.r0 + j) * nl;
+            int *dst = pieces + sl * SP + run0[j];
+            if (vec) {
+#pragma unroll 4
+                for (int li = 0; li < live; li += 4) cp_async16(dst + li, src + li);
+            } else {
+#pragma unroll 4
+                for (int li = 0; li < live; ++li) cp_async4(dst + li, src + li);
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        for (int f = tid; f < cs * rpn; f += nthr) {
+            const int sl = f / rpn, j = f - sl * rpn, s = c0 + sl;
+            const int live = ER + x.used[j];
+            const int *p = pieces + sl * SP + run0[j];
+            uint16_t *col = qc + (size_t)j * nl * x.RS + s;
+            int sum = 0;
+#pragma unroll 4
+            for (int li = 0; li < live; ++li) {
+                const int v = p[li];
+                sum += v;
+                col[(size_t)li * x.RS] = (uint16_t)v;
+            }
+            atomicAdd(&ssum[s], sum);
+        }
+        __syncthreads();
+    }
+    for (int s = tid; s < R; s += nthr)
+        if ((unsigned)ssum[s] > 65535u) over = 1;
+    __syncthreads();
+    return over == 0;
+}
+
 // The refinement loop (TopoEP §4.3, Eq. 10) over the state in shared memory.
-// kAll: qc holds every source; else only the domain's own sources, the others
-// read from and updated in global memory (atomic adds that do not wait, reads
-// past L1).
-template <bool kAll>
+//
+// A rank's instances are its E_R mains and then its slots, filled from the
+// first (placement fills slots in order; a new replica takes the first empty
+// one), so only the busiest rank's first E_R + used[jb] instances can be
+// moved: the candidates of an iteration are those rows times the other ranks.
+// They take as many warps as they fill (kRefineCpl per thread); with one warp
+// no winners meet in shared memory.  With kQOwnFetch the warps not evaluating
+// fetch the busiest rank's rows of q meanwhile (pf), so the commit reads them
+// from shared memory.  kOneWarp: a CTA of one warp (no barriers, one stride).
+template <int kMode, bool kOneWarp>
 __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int *iters_out, int64_t *tokd_out,
                                             int64_t *repd_out) {
+    using QT = typename std::conditional<kMode == kQAll16, uint16_t, int>::type;
     __shared__ Key kbuf[kRefineMaxWarps];
     __shared__ int cbuf[kRefineMaxWarps];
     __shared__ int lbuf[kRefineMaxWarps];
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int nthr = blockDim.x, nwarp = nthr >> 5;
+    __shared__ int s_done;
+    __shared__ int2 s_step[kRefineMaxWarps + 1];   // (lb, jt) stride of nact * 32 candidates
+    constexpr bool kAll = kMode == kQAll || kMode == kQAll16;
+    const int tid = threadIdx.x, lane = tid & 31, w = kOneWarp ? 0 : tid >> 5;
+    const int nthr = kOneWarp ? 32 : blockDim.x, nwarp = kOneWarp ? 1 : nthr >> 5;
     const int E = g.E, R = g.R, rpn = g.rpn, ns = g.n_slot, nl = g.n_local, ER = g.E_R;
-    int *Lr = x.Lr, *used = x.used, *U = x.U, *xe = x.xe, *xc = x.xc, *qc = x.qc;
+    int *Lr = x.Lr, *used = x.used, *U = x.U, *xe = x.xe, *xc = x.xc, *pf = x.pf;
+    QT *qc = static_cast<QT *>(x.qc);
     short *hl = x.hl;
     const int RS = x.RS, r0 = x.r0, src0 = x.src0;
     int32_t *Q = x.Q;
     const int64_t tok_cost = 2 * g.S_tok * g.c_intra;     // per token moved off or onto its own rank
     const int64_t w_intra = (int64_t)g.c_intra * g.W, w_inter = (int64_t)g.c_inter * g.W;
-    const int ncand = nl * rpn;
-    // this thread's first candidate (lb, jt) and the stride in (lb, jt) form
+    // this thread's first candidate (lb, jt): candidate c is (c / rpn, c % rpn)
     const int c_lb0 = tid / rpn, c_jt0 = tid % rpn;
-    const int s_lb = nthr / rpn, s_jt = nthr % rpn;
+    const int2 step1 = make_int2(32 / rpn, 32 % rpn);
+    if (!kOneWarp) {
+        if (tid == 0) s_done = 0;
+        if (tid <= kRefineMaxWarps) s_step[tid] = make_int2(tid * 32 / rpn, tid * 32 % rpn);
+        __syncthreads();
+    }
     int iters = 0;
     int64_t tokd = 0, repd = 0;
     constexpr int kHardCap = 1 << 24;   // commits provably end; guards a corrupted state only
     while ((g.max_iters == 0 || iters < g.max_iters) && iters < kHardCap) {
         // busiest rank, lowest index on ties (every warp computes it)
         const int myL = lane < rpn ? Lr[lane] : -1;
+        const int myU = !kOneWarp && lane < rpn ? used[lane] : 0;
         const int Lb = __reduce_max_sync(0xffffffffu, myL);
         const int jb = __ffs(__ballot_sync(0xffffffffu, myL == Lb)) - 1;
         const int col_b = r0 + jb - src0;
-        Key best{0ull, 0ull, 0u};
-        int bc = 0;                              // packed (lb << 5 | jt) of best
-        int blt = -1;                            // its local index on jt, -1: a new replica
-        int lb = c_lb0, jt = c_jt0;
-        for (int c0 = tid; c0 < ncand; c0 += kRefineCpl * nthr) {
-            // every load of the batch issued before any is used
-            int cl[kRefineCpl], cj[kRefineCpl], ub[kRefineCpl], ev[kRefineCpl], xv[kRefineCpl];
-            int lt[kRefineCpl], ldt[kRefineCpl], ut[kRefineCpl], qt[kRefineCpl], qb[kRefineCpl];
+        // (one warp: a single batch covers every row, so no bound is needed)
+        const int live = kOneWarp ? nl : ER + __shfl_sync(0xffffffffu, myU, jb);
+        const int ncand = live * rpn;
+        int nact = kOneWarp ? 1 : (ncand + 32 * kRefineCpl - 1) / (32 * kRefineCpl);
+        nact = nact < 1 ? 1 : (nact > nwarp ? nwarp : nact);
+        const int stride = nact * 32;
+        Key wk{0ull, 0ull, 0u};
+        int wc = 0, wlt = -1;
+        if (w < nact) {
+            Key best{0ull, 0ull, 0u};
+            int bc = 0;                          // packed (lb << 5 | jt) of best
+            int blt = -1;                        // its local index on jt, -1: a new replica
+            const int2 step = kOneWarp ? step1 : s_step[nact];
+            const int s_lb = step.x, s_jt = step.y;
+            int lb = c_lb0, jt = c_jt0;
+            for (int c0 = tid; c0 < ncand; c0 += kRefineCpl * stride) {
+                // every load of the batch issued before any is used
+                int cl[kRefineCpl], cj[kRefineCpl], ub[kRefineCpl], ev[kRefineCpl], xv[kRefineCpl];
+                int lt[kRefineCpl], ldt[kRefineCpl], ut[kRefineCpl], qt[kRefineCpl], qb[kRefineCpl];
 #pragma unroll
-            for (int i = 0; i < kRefineCpl; ++i) {
-                const bool ok = c0 + i * nthr < ncand && jt != jb;
-                const int row = jb * nl + lb;
-                cl[i] = lb;
-                cj[i] = jt;
-                ub[i] = ok ? U[row] : 0;         // 0: no candidate
-                ev[i] = ok ? xe[row] : -1;
-                xv[i] = ok ? xc[row] : 0;
-                qt[i] = ok ? qc[row * RS + (r0 + jt - src0)] : 0;
-                qb[i] = ok ? qc[row * RS + col_b] : 0;
-                ldt[i] = Lr[jt];
-                ut[i] = used[jt];
-                lb += s_lb;
-                jt += s_jt;
-                if (jt >= rpn) { jt -= rpn; ++lb; }
-            }
+                for (int i = 0; i < kRefineCpl; ++i) {
+                    const bool ok = c0 + i * stride < ncand && jt != jb;
+                    const int row = jb * nl + lb;
+                    cl[i] = lb;
+                    cj[i] = jt;
+                    ub[i] = ok ? U[row] : 0;     // 0: no candidate
+                    ev[i] = ok ? xe[row] : -1;
+                    xv[i] = ok ? xc[row] : 0;
+                    qt[i] = ok ? (int)qc[row * RS + (r0 + jt - src0)] : 0;
+                    qb[i] = ok ? (int)qc[row * RS + col_b] : 0;
+                    ldt[i] = Lr[jt];
+                    ut[i] = used[jt];
+                    lb += s_lb;
+                    jt += s_jt;
+                    if (jt >= rpn) { jt -= rpn; ++lb; }
+                }
 #pragma unroll
-            for (int i = 0; i < kRefineCpl; ++i) lt[i] = (ub[i] > 0 && ev[i] >= 0) ? hl[cj[i] * E + ev[i]] : -1;
+                for (int i = 0; i < kRefineCpl; ++i)
+                    lt[i] = (ub[i] > 0 && ev[i] >= 0) ? hl[cj[i] * E + ev[i]] : -1;
 #pragma unroll
-            for (int i = 0; i < kRefineCpl; ++i) {
-                const bool is_new = lt[i] < 0;
-                const int half = (Lb - ldt[i]) >> 1;
-                const int delta = ub[i] < half ? ub[i] : half;
-                if (ub[i] > 0 && ev[i] >= 0 && delta >= 1 && (!is_new || ut[i] < ns)) {
-                    const int m_rt = qt[i] < delta ? qt[i] : delta;
-                    const int rest = delta - m_rt;
-                    const int others = ub[i] - qt[i] - qb[i];
-                    const int m_o = others < rest ? others : rest;
-                    const int m_rb = rest - m_o;
-                    const int64_t repl = !is_new ? 0 : xv[i] < 0 ? w_inter : xv[i] == r0 + cj[i] ? 0 : w_intra;
-                    const int64_t cst = tok_cost * (int64_t)(m_rb - m_rt) + repl;
-                    Key k;
-                    k.a = ((unsigned long long)delta << 32) | (unsigned long long)(0xffffffffu - (unsigned)ldt[i]);
-                    k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
-                    k.c = ~(((unsigned)ev[i] << 5) | (unsigned)cj[i]);
-                    if (key_gt(k, best)) {
-                        best = k;
-                        bc = (cl[i] << 5) | cj[i];
-                        blt = lt[i];
+                for (int i = 0; i < kRefineCpl; ++i) {
+                    const bool is_new = lt[i] < 0;
+                    const int half = (Lb - ldt[i]) >> 1;
+                    const int delta = ub[i] < half ? ub[i] : half;
+                    if (ub[i] > 0 && ev[i] >= 0 && delta >= 1 && (!is_new || ut[i] < ns)) {
+                        const int m_rt = qt[i] < delta ? qt[i] : delta;
+                        const int rest = delta - m_rt;
+                        const int others = ub[i] - qt[i] - qb[i];
+                        const int m_o = others < rest ? others : rest;
+                        const int m_rb = rest - m_o;
+                        const int64_t repl = !is_new ? 0 : xv[i] < 0 ? w_inter : xv[i] == r0 + cj[i] ? 0 : w_intra;
+                        const int64_t cst = tok_cost * (int64_t)(m_rb - m_rt) + repl;
+                        Key k;
+                        k.a = ((unsigned long long)delta << 32) |
+                              (unsigned long long)(0xffffffffu - (unsigned)ldt[i]);
+                        k.b = ~((unsigned long long)cst ^ 0x8000000000000000ull);
+                        k.c = ~(((unsigned)ev[i] << 5) | (unsigned)cj[i]);
+                        if (key_gt(k, best)) {
+                            best = k;
+                            bc = (cl[i] << 5) | cj[i];
+                            blt = lt[i];
+                        }
                     }
                 }
             }
-        }
-        const unsigned win = warp_argmax_lanes(best);
-        const int wl = __ffs(win) - 1;
-        Key wk;
-        wk.a = __shfl_sync(0xffffffffu, best.a, wl);
-        wk.c = __shfl_sync(0xffffffffu, best.c, wl);
-        int wc = __shfl_sync(0xffffffffu, bc, wl);
-        int wlt = __shfl_sync(0xffffffffu, blt, wl);
-        if (nwarp > 1) {
-            // the warps' winners: every thread reads all of them, then a tree
-            wk.b = __shfl_sync(0xffffffffu, best.b, wl);
-            if (lane == 0) {
-                kbuf[w] = wk;
-                cbuf[w] = wc;
-                lbuf[w] = wlt;
+            const unsigned win = warp_argmax_lanes(best);
+            const int wl = __ffs(win) - 1;
+            wk.a = __shfl_sync(0xffffffffu, best.a, wl);
+            wk.c = __shfl_sync(0xffffffffu, best.c, wl);
+            wc = __shfl_sync(0xffffffffu, bc, wl);
+            wlt = __shfl_sync(0xffffffffu, blt, wl);
+            if (nact > 1) {
+                wk.b = __shfl_sync(0xffffffffu, best.b, wl);
+                if (lane == 0) {
+                    kbuf[w] = wk;
+                    cbuf[w] = wc;
+                    lbuf[w] = wlt;
+                }
             }
-            __syncthreads();
+        } else if (kMode == kQOwnFetch) {
+            // rows li < live of r_b over every source, from global memory
+            const int rb = r0 + jb, n = live * R;
+            for (int i0 = tid - stride; i0 < n; i0 += (nthr - stride) * 8) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * (nthr - stride);
+                    const int li = i / R, s = i - li * R;
+                    v[u] = i < n ? __ldcg(&Q[((int64_t)s * R + rb) * nl + li]) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * (nthr - stride);
+                    if (i < n) pf[i] = v[u];
+                }
+            }
+        }
+        const bool fetched = kMode == kQOwnFetch && nact < nwarp;   // else the commit reads q itself
+        // winners and rows in place; and no warp still reads this iteration's
+        // loads when warp 0 commits
+        if (nwarp > 1) __syncthreads();
+        if (w == 0 && nact > 1) {
+            // the warps' winners, tree over the first nact
             Key kk[kRefineMaxWarps];
             int cc[kRefineMaxWarps], ll[kRefineMaxWarps];
 #pragma unroll
             for (int v = 0; v < kRefineMaxWarps; ++v) {
-                if (v < nwarp) {
+                if (v < nact) {
                     kk[v] = kbuf[v];
                     cc[v] = cbuf[v];
                     ll[v] = lbuf[v];
@@ -498,7 +650,7 @@ __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int
             for (int st = 1; st < kRefineMaxWarps; st <<= 1)
 #pragma unroll
                 for (int v = 0; v + st < kRefineMaxWarps; v += 2 * st)
-                    if (key_gt(kk[v + st], kk[v])) {
+                    if (v + st < nact && key_gt(kk[v + st], kk[v])) {
                         kk[v] = kk[v + st];
                         cc[v] = cc[v + st];
                         ll[v] = ll[v + st];
@@ -507,8 +659,7 @@ __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int
             wc = cc[0];
             wlt = ll[0];
         }
-        if (wk.a == 0) break;                   // uniform: every thread saw the same keys
-        if (w == 0) {
+        if (w == 0 && wk.a != 0) {
             const int delta = (int)(wk.a >> 32);
             const int blb = wc >> 5, bjt = wc & 31;
             const int e = (int)((~wk.c) >> 5);
@@ -518,8 +669,9 @@ __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int
             const bool is_new = wlt < 0;
             const int lt = is_new ? ER + used[bjt] : wlt;
             const int rowt = bjt * nl + lt;
-            int *qB = qc + rowb * RS, *qT = qc + rowt * RS;      // indexed by source - src0
-            const int m_rt = min(qB[rt - src0], delta);
+            QT *qB = qc + rowb * RS, *qT = qc + rowt * RS;       // indexed by source - src0
+            const int *pB = pf + blb * R;                        // fetched row, by source
+            const int m_rt = min((int)qB[rt - src0], delta);
             int remaining = delta - m_rt;
             __syncwarp();
             if (is_new) {
@@ -546,7 +698,10 @@ __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int
                     const int s = s0 + u;
                     const bool in = u < per && s < base + nb && s != rt && s != rb;
                     const bool cached = kAll || (s >= r0 && s < r0 + rpn);
-                    v[u] = !in ? 0 : cached ? qB[s - src0] : __ldcg(&Q[((int64_t)s * R + rb) * nl + blb]);
+                    v[u] = !in ? 0
+                           : cached ? (int)qB[s - src0]
+                           : fetched ? pB[s]
+                                     : __ldcg(&Q[((int64_t)s * R + rb) * nl + blb]);
                     sum += v[u];
                 }
                 const int incl = warp_incl_scan(sum);
@@ -599,25 +754,61 @@ __device__ __forceinline__ void refine_loop(const RefState &x, const Geo &g, int
             tokd += tok_cost * (int64_t)(m_rb - m_rt);
             __syncwarp();
         }
+        bool done;
+        if (!kOneWarp) {
+            if (tid == 0 && wk.a == 0) s_done = 1;
+            __syncthreads();
+            done = s_done;
+        } else {
+            done = wk.a == 0;                    // uniform across the warp
+        }
+        if (done) break;
         ++iters;
-        if (nwarp > 1) __syncthreads();
     }
     *iters_out = iters;
     *tokd_out = tokd;
     *repd_out = repd;
 }
 
+// Writes the changed rows of the table back to q: warp 0 lists them (over xe,
+// no longer needed), then a thread per row writes it.
+template <typename QT>
+__device__ void write_rows(const RefState &x, const Geo &g) {
+    __shared__ int n_dirty;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int R = g.R, nl = g.n_local, n = g.rpn * nl;
+    int *list = x.xe;
+    const QT *qc = static_cast<const QT *>(x.qc);
+    if (w == 0) {
+        int cnt = 0;
+        for (int base = 0; base < n; base += 32) {
+            const int row = base + lane;
+            const bool dv = row < n && x.dirty[row];
+            const unsigned b = __ballot_sync(0xffffffffu, dv);
+            if (dv) list[cnt + __popc(b & ((1u << lane) - 1u))] = row;
+            cnt += __popc(b);
+        }
+        if (lane == 0) n_dirty = cnt;
+    }
+    __syncthreads();
+    for (int k = tid; k < n_dirty; k += blockDim.x) {
+        const int row = list[k], j = row / nl, li = row - j * nl;
+        int32_t *dst = x.Q + (int64_t)(x.r0 + j) * nl + li;
+        const QT *src = qc + (size_t)row * x.RS;
+#pragma unroll 4
+        for (int s = 0; s < R; ++s) dst[(int64_t)s * R * nl] = (int32_t)src[s];
+    }
+}
+
 // One CTA per (domain, layer) refines the domain (TopoEP §4.3, Eq. 10).
 // Candidates (instance at the busiest rank x other rank of the domain) are
 // spread over the CTA's warps, a few per thread with their loads batched; each
 // warp reduces with redux/ballot steps, the warps' winners meet in shared
-// memory (skipped with one warp, which then runs barrier-free), and warp 0
-// commits.  The domain's rows of q (every source, the domain's instances) live
-// in shared memory when they fit (all_src), else only the domain's own
-// sources do and the rest stays in global memory.
+// memory, and warp 0 commits.  qmode says where q lives (RefineQ); smem_ints:
+// the dynamic shared memory, whose tail past the table stages kQAll16's load.
 __global__ void __launch_bounds__(kRefineMaxWarps * 32)
 k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q, int32_t *inst_load,
-              int32_t *rank_load, int64_t *stats, Geo g, int all_src) {
+              int32_t *rank_load, int64_t *stats, Geo g, int qmode, int smem_ints) {
     extern __shared__ __align__(16) int sm[];
     const int d = blockIdx.x, l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nthr = blockDim.x;
@@ -633,8 +824,6 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
     x.hl = reinterpret_cast<short *>(x.dirty + rpn * nl);
     x.qc = sm + refine_q_offset(g);
     x.r0 = d * rpn;
-    x.src0 = all_src ? 0 : x.r0;
-    x.RS = refine_row_stride(g, all_src);
     x.Q = q + (int64_t)l * R * R * nl;
     x.SE = slot_expert + (int64_t)l * R * ns;
     const int r0 = x.r0;
@@ -663,48 +852,48 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
             x.xc[i] = 0;
         }
     }
-    // the routing kernel's output: q (asynchronous copies), U and L
+    if (qmode == kQAll16) {                     // the 16-bit table's empty rows stay zero
+        int4 *z = static_cast<int4 *>(x.qc);
+        const int nz = refine_q_ints(g, kQAll16) / 4;
+        for (int i = tid; i < nz; i += nthr) z[i] = make_int4(0, 0, 0, 0);
+    }
+    // the routing kernel's output: q, U and L
     pdl_wait();
     pdl_trigger();
-    if (all_src) load_q(x, g, 0, R);
-    else load_q(x, g, r0, r0 + rpn);
     for (int j = tid; j < rpn; j += nthr) x.Lr[j] = rank_load[(int64_t)l * R + r0 + j];
     for (int i = tid; i < rpn * nl; i += nthr) x.U[i] = inst_load[((int64_t)l * R + r0) * nl + i];
-    cp_async_wait_all();
-    __syncthreads();
+    __syncthreads();                            // used[] complete for load_q16
+    int mode = qmode;
+    if (mode == kQAll16) {
+        x.RS = refine_row_stride(g, kQAll16);
+        x.src0 = 0;
+        const int q_end = refine_q_offset(g) + refine_q_ints(g, kQAll16);
+        if (!load_q16(x, g, sm + q_end, smem_ints - q_end)) mode = kQOwn;   // uniform
+    }
+    if (mode != kQAll16) {
+        const bool all_src = mode == kQAll;
+        x.RS = refine_row_stride(g, mode);
+        x.src0 = all_src ? 0 : r0;
+        x.pf = static_cast<int *>(x.qc) + rpn * nl * x.RS;
+        if (all_src) load_q(x, g, 0, R);
+        else load_q(x, g, r0, r0 + rpn);
+        cp_async_wait_all();
+        __syncthreads();
+    }
 
     int iters;
     int64_t tokd, repd;
-    if (all_src) refine_loop<true>(x, g, &iters, &tokd, &repd);
-    else refine_loop<false>(x, g, &iters, &tokd, &repd);
+    if (mode == kQAll16) refine_loop<kQAll16, false>(x, g, &iters, &tokd, &repd);
+    else if (mode == kQAll && nthr == 32) refine_loop<kQAll, true>(x, g, &iters, &tokd, &repd);
+    else if (mode == kQAll) refine_loop<kQAll, false>(x, g, &iters, &tokd, &repd);
+    else if (mode == kQOwnFetch) refine_loop<kQOwnFetch, false>(x, g, &iters, &tokd, &repd);
+    else refine_loop<kQOwn, false>(x, g, &iters, &tokd, &repd);
 
     // write back the domain's state and statistics; q's changed rows only
-    // (without all_src, q in global memory is already current): warp 0 lists
-    // them (over xe, no longer needed), then a thread per row writes it
-    __shared__ int n_dirty;
+    // (in the other modes q in global memory is already current)
     __syncthreads();
-    if (all_src) {
-        int *list = x.xe;
-        if (w == 0) {
-            int n = 0;
-            for (int base = 0; base < rpn * nl; base += 32) {
-                const int row = base + lane;
-                const bool dv = row < rpn * nl && x.dirty[row];
-                const unsigned b = __ballot_sync(0xffffffffu, dv);
-                if (dv) list[n + __popc(b & ((1u << lane) - 1u))] = row;
-                n += __popc(b);
-            }
-            if (lane == 0) n_dirty = n;
-        }
-        __syncthreads();
-        for (int k = tid; k < n_dirty; k += nthr) {
-            const int row = list[k], j = row / nl, li = row - j * nl;
-            int32_t *dst = x.Q + (int64_t)(r0 + j) * nl + li;
-            const int *src = x.qc + row * x.RS;
-#pragma unroll 4
-            for (int s = 0; s < R; ++s) dst[(int64_t)s * R * nl] = src[s];
-        }
-    }
+    if (mode == kQAll16) write_rows<uint16_t>(x, g);
+    else if (mode == kQAll) write_rows<int>(x, g);
     for (int j = tid; j < rpn; j += nthr) rank_load[(int64_t)l * R + r0 + j] = x.Lr[j];
     for (int i = tid; i < rpn * nl; i += nthr) inst_load[((int64_t)l * R + r0) * nl + i] = x.U[i];
     if (w == 0) {
@@ -726,19 +915,33 @@ k_plan_refine(const int32_t *__restrict__ tab, int32_t *slot_expert, int32_t *q,
 
 }  // namespace
 
-// Shared memory of the refinement kernel; all_src: every source's rows of q.
-size_t refine_smem_bytes(const Geo &g, bool all_src) {
-    return ((size_t)refine_q_offset(g) + (size_t)g.rpn * g.n_local * refine_row_stride(g, all_src)) * 4;
+// Shared memory (bytes) of the refinement kernel in each q mode; kQAll16 takes
+// all the kernel may have, its tail staging the load.
+size_t refine_smem_bytes(const Geo &g, int qmode) {
+    if (qmode == kQAll16) return kRefineSmem;
+    const size_t pf = qmode == kQOwnFetch ? (size_t)g.n_local * g.R : 0;
+    return ((size_t)refine_q_offset(g) + (size_t)refine_q_ints(g, qmode) + pf) * 4;
 }
 
-// Warps of the refinement CTA: about kRefineCpl candidates per thread, at most 8.
-int refine_warps(const Geo &g) {
+int refine_qmode(const Geo &g) {
+    if (refine_smem_bytes(g, kQAll) <= 200 * 1024) return kQAll;
+    // the 16-bit table, the per-source sums and at least one source's pieces
+    const size_t q16 = ((size_t)refine_q_offset(g) + refine_q_ints(g, kQAll16) + ((g.R + 3) & ~3) +
+                        (size_t)g.rpn * ((g.n_local + 3) & ~3)) * 4;
+    if (q16 <= (size_t)kRefineSmem && refine_smem_bytes(g, kQOwn) <= (size_t)kRefineSmem) return kQAll16;
+    if (refine_smem_bytes(g, kQOwnFetch) <= 220 * 1024) return kQOwnFetch;
+    return kQOwn;
+}
+
+// Warps of the refinement CTA: with every source in 32-bit shared memory,
+// enough for kRefineCpl candidates per thread when all of a rank's slots are
+// used (at most 8); else 8 (they load the table, or fetch rows of q).
+int refine_warps(const Geo &g, int qmode) {
+    if (qmode != kQAll) return kRefineMaxWarps;
     const int ncand = g.n_local * g.rpn;
     int w = (ncand + 32 * kRefineCpl - 1) / (32 * kRefineCpl);
     return w < 1 ? 1 : (w > kRefineMaxWarps ? kRefineMaxWarps : w);
 }
-
-bool refine_all_sources(const Geo &g) { return refine_smem_bytes(g, true) <= 200 * 1024; }
 
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st) {
@@ -764,11 +967,12 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
     if ((e = launch_pdl(k_plan_route, dim3(g.R, g.L), dim3(256), (size_t)g.R * 4, st, hist, tab, rep,
                         p.route_cnt, p.inst_load, p.rank_load, p.stats, g)) != cudaSuccess)
         return e;
-    const bool all_src = refine_all_sources(g);
-    const size_t smem_ref = refine_smem_bytes(g, all_src);
+    const int qmode = refine_qmode(g);
+    const size_t smem_ref = refine_smem_bytes(g, qmode);
     if ((e = ensure_smem((const void *)k_plan_refine, smem_ref)) != cudaSuccess) return e;
-    return launch_pdl(k_plan_refine, dim3(g.M, g.L), dim3(refine_warps(g) * 32), smem_ref, st, tab,
-                      p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, all_src ? 1 : 0);
+    return launch_pdl(k_plan_refine, dim3(g.M, g.L), dim3(refine_warps(g, qmode) * 32), smem_ref, st, tab,
+                      p.slot_expert, p.route_cnt, p.inst_load, p.rank_load, p.stats, g, qmode,
+                      (int)(smem_ref / 4));
 }
 
 }  // namespace topo

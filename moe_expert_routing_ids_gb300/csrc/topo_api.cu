@@ -58,7 +58,9 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     if (nl > 32767) return TOPO_EINVAL;
     if ((2 * (R * nl + 3) + E + 4 + 2 * E) * 4 + 2560 > kSmemMax) return TOPO_EINVAL;       // row index
     if ((E * ((R + 31) / 32) + E + 1) * 4 + 256 > kSmemMax) return TOPO_EINVAL;             // instance list
-    if ((2 * rpn + 3 * rpn * nl + rpn * rpn * nl) * 4 + rpn * E * 2 > kSmemMax) return TOPO_EINVAL;  // refinement
+    if ((((2 * rpn + 4 * rpn * nl + (rpn * E + 1) / 2 + 3) & ~int64_t(3)) + rpn * nl * (rpn | 1)) * 4 >
+        kSmemMax - 4096)
+        return TOPO_EINVAL;                                                                 // refinement
     if (E >= (1 << 26)) return TOPO_EINVAL;
     int64_t npow = 2;                                                                       // placement sort
     while (npow < E) npow <<= 1;

@@ -114,6 +114,14 @@ EDGE = {
                        lambda c: W.random_small(14, c["T"], c["E"], c["k"], 1, s=1.1)),
     "k3_odd": (_cfg(8 * 777, 24, 3, 8, 4, 3, S=256, Wb=5_000),
                lambda c: W.random_small(15, c["T"], c["E"], c["k"], 1, s=1.3)),
+    # R = 256 with many slots: the refinement keeps only the domain's own
+    # sources' rows of q in shared memory, fetching the busiest rank's rows
+    "rows_in_global_memory": (_cfg(256 * 150, 512, 8, 256, 8, 48, S=1024, Wb=60_000),
+                              lambda c: W.random_small(17, c["T"], c["E"], c["k"], 1, s=1.3)),
+    # free replicas and 96 slots: about 47 used per rank, so several warps
+    # evaluate and the rest fetch
+    "rows_in_global_memory_many_slots": (_cfg(256 * 150, 512, 8, 256, 8, 96, S=1024, Wb=0),
+                                         lambda c: W.random_small(18, c["T"], c["E"], c["k"], 1, s=1.6)),
     "repeated_ids_in_a_token": (_cfg(8 * 700, 16, 4, 8, 4, 2, S=256, Wb=5_000),
                                 lambda c: _with_repeats(W.random_small(16, c["T"], c["E"], c["k"], 1, s=1.2))),
 }
@@ -190,6 +198,24 @@ def test_edge_cases(name):
     if name == "iteration_cap":
         cfg["max_refine_iters"] = 1
     check(cfg, mk(cfg))
+
+
+def test_refinement_beyond_16_bit_counts():
+    """Every token picks 8 of domain 0's 32 main experts and replicas cost too
+    much to place elsewhere, so each source sends 72000 pairs into domain 0:
+    that domain's refinement cannot keep q as 16-bit counts and keeps it in
+    global memory, the other domains do; the plan is the oracle's either way."""
+    R, rpn, E, k, ns = 64, 8, 256, 8, 100
+    T = R * 9000
+    cfg = _cfg(T, E, k, R, rpn, ns, S=1024, Wb=2_000_000_000)
+    rng = W.rng_for(23, 0)
+    ids = np.argsort(rng.random((T, 32)), axis=1)[:, :8].astype(np.int32)[None]
+    want = oracle_chain(cfg, ids)
+    share = want["route_cnt"][0][:, :rpn, :].sum(axis=(1, 2))   # kept by every move
+    assert share.max() > 65535 and want["stats"][0, 4] > 0
+    gpu, err = gpu_chain(cfg, ids)
+    assert err == 0
+    assert_same(gpu, want)
 
 
 def test_main_rank_map():
