@@ -89,10 +89,11 @@ __global__ void k_main_tables(const int32_t *__restrict__ main_rank, int32_t *ta
 __global__ void __launch_bounds__(512)
 k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, int32_t *slot_expert,
              int32_t *rep, int32_t *inst_load, int32_t *rank_load, int64_t *stats, Geo g, int npow) {
-    // candidates sorted by (benefit desc, expert asc) in shared memory:
-    // keyv[i] the benefit (LLONG_MIN: not a candidate), kid[i] the expert
-    extern __shared__ long long keyv[];          // [npow], then int kid[npow]
-    int *kid = reinterpret_cast<int *>(keyv + npow);
+    // Candidates ranked by (benefit desc, expert asc).  With S_tok > 0 the
+    // benefit 2 D S_tok - ||W|| rises strictly with the demand D < 2^31, so
+    // one unsigned key D << 32 | ~e orders them the same way (0: not a
+    // candidate); keys are distinct.
+    extern __shared__ __align__(16) unsigned long long keyv[];   // [npow]
     __shared__ int ncand;
     __shared__ int64_t red[32];
     __shared__ int stat_load[kMaxRanksPerNode];
@@ -106,19 +107,18 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
     if (threadIdx.x < rpn) stat_load[threadIdx.x] = 0;
     __syncthreads();
     for (int e = threadIdx.x; e < npow; e += blockDim.x) {
-        long long key = LLONG_MIN;
+        unsigned long long key = 0;
         if (e < E) {
             int64_t D = 0;
 #pragma unroll 8
             for (int j = 0; j < rpn; ++j) D += H[(int64_t)(d * rpn + j) * E + e];
             const int64_t b = 2 * D * g.S_tok - g.W;
             if ((main_of[e] / rpn != d) && b > 0) {
-                key = (long long)b;
+                key = ((unsigned long long)D << 32) | (0xffffffffu - (unsigned)e);
                 atomicAdd(&ncand, 1);
             }
         }
         keyv[e] = key;
-        kid[e] = e;
     }
     int32_t *SE = slot_expert + (int64_t)l * R * ns;
     for (int i = threadIdx.x; i < rpn * ns; i += blockDim.x) SE[(int64_t)d * rpn * ns + i] = -1;
@@ -127,48 +127,43 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
     const int cap = rpn * ns;
     const int placed = ncand < cap ? ncand : cap;
     int64_t repcost = 0;
-    if (npow <= 256) {
-        // few experts: each candidate counts the candidates ahead of it
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            const long long b = keyv[e];
-            if (b == LLONG_MIN) continue;
-            int rank = 0;
-            for (int x = 0; x < E; ++x) {
-                const long long bx = keyv[x];
-                rank += (bx > b) || (bx == b && x < e);
-            }
-            if (rank < cap) {
-                const int r = d * rpn + rank % rpn, slot = rank / rpn;
-                SE[(int64_t)r * ns + slot] = e;
-                rep[((int64_t)l * E + e) * g.M + d] = r * nl + g.E_R + slot;
-                repcost += cost_sr(g, main_of[e], r) * g.W;
-            }
-        }
-    } else {
-    // bitonic sort, descending by benefit, ascending by expert on ties
-    for (int size = 2; size <= npow; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < (npow >> 1); i += blockDim.x) {
-                const int a = 2 * i - (i & (stride - 1)), b = a + stride;
-                const long long ka = keyv[a], kb = keyv[b];
-                const int ia = kid[a], ib = kid[b];
-                const bool a_first = ka > kb || (ka == kb && ia < ib);   // a precedes b
-                const bool desc = (a & size) == 0;
-                if (desc != a_first) {
-                    keyv[a] = kb; keyv[b] = ka;
-                    kid[a] = ib; kid[b] = ia;
-                }
-            }
-            __syncthreads();
-        }
-    }
-    for (int rank = threadIdx.x; rank < placed; rank += blockDim.x) {
-        const int e = kid[rank];
+    auto place_one = [&](int rank, int e) {
         const int r = d * rpn + rank % rpn, slot = rank / rpn;
         SE[(int64_t)r * ns + slot] = e;
         rep[((int64_t)l * E + e) * g.M + d] = r * nl + g.E_R + slot;
         repcost += cost_sr(g, main_of[e], r) * g.W;
-    }
+    };
+    if (npow <= 512) {
+        // each candidate counts the keys above its own, two per load
+        const ulonglong2 *kv2 = reinterpret_cast<const ulonglong2 *>(keyv);
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const unsigned long long key = keyv[e];
+            if (key == 0) continue;
+            int rank = 0;
+#pragma unroll 4
+            for (int x = 0; x < (npow >> 1); ++x) {
+                const ulonglong2 v = kv2[x];
+                rank += (v.x > key) + (v.y > key);
+            }
+            if (rank < cap) place_one(rank, e);
+        }
+    } else {
+        // bitonic sort in shared memory, descending
+        for (int size = 2; size <= npow; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = threadIdx.x; i < (npow >> 1); i += blockDim.x) {
+                    const int a = 2 * i - (i & (stride - 1)), b = a + stride;
+                    const unsigned long long ka = keyv[a], kb = keyv[b];
+                    if (((a & size) == 0) != (ka > kb)) {
+                        keyv[a] = kb;
+                        keyv[b] = ka;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int rank = threadIdx.x; rank < placed; rank += blockDim.x)
+            place_one(rank, (int)(0xffffffffu - (unsigned)keyv[rank]));
     }
     // static loads of the domain's ranks (mains only): each thread sums one
     // main over a strided group of sources, the groups meet in shared atomics
@@ -199,6 +194,8 @@ k_plan_place(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab, 
     }
 }
 
+constexpr int kRouteRowMax = 16;     // domains whose replica row a thread holds in registers
+
 __global__ void __launch_bounds__(256)
 k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
              const int32_t *__restrict__ rep, int32_t *q, int32_t *inst_load, int32_t *rank_load,
@@ -227,6 +224,7 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
         atomicAdd(&lr[r], amt);
         tok += cost_sr(g, s, r) * amt;
     };
+    const bool rep_vec = (M & 3) == 0 && ((uintptr_t)REP & 15) == 0;
     // two experts per thread and pass, their table entries requested together
     for (int e0 = threadIdx.x; e0 < E; e0 += 2 * blockDim.x) {
         int ew[2], wv[2], me[2], ml[2], rc[2];
@@ -250,6 +248,45 @@ k_plan_route(const int32_t *__restrict__ hist, const int32_t *__restrict__ tab,
             // no instance in dom(s): every instance of e, in rank (= domain)
             // order; all are cross-domain, so (c, r) order is rank order
             const int32_t *re = REP + (int64_t)ew[u] * M;
+            if (M <= kRouteRowMax) {
+                // the expert's row of stage-1 replicas in registers (16-byte
+                // loads when the rows are 16-byte aligned)
+                int rr[kRouteRowMax];
+                if (rep_vec) {
+#pragma unroll
+                    for (int q4 = 0; q4 < kRouteRowMax / 4; ++q4) {
+                        const int4 v = 4 * q4 < M ? __ldg(reinterpret_cast<const int4 *>(re) + q4)
+                                                  : make_int4(-1, -1, -1, -1);
+                        rr[4 * q4] = v.x;
+                        rr[4 * q4 + 1] = v.y;
+                        rr[4 * q4 + 2] = v.z;
+                        rr[4 * q4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int dd = 0; dd < kRouteRowMax; ++dd) rr[dd] = dd < M ? __ldg(re + dd) : -1;
+                }
+                int n = 1;
+#pragma unroll
+                for (int dd = 0; dd < kRouteRowMax; ++dd) n += (dd != dm && rr[dd] >= 0);
+                const int base = w / n, rem = w % n;
+                int i = 0;
+#pragma unroll
+                for (int dd = 0; dd < kRouteRowMax; ++dd) {
+                    int r, li;
+                    if (dd == dm) {
+                        r = me[u];
+                        li = ml[u];
+                    } else {
+                        if (rr[dd] < 0) continue;
+                        r = rr[dd] / nl;
+                        li = rr[dd] % nl;
+                    }
+                    emit(r, li, base + (i < rem ? 1 : 0));
+                    ++i;
+                }
+                continue;
+            }
             int n = 1;
             for (int d = 0; d < M; ++d) n += (d != dm && __ldg(re + d) >= 0);
             const int base = w / n, rem = w % n;
@@ -958,7 +995,7 @@ cudaError_t launch_plan(const Geo &g, const int32_t *main_rank, const int32_t *h
         return e;
     int npow = 2;
     while (npow < g.E) npow <<= 1;
-    const size_t smem_place = (size_t)npow * 12;
+    const size_t smem_place = (size_t)npow * 8;
     if ((e = ensure_smem((const void *)k_plan_place, smem_place)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_plan_place, dim3(g.M, g.L), dim3(512), smem_place, st, hist, tab,
                         p.slot_expert, rep, p.inst_load, p.rank_load, p.stats, g, npow)) != cudaSuccess)

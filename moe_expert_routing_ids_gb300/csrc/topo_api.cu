@@ -64,7 +64,7 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     if (E >= (1 << 26)) return TOPO_EINVAL;
     int64_t npow = 2;                                                                       // placement sort
     while (npow < E) npow <<= 1;
-    if (npow * 12 > kSmemMax) return TOPO_EINVAL;
+    if (npow * 8 > kSmemMax) return TOPO_EINVAL;
     std::memset(g, 0, sizeof *g);
     g->T = c->T; g->E = c->E; g->k = c->k; g->R = c->R; g->rpn = c->ranks_per_node;
     g->n_slot = c->n_slot; g->M = c->R / c->ranks_per_node; g->E_R = c->E / c->R;
