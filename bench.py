@@ -378,7 +378,7 @@ def secondary_plan_latency(dev, stream):
     b.synchronize()
     us = a.elapsed_time(b) * 1e3 / 200 / w.n_layers
     return {"workload": w.name, "us_per_layer": round(us, 2), "reps": 200, "warmup": 20,
-            "target_us": 50, "timing": "200 calls in one CUDA graph"}
+            "target_us": 40, "timing": "200 calls in one CUDA graph"}
 
 
 def bf16_peak():
