@@ -255,6 +255,9 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
     }
     const int n_ent = __ldg(ro + E);
     const bool row_in_smem = n_ent <= kRankEntCap;
+    // every per-expert value of the tile requested at once (the tile's
+    // occurrence range [tb, te) parked in warp 0's base and mask words), the
+    // row's entries staged, the other warps' words zeroed; then one barrier
     if (row_in_smem)
         for (int j = threadIdx.x; j < n_ent; j += kRankThreads) {
             S.ent_ce[j] = __ldg(&re[j].cum_end);
@@ -263,31 +266,41 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
         }
     if (threadIdx.x == 0) S.ro[E] = n_ent;
     for (int e = threadIdx.x; e < E; e += kRankThreads) {
-        const int b = __ldg(ro + e), en = __ldg(ro + e + 1);
+        S.ro[e] = __ldg(ro + e);
+        S.base[e] = __ldg(tbase + e);
+        S.msk[e] = tg.last ? 0u : (unsigned)__ldg(tbase + E + e);
+#pragma unroll
+        for (int x = 1; x < kRankWarps; ++x) {
+            S.base[x * E + e] = 0;
+            S.msk[x * E + e] = 0;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRankThreads) {
+        const int b = S.ro[e], en = S.ro[e + 1];
         const int ne = en - b;
-        int code = ne == 1 ? __ldg(&re[b].code) : (ne == 0 ? -2 : -1);
+        auto ce = [&](int j) { return row_in_smem ? S.ent_ce[j] : __ldg(&re[j].cum_end); };
+        auto cd = [&](int j) { return row_in_smem ? S.ent_code[j] : __ldg(&re[j].code); };
+        auto ob = [&](int j) { return row_in_smem ? S.ent_ob[j] : __ldg(&re[j].out_base); };
+        int code = ne == 1 ? cd(b) : (ne == 0 ? -2 : -1);
         // per-warp base: tile base (+ out_base when the expert has one entry);
         // pass 1 then adds each warp's count into the following warps' bases
-        const int tb = __ldg(tbase + e);
-        int b0 = tb + (ne == 1 ? __ldg(&re[b].out_base) : 0);
+        const int tb = S.base[e];
+        int b0 = tb + (ne == 1 ? ob(b) : 0);
         if (ne > 1) {
             // several entries: when the tile's occurrences [tb, te) all fall in
             // one entry, the tile ranks e like a single-entry expert
-            const int te = !tg.last ? __ldg(tbase + E + e) : __ldg(&re[en - 1].cum_end);
+            const int te = !tg.last ? (int)S.msk[e] : ce(en - 1);
             int j = b;
-            while (j < en && tb >= __ldg(&re[j].cum_end)) ++j;
-            if (j < en && te <= __ldg(&re[j].cum_end)) {
-                code = __ldg(&re[j].code);
-                b0 = tb + __ldg(&re[j].out_base);
+            while (j < en && tb >= ce(j)) ++j;
+            if (j < en && te <= ce(j)) {
+                code = cd(j);
+                b0 = tb + ob(j);
             }
         }
         S.ec[e] = code;
-        S.ro[e] = b;
-#pragma unroll
-        for (int x = 0; x < kRankWarps; ++x) {
-            S.base[x * E + e] = x == 0 ? b0 : 0;
-            S.msk[x * E + e] = 0;
-        }
+        S.base[e] = b0;
+        S.msk[e] = 0;
     }
     if (fast) cp_async_wait_all();
     __syncthreads();
