@@ -10,6 +10,8 @@
 namespace topo {
 namespace {
 
+constexpr int kPrepBThreads = 1024;
+
 // Exclusive scan of a[0..n) in place by one CTA; returns the total.
 __device__ int block_excl_scan(int *a, int n, int *warp_tot) {
     __shared__ int carry;
@@ -64,12 +66,11 @@ __device__ __forceinline__ void stage_words(void *dst, const void *src, int n) {
 // bitmask over ranks of the instances of every expert (imask, zeroed before).
 // One thread per instance.  tab == nullptr: the contiguous main map (main of
 // e is e / (E/R)).
-__global__ void __launch_bounds__(256)
-k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict__ tab, int32_t *iexp,
-             unsigned *imask, WsHeader *hdr, Geo g) {
-    pdl_wait();                                  // the previous kernel's outputs
+__device__ __forceinline__ void inst_index(const int32_t *__restrict__ slot_expert,
+                                           const int32_t *__restrict__ tab, int32_t *iexp, unsigned *imask,
+                                           WsHeader *hdr, const Geo &g, int bx) {
     const int l = blockIdx.y;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int i = bx * blockDim.x + threadIdx.x;
     if (l == 0 && i == 0) hdr->route_fp = 0;
     if (i >= g.n_keys) return;
     const int E = g.E, R = g.R, nl = g.n_local, ER = g.E_R, ns = g.n_slot;
@@ -86,7 +87,6 @@ k_inst_index(const int32_t *__restrict__ slot_expert, const int32_t *__restrict_
         if (old & bit) bad = true;                             // expert twice on one rank
     }
     if (bad) set_error(hdr, TOPO_ESTATE);
-    pdl_trigger();
 }
 
 // Exclusive scan of one (count, sum) pair per thread over the CTA; returns
@@ -135,11 +135,8 @@ __device__ __forceinline__ int lower_idx(const int *a, int n, int v) {
 // and each expert's start in it (ioff).  An instance's place is its expert's
 // start plus the number of lower ranks in the expert's rank mask.  Every CTA
 // prefixes the layer's mask popcounts itself; CTA 0 stores the offsets.
-__global__ void __launch_bounds__(256)
-k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask, int32_t *ioff_g,
-            int32_t *ilist, Geo g) {
-    pdl_wait();                                  // the previous kernel's outputs
-    extern __shared__ __align__(16) int sml[];
+__device__ __forceinline__ void inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask,
+                                          int32_t *ioff_g, int32_t *ilist, const Geo &g, int bx, int *sml) {
     __shared__ int warp_tot[32];
     const int l = blockIdx.y, E = g.E, nk = g.n_keys, nl = g.n_local;
     const int RW = (g.R + 31) / 32;
@@ -155,12 +152,12 @@ k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask
     }
     __syncthreads();
     const int n_inst = block_excl_scan(ioff, E, warp_tot);
-    if (blockIdx.x == 0) {
+    if (bx == 0) {
         int32_t *o = ioff_g + (int64_t)l * (E + 1);
         for (int e = threadIdx.x; e < E; e += blockDim.x) o[e] = ioff[e];
         if (threadIdx.x == 0) o[E] = n_inst;
     }
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int i = bx * blockDim.x + threadIdx.x;
     if (i >= nk) return;
     const int e = __ldg(iexp + (int64_t)l * nk + i);
     if (e < 0) return;
@@ -169,7 +166,6 @@ k_inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask
     int j = ioff[e] + __popc(m[r >> 5] & ((1u << (r & 31)) - 1u));
     for (int w = 0; w < (r >> 5); ++w) j += __popc(m[w]);
     ilist[(int64_t)l * nk + j] = i;
-    pdl_trigger();
 }
 
 // Routing index of one source row: per expert, its nonzero instances in rank
@@ -253,13 +249,12 @@ k_row_index(const int32_t *__restrict__ q, const int32_t *__restrict__ ioff_g,
 // totals.  A CTA covers 32 columns; its 8 warps each scan one chunk of the
 // sources (16 loads in flight per lane), and the chunks are prefixed through
 // shared memory.
-__global__ void __launch_bounds__(256)
-k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
-    pdl_wait();                                  // the previous kernel's outputs
+__device__ __forceinline__ void lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt,
+                                         const Geo &g, int bx) {
     __shared__ int part[8][33];
     const int l = blockIdx.y;
     const int lane = threadIdx.x & 31, ch = threadIdx.x >> 5;
-    const int i = blockIdx.x * 32 + lane;
+    const int i = bx * 32 + lane;
     const int chunk = (g.R + 7) / 8;
     const int s0 = ch * chunk, s1 = min(g.R, s0 + chunk);
     const bool col = i < g.n_keys;
@@ -291,18 +286,16 @@ k_lay_cols(const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g) {
             run += v[u];
         }
     }
-    pdl_trigger();
 }
 
 // Segment offsets (exclusive prefix of the column totals); zeroes the layout
 // statistics.  One CTA per layer: each thread sums a contiguous run of the
 // totals, the runs' sums are scanned once, then each run is written out.
-__global__ void __launch_bounds__(1024)
-k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g) {
-    pdl_wait();                                  // the previous kernel's outputs
+__device__ __forceinline__ void lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat,
+                                        const Geo &g) {
     __shared__ int warp_tot[32];
     __shared__ int sums[1024];
-    const int l = blockIdx.x;
+    const int l = blockIdx.y;
     if (threadIdx.x < TOPO_LAYOUT_STATS) lstat[l * TOPO_LAYOUT_STATS + threadIdx.x] = 0;
     const int32_t *c = ccnt + (int64_t)l * g.n_keys;
     int32_t *o = lseg + (int64_t)l * (g.n_keys + 1);
@@ -337,6 +330,29 @@ k_lay_seg(const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g
         }
     }
     if (threadIdx.x == 0) o[n] = total;
+}
+
+// The prep's first two steps each pair two independent jobs in one launch:
+// blocks [0, n_a) build the instance index (or list), the rest the column
+// prefixes of q (or, one block per layer, the segment offsets), which need q
+// alone.
+__global__ void __launch_bounds__(256)
+k_prep_a(const int32_t *__restrict__ slot_expert, const int32_t *__restrict__ tab, int32_t *iexp,
+         unsigned *imask, WsHeader *hdr, const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g,
+         int n_a) {
+    pdl_wait();                                  // the previous kernel's outputs
+    if ((int)blockIdx.x < n_a) inst_index(slot_expert, tab, iexp, imask, hdr, g, blockIdx.x);
+    else lay_cols(q, soff, ccnt, g, blockIdx.x - n_a);
+    pdl_trigger();
+}
+
+__global__ void __launch_bounds__(kPrepBThreads)
+k_prep_b(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask, int32_t *ioff_g,
+         int32_t *ilist, const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g, int n_a) {
+    extern __shared__ __align__(16) int sml[];
+    pdl_wait();                                  // the previous kernel's outputs
+    if ((int)blockIdx.x < n_a) inst_list(iexp, imask, ioff_g, ilist, g, blockIdx.x, sml);
+    else lay_seg(ccnt, lseg, lstat, g);
     pdl_trigger();
 }
 
@@ -409,27 +425,26 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     if ((e = cudaMemsetAsync(ws_at<unsigned>(ws, g.off_imask), 0, (size_t)g.L * g.E * RW * 4, st)) !=
         cudaSuccess)
         return e;
-    if ((e = launch_pdl(k_inst_index, dim3((g.n_keys + 255) / 256, g.L), dim3(256), 0, st,
-        p.slot_expert, main_rank ? ws_at<int32_t>(ws, g.off_main) : nullptr,
-        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask), hdr, g)) != cudaSuccess)
+    const int na = (g.n_keys + 255) / 256, nb = (g.n_keys + 31) / 32;
+    if ((e = launch_pdl(k_prep_a, dim3(na + nb, g.L), dim3(256), 0, st, p.slot_expert,
+                        main_rank ? ws_at<int32_t>(ws, g.off_main) : nullptr, ws_at<int32_t>(ws, g.off_iexp),
+                        ws_at<unsigned>(ws, g.off_imask), hdr, p.route_cnt, ws_at<int32_t>(ws, g.off_soff),
+                        ws_at<int32_t>(ws, g.off_ccnt), g, na)) != cudaSuccess)
         return e;
+    const int nl_blocks = (g.n_keys + kPrepBThreads - 1) / kPrepBThreads;
     const size_t smem_list = ((size_t)g.E * RW + g.E + 1) * 4;
-    if ((e = ensure_smem((const void *)k_inst_list, smem_list)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_inst_list, dim3((g.n_keys + 255) / 256, g.L), dim3(256), smem_list, st,
-        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask), ws_at<int32_t>(ws, g.off_ioff),
-        ws_at<int32_t>(ws, g.off_ilist), g)) != cudaSuccess)
+    if ((e = ensure_smem((const void *)k_prep_b, smem_list)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_prep_b, dim3(nl_blocks + 1, g.L), dim3(kPrepBThreads), smem_list, st,
+                        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask),
+                        ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
+                        ws_at<int32_t>(ws, g.off_ccnt), ws_at<int32_t>(ws, g.off_lseg),
+                        ws_at<int64_t>(ws, g.off_lstat), g, nl_blocks)) != cudaSuccess)
         return e;
     const size_t smem_row = row_index_smem(g);
     if ((e = ensure_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_row_index, dim3(g.R, g.L), dim3(256), smem_row, st,
         p.route_cnt, ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), g)) != cudaSuccess)
-        return e;
-    if ((e = launch_pdl(k_lay_cols, dim3((g.n_keys + 31) / 32, g.L), dim3(256), 0, st,
-        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), g)) != cudaSuccess)
-        return e;
-    if ((e = launch_pdl(k_lay_seg, dim3(g.L), dim3(1024), 0, st, ws_at<int32_t>(ws, g.off_ccnt),
-                        ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lstat), g)) != cudaSuccess)
         return e;
     const size_t smem_e = (size_t)g.R * 8;
     if ((e = ensure_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
