@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 # algorithmic HBM bytes per (token, slot) pair: hist reads the id; the fused
 # reroute+layout reads the id and writes dst_inst and sorted_pairs
 BYTES_PER_PAIR = {"hist": 4, "reroute_layout": 12}
-KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 6, "cooccur": 2, "dedup": 4, "gate": 2, "shuffle": 2, "place": 1}
+KERNELS_PER_CALL = {"hist": 2, "plan": 4, "reroute_layout": 5, "cooccur": 2, "dedup": 4, "gate": 2, "shuffle": 2, "place": 1}
 CALLS = ("hist", "plan", "reroute_layout")
 # kernel sources of each call (with the shared header): recorded DRAM traffic
 # counts only while these are unchanged

@@ -229,9 +229,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Prep of the rerouting calls (instance index, routing index, layout
-// offsets), from the plan alone; defined in k_prep.cu.
+// offsets), from the plan alone; defined in k_prep.cu.  The segment offsets,
+// send counts and layout statistics go to seg_off / send_counts /
+// layout_stats when given (the fused call's outputs), else to the workspace.
 cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_t &p, void *ws,
-                        cudaStream_t st);
+                        int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, cudaStream_t st);
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
                                int n_stats, cudaStream_t st);
 // first[s] = first tile of source s for tiles of TT tokens over g.roff, and

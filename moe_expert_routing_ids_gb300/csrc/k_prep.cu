@@ -417,9 +417,12 @@ size_t row_index_smem(const Geo &g) {
 
 // Prep shared by topo_reroute and topo_reroute_layout.
 cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_t &p, void *ws,
-                        cudaStream_t st) {
+                        int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats, cudaStream_t st) {
     cudaError_t e;
     WsHeader *hdr = ws_at<WsHeader>(ws, 0);
+    int32_t *lseg = seg_off ? seg_off : ws_at<int32_t>(ws, g.off_lseg);
+    int64_t *lsend = send_counts ? send_counts : ws_at<int64_t>(ws, g.off_lsend);
+    int64_t *lstat = layout_stats ? layout_stats : ws_at<int64_t>(ws, g.off_lstat);
     if (main_rank && (e = launch_main_tables(g, main_rank, ws, nullptr, 0, st)) != cudaSuccess) return e;
     const int RW = (g.R + 31) / 32;
     if ((e = cudaMemsetAsync(ws_at<unsigned>(ws, g.off_imask), 0, (size_t)g.L * g.E * RW * 4, st)) !=
@@ -437,8 +440,7 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     if ((e = launch_pdl(k_prep_b, dim3(nl_blocks + 1, g.L), dim3(kPrepBThreads), smem_list, st,
                         ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask),
                         ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
-                        ws_at<int32_t>(ws, g.off_ccnt), ws_at<int32_t>(ws, g.off_lseg),
-                        ws_at<int64_t>(ws, g.off_lstat), g, nl_blocks)) != cudaSuccess)
+                        ws_at<int32_t>(ws, g.off_ccnt), lseg, lstat, g, nl_blocks)) != cudaSuccess)
         return e;
     const size_t smem_row = row_index_smem(g);
     if ((e = ensure_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;
@@ -450,8 +452,7 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     if ((e = ensure_smem((const void *)k_lay_entries, smem_e)) != cudaSuccess) return e;
     return launch_pdl(k_lay_entries, dim3(g.R, g.L), dim3(256), smem_e, st,
         ws_at<int32_t>(ws, g.off_roff), ws_at<Entry>(ws, g.off_rent), ws_at<int32_t>(ws, g.off_soff),
-        ws_at<int32_t>(ws, g.off_lseg), ws_at<int64_t>(ws, g.off_lsend),
-        ws_at<int64_t>(ws, g.off_lstat), g);
+        lseg, lsend, lstat, g);
 }
 
 }  // namespace topo

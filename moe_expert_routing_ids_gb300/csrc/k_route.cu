@@ -456,14 +456,15 @@ k_layout_scatter(const int32_t *__restrict__ pos_ws, int32_t *sorted, WsHeader *
     pdl_trigger();
 }
 
-// Copy the small layout outputs computed by the prep kernels.
+// Copy the small layout outputs the prep kernels left in the workspace
+// (topo_dispatch_layout, after topo_reroute).
 __global__ void __launch_bounds__(256)
 k_lay_copy(const int32_t *__restrict__ lseg, const int64_t *__restrict__ lsend,
            const int64_t *__restrict__ lstat, int32_t *seg_off, int64_t *send_counts,
-           int64_t *layout_stats, const WsHeader *hdr, Geo g, uint64_t route_part, int check) {
+           int64_t *layout_stats, const WsHeader *hdr, Geo g, uint64_t route_part) {
     pdl_wait();                                  // the previous kernel's outputs
     __shared__ int ok;
-    if (check && !check_fp(hdr, 0, true, route_part, &ok)) return;
+    if (!check_fp(hdr, 0, true, route_part, &ok)) return;
     const int64_t nseg = (int64_t)g.L * (g.n_keys + 1);
     const int64_t nsend = (int64_t)g.L * g.R * g.R;
     const int64_t nst = (int64_t)g.L * TOPO_LAYOUT_STATS;
@@ -510,13 +511,13 @@ cudaError_t launch_tiles(const Geo &g, const int32_t *ids, int32_t *dst, int32_t
 }
 
 cudaError_t launch_copy(const Geo &g, int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
-                        void *ws, uint64_t route_part, int check, cudaStream_t st) {
+                        void *ws, uint64_t route_part, cudaStream_t st) {
     const int64_t n = (int64_t)g.L * (g.n_keys + 1 + (int64_t)g.R * g.R + TOPO_LAYOUT_STATS);
     const int64_t want = (n + 255) / 256;
     const int blocks = (int)(want < 1024 ? want : 1024);
     return launch_pdl(k_lay_copy, dim3(blocks), dim3(256), 0, st, ws_at<int32_t>(ws, g.off_lseg),
                       ws_at<int64_t>(ws, g.off_lsend), ws_at<int64_t>(ws, g.off_lstat), seg_off, send_counts,
-                      layout_stats, ws_at<WsHeader>(ws, 0), g, route_part, check);
+                      layout_stats, ws_at<WsHeader>(ws, 0), g, route_part);
 }
 
 }  // namespace
@@ -530,7 +531,7 @@ cudaError_t launch_reroute(const Geo &g, const int32_t *main_rank, const int32_t
                            const topo_plan_t &p, int32_t *dst, void *ws, uint64_t hist_fp,
                            uint64_t route_part, cudaStream_t st) {
     cudaError_t e;
-    if ((e = launch_prep(g, main_rank, p, ws, st)) != cudaSuccess) return e;
+    if ((e = launch_prep(g, main_rank, p, ws, nullptr, nullptr, nullptr, st)) != cudaSuccess) return e;
     return launch_tiles<false>(g, ids, dst, nullptr, ws, hist_fp, route_part, st);
 }
 
@@ -541,7 +542,7 @@ cudaError_t launch_layout(const Geo &g, int32_t *sorted, int32_t *seg_off, int64
     if ((e = launch_pdl(k_layout_scatter, dim3((unsigned)tiles), dim3(256), 0, st, ws_at<int32_t>(ws, g.off_pos),
                         sorted, ws_at<WsHeader>(ws, 0), g, route_part)) != cudaSuccess)
         return e;
-    return launch_copy(g, seg_off, send_counts, layout_stats, ws, route_part, 1, st);
+    return launch_copy(g, seg_off, send_counts, layout_stats, ws, route_part, st);
 }
 
 cudaError_t launch_reroute_layout(const Geo &g, const int32_t *main_rank, const int32_t *ids,
@@ -549,9 +550,11 @@ cudaError_t launch_reroute_layout(const Geo &g, const int32_t *main_rank, const 
                                   int32_t *seg_off, int64_t *send_counts, int64_t *layout_stats,
                                   void *ws, uint64_t hist_fp, cudaStream_t st) {
     cudaError_t e;
-    if ((e = launch_prep(g, main_rank, p, ws, st)) != cudaSuccess) return e;
-    if ((e = launch_tiles<true>(g, ids, dst, sorted, ws, hist_fp, 0, st)) != cudaSuccess) return e;
-    return launch_copy(g, seg_off, send_counts, layout_stats, ws, 0, 0, st);
+    // the prep writes the layout's offsets, send counts and statistics
+    // straight to the outputs
+    if ((e = launch_prep(g, main_rank, p, ws, seg_off, send_counts, layout_stats, st)) != cudaSuccess)
+        return e;
+    return launch_tiles<true>(g, ids, dst, sorted, ws, hist_fp, 0, st);
 }
 
 }  // namespace topo
