@@ -62,10 +62,11 @@ def parse():
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--only", choices=("plan_latency", "cooccur", "pack", "dedup", "gate", "shuffle", "place",
-                                       "configs", "solver"),
-                    help="run one secondary measurement alone and print it (for profiling)")
+                                       "configs", "solver", "chain"),
+                    help="run one secondary measurement alone and print it (for profiling); chain: the "
+                         "hot path hist -> plan -> reroute_layout twice, untimed (an ncu target)")
     ap.add_argument("--microbatches", type=int, default=0,
-                    help="--only gate: microbatches of the workload to use (0 = all; 1 for ncu captures)")
+                    help="--only gate / chain: microbatches of the workload to use (0 = all; 1 for ncu captures)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds the oracle steps should take in total")
     return ap.parse_args()
@@ -946,6 +947,18 @@ def run_only(name, microbatches=0):
         res = {"configs": config_lines(dev, stream, hbm)}
     elif name == "solver":
         res = solver_sweep(dev, stream)
+    elif name == "chain":
+        w = W.STRESS
+        L = min(w.n_layers, microbatches) if microbatches else w.n_layers
+        ids = torch.as_tensor(w.ids()[:L], device=dev).contiguous()
+        P = Planner(w.plan_cfg, L, dev, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                P.run(ids)
+        torch.cuda.synchronize(dev)
+        if P.error() != 0:
+            raise RuntimeError("device error in the plan chain")
+        res = {"workload": f"{w.name}, {L} microbatch(es)", "pairs": int(ids.numel()), "runs": 2}
     else:
         w = W.STRESS
         P = Planner(w.plan_cfg, w.n_layers, dev, stream=stream)
