@@ -970,14 +970,13 @@ int refine_qmode(const Geo &g) {
     return kQOwn;
 }
 
-// Warps of the refinement CTA: with every source in 32-bit shared memory,
-// enough for kRefineCpl candidates per thread when all of a rank's slots are
-// used (at most 8); else 8 (they load the table, or fetch rows of q).
+// Warps of the refinement CTA: one when a single warp holds every candidate
+// of an iteration at kRefineCpl per thread (no barriers then); else 8 -- all
+// of them load the table (or fetch rows of q), and each iteration's
+// candidates take as many as they fill.
 int refine_warps(const Geo &g, int qmode) {
-    if (qmode != kQAll) return kRefineMaxWarps;
-    const int ncand = g.n_local * g.rpn;
-    int w = (ncand + 32 * kRefineCpl - 1) / (32 * kRefineCpl);
-    return w < 1 ? 1 : (w > kRefineMaxWarps ? kRefineMaxWarps : w);
+    if (qmode == kQAll && g.n_local * g.rpn <= 32 * kRefineCpl) return 1;
+    return kRefineMaxWarps;
 }
 
 cudaError_t launch_main_tables(const Geo &g, const int32_t *main_rank, void *ws, int64_t *stats,
