@@ -322,32 +322,60 @@ def capture_steps(P, d_ids, n_steps, stream, gev):
     return graph
 
 
+def capture_plain(P, d_ids, n_steps, stream):
+    """One CUDA graph of n_steps whole steps, nothing between the calls."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(n_steps):
+            P.hist(d_ids)
+            P.make_plan()
+            P.reroute_layout(d_ids)
+    return graph
+
+
+CALL_REPLAYS = 5      # replays of the event-instrumented graph for the per-call times
+
+
 def time_chain(P, d_ids, steps, stream):
-    """Replays a captured 20-step graph until `steps` steps ran; returns total
-    ms (events around all replays) and mean ms per call."""
+    """Times exactly `steps` steps, replayed from CUDA graphs of up to 20 steps
+    with nothing between the calls (an event node between calls breaks the
+    programmatic launch chain and costs about 4% of the step); returns total
+    ms (events around all replays).  Then, for the per-call times, replays the
+    same steps captured with an event node before every call CALL_REPLAYS
+    times and returns each call's mean."""
     import torch
     n_in = min(STEPS_PER_GRAPH, steps)
-    reps = -(-steps // n_in)
+    full, rem = divmod(steps, n_in)
+    g_main = capture_plain(P, d_ids, n_in, stream)
+    g_rem = capture_plain(P, d_ids, rem, stream) if rem else None
     gev = GraphEvents(n_in * len(CALLS) + 1)
-    graph = capture_steps(P, d_ids, n_in, stream, gev)
-    graph.replay()                                  # settle
+    g_ev = capture_steps(P, d_ids, n_in, stream, gev)
+    for g in (g_main, g_rem, g_ev):                 # settle
+        if g is not None:
+            g.replay()
     torch.cuda.synchronize()
-    per_call = {c: [] for c in CALLS}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    total = 0.0
-    for _ in range(reps):
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(full):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record(stream)
+    t1.synchronize()
+    total = t0.elapsed_time(t1)
+    per_call = {c: [] for c in CALLS}
+    for _ in range(CALL_REPLAYS):
         with torch.cuda.stream(stream):
-            t0.record(stream)
-            graph.replay()
-            t1.record(stream)
-        t1.synchronize()
-        total += t0.elapsed_time(t1)
+            g_ev.replay()
+        torch.cuda.synchronize()
         for k in range(n_in):
             for i, c in enumerate(CALLS):
                 per_call[c].append(gev.elapsed(k * len(CALLS) + i, k * len(CALLS) + i + 1))
     gev.close()
-    del graph
-    return total, reps * n_in, {c: statistics.mean(v) for c, v in per_call.items()}
+    del g_main, g_rem, g_ev
+    return total, steps, {c: statistics.mean(v) for c, v in per_call.items()}
 
 
 def secondary_plan_latency(dev, stream):
@@ -1029,8 +1057,11 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": f"replicas x{world}",
                        "l2": "ids 168 MB > 129 MB L2 per step, no flush"},
             "gpu_launches": steps_run * sum(KERNELS_PER_CALL[c] for c in CALLS),
-            "timing": f"CUDA graph of {min(STEPS_PER_GRAPH, args.steps)} steps replayed; "
-                      "per-call times from event nodes inside the graph",
+            "timing": f"exactly {steps_run} steps replayed from CUDA graphs of "
+                      f"{min(STEPS_PER_GRAPH, args.steps)} steps with nothing between the calls, CUDA "
+                      "events around all replays; per-call times (and the roofline) from the same steps "
+                      f"captured with an event node before every call, replayed {CALL_REPLAYS} times after "
+                      "them (those nodes break the programmatic launch chain: about 4% slower)",
             "calls": calls,
             "roofline": {"bound": "hbm", "kernel": f"{dom} call ({CALL_KERNEL[dom]} + its index kernels)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
