@@ -61,7 +61,6 @@ struct Geo {
     size_t off_main;        // int32 [2E + R*E_R]     main(e), local index, mains[r][j]
     size_t off_rep;         // int32 [L][E][M]        stage-1 replica instance per domain
     size_t off_iexp;        // int32 [L][n_keys]      expert held by each instance
-    size_t off_imask;       // u32   [L][E][ceil(R/32)] ranks holding an instance of each expert
     size_t off_ioff;        // int32 [L][E+1]         start of each expert's instances in ilist
     size_t off_ilist;       // int32 [L][n_keys]      instances grouped by expert, ascending rank
     size_t off_roff;        // int32 [L][R][E+1]      per-(s,e) entry offsets in row s

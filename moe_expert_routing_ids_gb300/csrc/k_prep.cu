@@ -62,31 +62,25 @@ __device__ __forceinline__ void stage_words(void *dst, const void *src, int n) {
 // Prep: instance index, routing index, layout offsets (from the plan only)
 // ---------------------------------------------------------------------------
 
-// Instance index of a layer: the expert of every instance (iexp) and a
-// bitmask over ranks of the instances of every expert (imask, zeroed before).
-// One thread per instance.  tab == nullptr: the contiguous main map (main of
-// e is e / (E/R)).
+// Instance index of a layer: the expert of every instance (iexp).  One thread
+// per instance.  tab == nullptr: the contiguous main map (main of e is
+// e / (E/R)).
 __device__ __forceinline__ void inst_index(const int32_t *__restrict__ slot_expert,
-                                           const int32_t *__restrict__ tab, int32_t *iexp, unsigned *imask,
-                                           WsHeader *hdr, const Geo &g, int bx) {
+                                           const int32_t *__restrict__ tab, int32_t *iexp, WsHeader *hdr,
+                                           const Geo &g, int bx) {
     const int l = blockIdx.y;
     const int i = bx * blockDim.x + threadIdx.x;
     if (l == 0 && i == 0) hdr->route_fp = 0;
     if (i >= g.n_keys) return;
     const int E = g.E, R = g.R, nl = g.n_local, ER = g.E_R, ns = g.n_slot;
-    const int RW = (R + 31) / 32;
     const int r = i / nl, li = i - r * nl;
     int e = li < ER ? (tab ? __ldg(tab + 2 * E + r * ER + li) : r * ER + li)
                     : __ldg(slot_expert + ((int64_t)l * R + r) * ns + (li - ER));
-    bool bad = false;
-    if (e >= E || e < -1) { bad = true; e = -1; }
-    iexp[(int64_t)l * g.n_keys + i] = e;
-    if (e >= 0) {
-        const unsigned bit = 1u << (r & 31);
-        const unsigned old = atomicOr(&imask[((int64_t)l * E + e) * RW + (r >> 5)], bit);
-        if (old & bit) bad = true;                             // expert twice on one rank
+    if (e >= E || e < -1) {
+        set_error(hdr, TOPO_ESTATE);
+        e = -1;
     }
-    if (bad) set_error(hdr, TOPO_ESTATE);
+    iexp[(int64_t)l * g.n_keys + i] = e;
 }
 
 // Exclusive scan of one (count, sum) pair per thread over the CTA; returns
@@ -132,18 +126,32 @@ __device__ __forceinline__ int lower_idx(const int *a, int n, int v) {
 }
 
 // Instances of a layer grouped by expert, in ascending rank order (ilist),
-// and each expert's start in it (ioff).  An instance's place is its expert's
-// start plus the number of lower ranks in the expert's rank mask.  Every CTA
-// prefixes the layer's mask popcounts itself; CTA 0 stores the offsets.
-__device__ __forceinline__ void inst_list(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask,
-                                          int32_t *ioff_g, int32_t *ilist, const Geo &g, int bx, int *sml) {
+// and each expert's start in it (ioff).  Every CTA stages the layer's
+// instance experts and builds each expert's bitmask over ranks in shared
+// memory (an expert twice on one rank raises ESTATE); an instance's place is
+// its expert's start plus the number of lower ranks in the mask.  Every CTA
+// prefixes the mask popcounts itself; CTA 0 stores the offsets.
+__device__ __forceinline__ void inst_list(const int32_t *__restrict__ iexp, int32_t *ioff_g, int32_t *ilist,
+                                          WsHeader *hdr, const Geo &g, int bx, int *sml) {
     __shared__ int warp_tot[32];
     const int l = blockIdx.y, E = g.E, nk = g.n_keys, nl = g.n_local;
     const int RW = (g.R + 31) / 32;
     unsigned *msk = reinterpret_cast<unsigned *>(sml);          // [E][RW]
     int *ioff = reinterpret_cast<int *>(msk + E * RW);          // [E+1]
-    stage_words(msk, imask + (int64_t)l * E * RW, E * RW);
+    int *ie = ioff + ((E + 4) & ~3);                            // [nk] the layer's instance experts
+    stage_words(ie, iexp + (int64_t)l * nk, nk);
+    for (int i = threadIdx.x; i < E * RW; i += blockDim.x) msk[i] = 0u;
     cp_async_wait_all();
+    __syncthreads();
+    bool dup = false;
+    for (int i = threadIdx.x; i < nk; i += blockDim.x) {
+        const int e = ie[i];
+        if (e < 0) continue;
+        const int r = i / nl;
+        const unsigned bit = 1u << (r & 31);
+        dup |= (atomicOr(&msk[e * RW + (r >> 5)], bit) & bit) != 0;   // expert twice on one rank
+    }
+    if (dup && bx == 0) set_error(hdr, TOPO_ESTATE);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c = 0;
@@ -159,7 +167,7 @@ __device__ __forceinline__ void inst_list(const int32_t *__restrict__ iexp, cons
     }
     const int i = bx * blockDim.x + threadIdx.x;
     if (i >= nk) return;
-    const int e = __ldg(iexp + (int64_t)l * nk + i);
+    const int e = ie[i];
     if (e < 0) return;
     const int r = i / nl;
     const unsigned *m = msk + e * RW;
@@ -338,20 +346,19 @@ __device__ __forceinline__ void lay_seg(const int32_t *__restrict__ ccnt, int32_
 // alone.
 __global__ void __launch_bounds__(256)
 k_prep_a(const int32_t *__restrict__ slot_expert, const int32_t *__restrict__ tab, int32_t *iexp,
-         unsigned *imask, WsHeader *hdr, const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g,
-         int n_a) {
+         WsHeader *hdr, const int32_t *__restrict__ q, int32_t *soff, int32_t *ccnt, Geo g, int n_a) {
     pdl_wait();                                  // the previous kernel's outputs
-    if ((int)blockIdx.x < n_a) inst_index(slot_expert, tab, iexp, imask, hdr, g, blockIdx.x);
+    if ((int)blockIdx.x < n_a) inst_index(slot_expert, tab, iexp, hdr, g, blockIdx.x);
     else lay_cols(q, soff, ccnt, g, blockIdx.x - n_a);
     pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kPrepBThreads)
-k_prep_b(const int32_t *__restrict__ iexp, const unsigned *__restrict__ imask, int32_t *ioff_g,
-         int32_t *ilist, const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g, int n_a) {
+k_prep_b(const int32_t *__restrict__ iexp, int32_t *ioff_g, int32_t *ilist, WsHeader *hdr,
+         const int32_t *__restrict__ ccnt, int32_t *lseg, int64_t *lstat, Geo g, int n_a) {
     extern __shared__ __align__(16) int sml[];
     pdl_wait();                                  // the previous kernel's outputs
-    if ((int)blockIdx.x < n_a) inst_list(iexp, imask, ioff_g, ilist, g, blockIdx.x, sml);
+    if ((int)blockIdx.x < n_a) inst_list(iexp, ioff_g, ilist, hdr, g, blockIdx.x, sml);
     else lay_seg(ccnt, lseg, lstat, g);
     pdl_trigger();
 }
@@ -410,6 +417,11 @@ k_lay_entries(const int32_t *__restrict__ roff, Entry *rent, const int32_t *__re
 
 }  // namespace
 
+// Shared memory of the instance list: rank masks, offsets, the instance experts.
+size_t inst_list_smem(const Geo &g) {
+    return ((size_t)g.E * ((g.R + 31) / 32) + (((size_t)g.E + 4) & ~(size_t)3) + g.n_keys) * 4;
+}
+
 size_t row_index_smem(const Geo &g) {
     const size_t nk4 = ((size_t)g.n_keys + 3) & ~(size_t)3;
     return (2 * nk4 + (((size_t)g.E + 4) & ~(size_t)3) + 2 * (size_t)g.E) * 4;
@@ -424,23 +436,19 @@ cudaError_t launch_prep(const Geo &g, const int32_t *main_rank, const topo_plan_
     int64_t *lsend = send_counts ? send_counts : ws_at<int64_t>(ws, g.off_lsend);
     int64_t *lstat = layout_stats ? layout_stats : ws_at<int64_t>(ws, g.off_lstat);
     if (main_rank && (e = launch_main_tables(g, main_rank, ws, nullptr, 0, st)) != cudaSuccess) return e;
-    const int RW = (g.R + 31) / 32;
-    if ((e = cudaMemsetAsync(ws_at<unsigned>(ws, g.off_imask), 0, (size_t)g.L * g.E * RW * 4, st)) !=
-        cudaSuccess)
-        return e;
     const int na = (g.n_keys + 255) / 256, nb = (g.n_keys + 31) / 32;
     if ((e = launch_pdl(k_prep_a, dim3(na + nb, g.L), dim3(256), 0, st, p.slot_expert,
-                        main_rank ? ws_at<int32_t>(ws, g.off_main) : nullptr, ws_at<int32_t>(ws, g.off_iexp),
-                        ws_at<unsigned>(ws, g.off_imask), hdr, p.route_cnt, ws_at<int32_t>(ws, g.off_soff),
-                        ws_at<int32_t>(ws, g.off_ccnt), g, na)) != cudaSuccess)
+                        main_rank ? ws_at<int32_t>(ws, g.off_main) : nullptr, ws_at<int32_t>(ws, g.off_iexp), hdr,
+                        p.route_cnt, ws_at<int32_t>(ws, g.off_soff), ws_at<int32_t>(ws, g.off_ccnt), g, na)) !=
+        cudaSuccess)
         return e;
     const int nl_blocks = (g.n_keys + kPrepBThreads - 1) / kPrepBThreads;
-    const size_t smem_list = ((size_t)g.E * RW + g.E + 1) * 4;
+    const size_t smem_list = inst_list_smem(g);
     if ((e = ensure_smem((const void *)k_prep_b, smem_list)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_prep_b, dim3(nl_blocks + 1, g.L), dim3(kPrepBThreads), smem_list, st,
-                        ws_at<int32_t>(ws, g.off_iexp), ws_at<unsigned>(ws, g.off_imask),
-                        ws_at<int32_t>(ws, g.off_ioff), ws_at<int32_t>(ws, g.off_ilist),
-                        ws_at<int32_t>(ws, g.off_ccnt), lseg, lstat, g, nl_blocks)) != cudaSuccess)
+                        ws_at<int32_t>(ws, g.off_iexp), ws_at<int32_t>(ws, g.off_ioff),
+                        ws_at<int32_t>(ws, g.off_ilist), hdr, ws_at<int32_t>(ws, g.off_ccnt), lseg, lstat, g,
+                        nl_blocks)) != cudaSuccess)
         return e;
     const size_t smem_row = row_index_smem(g);
     if ((e = ensure_smem((const void *)k_row_index, smem_row)) != cudaSuccess) return e;

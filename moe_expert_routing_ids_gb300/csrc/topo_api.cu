@@ -15,7 +15,8 @@ using namespace topo;
 namespace topo {
 
 cudaError_t ensure_smem(const void *fn, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    // the default limit, 48 KB, covers a kernel's static and dynamic shared
+    // memory together; beyond it the kernel must opt in
     static std::mutex mu;
     static std::map<std::pair<const void *, int>, size_t> done;
     int dev = 0;
@@ -24,7 +25,10 @@ cudaError_t ensure_smem(const void *fn, size_t bytes) {
     std::lock_guard<std::mutex> lock(mu);
     size_t &have = done[{fn, dev}];
     if (have >= bytes) return cudaSuccess;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaFuncAttributes a;
+    if ((e = cudaFuncGetAttributes(&a, fn)) != cudaSuccess) return e;
+    if (a.sharedSizeBytes + bytes > 48 * 1024)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e == cudaSuccess) have = bytes;
     return e;
 }
@@ -57,7 +61,7 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     const int64_t nl = E / R + c->n_slot;
     if (nl > 32767) return TOPO_EINVAL;
     if ((2 * (R * nl + 3) + E + 4 + 2 * E) * 4 + 2560 > kSmemMax) return TOPO_EINVAL;       // row index
-    if ((E * ((R + 31) / 32) + E + 1) * 4 + 256 > kSmemMax) return TOPO_EINVAL;             // instance list
+    if ((E * ((R + 31) / 32) + E + 4 + R * nl) * 4 + 8192 > kSmemMax) return TOPO_EINVAL;   // instance list
     if ((((2 * rpn + 4 * rpn * nl + (rpn * E + 1) / 2 + 3) & ~int64_t(3)) + rpn * nl * (rpn | 1)) * 4 >
         kSmemMax - 4096)
         return TOPO_EINVAL;                                                                 // refinement
@@ -119,7 +123,6 @@ int make_geo(const topo_cfg *c, int32_t n_layers, Geo *g) {
     g->off_main = off;  off = align_up(off + 3 * E * 4);
     g->off_rep = off;   off = align_up(off + L * E * g->M * 4);
     g->off_iexp = off;  off = align_up(off + L * g->n_keys * 4);
-    g->off_imask = off; off = align_up(off + L * E * ((R + 31) / 32) * 4);
     g->off_ioff = off;  off = align_up(off + L * (E + 1) * 4);
     g->off_ilist = off; off = align_up(off + L * g->n_keys * 4);
     g->off_roff = off;  off = align_up(off + L * R * (E + 1) * 4);

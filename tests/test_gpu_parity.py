@@ -381,6 +381,31 @@ def test_reroute_without_hist_index_is_rejected():
     assert P.error() == 0
 
 
+def test_expert_twice_on_a_rank_sets_estate():
+    """A plan whose slots hold an expert the rank already hosts, or an id
+    outside [0, E), is a bad state: the reroute's instance index says so."""
+    from moe_expert_routing_ids_gb300 import TOPO_ESTATE
+    from moe_expert_routing_ids_gb300.planner import Planner
+    dev = _dev()
+    cfg = _cfg(400, 8, 2, 4, 2, 1, S=8, Wb=10)       # E_R = 2: rank 0 hosts experts 0 and 1
+    ids = torch.as_tensor(W.random_small(4, 400, 8, 2, 1), device=dev)
+    P = Planner(cfg, 1, dev)
+    P.run(ids)
+    assert P.error() == 0
+    P.buf.slot_expert[0, 0, 0] = 0                   # rank 0's own main in its slot
+    P.reroute_layout(ids)
+    assert P.error() == TOPO_ESTATE
+    P.reset_error()
+    P.run(ids)
+    assert P.error() == 0
+    P.buf.slot_expert[0, 1, 0] = 99                  # not an expert
+    P.reroute_layout(ids)
+    assert P.error() == TOPO_ESTATE
+    P.reset_error()
+    P.run(ids)
+    assert P.error() == 0
+
+
 def test_layout_with_foreign_dst_is_rejected():
     from moe_expert_routing_ids_gb300 import TOPO_ESTATE
     from moe_expert_routing_ids_gb300.planner import Planner
