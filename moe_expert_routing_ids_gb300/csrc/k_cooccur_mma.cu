@@ -61,16 +61,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Byte of (layer x, expert e, token tt) in a stage laid out [K-atom][layer]
-// [row][128 B]: tokens 128a .. 128a+127 in K-atom a; row e is 128 bytes with
-// its 16-byte chunks permuted by XOR with e % 8 (the 128-byte swizzle).  The
-// two layers' rows of one K-atom are contiguous: one operand of 256 rows.
-__device__ __forceinline__ uint32_t tile_off(int x, int e, int tt) {
-    const int c = tt & 127;
-    return (uint32_t)(tt >> 7) * 2u * kAtomRows + (uint32_t)x * kAtomRows + (uint32_t)e * 128u +
-           ((uint32_t)((c >> 4) ^ (e & 7)) << 4) + (uint32_t)(c & 15);
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -255,6 +245,11 @@ k_cooccur_mma(const int32_t *__restrict__ ids, int32_t *__restrict__ part, WsHea
         const int x = tid / kMmaKB, tt = tid % kMmaKB;
         const bool builds = x == 0 || has_tr;
         const int32_t *lay = ids + (int64_t)(l + x) * T * kk;
+        // byte of (layer x, expert e, token tt) in a stage laid out [K-atom]
+        // [layer][row][128 B]: tokens 128a .. 128a+127 in K-atom a; row e is
+        // 128 bytes with its 16-byte chunks permuted by XOR with e % 8 (the
+        // 128-byte swizzle); the two layers' rows of one K-atom are contiguous,
+        // one operand of 256 rows.  off = colb + 128 e + (((cb ^ e) & 7) << 4).
         const int cc = tt & 127;
         const uint32_t colb = (uint32_t)(tt >> 7) * 2u * kAtomRows + (uint32_t)x * kAtomRows + (uint32_t)(cc & 15);
         const int cb = cc >> 4;
