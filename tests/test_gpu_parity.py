@@ -157,6 +157,15 @@ OFFSETS = {
     "ragged_k10_r128": (_cfg(128 * 1200 + 77, 512, 10, 128, 8, 16, S=14336, Wb=66_060_288),
                         lambda c: W.random_small(44, c["T"], c["E"], c["k"], 2, s=1.4),
                         lambda c: _ragged(c["T"], c["R"], 2)),
+    # R = 256 with 48 slots (the refinement's q as 16-bit counts in shared
+    # memory), ragged blocks with empty sources
+    "ragged_q16": (_cfg(256 * 150, 512, 8, 256, 8, 48, S=1024, Wb=60_000),
+                   lambda c: W.random_small(46, c["T"], c["E"], c["k"], 1, s=1.3),
+                   lambda c: _ragged(c["T"], c["R"], 4)),
+    # R = 256 with 96 slots and free replicas (q in global memory, rows fetched)
+    "ragged_fetch": (_cfg(256 * 150, 512, 8, 256, 8, 96, S=1024, Wb=0),
+                     lambda c: W.random_small(47, c["T"], c["E"], c["k"], 1, s=1.6),
+                     lambda c: _ragged(c["T"], c["R"], 5)),
     # repeated ids inside a token with unequal blocks (the exact path)
     "ragged_repeats": (_cfg(8 * 700 + 5, 16, 4, 8, 4, 2, S=256, Wb=5_000),
                        lambda c: _with_repeats(W.random_small(45, c["T"], c["E"], c["k"], 1, s=1.2)),
