@@ -329,12 +329,15 @@ k_route_tiles(const int32_t *__restrict__ ids, const int32_t *__restrict__ tile_
             }
         }
         __syncthreads();
-        // pass 2: inclusive prefix over warps
+        // pass 2: inclusive prefix over warps (the expert's words all read first)
         for (int e = threadIdx.x; e < E; e += kRankThreads) {
+            int v[kRankWarps];
+#pragma unroll
+            for (int x = 0; x < kRankWarps; ++x) v[x] = S.base[x * E + e];
             int run = 0;
 #pragma unroll
             for (int x = 0; x < kRankWarps; ++x) {
-                run += S.base[x * E + e];
+                run += v[x];
                 S.base[x * E + e] = run;
             }
         }
