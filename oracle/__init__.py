@@ -270,7 +270,9 @@ def plan(cfg: dict, hist_arr, max_refine_iters: int | None = None):
 
 
 def reroute(cfg: dict, ids, plan_out: dict):
-    """dst_inst int32 [L, T*k] for ids [L, T, k] under the plan (O7 reading)."""
+    """dst_inst int32 [L, T*k] for ids [L, T, k] under the plan: within a source the
+    pairs of expert e, in pair order, fill e's instances in ascending (rank,
+    slot) order, each up to its routed count q (oracle.c, section O7)."""
     a = _i32(ids)
     squeeze = a.ndim == 2
     if squeeze:

@@ -33,8 +33,10 @@ def test_reroute_and_layout_hand_case(golden):
 
 
 def test_reroute_t1_source0_expert0(golden):
-    """The survey's T2 reading on the Fig. 9-shaped plan: source 0's six e0
-    assignments -> first 2 to the main on r0, next 4 to r1's replica."""
+    """Pair-to-instance order on the Fig. 9-shaped plan: a source's pairs for
+    an expert fill that expert's instances in ascending rank order, each up
+    to its routed count, so source 0's six e0 assignments go 2 to the main
+    on r0, then 4 to r1's replica."""
     g = golden("plan_t1_fig9_shape.json")
     cfg = dict(g["cfg"])
     # ids consistent with the hist rows: 14 pairs per source would need equal
