@@ -245,12 +245,18 @@ __global__ void __launch_bounds__(kDdTile, kDdFillCtas)
 k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
           const int32_t *__restrict__ src_base, const int32_t *__restrict__ seg,
           int32_t *__restrict__ row_token, unsigned long long *__restrict__ row_slots, DdGeo g) {
-    extern __shared__ unsigned ddf[];
-    unsigned *lm = ddf;                                    // [kDdWarps][R] lane masks
-    int *base = reinterpret_cast<int *>(lm + kDdWarps * g.R);   // [kDdWarps][R] tile positions
-    int *dlt = base + kDdWarps * g.R;                      // [R] global - tile position
-    unsigned *srow = reinterpret_cast<unsigned *>(dlt + g.R);   // [kDdTile*KB] token | slots << 8
-    unsigned short *srk = reinterpret_cast<unsigned short *>(srow + kDdTile * KB);  // row rank
+    extern __shared__ __align__(16) unsigned ddf[];
+    // [kDdWarps][R] (lane mask, tile position) pairs: a slot reads both of its
+    // group's words with one 64-bit load
+    uint2 *lmb = reinterpret_cast<uint2 *>(ddf);
+    int *dlt = reinterpret_cast<int *>(lmb + kDdWarps * g.R);   // [R] global - tile position
+    // staged rows [kDdTile*KB]: token | slots << 8 | rank << (8 + k) when the
+    // rank fits the word's remaining 24 - k bits (every slot of a row ORs the
+    // same rank in); otherwise the rank goes to srk
+    unsigned *srow = reinterpret_cast<unsigned *>(dlt + g.R);
+    unsigned short *srk = reinterpret_cast<unsigned short *>(srow + kDdTile * KB);
+    const bool rk_in_row = g.R <= (1 << (24 - g.k));
+    const int rk_shift = 8 + g.k;
     __shared__ int warp_tot[32];
     const DdTile d = dd_tile(g);
     if (d.s < 0) return;                                   // past the last source's tiles
@@ -259,7 +265,7 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
     const int64_t tokb = d.tok0;
     int v[KB];
     dd_load<KB>(dst + (int64_t)d.l * g.npairs + tokb * g.k, n, v);
-    for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lm[x] = 0;
+    for (int x = tid; x < kDdWarps * g.R; x += kDdTile) lmb[x].x = 0u;
 #pragma unroll
     for (int u = 0; u < KB; ++u) srow[u * kDdTile + tid] = 0;
     __syncthreads();
@@ -273,7 +279,7 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
         pk[u] = -1;
         if (e < n && dd_elem(e, v[u], g, i, j, r)) {
             pk[u] = r | (i << 10) | (j << 18);
-            atomicOr(&lm[(i >> 5) * g.R + r], 1u << (i & 31));
+            atomicOr(&lmb[(i >> 5) * g.R + r].x, 1u << (i & 31));
         }
     }
     __syncthreads();
@@ -283,7 +289,7 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
     int mine = 0;
     for (int r = r0; r < r1; ++r)
 #pragma unroll
-        for (int x = 0; x < kDdWarps; ++x) mine += __popc(lm[x * g.R + r]);
+        for (int x = 0; x < kDdWarps; ++x) mine += __popc(lmb[x * g.R + r].x);
     int nrows;
     int run = dd_block_scan(mine, warp_tot, nrows);
     const int64_t tile = blockIdx.x;
@@ -293,8 +299,8 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
                  __ldg(tile_pre + tile * g.R + r) - run;
 #pragma unroll
         for (int x = 0; x < kDdWarps; ++x) {
-            base[x * g.R + r] = run;
-            run += __popc(lm[x * g.R + r]);
+            lmb[x * g.R + r].y = (unsigned)run;
+            run += __popc(lmb[x * g.R + r].x);
         }
     }
     __syncthreads();
@@ -305,20 +311,27 @@ k_dd_fill(const int32_t *__restrict__ dst, const int32_t *__restrict__ tile_pre,
         if (pk[u] >= 0) {
             const int r = pk[u] & 1023, i = (pk[u] >> 10) & 255, j = pk[u] >> 18;
             const int x = (i >> 5) * g.R + r;
-            const int p = base[x] + __popc(lm[x] & ((1u << (i & 31)) - 1u));
-            atomicOr(&srow[p], (unsigned)i | (1u << (j + 8)));
-            srk[p] = (unsigned short)r;
+            const uint2 mb = lmb[x];
+            const int p = (int)mb.y + __popc(mb.x & ((1u << (i & 31)) - 1u));
+            if (rk_in_row) {
+                atomicOr(&srow[p], (unsigned)i | (1u << (j + 8)) | ((unsigned)r << rk_shift));
+            } else {
+                atomicOr(&srow[p], (unsigned)i | (1u << (j + 8)));
+                srk[p] = (unsigned short)r;
+            }
         }
     __syncthreads();
     // consecutive threads write consecutive rows: runs of one rank are contiguous
     int32_t *rt = row_token + (int64_t)d.l * g.npairs;
     unsigned long long *rs = row_slots + (int64_t)d.l * g.npairs;
+    const unsigned slot_mask = (1u << g.k) - 1u;             // k <= 16
     for (int p = tid; p < nrows; p += kDdTile) {
         const unsigned v = srow[p];
-        const int64_t pos = (int64_t)dlt[srk[p]] + p;
+        const int r = rk_in_row ? (int)(v >> rk_shift) : (int)srk[p];
+        const int64_t pos = (int64_t)dlt[r] + p;
         if (pos >= 0 && pos < g.npairs) {
             rt[pos] = (int32_t)(tokb + (v & 255u));
-            rs[pos] = v >> 8;
+            rs[pos] = (v >> 8) & slot_mask;
         }
     }
 }
