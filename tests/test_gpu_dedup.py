@@ -122,6 +122,11 @@ DIRECT = {
     "k2_r64": (_cfg(64 * 513, 64, 2, 64, 8, 1), 1),
     "k5_r1": (_cfg(1000, 4, 5, 1, 1, 1), 1),
     "k4_r192_three_words": (_cfg(192 * 20, 192, 4, 192, 8, 1), 1),
+    # the fill kernel keeps a row's rank in the row's 32-bit word while
+    # R <= 2^(24 - k): at the limit (rank in the top 8 or 9 bits) and past it
+    "k16_r256_rank_at_the_word_limit": (_cfg(256 * 12, 256, 16, 256, 8, 1), 1),
+    "k15_r512_rank_at_the_word_limit": (_cfg(512 * 6, 512, 15, 512, 8, 1), 1),
+    "k15_r1024_rank_apart": (_cfg(1024 * 3, 1024, 15, 1024, 32, 1), 1),
 }
 
 
